@@ -1,0 +1,446 @@
+/*
+ * CPU oracle for split-tier paged decode attention (test infrastructure only).
+ *
+ * A plain, slow, double-precision statement of what the hot path computes, used
+ * to check the CUDA library.  It shares no code, header or constant with the
+ * CUDA path; only the seeded input generator is common to both.  Nothing in the
+ * product path may call it.
+ *
+ * Sources (web pages about ActiveKV, by their titles):
+ *   [FMT]   "model quantization", section "An 8-bit page format shaped for its
+ *           kernel": key scale per channel = sqrt of the channel's RMS over the
+ *           page, normalised so the channel scales multiply to one, clamped to
+ *           2^+-14; a per-token-and-head factor covers the rest; symmetric codes
+ *           in -127..127; values carry one scale per channel per page.
+ *   [ATT]   "SYCL", section "Attention that reads 8-bit history": the separable
+ *           key scale (per-token factor applied after the dot), PV on raw codes
+ *           rescaled per page.  The method is an exact re-association of
+ *           "dequantise, then attend", so this oracle dequantises and attends.
+ *   [MERGE] "SYCL", section "A merge that joins the tiers": partials (output plus
+ *           log-sum-exp) folded into one accumulator; -inf is a valid empty partial.
+ *   [TIERS] "ActiveKV", section "The idea": recent context exact, older history
+ *           8-bit, joined with exact attention arithmetic.
+ *
+ * Readings where the pages are silent (each is listed in the design notes):
+ *   - scales are stored as float32; key channel scales are rounded to float32 by
+ *     compensated rounding so that their product stays 1;
+ *   - normalisation is by the geometric mean, applied before the clamp; a channel
+ *     with zero RMS takes a = 2^-63 before the logarithm;
+ *   - per-token key factor r_t = max_c |k_tc / s_c| / 127, value scale
+ *     u_c = max_t |v_tc| / 127 (absmax), both in float32;
+ *   - codes: two correctly rounded float32 divisions (k / s_c, then / r_t),
+ *     rint (half to even), clamp to +-127; a zero scale gives zero codes;
+ *   - softmax scale 1/sqrt(d), log-sum-exp in natural-log units; an empty range
+ *     gives o = 0, lse = -inf.
+ *
+ * Record layout of one 8-bit page-head (35,072 bytes):
+ *   int8  kc[64][256]      keys, token-major       offset 0
+ *   int8  vc[64][256]      values, token-major     offset 16384
+ *   f32   ks_chan[256]     key channel scale s_c   offset 32768
+ *   f32   ks_tok[64]       key token factor r_t    offset 33792
+ *   f32   vs_chan[256]     value channel scale u_c offset 34048
+ * Dequantised: k_tc = kc_tc * s_c * r_t,  v_tc = vc_tc * u_c.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define T_PAGE 64
+#define D_HEAD 256
+#define REC_BYTES 35072
+#define OFF_KC 0
+#define OFF_VC 16384
+#define OFF_KS_CHAN 32768
+#define OFF_KS_TOK 33792
+#define OFF_VS_CHAN 34048
+
+static double bf16_value(uint16_t b) {
+  uint32_t u = (uint32_t)b << 16;
+  float f;
+  memcpy(&f, &u, 4);
+  return (double)f;
+}
+
+static float bf16_float(uint16_t b) {
+  uint32_t u = (uint32_t)b << 16;
+  float f;
+  memcpy(&f, &u, 4);
+  return f;
+}
+
+/* ================================================================ quantiser */
+
+/*
+ * Key channel scales of one page-head [FMT].
+ *   ms_c  = mean_t k_tc^2 (double);  a_c = sqrt(sqrt(ms_c))   (sqrt of the RMS)
+ *   g     = exp(mean_c ln a_c)       (geometric mean, so prod_c a_c/g = 1)
+ *   shat_c= clamp(a_c / g, 2^-14, 2^14)
+ *   s_c   = a float32 neighbour of shat_c chosen by compensated rounding: walk the
+ *           channels in order keeping E = sum (ln s - ln shat); take whichever
+ *           neighbour leaves |E| smaller (the lower one on a tie).
+ * Returns the number of channels the clamp engaged.
+ */
+int orc_channel_scales(const uint16_t* k, float* s_out, double* shat_out) {
+  double a[D_HEAD], shat[D_HEAD];
+  double sum_ln = 0.0;
+  for (int c = 0; c < D_HEAD; ++c) {
+    double ms = 0.0;
+    for (int t = 0; t < T_PAGE; ++t) {
+      double x = bf16_value(k[t * D_HEAD + c]);
+      ms += x * x;
+    }
+    ms /= T_PAGE;
+    double rms = sqrt(ms);
+    a[c] = rms > 0.0 ? sqrt(rms) : ldexp(1.0, -63);
+    sum_ln += log(a[c]);
+  }
+  double g = exp(sum_ln / D_HEAD);
+  int clamped = 0;
+  const double lo_b = ldexp(1.0, -14), hi_b = ldexp(1.0, 14);
+  for (int c = 0; c < D_HEAD; ++c) {
+    double v = a[c] / g;
+    if (v < lo_b) { v = lo_b; ++clamped; }
+    if (v > hi_b) { v = hi_b; ++clamped; }
+    shat[c] = v;
+  }
+  double E = 0.0;
+  for (int c = 0; c < D_HEAD; ++c) {
+    double sh = shat[c];
+    float f = (float)sh;
+    if ((double)f == sh) {
+      s_out[c] = f;
+      continue;
+    }
+    float lo = ((double)f < sh) ? f : nextafterf(f, 0.0f);
+    float hi = nextafterf(lo, INFINITY);
+    double dlo = log((double)lo / sh), dhi = log((double)hi / sh);
+    if (fabs(E + dlo) <= fabs(E + dhi)) {
+      s_out[c] = lo;
+      E += dlo;
+    } else {
+      s_out[c] = hi;
+      E += dhi;
+    }
+  }
+  if (shat_out)
+    for (int c = 0; c < D_HEAD; ++c) shat_out[c] = shat[c];
+  return clamped;
+}
+
+static int8_t code_of(float x, float scale) {
+  if (!(scale > 0.0f)) return 0;
+  float y = rintf(x / scale); /* float32 IEEE division, then half-to-even */
+  if (y > 127.0f) y = 127.0f;
+  if (y < -127.0f) y = -127.0f;
+  return (int8_t)y;
+}
+
+/*
+ * Codes of one page-head given all three scale arrays [FMT]:
+ *   kc_tc = clamp(rint((k_tc / s_c) / r_t)),  vc_tc = clamp(rint(v_tc / u_c)).
+ * The scales are copied into the record unchanged.
+ */
+void orc_codes_given(const uint16_t* k, const uint16_t* v, const float* ks_chan, const float* ks_tok,
+                     const float* vs_chan, uint8_t* rec) {
+  int8_t* kc = (int8_t*)(rec + OFF_KC);
+  int8_t* vc = (int8_t*)(rec + OFF_VC);
+  for (int t = 0; t < T_PAGE; ++t)
+    for (int c = 0; c < D_HEAD; ++c) {
+      float y = bf16_float(k[t * D_HEAD + c]) / ks_chan[c];
+      kc[t * D_HEAD + c] = code_of(y, ks_tok[t]);
+      vc[t * D_HEAD + c] = code_of(bf16_float(v[t * D_HEAD + c]), vs_chan[c]);
+    }
+  memcpy(rec + OFF_KS_CHAN, ks_chan, 4 * D_HEAD);
+  memcpy(rec + OFF_KS_TOK, ks_tok, 4 * T_PAGE);
+  memcpy(rec + OFF_VS_CHAN, vs_chan, 4 * D_HEAD);
+}
+
+/* Full conversion of one page-head [FMT]: scales, then codes.  Returns clamp count. */
+int orc_quantize_page_head(const uint16_t* k, const uint16_t* v, uint8_t* rec) {
+  float s[D_HEAD], r[T_PAGE], u[D_HEAD];
+  int clamped = orc_channel_scales(k, s, 0);
+  for (int t = 0; t < T_PAGE; ++t) {
+    float m = 0.0f;
+    for (int c = 0; c < D_HEAD; ++c) {
+      float y = fabsf(bf16_float(k[t * D_HEAD + c]) / s[c]);
+      if (y > m) m = y;
+    }
+    r[t] = m / 127.0f;
+  }
+  for (int c = 0; c < D_HEAD; ++c) {
+    float m = 0.0f;
+    for (int t = 0; t < T_PAGE; ++t) {
+      float y = fabsf(bf16_float(v[t * D_HEAD + c]));
+      if (y > m) m = y;
+    }
+    u[c] = m / 127.0f;
+  }
+  orc_codes_given(k, v, s, r, u, rec);
+  return clamped;
+}
+
+/* Convert n_pages pages of a [slot][H][64][256] BF16 pool into records at
+ * rec_pool + (dst_slot * H + h) * 35072. */
+void orc_quantize_pages(int H, const uint16_t* k_pool, const uint16_t* v_pool, const int32_t* src_slots,
+                        const int32_t* dst_slots, int n_pages, uint8_t* rec_pool) {
+  const int64_t ph = (int64_t)T_PAGE * D_HEAD;
+  for (int p = 0; p < n_pages; ++p)
+    for (int h = 0; h < H; ++h) {
+      int64_t src = ((int64_t)src_slots[p] * H + h) * ph;
+      orc_quantize_page_head(k_pool + src, v_pool + src,
+                             rec_pool + ((int64_t)dst_slots[p] * H + h) * REC_BYTES);
+    }
+}
+
+/* ================================================================ attention */
+
+/*
+ * Softmax attention of `rows` query rows over n tokens, in double:
+ *   s_t = scale * q . k_t;  m = max_t s_t;  l = sum_t exp(s_t - m)
+ *   o = sum_t exp(s_t - m) v_t / l;  lse = m + ln l.
+ * n = 0 gives o = 0 and lse = -inf (the empty partial).
+ */
+void orc_attend(int n, int d, int rows, const double* q, const double* K, const double* V, double scale,
+                double* o, double* lse) {
+  double* s = (double*)malloc(sizeof(double) * (n > 0 ? n : 1));
+  for (int r = 0; r < rows; ++r) {
+    double* orow = o + (int64_t)r * d;
+    for (int c = 0; c < d; ++c) orow[c] = 0.0;
+    if (n == 0) {
+      lse[r] = -INFINITY;
+      continue;
+    }
+    double m = -INFINITY;
+    for (int t = 0; t < n; ++t) {
+      double acc = 0.0;
+      for (int c = 0; c < d; ++c) acc += q[(int64_t)r * d + c] * K[(int64_t)t * d + c];
+      s[t] = scale * acc;
+      if (s[t] > m) m = s[t];
+    }
+    double l = 0.0;
+    for (int t = 0; t < n; ++t) {
+      double w = exp(s[t] - m);
+      l += w;
+      for (int c = 0; c < d; ++c) orow[c] += w * V[(int64_t)t * d + c];
+    }
+    for (int c = 0; c < d; ++c) orow[c] /= l;
+    lse[r] = m + log(l);
+  }
+  free(s);
+}
+
+/* Exact-tier partial for KV head h [ATT, MERGE]: BF16 tokens [tok_begin, tok_end)
+ * of a paged history (token t lives in slot page_table[t / 64], row t % 64). */
+static void partial_exact_head(int H, int G, int h, const uint16_t* q, const uint16_t* k_pool,
+                               const uint16_t* v_pool, const int32_t* page_table, int tok_begin, int tok_end,
+                               double* o, double* lse) {
+  const int d = D_HEAD;
+  int n = tok_end > tok_begin ? tok_end - tok_begin : 0;
+  double* K = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1) * d);
+  double* V = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1) * d);
+  double* qd = (double*)malloc(sizeof(double) * (size_t)G * d);
+  for (int i = 0; i < n; ++i) {
+    int t = tok_begin + i;
+    int64_t slot = page_table[t / T_PAGE];
+    int64_t base = ((slot * H + h) * T_PAGE + t % T_PAGE) * (int64_t)d;
+    for (int c = 0; c < d; ++c) {
+      K[(int64_t)i * d + c] = bf16_value(k_pool[base + c]);
+      V[(int64_t)i * d + c] = bf16_value(v_pool[base + c]);
+    }
+  }
+  for (int g = 0; g < G; ++g)
+    for (int c = 0; c < d; ++c) qd[g * d + c] = bf16_value(q[((int64_t)h * G + g) * d + c]);
+  orc_attend(n, d, G, qd, K, V, 1.0 / sqrt((double)d), o + (int64_t)h * G * d, lse + h * G);
+  free(K);
+  free(V);
+  free(qd);
+}
+
+/* 8-bit-tier partial for KV head h [FMT, ATT]: pages [page_begin, page_end) of the
+ * record pool, page p in slot page_table8[p]; dequantise, then attend. */
+static void partial_int8_head(int H, int G, int h, const uint16_t* q, const uint8_t* rec_pool,
+                              const int32_t* page_table8, int page_begin, int page_end, double* o, double* lse) {
+  const int d = D_HEAD;
+  int np = page_end > page_begin ? page_end - page_begin : 0;
+  int n = np * T_PAGE;
+  double* K = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1) * d);
+  double* V = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1) * d);
+  double* qd = (double*)malloc(sizeof(double) * (size_t)G * d);
+  for (int p = 0; p < np; ++p) {
+    const uint8_t* rec = rec_pool + ((int64_t)page_table8[page_begin + p] * H + h) * REC_BYTES;
+    const int8_t* kc = (const int8_t*)(rec + OFF_KC);
+    const int8_t* vc = (const int8_t*)(rec + OFF_VC);
+    float s[D_HEAD], r[T_PAGE], u[D_HEAD];
+    memcpy(s, rec + OFF_KS_CHAN, sizeof s);
+    memcpy(r, rec + OFF_KS_TOK, sizeof r);
+    memcpy(u, rec + OFF_VS_CHAN, sizeof u);
+    for (int t = 0; t < T_PAGE; ++t)
+      for (int c = 0; c < d; ++c) {
+        int64_t i = ((int64_t)p * T_PAGE + t) * d + c;
+        K[i] = (double)kc[t * d + c] * (double)s[c] * (double)r[t];
+        V[i] = (double)vc[t * d + c] * (double)u[c];
+      }
+  }
+  for (int g = 0; g < G; ++g)
+    for (int c = 0; c < d; ++c) qd[g * d + c] = bf16_value(q[((int64_t)h * G + g) * d + c]);
+  orc_attend(n, d, G, qd, K, V, 1.0 / sqrt((double)d), o + (int64_t)h * G * d, lse + h * G);
+  free(K);
+  free(V);
+  free(qd);
+}
+
+void orc_partial_exact(int H, int G, const uint16_t* q, const uint16_t* k_pool, const uint16_t* v_pool,
+                       const int32_t* page_table, int tok_begin, int tok_end, double* o, double* lse) {
+  for (int h = 0; h < H; ++h)
+    partial_exact_head(H, G, h, q, k_pool, v_pool, page_table, tok_begin, tok_end, o, lse);
+}
+
+void orc_partial_int8(int H, int G, const uint16_t* q, const uint8_t* rec_pool, const int32_t* page_table8,
+                      int page_begin, int page_end, double* o, double* lse) {
+  for (int h = 0; h < H; ++h)
+    partial_int8_head(H, G, h, q, rec_pool, page_table8, page_begin, page_end, o, lse);
+}
+
+/*
+ * Fold n_parts partials (o_i, lse_i) of `rows` rows [MERGE]:
+ *   lse = ln sum_i exp(lse_i);  o = sum_i exp(lse_i - lse) o_i.
+ * Partials with lse_i = -inf are skipped (their o_i is never read); if every
+ * partial is empty the result is o = 0, lse = -inf.
+ */
+void orc_merge(int n_parts, int rows, int d, const double* o_parts, const double* lse_parts, double* o,
+               double* lse) {
+  for (int r = 0; r < rows; ++r) {
+    double m = -INFINITY;
+    for (int i = 0; i < n_parts; ++i) {
+      double x = lse_parts[(int64_t)i * rows + r];
+      if (x > m) m = x;
+    }
+    double* orow = o + (int64_t)r * d;
+    for (int c = 0; c < d; ++c) orow[c] = 0.0;
+    if (m == -INFINITY) {
+      lse[r] = -INFINITY;
+      continue;
+    }
+    double l = 0.0;
+    for (int i = 0; i < n_parts; ++i) {
+      double x = lse_parts[(int64_t)i * rows + r];
+      if (x == -INFINITY) continue;
+      l += exp(x - m);
+    }
+    double L = m + log(l);
+    for (int i = 0; i < n_parts; ++i) {
+      double x = lse_parts[(int64_t)i * rows + r];
+      if (x == -INFINITY) continue;
+      double w = exp(x - L);
+      const double* oi = o_parts + ((int64_t)i * rows + r) * d;
+      for (int c = 0; c < d; ++c) orow[c] += w * oi[c];
+    }
+    lse[r] = L;
+  }
+}
+
+/* ====================================================== multi-request hybrid */
+
+typedef struct {
+  int B, H, G;
+  const uint16_t *q, *k_pool, *v_pool;
+  const uint8_t* rec_pool;
+  const int32_t *page_table, *req_page_off, *n_exact_tokens;
+  const int32_t *page_table8, *req_page_off8, *n_int8_pages;
+  double *o, *lse;
+  int next; /* next (request, head) item, under the lock */
+  pthread_mutex_t lock;
+} hybrid_job;
+
+static void hybrid_item(hybrid_job* J, int item) {
+  const int d = D_HEAD;
+  int b = item / J->H, h = item % J->H;
+  int rows = J->H * J->G;
+  double* parts_o = (double*)malloc(sizeof(double) * 2 * (size_t)rows * d);
+  double* parts_lse = (double*)malloc(sizeof(double) * 2 * (size_t)rows);
+  const uint16_t* qb = J->q + (int64_t)b * rows * d;
+  partial_exact_head(J->H, J->G, h, qb, J->k_pool, J->v_pool, J->page_table + J->req_page_off[b], 0,
+                     J->n_exact_tokens[b], parts_o, parts_lse);
+  partial_int8_head(J->H, J->G, h, qb, J->rec_pool, J->page_table8 + J->req_page_off8[b], 0,
+                    J->n_int8_pages[b], parts_o + (int64_t)rows * d, parts_lse + rows);
+  /* gather this head's G rows of both partials and fold them [TIERS, MERGE] */
+  double po[2 * 8 * D_HEAD], pl[2 * 8], oo[8 * D_HEAD], ll[8];
+  double *po_h = po, *pl_h = pl, *oo_h = oo, *ll_h = ll;
+  int G = J->G;
+  double* heap = 0;
+  if (G > 8) {
+    heap = (double*)malloc(sizeof(double) * (size_t)(2 * G * d + 2 * G + G * d + G));
+    po_h = heap;
+    pl_h = po_h + 2 * G * d;
+    oo_h = pl_h + 2 * G;
+    ll_h = oo_h + G * d;
+  }
+  for (int i = 0; i < 2; ++i)
+    for (int g = 0; g < G; ++g) {
+      int r = h * G + g;
+      pl_h[i * G + g] = parts_lse[(int64_t)i * rows + r];
+      memcpy(po_h + ((int64_t)i * G + g) * d, parts_o + ((int64_t)i * rows + r) * d, sizeof(double) * d);
+    }
+  orc_merge(2, G, d, po_h, pl_h, oo_h, ll_h);
+  for (int g = 0; g < G; ++g) {
+    int r = h * G + g;
+    J->lse[(int64_t)b * rows + r] = ll_h[g];
+    memcpy(J->o + ((int64_t)b * rows + r) * d, oo_h + (int64_t)g * d, sizeof(double) * d);
+  }
+  free(heap);
+  free(parts_o);
+  free(parts_lse);
+}
+
+static void* hybrid_worker(void* arg) {
+  hybrid_job* J = (hybrid_job*)arg;
+  for (;;) {
+    pthread_mutex_lock(&J->lock);
+    int item = J->next++;
+    pthread_mutex_unlock(&J->lock);
+    if (item >= J->B * J->H) break;
+    hybrid_item(J, item);
+  }
+  return 0;
+}
+
+/*
+ * One hybrid decode step for B requests [TIERS]: per request and KV head, the
+ * exact partial over the request's BF16 tokens [0, n_exact_tokens[b]) (CSR page
+ * table page_table / req_page_off) and the 8-bit partial over its pages
+ * [0, n_int8_pages[b]) (CSR page_table8 / req_page_off8), folded by orc_merge.
+ * o is [B][H*G][256], lse is [B][H*G].  Work is spread over n_threads threads by
+ * (request, KV head); the result does not depend on the thread count.
+ */
+void orc_hybrid_batched(int B, int H, int G, const uint16_t* q, const uint16_t* k_pool, const uint16_t* v_pool,
+                        const uint8_t* rec_pool, const int32_t* page_table, const int32_t* req_page_off,
+                        const int32_t* n_exact_tokens, const int32_t* page_table8, const int32_t* req_page_off8,
+                        const int32_t* n_int8_pages, double* o, double* lse, int n_threads) {
+  hybrid_job J;
+  J.B = B;
+  J.H = H;
+  J.G = G;
+  J.q = q;
+  J.k_pool = k_pool;
+  J.v_pool = v_pool;
+  J.rec_pool = rec_pool;
+  J.page_table = page_table;
+  J.req_page_off = req_page_off;
+  J.n_exact_tokens = n_exact_tokens;
+  J.page_table8 = page_table8;
+  J.req_page_off8 = req_page_off8;
+  J.n_int8_pages = n_int8_pages;
+  J.o = o;
+  J.lse = lse;
+  J.next = 0;
+  pthread_mutex_init(&J.lock, 0);
+  if (n_threads < 1) n_threads = 1;
+  if (n_threads > 256) n_threads = 256;
+  pthread_t th[256];
+  for (int i = 1; i < n_threads; ++i) pthread_create(&th[i], 0, hybrid_worker, &J);
+  hybrid_worker(&J);
+  for (int i = 1; i < n_threads; ++i) pthread_join(th[i], 0);
+  pthread_mutex_destroy(&J.lock);
+}

@@ -1,0 +1,204 @@
+"""Pins of the oracle's page conversion against facts that do not come from the
+oracle itself: a hand-derived golden page, invariances the scale rules imply,
+and per-element error bounds.
+
+Source: "model quantization", section "An 8-bit page format shaped for its kernel".
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from tiered_paged_kv_gb300 import synth
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden", "quant_powers_of_two.json")
+T, D = 64, 256
+
+
+def bf16_bits(x):
+    """Exact float -> bfloat16 bits for values that are representable."""
+    b = synth.f32_to_bf16(np.asarray(x, np.float32))
+    assert np.array_equal(synth.bf16_to_f32(b), np.asarray(x, np.float32)), "not representable"
+    return b
+
+
+def golden_page():
+    t = np.arange(T)[:, None]
+    c = np.arange(D)[None, :]
+    m = np.array([-3, -2, -1, 0, 0, 1, 2, 3])[c % 8]
+    w = (t % 4) - 1
+    sk = np.where((t + c) % 3 == 0, 1.0, -1.0)
+    K = sk * np.exp2(2 * m + 2 * w)
+    K[63, :] = 0.0
+    n = (c % 5) - 2
+    kt = np.array([8, 4, 6, 3, 1, 0, 2, 5, 7])[t % 9]
+    sv = np.where((t * 7 + c) % 4 == 1, -1.0, 1.0)
+    V = sv * np.exp2(n) * kt / 8.0
+    V[:, 255] = 0.0
+    return K, V, m, w, n, kt, sk, sv
+
+
+def test_golden_powers_of_two_page():
+    g = json.load(open(GOLD))
+    K, V, m, w, n, kt, sk, sv = golden_page()
+    rec, clamped = oracle.quantize_page_head(bf16_bits(K), bf16_bits(V))
+    kc, vc, s, r, u = oracle.record_fields(rec)
+    assert clamped == 0
+    mm = m[0]
+    exp_s = np.array([float.fromhex(g["keys"]["s_by_m"][str(x)]) for x in mm], np.float32)
+    assert np.array_equal(s, exp_s)
+    ww = w[:, 0]
+    exp_r = np.array([float.fromhex(g["keys"]["r_by_w"][str(x)]) for x in ww], np.float32)
+    exp_r[63] = 0.0
+    assert np.array_equal(r, exp_r)
+    code_m = np.array([g["keys"]["code_by_m"][str(x)] for x in mm])
+    exp_kc = (sk * code_m[None, :]).astype(np.int8)
+    exp_kc[63, :] = 0
+    assert np.array_equal(kc, exp_kc)
+    nn = n[0]
+    exp_u = np.array([float.fromhex(g["values"]["u_by_n"][str(x)]) for x in nn], np.float32)
+    exp_u[255] = 0.0
+    assert np.array_equal(u, exp_u)
+    code_k = np.array([g["values"]["code_by_k"][str(x)] for x in kt[:, 0]])
+    exp_vc = (sv * code_k[:, None]).astype(np.int8)
+    exp_vc[:, 255] = 0
+    assert np.array_equal(vc, exp_vc)
+
+
+def random_page(seed, kind="loguniform"):
+    sig = None
+    if kind == "loguniform":
+        sig = 10.0 ** (2.0 * synth.uniform(seed, 100, D) - 1.0)
+    elif kind == "outliers":
+        sig = np.ones(D)
+        sig[synth.permutation(seed, 101, D)[:4]] = 20.0
+    k = synth.normal_bf16(seed, 102, T * D, sigma=sig).reshape(T, D)
+    v = synth.normal_bf16(seed, 103, T * D, sigma=sig).reshape(T, D)
+    return k, v
+
+
+PAGES = [(s, kind) for s in range(6) for kind in ("unit", "loguniform", "outliers")]
+
+
+@pytest.mark.parametrize("seed,kind", PAGES)
+def test_code_range_and_saturation(seed, kind):
+    k, v = random_page(seed, kind)
+    rec, _ = oracle.quantize_page_head(k, v)
+    kc, vc, s, r, u = oracle.record_fields(rec)
+    for codes in (kc, vc):
+        assert codes.min() >= -127 and codes.max() <= 127
+    # the absmax element of every row / channel reaches full scale
+    assert np.all(np.abs(kc).max(axis=1)[r > 0] == 127)
+    assert np.all(np.abs(vc).max(axis=0)[u > 0] == 127)
+
+
+@pytest.mark.parametrize("seed,kind", PAGES)
+def test_channel_scales_multiply_to_one(seed, kind):
+    k, v = random_page(seed, kind)
+    s, shat, clamped = oracle.channel_scales(k)
+    assert clamped == 0
+    assert np.all(s >= 2.0 ** -14) and np.all(s <= 2.0 ** 14)
+    prod = np.exp(np.sum(np.log(s.astype(np.float64))))
+    assert abs(prod - 1.0) <= 1e-6
+    # every stored scale is a float32 neighbour of the exact one
+    lo = np.nextafter(s, np.float32(0))
+    hi = np.nextafter(s, np.float32(np.inf))
+    assert np.all((lo.astype(np.float64) <= shat) & (shat <= hi.astype(np.float64)))
+
+
+def test_channel_scale_is_sqrt_rms_ratio():
+    """Two channel groups with RMS ratio 16 -> scale ratio 4 (sqrt of RMS), product 1."""
+    K = np.ones((T, D))
+    K[:, :128] *= 16.0
+    s, _, _ = oracle.channel_scales(bf16_bits(K))
+    assert np.array_equal(s[:128], np.full(128, 2.0, np.float32))
+    assert np.array_equal(s[128:], np.full(128, 0.5, np.float32))
+
+
+def test_identical_channel_rms_gives_unit_scales():
+    sign = np.where(synth.uniform(7, 1, T * D).reshape(T, D) < 0.5, -1.0, 1.0) * 3.0
+    s, _, _ = oracle.channel_scales(bf16_bits(sign))
+    assert np.array_equal(s, np.ones(D, np.float32))
+
+
+def test_clamp_engages_at_bounds():
+    K = np.ones((T, D))
+    K[:, 3] = 2.0 ** 60      # a_3 = 2^30: far above the 2^14 clamp
+    K[:, 9] = 2.0 ** -60     # a_9 = 2^-30: far below 2^-14
+    s, shat, clamped = oracle.channel_scales(bf16_bits(K))
+    assert clamped == 2
+    assert s[3] == np.float32(2.0 ** 14) and s[9] == np.float32(2.0 ** -14)
+
+
+def test_zero_channel_and_rows():
+    k, v = random_page(3, "unit")
+    k = k.copy()
+    v = v.copy()
+    k[:, 17] = 0          # silent key channel
+    k[5, :] = 0           # silent key row
+    v[:, 40] = 0          # silent value channel
+    rec, clamped = oracle.quantize_page_head(k, v)
+    kc, vc, s, r, u = oracle.record_fields(rec)
+    assert s[17] == np.float32(2.0 ** -14) and clamped == 1
+    assert np.all(kc[:, 17] == 0) and r[5] == 0 and np.all(kc[5] == 0)
+    assert u[40] == 0 and np.all(vc[:, 40] == 0)
+
+
+@pytest.mark.parametrize("seed", range(4))
+@pytest.mark.parametrize("j", [-2, -1, 1, 3])
+def test_power_of_four_scaling(seed, j):
+    """Scaling a page by 4^j leaves s and the codes unchanged and scales r, u by 4^j."""
+    k, v = random_page(seed, "loguniform")
+    f = 4.0 ** j
+    k2 = synth.f32_to_bf16(synth.bf16_to_f32(k) * np.float32(f))
+    v2 = synth.f32_to_bf16(synth.bf16_to_f32(v) * np.float32(f))
+    a = oracle.record_fields(oracle.quantize_page_head(k, v)[0])
+    b = oracle.record_fields(oracle.quantize_page_head(k2, v2)[0])
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1]) and np.array_equal(a[2], b[2])
+    assert np.array_equal(a[3] * np.float32(f), b[3]) and np.array_equal(a[4] * np.float32(f), b[4])
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_negation_negates_codes(seed):
+    k, v = random_page(seed, "outliers")
+    a = oracle.record_fields(oracle.quantize_page_head(k, v)[0])
+    b = oracle.record_fields(oracle.quantize_page_head(k ^ 0x8000, v ^ 0x8000)[0])
+    assert np.array_equal(a[0], -b[0]) and np.array_equal(a[1], -b[1])
+    for i in (2, 3, 4):
+        assert np.array_equal(a[i], b[i])
+
+
+@pytest.mark.parametrize("seed,kind", PAGES)
+def test_reconstruction_error_bound(seed, kind):
+    """|k - s r kc| <= s r (1/2 + 127 * 2^-22); |v - u vc| <= u (1/2 + 127 * 2^-23)."""
+    k, v = random_page(seed, kind)
+    kc, vc, s, r, u = oracle.record_fields(oracle.quantize_page_head(k, v)[0])
+    K = synth.bf16_to_f32(k).astype(np.float64)
+    V = synth.bf16_to_f32(v).astype(np.float64)
+    sr = s.astype(np.float64)[None, :] * r.astype(np.float64)[:, None]
+    assert np.all(np.abs(K - sr * kc) <= sr * (0.5 + 127 * 2.0 ** -22))
+    uu = u.astype(np.float64)[None, :]
+    assert np.all(np.abs(V - uu * vc) <= uu * (0.5 + 127 * 2.0 ** -23))
+
+
+def test_given_scales_reproduce_codes():
+    """Codes from the given-scales path equal the full conversion's codes."""
+    k, v = random_page(11, "outliers")
+    rec, _ = oracle.quantize_page_head(k, v)
+    kc, vc, s, r, u = oracle.record_fields(rec)
+    rec2 = oracle.codes_given(k, v, s, r, u)
+    assert np.array_equal(rec, rec2)
+
+
+def test_pool_conversion_places_records():
+    w = synth.make_workload([200, 70], 64, H=2, seed=5)
+    src = w.int8_slots()
+    rec_pool = np.zeros(w.n_slots * w.H * oracle.REC_BYTES, np.uint8)
+    oracle.quantize_pages(w.H, w.k_pool, w.v_pool, src, src, rec_pool)
+    for slot in src:
+        for h in range(w.H):
+            one, _ = oracle.quantize_page_head(w.k_pool[slot, h], w.v_pool[slot, h])
+            at = (slot * w.H + h) * oracle.REC_BYTES
+            assert np.array_equal(rec_pool[at:at + oracle.REC_BYTES], one)
