@@ -1,0 +1,432 @@
+"""Benchmark: one hybrid decode step at 128K tokens (history GB/s and us/step).
+
+Workload: 1 request, 4 KV heads x 8 query rows, head size 256, 131,072-token
+history = 1,984 8-bit pages + 4,096 recent BF16 tokens, keys with 4 outlier
+channels per head at 20x std, values and q ~ N(0, 1), seed 2; the 8-bit pages
+are converted on the GPU before timing.  A step is one call of
+tpk_decode_hybrid_batched (both tiers, split over thread blocks, merged in the
+same launch).
+
+value  = algorithmic history bytes / device time per step, inputs resident in
+         HBM, L2 flushed (256 MB write) between timed steps.
+e2e    = the same metric through the same C-ABI call with the history in pinned
+         host memory: each step copies the step's 8-bit records, recent BF16
+         pages, q and page tables host->device, runs the call, and reads o and
+         lse back.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl {tpk,reference}]
+Under torchrun (N > 1) every rank runs an independent replica on its GPU.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode-attn history GB/s (% of HBM peak) and µs/step at 128K hybrid, 1 GB300"
+WORKLOAD = ("hybrid 128K: 1 request, 4 KV heads x 8 q rows, head_dim 256, 131072 tokens = "
+            "1984 8-bit pages + 4096 BF16 tokens, 4 outlier key channels at 20x std, seed 2")
+KERNEL_SOURCES = ["tiered_paged_kv_gb300/csrc/common.cuh", "tiered_paged_kv_gb300/csrc/decode_common.cuh",
+                  "tiered_paged_kv_gb300/csrc/decode_simt.cu", "tiered_paged_kv_gb300/csrc/decode_mma.cu",
+                  "tiered_paged_kv_gb300/csrc/api.cu"]
+FALLBACK_HBM_GBS = 6800.0
+
+
+def kernel_hash():
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        p = os.path.join(ROOT, f)
+        if os.path.exists(p):
+            h.update(open(p, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def hbm_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            return float(json.load(open(p))["hbm_gbs"]), "measured"
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def measured_traffic(impl_name):
+    """Per-launch DRAM bytes from the committed ncu summary, if it was taken on
+    the current kernel sources."""
+    p = os.path.join(ROOT, "profiles", "decode_hybrid_128k_traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        d = json.load(open(p))
+        e = d.get(impl_name)
+        if e and e.get("kernel_hash") == kernel_hash():
+            return float(e["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 7:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx.append(float(f[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_init():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+        return dist, dist.get_rank(), ws
+    return None, 0, 1
+
+
+def max_over_ranks(dist, x):
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def build_workload():
+    from tiered_paged_kv_gb300 import synth
+    return synth.hybrid_128k(seed=2)
+
+
+# --------------------------------------------------------------------- oracle
+def oracle_time(w, rec_host, n_threads, sample_heads=None):
+    """Time the oracle's hybrid step (as it stands) on host cores."""
+    import oracle
+    if sample_heads is not None:
+        w = head_slice(w, sample_heads, rec_host)
+        rec_host = w.meta["rec"]
+    t0 = time.perf_counter()
+    oracle.hybrid_workload(w, rec_host, n_threads=n_threads)
+    dt = time.perf_counter() - t0
+    return dt, w.history_bytes(), min(n_threads, w.B * w.H)
+
+
+def head_slice(w, heads, rec_host):
+    """The same history restricted to the first `heads` KV heads (a sample)."""
+    from tiered_paged_kv_gb300 import synth
+    H = w.H
+    rec = rec_host.reshape(w.n_slots, H, -1)[:, :heads].copy().reshape(-1)
+    w2 = synth.Workload(H=heads, G=w.G, d=w.d, seed=w.seed, n_tokens=w.n_tokens, n8=w.n8, n_ex=w.n_ex,
+                        pages=w.pages, n_slots=w.n_slots, q=w.q[:, :heads * w.G].copy(),
+                        k_pool=w.k_pool[:, :heads].copy(), v_pool=w.v_pool[:, :heads].copy())
+    w2.meta["rec"] = rec
+    return w2
+
+
+# ------------------------------------------------------------------ GPU arm
+def run_gpu(args, dist, rank, world):
+    import torch
+
+    import tiered_paged_kv_gb300 as tpk
+    from tiered_paged_kv_gb300 import build as tbuild
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    tbuild.build()
+    impl = {"simt": tpk.IMPL_SIMT, "tensor": tpk.IMPL_TENSOR, "default": tpk.IMPL_DEFAULT}[args.kernel]
+    w = build_workload()
+    H, G = w.H, w.G
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.Stream(dev)
+    shape = tpk.Shape(H, impl=impl, kv_slots=w.n_slots, rec_slots=w.n_slots)
+    with torch.cuda.stream(stream):
+        kp = torch.from_numpy(w.k_pool.view(np.int16)).to(dev)
+        vp = torch.from_numpy(w.v_pool.view(np.int16)).to(dev)
+        q = torch.from_numpy(w.q.view(np.int16)).to(dev)
+        rec = torch.zeros(w.n_slots * H * tpk.RECORD_BYTES, dtype=torch.uint8, device=dev)
+        slots = torch.from_numpy(w.int8_slots()).to(dev)
+        pt, off = w.exact_page_table()
+        pt8, off8 = w.int8_page_table()
+        pt_d = torch.from_numpy(pt).to(dev)
+        pt8_d = torch.from_numpy(pt8).to(dev)
+        o = torch.empty(1, H * G, 256, dtype=torch.float32, device=dev)
+        lse = torch.empty(1, H * G, dtype=torch.float32, device=dev)
+        nbytes = tpk.hybrid_workspace_bytes(shape, 1)
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        tpk.workspace_init(ws, nbytes, stream)
+        # fresh page conversion of every 8-bit page (timed separately)
+        q_ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        q_ev[0].record(stream)
+        tpk.kv_quantize_pages(shape, kp, vp, slots, slots, len(slots), rec, stream)
+        q_ev[1].record(stream)
+        flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    stream.synchronize()
+    quant_ms = q_ev[0].elapsed_time(q_ev[1])
+    st, flags = tpk.get_device_status(reset=True, stream=stream)
+    if st != 0:
+        raise RuntimeError(f"device status {st} flags {flags}")
+
+    def step():
+        tpk.decode_hybrid_batched(shape, 1, q, kp, vp, rec, pt_d, off, w.n_ex, pt8_d, off8, w.n8, o, lse, ws,
+                                  nbytes, stream)
+
+    hist_bytes = w.history_bytes()
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+        stream.synchronize()
+        barrier(dist)
+        torch.cuda.synchronize()
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        with ClockSampler(local) as clk:
+            for i in range(args.steps):
+                flush.fill_(float(i))          # evict the previous step's lines from L2
+                starts[i].record(stream)
+                step()
+                ends[i].record(stream)
+            stream.synchronize()
+        torch.cuda.synchronize()
+        barrier(dist)
+    times = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms_mean = sum(times) / len(times)
+    ms_max = max_over_ranks(dist, ms_mean)
+    st, flags = tpk.get_device_status(reset=True, stream=stream)
+    if st != 0:
+        raise RuntimeError(f"device status {st} flags {flags} after timing")
+
+    # ---- end to end from pinned host memory (packed history, identity page tables)
+    e2e = run_e2e(args, w, rec, shape, stream, dev, dist)
+
+    # ---- CPU oracle baseline (rank 0, N = 1)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        rec_host = rec.cpu().numpy()
+        n_thr = os.cpu_count() or 1
+        dt, nb, cores = oracle_time(w, rec_host, n_thr)
+        cpu = {"value": round(nb / dt / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+               "sample": f"the full 128K hybrid step (all 4 KV heads), once, {dt:.1f} s; "
+                         f"threads over (request, KV head)"}
+    peak, peak_kind = hbm_peak()
+    achieved = hist_bytes / (ms_mean * 1e-3) / 1e9
+    value = world * hist_bytes / (ms_max * 1e-3) / 1e9
+    traffic = measured_traffic(args.kernel)
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_max, 5), "us_per_step": round(ms_max * 1e3, 2),
+        "us_per_step_median": round(statistics.median(times) * 1e3, 2),
+        "us_per_step_p10_p90": [round(np.percentile(times, 10) * 1e3, 2), round(np.percentile(times, 90) * 1e3, 2)],
+        "hbm_frac": round(achieved / peak, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "history_bytes_per_step": hist_bytes, "kernel": args.kernel,
+                   "l2": "flushed between timed steps (256 MB write); inputs 295 MB also exceed L2",
+                   "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
+                   "page_conversion_us": round(quant_ms * 1e3, 1),
+                   "page_conversion_GBps": round((w.H * int(w.n8.sum()) * (65536 + 35072)) / (quant_ms * 1e-3) / 1e9, 1)},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)" if peak_kind == "measured"
+                     else "fallback 6.8 TB/s"},
+        "e2e": e2e,
+        "gpu_launches": args.steps,
+        "clocks": clk.summary(),
+        "cpu_baseline": cpu,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_e2e(args, w, rec_dev, shape, stream, dev, dist):
+    import torch
+
+    import tiered_paged_kv_gb300 as tpk
+
+    H, G = w.H, w.G
+    slots8 = w.int8_slots()
+    n8 = len(slots8)
+    rec_view = rec_dev.view(w.n_slots, H * tpk.RECORD_BYTES)
+    # packed host copies: the step's 8-bit records and recent BF16 pages, in page order
+    rec_h = torch.empty(n8, H * tpk.RECORD_BYTES, dtype=torch.uint8).pin_memory()
+    rec_h.copy_(rec_view[torch.from_numpy(slots8).to(dev)].cpu())
+    ex_slots = np.asarray(w.pages[0][w.n8[0]:])
+    ne = len(ex_slots)
+    k_h = torch.from_numpy(w.k_pool[ex_slots].view(np.int16)).pin_memory()
+    v_h = torch.from_numpy(w.v_pool[ex_slots].view(np.int16)).pin_memory()
+    q_h = torch.from_numpy(w.q.view(np.int16)).pin_memory()
+    pt_h = torch.arange(ne, dtype=torch.int32).pin_memory()
+    pt8_h = torch.arange(n8, dtype=torch.int32).pin_memory()
+    o_h = torch.empty(1, H * G, 256, dtype=torch.float32).pin_memory()
+    lse_h = torch.empty(1, H * G, dtype=torch.float32).pin_memory()
+    rec_d = torch.empty_like(rec_h, device=dev)
+    k_d = torch.empty_like(k_h, device=dev)
+    v_d = torch.empty_like(v_h, device=dev)
+    q_d = torch.empty_like(q_h, device=dev)
+    pt_d = torch.empty_like(pt_h, device=dev)
+    pt8_d = torch.empty_like(pt8_h, device=dev)
+    o_d = torch.empty_like(o_h, device=dev)
+    lse_d = torch.empty_like(lse_h, device=dev)
+    shape2 = tpk.Shape(H, impl=shape.impl, kv_slots=ne, rec_slots=n8)
+    nbytes = tpk.hybrid_workspace_bytes(shape2, 1)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    off = np.array([0, ne], np.int32)
+    off8 = np.array([0, n8], np.int32)
+    h2d = [(rec_d, rec_h), (k_d, k_h), (v_d, v_h), (q_d, q_h), (pt_d, pt_h), (pt8_d, pt8_h)]
+    h2d_bytes = sum(h.numel() * h.element_size() for _, h in h2d)
+    d2h_bytes = o_h.numel() * 4 + lse_h.numel() * 4
+
+    def step():
+        for d, h in h2d:
+            d.copy_(h, non_blocking=True)
+        tpk.decode_hybrid_batched(shape2, 1, q_d, k_d, v_d, rec_d, pt_d, off, w.n_ex, pt8_d, off8, w.n8, o_d, lse_d,
+                                  ws, nbytes, stream)
+        o_h.copy_(o_d, non_blocking=True)
+        lse_h.copy_(lse_d, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        tpk.workspace_init(ws, nbytes, stream)
+        for _ in range(max(1, args.warmup)):
+            step()
+        stream.synchronize()
+        barrier(dist)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        steps = max(3, args.steps // 2)
+        ev[0].record(stream)
+        for _ in range(steps):
+            step()
+        ev[1].record(stream)
+        stream.synchronize()
+        barrier(dist)
+    ms = ev[0].elapsed_time(ev[1]) / steps
+    ms = max_over_ranks(dist, ms)
+    world = dist.get_world_size() if dist is not None else 1
+    return {"value": round(world * w.history_bytes() / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+            "us_per_step": round(ms * 1e3, 1), "h2d_bytes_per_step": int(h2d_bytes),
+            "d2h_bytes_per_step": int(d2h_bytes), "steps": steps}
+
+
+# ------------------------------------------------------------- reference arm
+def run_reference(args, dist, rank, world):
+    """The CPU oracle as the reference arm: each step is a bounded sample of the
+    same workload (one KV head of the 128K hybrid step)."""
+    if rank != 0:
+        return
+    import oracle
+    from tiered_paged_kv_gb300 import synth
+
+    oracle.build()
+    synth.build()
+    w = build_workload()
+    rec = np.zeros(w.n_slots * w.H * oracle.REC_BYTES, np.uint8)
+    s = w.int8_slots()
+    oracle.quantize_pages(w.H, w.k_pool, w.v_pool, s, s, rec)
+    sw = head_slice(w, 1, rec)
+    n_thr = 1
+    for _ in range(args.warmup):
+        oracle.hybrid_workload(sw, sw.meta["rec"], n_threads=n_thr)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.hybrid_workload(sw, sw.meta["rec"], n_threads=n_thr)
+        times.append(time.perf_counter() - t0)
+    sec = sum(times) / len(times)
+    value = sw.history_bytes() / sec / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sec * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "sample": "one KV head of the 128K hybrid step per timed step"},
+            "cpu_baseline": {"kind": "oracle", "cores": n_thr, "value": round(value, 4), "unit": "GB/s",
+                             "sample": "one KV head (8 query rows) over the full 131072-token history per step"},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="tpk", choices=["tpk", "reference"])
+    ap.add_argument("--kernel", default="default", choices=["default", "simt", "tensor"])
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "tpk":
+        args.warmup = 3
+    dist, rank, world = dist_init()
+    try:
+        if args.impl == "reference":
+            run_reference(args, dist, rank, world)
+        else:
+            run_gpu(args, dist, rank, world)
+    finally:
+        if dist is not None:
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

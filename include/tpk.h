@@ -1,0 +1,201 @@
+/*
+ * tpk -- split-tier paged decode attention for GB300 (sm_103a).  C ABI.
+ *
+ * One decode step attends the G query rows of each KV head over a long paged
+ * history held in two tiers (pages by their titles: "ActiveKV", section "The
+ * idea"; "SYCL", sections "Attention that reads 8-bit history" and "A merge that
+ * joins the tiers"; "model quantization", section "An 8-bit page format shaped
+ * for its kernel"):
+ *   - a recent tier of BF16 pages, attended exactly;
+ *   - an older tier of 8-bit page records read directly, never expanded;
+ *   - per-tier partials (output o, log-sum-exp lse) folded by an exact FP32 merge.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * Ownership  The caller owns every buffer.  The library allocates no device
+ *            memory; the multi-request call takes a caller-provided workspace.
+ * Pointers   "dev" pointers are device memory of the current device; "host"
+ *            pointers are read on the host before the call returns.  Device
+ *            pointers must be 16-byte aligned.
+ * Streams    Every call is asynchronous on `stream` (a cudaStream_t; NULL is the
+ *            legacy default stream).
+ * Errors     Argument errors are detected on the host before any launch and
+ *            returned as a status; nothing is launched then.  Launch failures
+ *            map to TPK_ERR_CUDA.  Page-table entries outside the pool sizes
+ *            given in tpk_shape are skipped by the kernels (that page then
+ *            contributes nothing) and recorded in a device status word read by
+ *            tpk_get_device_status.  The library never aborts or traps.
+ *            tpk_last_error_string describes the last failure on this thread.
+ * Layouts    BF16 pools:  [slot][kv_heads][64][256] bfloat16, K and V separate.
+ *            8-bit pool:  record (slot, h) at byte (slot * kv_heads + h) * 35072.
+ *            q:           [rows = kv_heads * group][256] bfloat16 (per request);
+ *                         query row j belongs to KV head j / group.
+ *            o:           float32 [rows][256], normalised (sum of weights 1).
+ *            lse:         float32 [rows], natural log of sum exp(sm_scale q.k).
+ * Empty      An empty token or page range yields lse = -inf and o = 0, the valid
+ *            empty partial; a merge never reads the o of a -inf partial.
+ */
+#ifndef TPK_H
+#define TPK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* tpk_stream_t; /* identical to cudaStream_t */
+
+typedef enum {
+  TPK_OK = 0,
+  TPK_ERR_INVALID = 1,     /* bad argument (null pointer, bad range, misalignment, too small buffer) */
+  TPK_ERR_UNSUPPORTED = 2, /* shape outside what the kernels implement */
+  TPK_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed */
+  TPK_ERR_BOUNDS = 4,      /* a kernel met a page-table entry outside the pool */
+  TPK_ERR_NOMEM = 5,       /* a caller-provided buffer is smaller than required */
+  TPK_ERR_TIMEOUT = 6      /* reserved: a bounded device-side wait gave up */
+} tpk_status;
+
+/* Which dot-product engine the decode kernels use. */
+enum { TPK_IMPL_DEFAULT = 0, TPK_IMPL_SIMT = 1, TPK_IMPL_TENSOR = 2 };
+
+/* Bytes of one 8-bit page-head record:
+ *   int8 kc[64][256]   key codes, token-major          offset 0
+ *   int8 vc[64][256]   value codes, token-major        offset 16384
+ *   f32  ks_chan[256]  key channel scale s_c           offset 32768
+ *   f32  ks_tok[64]    key per-token factor r_t        offset 33792
+ *   f32  vs_chan[256]  value channel scale u_c         offset 34048
+ * Dequantised: k_tc = kc_tc * s_c * r_t and v_tc = vc_tc * u_c. */
+#define TPK_RECORD_BYTES 35072
+
+typedef struct {
+  int kv_heads;      /* H >= 1 */
+  int group;         /* G query rows per KV head; must be 8 */
+  int head_dim;      /* must be 256 */
+  int page_tokens;   /* must be 64 */
+  float sm_scale;    /* softmax scale; 0 selects 1/sqrt(head_dim) (the only value supported) */
+  int impl;          /* TPK_IMPL_* */
+  int64_t kv_slots;  /* slots in the BF16 pools (bounds for page_table entries); 0 = unchecked */
+  int64_t rec_slots; /* slots in the 8-bit pool (bounds for page_table8 entries); 0 = unchecked */
+} tpk_shape;
+
+const char* tpk_version(void);
+const char* tpk_last_error_string(void);
+
+/*
+ * Page conversion ("model quantization", section "An 8-bit page format shaped for
+ * its kernel").  For each of n_pages pages and each KV head h, read the BF16 page
+ * (src_slots[i], h) of k_pool / v_pool and write record (dst_slots[i], h) of
+ * rec_pool:
+ *   key channel scale  s_c = sqrt(RMS_t k_tc), normalised by the geometric mean so
+ *                      prod_c s_c = 1, clamped to [2^-14, 2^14], rounded to float32
+ *                      with compensated rounding (the running log-error of the
+ *                      product is kept nearest zero);
+ *   key token factor   r_t = max_c |k_tc / s_c| / 127;
+ *   value scale        u_c = max_t |v_tc| / 127;
+ *   codes              kc = rint((k / s_c) / r_t), vc = rint(v / u_c), clamped to
+ *                      +-127, with IEEE float32 divisions and half-to-even rint;
+ *                      a zero factor gives zero codes.
+ * src_slots, dst_slots: dev int32[n_pages].  k_pool, v_pool: dev BF16 pools.
+ * rec_pool: dev, 16-byte aligned.  Pages may be converted in any order; distinct
+ * dst_slots must not alias.  n_pages == 0 is a no-op.
+ */
+tpk_status tpk_kv_quantize_pages(const tpk_shape* shape, const void* k_pool, const void* v_pool,
+                                 const int32_t* src_slots, const int32_t* dst_slots, int n_pages,
+                                 void* rec_pool, tpk_stream_t stream);
+
+/*
+ * As tpk_kv_quantize_pages, but with all three scale arrays given (dev float32
+ * ks_chan[n_pages][H][256], ks_tok[n_pages][H][64], vs_chan[n_pages][H][256]);
+ * only the codes are computed, and the given scales are copied into the records.
+ * Used to check the codes bit for bit against a reference that fixed the scales.
+ */
+tpk_status tpk_kv_quantize_pages_given_scales(const tpk_shape* shape, const void* k_pool, const void* v_pool,
+                                              const int32_t* src_slots, const int32_t* dst_slots, int n_pages,
+                                              const float* ks_chan, const float* ks_tok, const float* vs_chan,
+                                              void* rec_pool, tpk_stream_t stream);
+
+/*
+ * Exact-tier partial attention ("SYCL", section "A merge that joins the tiers":
+ * paged decode with a log-sum-exp output).  For every KV head, the G query rows
+ * attend BF16 tokens [tok_begin, tok_end) of one paged history whose token t lives
+ * in slot page_table[t / 64], row t % 64.  The range is cut into num_splits
+ * consecutive pieces on page boundaries (1 <= num_splits <= 4096); piece s writes
+ * o_part[s] (dev float32 [num_splits][H*G][256]) and lse_part[s] (dev float32
+ * [num_splits][H*G]).  A piece with no tokens writes the empty partial.
+ * q: dev bf16 [H*G][256].  page_table: dev int32[ceil(tok_end / 64)].
+ */
+tpk_status tpk_decode_attn_exact(const tpk_shape* shape, const void* q, const void* k_pool, const void* v_pool,
+                                 const int32_t* page_table, int tok_begin, int tok_end, int num_splits,
+                                 float* o_part, float* lse_part, tpk_stream_t stream);
+
+/*
+ * 8-bit-tier partial attention ("SYCL", section "Attention that reads 8-bit
+ * history").  As tpk_decode_attn_exact over pages [page_begin, page_end) of the
+ * record pool, page p in slot page_table8[p] (dev int32[page_end]).  Keys enter
+ * as q'_c = q_c * s_c folded once per page and score_t = r_t * sum_c q'_c kc_tc;
+ * values accumulate on raw codes and are rescaled by u_c per page.
+ */
+tpk_status tpk_decode_attn_int8(const tpk_shape* shape, const void* q, const void* rec_pool,
+                                const int32_t* page_table8, int page_begin, int page_end, int num_splits,
+                                float* o_part, float* lse_part, tpk_stream_t stream);
+
+/*
+ * Log-sum-exp merge ("SYCL", section "A merge that joins the tiers"): fold
+ * n_parts partials (dev o_parts [n_parts][rows][head_dim], lse_parts
+ * [n_parts][rows]) into the accumulator (dev o_acc [rows][head_dim], lse_acc
+ * [rows], read and written):
+ *   lse = ln(exp(lse_acc) + sum_i exp(lse_i)),
+ *   o   = exp(lse_acc - lse) o_acc + sum_i exp(lse_i - lse) o_i.
+ * Partials with lse = -inf contribute nothing and their o is not read; a fresh
+ * accumulator is (o = 0, lse = -inf).  The fold order is fixed (accumulator, then
+ * parts in index order), so results are bit-reproducible.  head_dim must be 256.
+ */
+tpk_status tpk_merge_lse(int n_parts, int rows, int head_dim, const float* o_parts, const float* lse_parts,
+                         float* o_acc, float* lse_acc, tpk_stream_t stream);
+
+/*
+ * Workspace bytes tpk_decode_hybrid_batched needs for n_req requests (an upper
+ * bound independent of the lengths).  The workspace must be zeroed once before
+ * first use (tpk_workspace_init); the kernels leave it zeroed again.
+ */
+size_t tpk_hybrid_workspace_bytes(const tpk_shape* shape, int n_req);
+tpk_status tpk_workspace_init(void* ws, size_t ws_bytes, tpk_stream_t stream);
+
+/*
+ * Multi-request hybrid decode in one launch ("SYCL", section "Exact tricks and a
+ * two-owner decoder": requests in one launch, each with its own page metadata and
+ * its own merge accumulator).  For each request b and KV head h: the exact partial
+ * over its BF16 tokens [0, n_exact_tokens[b]) and the 8-bit partial over its pages
+ * [0, n_int8_pages[b]), split across thread blocks and folded, in a fixed order,
+ * into o[b] (dev float32 [n_req][H*G][256]) and lse[b] (dev float32 [n_req][H*G]),
+ * which are overwritten.
+ *   q           dev bf16 [n_req][H*G][256]
+ *   page_table  dev int32, flat; request b's exact-tier slots start at
+ *               req_page_off[b] (host int32 [n_req + 1])
+ *   page_table8 dev int32, flat; request b's 8-bit slots start at req_page_off8[b]
+ *               (host int32 [n_req + 1])
+ *   n_exact_tokens, n_int8_pages: host int32 [n_req]
+ * The host arrays are read during the call (the split plan is built on the host
+ * and passed by value to the kernel, so the call can be captured in a CUDA graph).
+ * ws: dev workspace of at least tpk_hybrid_workspace_bytes(shape, n_req) bytes,
+ * zeroed before first use.  Calls sharing a workspace must not overlap on the GPU.
+ */
+tpk_status tpk_decode_hybrid_batched(const tpk_shape* shape, int n_req, const void* q, const void* k_pool,
+                                     const void* v_pool, const void* rec_pool, const int32_t* page_table,
+                                     const int32_t* req_page_off, const int32_t* n_exact_tokens,
+                                     const int32_t* page_table8, const int32_t* req_page_off8,
+                                     const int32_t* n_int8_pages, float* o, float* lse, void* ws, size_t ws_bytes,
+                                     tpk_stream_t stream);
+
+/*
+ * Device status word: bit 0 = a page-table entry outside the pool was skipped.
+ * Synchronises `stream`, stores the word in *flags and, if reset != 0, clears it.
+ */
+tpk_status tpk_get_device_status(int* flags, int reset, tpk_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TPK_H */

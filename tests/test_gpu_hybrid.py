@@ -1,0 +1,82 @@
+"""The one-launch multi-request hybrid decode against the oracle: the tiny
+hybrid, ragged multi-request batches, the all-exact 32K history, the 128K
+hybrid and the 16-request batch at full size, bit-for-bit determinism, and the
+hybrid error against unquantised attention reported beside the oracle's."""
+import numpy as np
+import pytest
+
+import oracle
+import tiered_paged_kv_gb300 as tpk
+from tiered_paged_kv_gb300 import synth
+from tpk_testutil import DevWorkload, assert_close, oracle_records
+
+pytestmark = pytest.mark.gpu
+IMPLS = [tpk.IMPL_SIMT, tpk.IMPL_TENSOR]
+NT = 16  # oracle threads
+
+
+def check_hybrid(w, impl, gpu_records=False, what=""):
+    d = DevWorkload(w, impl)
+    rec = d.quantize_gpu() if gpu_records else oracle_records(w)
+    if not gpu_records:
+        d.load_records(rec)
+    o, lse = d.hybrid()
+    oo, ol = oracle.hybrid_workload(w, rec, n_threads=NT)
+    err = assert_close(o, lse, oo, ol, what)
+    return d, o, lse, oo, ol, rec, err
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+def test_tiny_hybrid(impl):
+    check_hybrid(synth.tiny_hybrid(seed=0), impl, what="tiny")
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+@pytest.mark.parametrize("gpu_records", [False, True])
+def test_ragged_batch(impl, gpu_records):
+    lengths = [1, 63, 64, 65, 700, 2 * 64 + 7, 2000, 0, 129]
+    w = synth.make_workload(lengths, 100, H=2, seed=21, key_sigma="outliers")
+    check_hybrid(w, impl, gpu_records, "ragged")
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+def test_only_one_tier(impl):
+    check_hybrid(synth.make_workload([5000, 77], None, H=2, seed=22), impl, what="all exact")
+    w = synth.make_workload([64 * 30, 64 * 3], 0, H=2, seed=23)
+    assert (w.n_ex == 0).all()
+    check_hybrid(w, impl, what="all 8-bit")
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+def test_deterministic(impl):
+    w = synth.make_workload([20000, 3000, 9000], 1024, H=4, seed=24, key_sigma="outliers")
+    d = DevWorkload(w, impl)
+    d.load_records(oracle_records(w))
+    a = d.hybrid()
+    b = d.hybrid()
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+def test_full_exact_32k(impl):
+    w = synth.exact_32k(seed=1)
+    check_hybrid(w, impl, what="exact 32K")
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+def test_full_hybrid_128k(impl):
+    w = synth.hybrid_128k(seed=2)
+    d, o, lse, oo, ol, rec, err = check_hybrid(w, impl, gpu_records=True, what="hybrid 128K")
+    # the hybrid error against unquantised attention, GPU beside oracle
+    of, lf = oracle.full_precision_workload(w, n_threads=NT)
+    e_gpu = np.abs(o - of).max()
+    e_orc = np.abs(oo - of).max()
+    print(f"hybrid 128K: worst merged error vs unquantised: gpu {e_gpu:.4g}, oracle {e_orc:.4g} "
+          f"(max|o| {np.abs(of).max():.4g}); parity {err}")
+    assert abs(e_gpu - e_orc) <= 1e-3 * np.abs(oo).max()
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+def test_full_batched_16(impl):
+    w = synth.batched_hybrid(seed=3)
+    check_hybrid(w, impl, gpu_records=True, what="batched 16")

@@ -1,0 +1,102 @@
+"""GPU page conversion against the oracle ("model quantization", section "An
+8-bit page format shaped for its kernel"): codes bit-exact given the oracle's
+scales, the GPU's own scales within 1 ulp of the oracle's, and the format's
+invariants on the GPU's own output."""
+import numpy as np
+import pytest
+
+import oracle
+import tiered_paged_kv_gb300 as tpk
+from tiered_paged_kv_gb300 import synth
+from tpk_testutil import DevWorkload, dev_f32, dev_i32, oracle_records
+
+pytestmark = pytest.mark.gpu
+
+WORKLOADS = {
+    "tiny_loguniform": lambda: synth.tiny_hybrid(seed=0),
+    "outliers": lambda: synth.make_workload([64 * 40 + 17], 17, H=4, seed=2, key_sigma="outliers"),
+    "unit": lambda: synth.make_workload([64 * 24 + 5, 64 * 9], 5, H=2, seed=7),
+}
+
+
+def ulp_distance(a, b):
+    ai = a.view(np.int32).astype(np.int64)
+    bi = b.view(np.int32).astype(np.int64)
+    return np.abs(ai - bi)
+
+
+@pytest.mark.parametrize("name", sorted(WORKLOADS))
+def test_codes_bit_exact_given_oracle_scales(name):
+    w = WORKLOADS[name]()
+    ref = oracle_records(w)
+    slots = w.int8_slots()
+    H = w.H
+    recs = ref.reshape(w.n_slots, H, oracle.REC_BYTES)[slots]  # [n][H][rec]
+    ks = recs[:, :, oracle.OFF_KS_CHAN:oracle.OFF_KS_TOK].copy().view(np.float32)
+    kt = recs[:, :, oracle.OFF_KS_TOK:oracle.OFF_VS_CHAN].copy().view(np.float32)
+    vs = recs[:, :, oracle.OFF_VS_CHAN:].copy().view(np.float32)
+    d = DevWorkload(w)
+    s = dev_i32(slots)
+    tpk.kv_quantize_pages_given_scales(d.shape, d.k, d.v, s, s, len(slots), dev_f32(ks), dev_f32(kt), dev_f32(vs),
+                                       d.rec)
+    got = d.rec.cpu().numpy().reshape(w.n_slots, H, oracle.REC_BYTES)[slots]
+    assert np.array_equal(got, recs)
+
+
+@pytest.mark.parametrize("name", sorted(WORKLOADS))
+def test_own_scales_within_one_ulp_and_invariants(name):
+    w = WORKLOADS[name]()
+    ref = oracle_records(w).reshape(w.n_slots, w.H, oracle.REC_BYTES)
+    d = DevWorkload(w)
+    got = d.quantize_gpu().reshape(w.n_slots, w.H, oracle.REC_BYTES)
+    n_diff = 0
+    for slot in w.int8_slots():
+        for h in range(w.H):
+            kc, vc, s, r, u = oracle.record_fields(got[slot, h])
+            _, _, s_o, r_o, u_o = oracle.record_fields(ref[slot, h])
+            assert ulp_distance(s, s_o).max() <= 1
+            n_diff += int((s != s_o).sum())
+            assert np.array_equal(u, u_o)          # u depends on V alone: same float32 ops
+            assert kc.min() >= -127 and vc.min() >= -127
+            assert np.all(np.abs(kc).max(axis=1)[r > 0] == 127)
+            assert np.all(np.abs(vc).max(axis=0)[u > 0] == 127)
+            clamped = (s == np.float32(2.0 ** -14)) | (s == np.float32(2.0 ** 14))
+            if not clamped.any():
+                assert abs(np.exp(np.log(s.astype(np.float64)).sum()) - 1.0) <= 1e-6
+            # the GPU's codes follow from its own scales exactly
+            k = w.k_pool[slot, h]
+            v = w.v_pool[slot, h]
+            again = oracle.codes_given(k, v, s, r, u)
+            assert np.array_equal(again, got[slot, h])
+    print(f"{name}: {n_diff} channel scales differ from the oracle by 1 ulp")
+
+
+def test_zero_rows_channels_and_clamp():
+    w = synth.make_workload([128], 0, H=1, seed=3)
+    for slot in w.int8_slots():
+        k = w.k_pool[slot, 0]
+        k[:, 5] = 0                                   # silent channel -> clamped 2^-14
+        k[9, :] = 0                                   # silent row -> r = 0
+        k[:, 200] = synth.f32_to_bf16(np.full(64, 2.0 ** 60, np.float32))  # far above the clamp
+        w.v_pool[slot, 0][:, 7] = 0
+    ref = oracle_records(w).reshape(w.n_slots, 1, oracle.REC_BYTES)
+    d = DevWorkload(w)
+    got = d.quantize_gpu().reshape(w.n_slots, 1, oracle.REC_BYTES)
+    for slot in w.int8_slots():
+        kc, vc, s, r, u = oracle.record_fields(got[slot, 0])
+        _, _, s_o, r_o, u_o = oracle.record_fields(ref[slot, 0])
+        assert s[5] == np.float32(2.0 ** -14) and s[200] == np.float32(2.0 ** 14)
+        assert np.all(kc[:, 5] == 0) and r[9] == 0 and np.all(kc[9] == 0)
+        assert u[7] == 0 and np.all(vc[:, 7] == 0)
+        assert ulp_distance(s, s_o).max() <= 1
+
+
+def test_bad_slot_is_skipped_and_reported():
+    w = synth.make_workload([128], 0, H=1, seed=4)
+    d = DevWorkload(w)
+    tpk.get_device_status(reset=True)
+    src = dev_i32(np.array([w.n_slots + 5], np.int32))
+    tpk.kv_quantize_pages(d.shape, d.k, d.v, src, src, 1, d.rec)
+    st, flags = tpk.get_device_status(reset=True)
+    assert st == 4 and flags & 1
+    assert int(d.rec.sum().item()) == 0

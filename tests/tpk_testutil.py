@@ -1,0 +1,120 @@
+"""Helpers shared by the GPU parity tests: move synthetic workloads to the
+device, call the library through its C ABI, and compare with the oracle."""
+import numpy as np
+
+import oracle
+import tiered_paged_kv_gb300 as tpk
+from tiered_paged_kv_gb300 import synth
+
+# Parity tolerances.  Outputs: max |o_gpu - o_oracle| <= O_TOL * max |o_oracle|
+# (the bar the method is held to against the oracle on the same codes).  lse:
+# absolute, natural-log units; a shift d of lse scales a partial's merge weight
+# by exp(d), so 1e-3 matches the relative bar on o.
+O_TOL = 1e-3
+LSE_TOL = 1e-3
+
+
+def torch():
+    import torch as t
+    return t
+
+
+def dev_u16(a):
+    t = torch()
+    return t.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda()
+
+
+def dev_i32(a):
+    t = torch()
+    a = np.ascontiguousarray(a, np.int32)
+    if a.size == 0:
+        a = np.zeros(1, np.int32)
+    return t.from_numpy(a).cuda()
+
+
+def dev_u8(a):
+    t = torch()
+    return t.from_numpy(np.ascontiguousarray(a, np.uint8)).cuda()
+
+
+def dev_f32(a):
+    t = torch()
+    return t.from_numpy(np.ascontiguousarray(a, np.float32)).cuda()
+
+
+class DevWorkload:
+    """A synth.Workload resident on the GPU."""
+
+    def __init__(self, w, impl=tpk.IMPL_DEFAULT):
+        t = torch()
+        self.w = w
+        self.shape = tpk.Shape(w.H, impl=impl, kv_slots=w.n_slots, rec_slots=w.n_slots)
+        self.k = dev_u16(w.k_pool)
+        self.v = dev_u16(w.v_pool)
+        self.q = dev_u16(w.q)
+        self.rec = t.zeros(w.n_slots * w.H * tpk.RECORD_BYTES, dtype=t.uint8, device="cuda")
+        pt, self.off = w.exact_page_table()
+        pt8, self.off8 = w.int8_page_table()
+        self.pt = dev_i32(pt)
+        self.pt8 = dev_i32(pt8)
+
+    def quantize_gpu(self):
+        slots = dev_i32(self.w.int8_slots())
+        n = len(self.w.int8_slots())
+        tpk.kv_quantize_pages(self.shape, self.k, self.v, slots, slots, n, self.rec)
+        return self.rec.cpu().numpy()
+
+    def load_records(self, rec_host):
+        self.rec.copy_(torch().from_numpy(np.ascontiguousarray(rec_host, np.uint8)))
+
+    def hybrid(self):
+        t = torch()
+        w = self.w
+        o = t.empty(w.B, w.H * w.G, 256, dtype=t.float32, device="cuda")
+        lse = t.empty(w.B, w.H * w.G, dtype=t.float32, device="cuda")
+        nbytes = tpk.hybrid_workspace_bytes(self.shape, w.B)
+        ws = t.empty(nbytes, dtype=t.uint8, device="cuda")
+        tpk.workspace_init(ws, nbytes)
+        tpk.decode_hybrid_batched(self.shape, w.B, self.q, self.k, self.v, self.rec, self.pt, self.off, w.n_ex,
+                                  self.pt8, self.off8, w.n8, o, lse, ws, nbytes)
+        t.cuda.synchronize()
+        return o.cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64)
+
+
+def oracle_records(w):
+    rec = np.zeros(w.n_slots * w.H * oracle.REC_BYTES, np.uint8)
+    s = w.int8_slots()
+    oracle.quantize_pages(w.H, w.k_pool, w.v_pool, s, s, rec)
+    return rec
+
+
+def assert_close(o, lse, oo, ol, what=""):
+    scale = max(np.abs(oo).max(), 1e-30)
+    err = np.abs(o - oo).max() / scale
+    fin = np.isfinite(ol)
+    assert np.array_equal(np.isfinite(lse), fin), f"{what}: -inf pattern differs"
+    assert np.all(lse[~fin] == ol[~fin]), f"{what}: empty rows differ"
+    lerr = np.abs(lse[fin] - ol[fin]).max() if fin.any() else 0.0
+    assert err <= O_TOL, f"{what}: max|do|/max|o| = {err:.3e} > {O_TOL}"
+    assert lerr <= LSE_TOL, f"{what}: max|dlse| = {lerr:.3e} > {LSE_TOL}"
+    return err, lerr
+
+
+def split_ranges_exact(tok_begin, tok_end, S):
+    """Token pieces of tpk_decode_attn_exact: page-aligned cuts of the range."""
+    pg0 = tok_begin // 64
+    pg1 = (tok_end + 63) // 64
+    P = pg1 - pg0
+    out = []
+    for s in range(S):
+        pa = pg0 + (P * s) // S
+        pb = pg0 + (P * (s + 1)) // S
+        b = max(tok_begin, pa * 64)
+        e = min(tok_end, pb * 64)
+        out.append((b, max(b, e)))
+    return out
+
+
+def split_ranges_int8(page_begin, page_end, S):
+    P = page_end - page_begin
+    return [(page_begin + (P * s) // S, page_begin + (P * (s + 1)) // S) for s in range(S)]

@@ -1,0 +1,163 @@
+"""tiered_paged_kv_gb300 -- split-tier paged decode attention on GB300 (sm_103a).
+
+A thin ctypes binding over the C ABI in ``include/tpk.h`` (``libtpk.so``).  Every
+function here only marshals arguments: device buffers are passed as raw
+pointers (torch tensors are accepted and their ``data_ptr()`` is used), streams
+as ``torch.cuda.Stream`` or raw handles.  All computation runs in the library's
+CUDA kernels; there is no CPU fallback, and loading fails loudly when the
+library has not been built.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build_mod
+
+__all__ = [
+    "Shape", "TpkError", "lib", "RECORD_BYTES", "IMPL_DEFAULT", "IMPL_SIMT", "IMPL_TENSOR",
+    "kv_quantize_pages", "kv_quantize_pages_given_scales", "decode_attn_exact", "decode_attn_int8",
+    "merge_lse", "hybrid_workspace_bytes", "workspace_init", "decode_hybrid_batched", "get_device_status",
+]
+
+RECORD_BYTES = 35072
+IMPL_DEFAULT, IMPL_SIMT, IMPL_TENSOR = 0, 1, 2
+STATUS_NAMES = {0: "TPK_OK", 1: "TPK_ERR_INVALID", 2: "TPK_ERR_UNSUPPORTED", 3: "TPK_ERR_CUDA",
+                4: "TPK_ERR_BOUNDS", 5: "TPK_ERR_NOMEM", 6: "TPK_ERR_TIMEOUT"}
+
+
+class Shape(ctypes.Structure):
+    _fields_ = [("kv_heads", ctypes.c_int), ("group", ctypes.c_int), ("head_dim", ctypes.c_int),
+                ("page_tokens", ctypes.c_int), ("sm_scale", ctypes.c_float), ("impl", ctypes.c_int),
+                ("kv_slots", ctypes.c_int64), ("rec_slots", ctypes.c_int64)]
+
+    def __init__(self, kv_heads, group=8, head_dim=256, page_tokens=64, sm_scale=0.0, impl=IMPL_DEFAULT,
+                 kv_slots=0, rec_slots=0):
+        super().__init__(kv_heads, group, head_dim, page_tokens, sm_scale, impl, kv_slots, rec_slots)
+
+
+class TpkError(RuntimeError):
+    def __init__(self, status, message):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+_lib = None
+
+
+def lib():
+    """Load libtpk.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        path = _build_mod.LIB
+        if not os.path.exists(path):
+            raise RuntimeError(f"libtpk.so not built ({path}); run tiered_paged_kv_gb300.build.build()")
+        L = ctypes.CDLL(path)
+        vp, i32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+        sp = ctypes.POINTER(Shape)
+        L.tpk_version.restype = ctypes.c_char_p
+        L.tpk_last_error_string.restype = ctypes.c_char_p
+        L.tpk_kv_quantize_pages.argtypes = [sp, vp, vp, vp, vp, i32, vp, vp]
+        L.tpk_kv_quantize_pages_given_scales.argtypes = [sp, vp, vp, vp, vp, i32, vp, vp, vp, vp, vp]
+        L.tpk_decode_attn_exact.argtypes = [sp, vp, vp, vp, vp, i32, i32, i32, vp, vp, vp]
+        L.tpk_decode_attn_int8.argtypes = [sp, vp, vp, vp, i32, i32, i32, vp, vp, vp]
+        L.tpk_merge_lse.argtypes = [i32, i32, i32, vp, vp, vp, vp, vp]
+        L.tpk_hybrid_workspace_bytes.argtypes = [sp, i32]
+        L.tpk_hybrid_workspace_bytes.restype = sz
+        L.tpk_workspace_init.argtypes = [vp, sz, vp]
+        L.tpk_decode_hybrid_batched.argtypes = [sp, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+        L.tpk_get_device_status.argtypes = [ctypes.POINTER(ctypes.c_int), i32, vp]
+        for name in ("tpk_kv_quantize_pages", "tpk_kv_quantize_pages_given_scales", "tpk_decode_attn_exact",
+                     "tpk_decode_attn_int8", "tpk_merge_lse", "tpk_workspace_init", "tpk_decode_hybrid_batched",
+                     "tpk_get_device_status"):
+            getattr(L, name).restype = i32
+        _lib = L
+    return _lib
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if hasattr(x, "data_ptr"):
+        return x.data_ptr()
+    raise TypeError(f"cannot take a device pointer from {type(x)}")
+
+
+def _stream(s):
+    if s is None:
+        return None
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream
+
+
+def _host_i32(a):
+    arr = np.ascontiguousarray(np.asarray(a), dtype=np.int32)
+    return arr, arr.ctypes.data_as(ctypes.c_void_p)
+
+
+def _check(status):
+    if status != 0:
+        raise TpkError(status, lib().tpk_last_error_string().decode())
+
+
+def kv_quantize_pages(shape, k_pool, v_pool, src_slots, dst_slots, n_pages, rec_pool, stream=None):
+    _check(lib().tpk_kv_quantize_pages(ctypes.byref(shape), _ptr(k_pool), _ptr(v_pool), _ptr(src_slots),
+                                       _ptr(dst_slots), int(n_pages), _ptr(rec_pool), _stream(stream)))
+
+
+def kv_quantize_pages_given_scales(shape, k_pool, v_pool, src_slots, dst_slots, n_pages, ks_chan, ks_tok,
+                                   vs_chan, rec_pool, stream=None):
+    _check(lib().tpk_kv_quantize_pages_given_scales(ctypes.byref(shape), _ptr(k_pool), _ptr(v_pool),
+                                                    _ptr(src_slots), _ptr(dst_slots), int(n_pages), _ptr(ks_chan),
+                                                    _ptr(ks_tok), _ptr(vs_chan), _ptr(rec_pool), _stream(stream)))
+
+
+def decode_attn_exact(shape, q, k_pool, v_pool, page_table, tok_begin, tok_end, num_splits, o_part, lse_part,
+                      stream=None):
+    _check(lib().tpk_decode_attn_exact(ctypes.byref(shape), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(page_table),
+                                       int(tok_begin), int(tok_end), int(num_splits), _ptr(o_part), _ptr(lse_part),
+                                       _stream(stream)))
+
+
+def decode_attn_int8(shape, q, rec_pool, page_table8, page_begin, page_end, num_splits, o_part, lse_part,
+                     stream=None):
+    _check(lib().tpk_decode_attn_int8(ctypes.byref(shape), _ptr(q), _ptr(rec_pool), _ptr(page_table8),
+                                      int(page_begin), int(page_end), int(num_splits), _ptr(o_part), _ptr(lse_part),
+                                      _stream(stream)))
+
+
+def merge_lse(n_parts, rows, head_dim, o_parts, lse_parts, o_acc, lse_acc, stream=None):
+    _check(lib().tpk_merge_lse(int(n_parts), int(rows), int(head_dim), _ptr(o_parts), _ptr(lse_parts), _ptr(o_acc),
+                               _ptr(lse_acc), _stream(stream)))
+
+
+def hybrid_workspace_bytes(shape, n_req):
+    return int(lib().tpk_hybrid_workspace_bytes(ctypes.byref(shape), int(n_req)))
+
+
+def workspace_init(ws, ws_bytes, stream=None):
+    _check(lib().tpk_workspace_init(_ptr(ws), int(ws_bytes), _stream(stream)))
+
+
+def decode_hybrid_batched(shape, n_req, q, k_pool, v_pool, rec_pool, page_table, req_page_off, n_exact_tokens,
+                          page_table8, req_page_off8, n_int8_pages, o, lse, ws, ws_bytes, stream=None):
+    """req_page_off, n_exact_tokens, req_page_off8, n_int8_pages are host arrays."""
+    a, pa = _host_i32(req_page_off)
+    b, pb = _host_i32(n_exact_tokens)
+    c, pc = _host_i32(req_page_off8)
+    d, pd = _host_i32(n_int8_pages)
+    _check(lib().tpk_decode_hybrid_batched(ctypes.byref(shape), int(n_req), _ptr(q), _ptr(k_pool), _ptr(v_pool),
+                                           _ptr(rec_pool), _ptr(page_table), pa, pb, _ptr(page_table8), pc, pd,
+                                           _ptr(o), _ptr(lse), _ptr(ws), int(ws_bytes), _stream(stream)))
+
+
+def get_device_status(reset=True, stream=None):
+    """Returns (status, flags); status is a tpk_status, not raised."""
+    flags = ctypes.c_int(0)
+    st = lib().tpk_get_device_status(ctypes.byref(flags), 1 if reset else 0, _stream(stream))
+    return st, flags.value

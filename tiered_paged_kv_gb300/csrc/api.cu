@@ -1,0 +1,343 @@
+// Host side of the tpk C ABI: argument validation, the split planner and the
+// kernel launches.  Every entry point validates before launching and reports
+// failures as a tpk_status plus a thread-local message.
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "common.cuh"
+#include "tpk.h"
+
+namespace tpk {
+cudaError_t launch_decode_simt(const DecodeParams& p, cudaStream_t stream);
+int decode_simt_blocks_per_sm();
+cudaError_t launch_merge(int n_parts, int rows, const float* o_parts, const float* lse_parts, float* o_acc,
+                         float* lse_acc, cudaStream_t stream);
+cudaError_t launch_quantize(const QuantParams& p, int n_pages, cudaStream_t stream);
+}  // namespace tpk
+
+using namespace tpk;
+
+__device__ int g_tpk_status;
+
+namespace {
+
+constexpr int kMaxUnits = 4096;       // partial slots in the hybrid workspace
+constexpr int kMaxSplits = 4096;      // primitive calls
+constexpr int kMaxHeads = 1024;
+
+thread_local std::string g_err;
+
+tpk_status fail(tpk_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return s;
+}
+
+tpk_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(TPK_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+tpk_status check_shape(const tpk_shape* s) {
+  if (!s) return fail(TPK_ERR_INVALID, "shape is null");
+  if (s->kv_heads < 1 || s->kv_heads > kMaxHeads) return fail(TPK_ERR_INVALID, "kv_heads %d out of [1, %d]", s->kv_heads, kMaxHeads);
+  if (s->group != kGroup) return fail(TPK_ERR_UNSUPPORTED, "group %d (only 8 supported)", s->group);
+  if (s->head_dim != kHeadDim) return fail(TPK_ERR_UNSUPPORTED, "head_dim %d (only 256 supported)", s->head_dim);
+  if (s->page_tokens != kPageTokens) return fail(TPK_ERR_UNSUPPORTED, "page_tokens %d (only 64 supported)", s->page_tokens);
+  if (!(s->sm_scale == 0.f || s->sm_scale == 0.0625f))
+    return fail(TPK_ERR_UNSUPPORTED, "sm_scale %g (only 1/sqrt(256) supported)", (double)s->sm_scale);
+  if (s->impl < TPK_IMPL_DEFAULT || s->impl > TPK_IMPL_TENSOR) return fail(TPK_ERR_INVALID, "impl %d", s->impl);
+  if (s->kv_slots < 0 || s->rec_slots < 0) return fail(TPK_ERR_INVALID, "negative pool size");
+  return TPK_OK;
+}
+
+int* status_ptr() {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  static int* ptrs[64] = {nullptr};
+  if (dev < 0 || dev >= 64) return nullptr;
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_tpk_status) != cudaSuccess) return nullptr;
+    ptrs[dev] = static_cast<int*>(p);
+  }
+  return ptrs[dev];
+}
+
+int num_sms() {
+  int dev = 0, n = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n > 0 ? n : 1;
+}
+
+void fill_common(DecodeParams& p, const tpk_shape* s, const void* q) {
+  std::memset(&p, 0, sizeof(p));
+  p.q = static_cast<const uint16_t*>(q);
+  p.kv_slots = s->kv_slots;
+  p.rec_slots = s->rec_slots;
+  p.qscale = 0.0625f * kLog2e;
+  p.H = s->kv_heads;
+}
+
+tpk_status launch_decode(const tpk_shape* s, const DecodeParams& p, cudaStream_t st) {
+  (void)s;
+  cudaError_t e = launch_decode_simt(p, st);
+  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  return TPK_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* tpk_version(void) { return "tpk 0.1 (sm_103a)"; }
+
+const char* tpk_last_error_string(void) { return g_err.c_str(); }
+
+static tpk_status quantize_common(const tpk_shape* shape, const void* k_pool, const void* v_pool,
+                                  const int32_t* src_slots, const int32_t* dst_slots, int n_pages,
+                                  const float* ks_chan, const float* ks_tok, const float* vs_chan, void* rec_pool,
+                                  tpk_stream_t stream) {
+  tpk_status st = check_shape(shape);
+  if (st != TPK_OK) return st;
+  if (n_pages < 0) return fail(TPK_ERR_INVALID, "n_pages %d < 0", n_pages);
+  if (n_pages == 0) return TPK_OK;
+  if (!k_pool || !v_pool || !src_slots || !dst_slots || !rec_pool)
+    return fail(TPK_ERR_INVALID, "null pointer argument");
+  if (!aligned16(k_pool) || !aligned16(v_pool) || !aligned16(rec_pool))
+    return fail(TPK_ERR_INVALID, "pools must be 16-byte aligned");
+  if ((int64_t)n_pages * shape->kv_heads > 0x7fffffffLL) return fail(TPK_ERR_INVALID, "too many pages");
+  int* status = status_ptr();
+  if (!status) return fail(TPK_ERR_CUDA, "cannot resolve the device status word");
+  QuantParams p;
+  p.k_pool = static_cast<const uint16_t*>(k_pool);
+  p.v_pool = static_cast<const uint16_t*>(v_pool);
+  p.src = src_slots;
+  p.dst = dst_slots;
+  p.rec_pool = static_cast<uint8_t*>(rec_pool);
+  p.g_kchan = ks_chan;
+  p.g_ktok = ks_tok;
+  p.g_vchan = vs_chan;
+  p.kv_slots = shape->kv_slots;
+  p.rec_slots = shape->rec_slots;
+  p.status = status;
+  p.H = shape->kv_heads;
+  cudaError_t e = launch_quantize(p, n_pages, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
+  return TPK_OK;
+}
+
+tpk_status tpk_kv_quantize_pages(const tpk_shape* shape, const void* k_pool, const void* v_pool,
+                                 const int32_t* src_slots, const int32_t* dst_slots, int n_pages, void* rec_pool,
+                                 tpk_stream_t stream) {
+  return quantize_common(shape, k_pool, v_pool, src_slots, dst_slots, n_pages, nullptr, nullptr, nullptr,
+                         rec_pool, stream);
+}
+
+tpk_status tpk_kv_quantize_pages_given_scales(const tpk_shape* shape, const void* k_pool, const void* v_pool,
+                                              const int32_t* src_slots, const int32_t* dst_slots, int n_pages,
+                                              const float* ks_chan, const float* ks_tok, const float* vs_chan,
+                                              void* rec_pool, tpk_stream_t stream) {
+  if (n_pages > 0 && (!ks_chan || !ks_tok || !vs_chan)) return fail(TPK_ERR_INVALID, "null scale array");
+  return quantize_common(shape, k_pool, v_pool, src_slots, dst_slots, n_pages, ks_chan, ks_tok, vs_chan,
+                         rec_pool, stream);
+}
+
+tpk_status tpk_decode_attn_exact(const tpk_shape* shape, const void* q, const void* k_pool, const void* v_pool,
+                                 const int32_t* page_table, int tok_begin, int tok_end, int num_splits,
+                                 float* o_part, float* lse_part, tpk_stream_t stream) {
+  tpk_status st = check_shape(shape);
+  if (st != TPK_OK) return st;
+  if (tok_begin < 0 || tok_end < tok_begin) return fail(TPK_ERR_INVALID, "bad token range [%d, %d)", tok_begin, tok_end);
+  if (num_splits < 1 || num_splits > kMaxSplits) return fail(TPK_ERR_INVALID, "num_splits %d out of [1, %d]", num_splits, kMaxSplits);
+  if (!q || !o_part || !lse_part) return fail(TPK_ERR_INVALID, "null pointer argument");
+  if (tok_end > tok_begin && (!k_pool || !v_pool || !page_table)) return fail(TPK_ERR_INVALID, "null pool or page table");
+  if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(o_part))
+    return fail(TPK_ERR_INVALID, "q, pools and o_part must be 16-byte aligned");
+  if ((int64_t)num_splits * shape->kv_heads > 0x7fffffffLL) return fail(TPK_ERR_INVALID, "grid too large");
+  DecodeParams p;
+  fill_common(p, shape, q);
+  p.k_pool = static_cast<const uint16_t*>(k_pool);
+  p.v_pool = static_cast<const uint16_t*>(v_pool);
+  p.page_table = page_table;
+  p.part_o = o_part;
+  p.part_lse = lse_part;
+  p.status = status_ptr();
+  if (!p.status) return fail(TPK_ERR_CUDA, "cannot resolve the device status word");
+  p.mode = kModePrimitive;
+  p.n_req = 1;
+  p.req[0] = ReqPlan{0, 0, tok_begin, tok_end, 0, 0, 0, (int16_t)0, (int16_t)0};
+  // int16 split counts: fold larger counts through the unit decode's int arithmetic
+  if (num_splits > 32767) return fail(TPK_ERR_INVALID, "num_splits too large");
+  p.req[0].splits_e = (int16_t)num_splits;
+  p.n_units = num_splits * shape->kv_heads;
+  return launch_decode(shape, p, reinterpret_cast<cudaStream_t>(stream));
+}
+
+tpk_status tpk_decode_attn_int8(const tpk_shape* shape, const void* q, const void* rec_pool,
+                                const int32_t* page_table8, int page_begin, int page_end, int num_splits,
+                                float* o_part, float* lse_part, tpk_stream_t stream) {
+  tpk_status st = check_shape(shape);
+  if (st != TPK_OK) return st;
+  if (page_begin < 0 || page_end < page_begin) return fail(TPK_ERR_INVALID, "bad page range [%d, %d)", page_begin, page_end);
+  if (page_end > 0x7fffffff / kPageTokens) return fail(TPK_ERR_INVALID, "page range too large");
+  if (num_splits < 1 || num_splits > kMaxSplits) return fail(TPK_ERR_INVALID, "num_splits %d out of [1, %d]", num_splits, kMaxSplits);
+  if (!q || !o_part || !lse_part) return fail(TPK_ERR_INVALID, "null pointer argument");
+  if (page_end > page_begin && (!rec_pool || !page_table8)) return fail(TPK_ERR_INVALID, "null pool or page table");
+  if (!aligned16(q) || !aligned16(rec_pool) || !aligned16(o_part))
+    return fail(TPK_ERR_INVALID, "q, rec_pool and o_part must be 16-byte aligned");
+  DecodeParams p;
+  fill_common(p, shape, q);
+  p.rec_pool = static_cast<const uint8_t*>(rec_pool);
+  p.page_table8 = page_table8;
+  p.part_o = o_part;
+  p.part_lse = lse_part;
+  p.status = status_ptr();
+  if (!p.status) return fail(TPK_ERR_CUDA, "cannot resolve the device status word");
+  p.mode = kModePrimitive;
+  p.n_req = 1;
+  p.req[0] = ReqPlan{0, 0, 0, 0, 0, page_begin, page_end, (int16_t)0, (int16_t)num_splits};
+  p.n_units = num_splits * shape->kv_heads;
+  return launch_decode(shape, p, reinterpret_cast<cudaStream_t>(stream));
+}
+
+tpk_status tpk_merge_lse(int n_parts, int rows, int head_dim, const float* o_parts, const float* lse_parts,
+                         float* o_acc, float* lse_acc, tpk_stream_t stream) {
+  if (head_dim != kHeadDim) return fail(TPK_ERR_UNSUPPORTED, "head_dim %d (only 256 supported)", head_dim);
+  if (n_parts < 0 || rows < 0) return fail(TPK_ERR_INVALID, "negative n_parts or rows");
+  if (rows == 0) return TPK_OK;
+  if (!o_acc || !lse_acc || (n_parts > 0 && (!o_parts || !lse_parts)))
+    return fail(TPK_ERR_INVALID, "null pointer argument");
+  cudaError_t e = launch_merge(n_parts, rows, o_parts, lse_parts, o_acc, lse_acc,
+                               reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "merge launch");
+  return TPK_OK;
+}
+
+static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+size_t tpk_hybrid_workspace_bytes(const tpk_shape* shape, int n_req) {
+  if (!shape || n_req < 1 || shape->kv_heads < 1) return 0;
+  return align256((size_t)n_req * shape->kv_heads * sizeof(int)) + align256((size_t)kMaxUnits * kGroup * 4) +
+         (size_t)kMaxUnits * kGroup * kHeadDim * 4;
+}
+
+tpk_status tpk_workspace_init(void* ws, size_t ws_bytes, tpk_stream_t stream) {
+  if (!ws) return fail(TPK_ERR_INVALID, "null workspace");
+  cudaError_t e = cudaMemsetAsync(ws, 0, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "workspace memset");
+  return TPK_OK;
+}
+
+tpk_status tpk_decode_hybrid_batched(const tpk_shape* shape, int n_req, const void* q, const void* k_pool,
+                                     const void* v_pool, const void* rec_pool, const int32_t* page_table,
+                                     const int32_t* req_page_off, const int32_t* n_exact_tokens,
+                                     const int32_t* page_table8, const int32_t* req_page_off8,
+                                     const int32_t* n_int8_pages, float* o, float* lse, void* ws, size_t ws_bytes,
+                                     tpk_stream_t stream) {
+  tpk_status st = check_shape(shape);
+  if (st != TPK_OK) return st;
+  if (n_req < 1 || n_req > kMaxReqPerLaunch) return fail(TPK_ERR_INVALID, "n_req %d out of [1, %d]", n_req, kMaxReqPerLaunch);
+  if (!q || !o || !lse || !ws || !req_page_off || !n_exact_tokens || !req_page_off8 || !n_int8_pages)
+    return fail(TPK_ERR_INVALID, "null pointer argument");
+  if (!aligned16(q) || !aligned16(o) || !aligned16(ws) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(rec_pool))
+    return fail(TPK_ERR_INVALID, "device buffers must be 16-byte aligned");
+  const int H = shape->kv_heads;
+  size_t need = tpk_hybrid_workspace_bytes(shape, n_req);
+  if (ws_bytes < need) return fail(TPK_ERR_NOMEM, "workspace %zu bytes < %zu required", ws_bytes, need);
+  // ---- validate the host metadata and measure the work
+  double total = 0.0;
+  bool any_e = false, any_8 = false;
+  for (int b = 0; b < n_req; ++b) {
+    int ne = n_exact_tokens[b], n8 = n_int8_pages[b];
+    if (ne < 0 || n8 < 0) return fail(TPK_ERR_INVALID, "request %d: negative length", b);
+    if (n8 > 0x7fffffff / kPageTokens) return fail(TPK_ERR_INVALID, "request %d: too many pages", b);
+    int have_e = req_page_off[b + 1] - req_page_off[b];
+    int have_8 = req_page_off8[b + 1] - req_page_off8[b];
+    if (req_page_off[b] < 0 || have_e < (ne + kPageTokens - 1) / kPageTokens)
+      return fail(TPK_ERR_INVALID, "request %d: exact page table holds %d pages, %d tokens need %d", b, have_e, ne,
+                  (ne + kPageTokens - 1) / kPageTokens);
+    if (req_page_off8[b] < 0 || have_8 < n8)
+      return fail(TPK_ERR_INVALID, "request %d: 8-bit page table holds %d pages, need %d", b, have_8, n8);
+    any_e |= ne > 0;
+    any_8 |= n8 > 0;
+    total += (double)H * (1024.0 * ne + (double)kRecordBytes * n8);
+  }
+  if (any_e && (!k_pool || !v_pool || !page_table)) return fail(TPK_ERR_INVALID, "null BF16 pool or page table");
+  if (any_8 && (!rec_pool || !page_table8)) return fail(TPK_ERR_INVALID, "null 8-bit pool or page table");
+  // ---- split plan: about one resident wave of equal-byte units
+  static int blocks_per_sm = 0;
+  if (!blocks_per_sm) blocks_per_sm = decode_simt_blocks_per_sm();
+  const int target = num_sms() * blocks_per_sm;
+  double chunk = std::max(total / target, 16384.0);
+  DecodeParams p;
+  fill_common(p, shape, q);
+  for (int attempt = 0; attempt < 40; ++attempt, chunk *= 1.25) {
+    int units = 0;
+    bool fits = true;
+    for (int b = 0; b < n_req; ++b) {
+      int ne = n_exact_tokens[b], n8 = n_int8_pages[b];
+      int pe = (ne + kPageTokens - 1) / kPageTokens;
+      int se = ne > 0 ? (int)std::min<double>(pe, std::ceil(1024.0 * ne / chunk)) : 0;
+      int s8 = n8 > 0 ? (int)std::min<double>(n8, std::ceil((double)kRecordBytes * n8 / chunk)) : 0;
+      if (se == 0 && s8 == 0) se = 1;  // an empty unit writes the empty result
+      if (se > 32767 || s8 > 32767) { fits = false; break; }
+      p.req[b] = ReqPlan{units, req_page_off[b], 0, ne, req_page_off8[b], 0, n8, (int16_t)se, (int16_t)s8};
+      units += H * (se + s8);
+      if (units > kMaxUnits) { fits = false; break; }
+    }
+    if (fits) {
+      p.n_units = units;
+      break;
+    }
+    if (attempt == 39) return fail(TPK_ERR_UNSUPPORTED, "could not plan within %d units", kMaxUnits);
+  }
+  p.k_pool = static_cast<const uint16_t*>(k_pool);
+  p.v_pool = static_cast<const uint16_t*>(v_pool);
+  p.rec_pool = static_cast<const uint8_t*>(rec_pool);
+  p.page_table = page_table;
+  p.page_table8 = page_table8;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  p.tickets = reinterpret_cast<int*>(w);
+  w += align256((size_t)n_req * H * sizeof(int));
+  p.part_lse = reinterpret_cast<float*>(w);
+  w += align256((size_t)kMaxUnits * kGroup * 4);
+  p.part_o = reinterpret_cast<float*>(w);
+  p.out_o = o;
+  p.out_lse = lse;
+  p.mode = kModeFold;
+  p.n_req = n_req;
+  p.status = status_ptr();
+  if (!p.status) return fail(TPK_ERR_CUDA, "cannot resolve the device status word");
+  return launch_decode(shape, p, reinterpret_cast<cudaStream_t>(stream));
+}
+
+tpk_status tpk_get_device_status(int* flags, int reset, tpk_stream_t stream) {
+  if (!flags) return fail(TPK_ERR_INVALID, "null flags");
+  int* d = status_ptr();
+  if (!d) return fail(TPK_ERR_CUDA, "cannot resolve the device status word");
+  cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
+  e = cudaMemcpy(flags, d, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "status read");
+  if (reset) {
+    e = cudaMemset(d, 0, sizeof(int));
+    if (e != cudaSuccess) return cuda_fail(e, "status reset");
+  }
+  if (*flags & kStatusTimeout) return fail(TPK_ERR_TIMEOUT, "a device-side wait gave up (status %d)", *flags);
+  if (*flags & kStatusBadSlot) return fail(TPK_ERR_BOUNDS, "a page-table entry outside the pool was skipped");
+  return TPK_OK;
+}
+
+}  // extern "C"

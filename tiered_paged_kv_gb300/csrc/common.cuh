@@ -1,0 +1,206 @@
+// Device-side helpers shared by the tpk kernels: sizes of the page formats,
+// mbarrier and bulk-copy (cp.async.bulk) wrappers written as inline PTX for
+// sm_103a, and the per-launch split plan passed by value to the decode kernels.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace tpk {
+
+constexpr int kHeadDim = 256;
+constexpr int kPageTokens = 64;
+constexpr int kGroup = 8;  // query rows per KV head
+constexpr int kRecordBytes = 35072;
+constexpr int kOffKc = 0;
+constexpr int kOffVc = 16384;
+constexpr int kOffKsChan = 32768;
+constexpr int kOffKsTok = 33792;
+constexpr int kOffVsChan = 34048;
+constexpr int kBf16PageHeadBytes = kPageTokens * kHeadDim * 2;  // 32 KB (K or V)
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// Device status bits (read by tpk_get_device_status).
+constexpr int kStatusBadSlot = 1;
+
+// ----------------------------------------------------------------- split plan
+// One request's share of a decode launch.  Thread block u belongs to the request
+// with the largest unit_base <= u; within the request, units are laid out
+// [kv_head][exact splits..., 8-bit splits...], so the units of one (request,
+// head) are consecutive and are folded in that order.
+struct ReqPlan {
+  int32_t unit_base;  // first unit of this request
+  int32_t pt_off;     // offset of the request's exact-tier slots in page_table
+  int32_t e_begin;    // exact-tier token range [e_begin, e_end)
+  int32_t e_end;
+  int32_t pt_off8;    // offset of the request's 8-bit slots in page_table8
+  int32_t p_begin;    // 8-bit page range [p_begin, p_end)
+  int32_t p_end;
+  int16_t splits_e;   // exact-tier units per KV head (0 if the tier is empty)
+  int16_t splits_8;   // 8-bit units per KV head
+};
+
+constexpr int kMaxReqPerLaunch = 256;
+
+enum : int { kModePrimitive = 0, kModeFold = 1 };
+
+struct DecodeParams {
+  const uint16_t* q;        // bf16 [n_req][H*G][256]
+  const uint16_t* k_pool;   // bf16 [slot][H][64][256]
+  const uint16_t* v_pool;
+  const uint8_t* rec_pool;  // records [slot][H]
+  const int32_t* page_table;
+  const int32_t* page_table8;
+  int64_t kv_slots;         // 0 = unchecked
+  int64_t rec_slots;
+  float* part_o;            // primitive: o_part [split][H*G][256]; fold: workspace [unit][G][256]
+  float* part_lse;
+  float* out_o;             // fold: final o [n_req][H*G][256]
+  float* out_lse;
+  int* tickets;             // fold: [n_req][H], zero between launches
+  int* status;              // device status word
+  float qscale;             // sm_scale * log2(e)
+  int H;
+  int mode;
+  int n_req;
+  int n_units;
+  ReqPlan req[kMaxReqPerLaunch];
+};
+
+struct UnitInfo {
+  int b, h, tier, split, n_splits, per_head, unit_in_head;
+  int tok_begin, tok_end;  // exact tier: tokens; 8-bit tier: tokens of whole pages (page * 64)
+  int pt_off;
+};
+
+__device__ __forceinline__ UnitInfo decode_unit(const DecodeParams& p, int u) {
+  int lo = 0, hi = p.n_req - 1;
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if (p.req[mid].unit_base <= u) lo = mid; else hi = mid - 1;
+  }
+  const ReqPlan& r = p.req[lo];
+  UnitInfo ui;
+  ui.b = lo;
+  int local = u - r.unit_base;
+  ui.per_head = r.splits_e + r.splits_8;
+  ui.h = local / ui.per_head;
+  int k = local - ui.h * ui.per_head;
+  ui.unit_in_head = k;
+  if (k < r.splits_e) {
+    ui.tier = 0;
+    ui.split = k;
+    ui.n_splits = r.splits_e;
+    int pg0 = r.e_begin / kPageTokens;
+    int pg1 = (r.e_end + kPageTokens - 1) / kPageTokens;
+    int P = pg1 - pg0;
+    int pa = pg0 + (int)((int64_t)P * k / r.splits_e);
+    int pb = pg0 + (int)((int64_t)P * (k + 1) / r.splits_e);
+    ui.tok_begin = max(r.e_begin, pa * kPageTokens);
+    ui.tok_end = min(r.e_end, pb * kPageTokens);
+    if (ui.tok_end < ui.tok_begin) ui.tok_end = ui.tok_begin;
+    ui.pt_off = r.pt_off;
+  } else {
+    ui.tier = 1;
+    ui.split = k - r.splits_e;
+    ui.n_splits = r.splits_8;
+    int P = r.p_end - r.p_begin;
+    int pa = r.p_begin + (int)((int64_t)P * ui.split / r.splits_8);
+    int pb = r.p_begin + (int)((int64_t)P * (ui.split + 1) / r.splits_8);
+    ui.tok_begin = pa * kPageTokens;
+    ui.tok_end = pb * kPageTokens;
+    ui.pt_off = r.pt_off8;
+  }
+  return ui;
+}
+
+// Page conversion launch parameters (given-scale arrays are null for a full
+// conversion).
+struct QuantParams {
+  const uint16_t* k_pool;
+  const uint16_t* v_pool;
+  const int32_t* src;
+  const int32_t* dst;
+  uint8_t* rec_pool;
+  const float* g_kchan;  // given scales, or null
+  const float* g_ktok;
+  const float* g_vchan;
+  int64_t kv_slots;
+  int64_t rec_slots;
+  int* status;
+  int H;
+};
+
+// ------------------------------------------------------------- PTX wrappers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded wait on an mbarrier phase: gives up after about two seconds of wall
+// time, sets kStatusTimeout in the device status word and returns false.
+constexpr int kStatusTimeout = 2;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (;;) {
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (global_ns() - t0 > kWaitLimitNs) {
+      atomicOr(status, kStatusTimeout);
+      return false;
+    }
+  }
+}
+
+// 1-D bulk copy global -> shared, completion counted on an mbarrier (bytes and
+// both addresses must be multiples of 16).
+__device__ __forceinline__ void bulk_g2s(void* smem_dst, const void* gmem_src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(smem_dst)),
+      "l"(gmem_src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+}  // namespace tpk

@@ -1,0 +1,262 @@
+// Page conversion: BF16 page-heads -> 8-bit records.
+//
+// "model quantization", section "An 8-bit page format shaped for its kernel":
+// the key scale of a channel is the square root of its RMS over the page,
+// normalised so the channel scales multiply to one and clamped to 2^+-14; a
+// per-token-and-head factor covers the rest of the key's range; codes are
+// symmetric in -127..127; values carry one scale per channel per page.
+//
+// One thread block converts one page-head (64 tokens x 256 channels of K and V):
+//   1. the page-head is bulk-copied into shared memory;
+//   2. thread c owns channel c: the key channel's mean square is accumulated
+//      exactly (bfloat16 squares summed as 64-bit fixed point), the value
+//      channel's absolute maximum gives u_c = max|v| / 127;
+//   3. the geometric mean of the mean squares is formed as a product of
+//      mantissas (double) and a sum of exponents, so the normalised fourth power
+//      x_c = ms_c / G needs one multiplication; shat_c = x_c^(1/4);
+//   4. the float32 neighbours of shat_c are found exactly (c^4 against x_c with
+//      an FMA-exact product), and one thread walks the channels choosing the
+//      neighbour that keeps the running log-error of the product nearest zero;
+//   5. threads (token, quarter row) divide keys by s_c, take the per-token
+//      absolute maximum r_t = max|y| / 127 and form the codes with IEEE float32
+//      divisions and half-to-even rint; values likewise with u_c.
+#include "common.cuh"
+
+namespace tpk {
+
+struct QSmem {
+  alignas(128) uint16_t k[kPageTokens][kHeadDim];
+  alignas(128) uint16_t v[kPageTokens][kHeadDim];
+  uint64_t bar;
+  double red_m[8];
+  int red_e[8];
+  double invG;
+  float s[kHeadDim];
+  float u[kHeadDim];
+  float slo[kHeadDim], shi[kHeadDim], dlo[kHeadDim], dhi[kHeadDim];
+  int exact[kHeadDim];
+  int bad;
+};
+
+// c^4 - x, with c^2 exact in double and c^4 = hi + lo exact by FMA.
+__device__ __forceinline__ double pow4_minus(float c, double x) {
+  double c2 = (double)c * (double)c;
+  double hi = c2 * c2;
+  double lo = fma(c2, c2, -hi);
+  return (hi - x) + lo;
+}
+
+__device__ __forceinline__ int8_t code_of(float x, float scale) {
+  if (!(scale > 0.f)) return 0;
+  float z = rintf(__fdiv_rn(x, scale));
+  z = fminf(fmaxf(z, -127.f), 127.f);
+  return (int8_t)(int)z;
+}
+
+__global__ void __launch_bounds__(256) quantize_kernel(const __grid_constant__ QuantParams p) {
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  QSmem& S = *reinterpret_cast<QSmem*>(smem_raw);
+  const int tid = threadIdx.x;
+  const int i = blockIdx.x / p.H, h = blockIdx.x % p.H;
+  const bool given = p.g_kchan != nullptr;
+
+  if (tid == 0) {
+    int64_t src = p.src[i], dst = p.dst[i];
+    bool ok = src >= 0 && (p.kv_slots == 0 || src < p.kv_slots) && dst >= 0 && (p.rec_slots == 0 || dst < p.rec_slots);
+    S.bad = ok ? 0 : 1;
+    if (!ok) atomicOr(p.status, kStatusBadSlot);
+    mbar_init(&S.bar, 1);
+    fence_mbar_init();
+    if (ok) {
+      int64_t off = (src * p.H + h) * (int64_t)(kPageTokens * kHeadDim);
+      mbar_arrive_expect_tx(&S.bar, 2 * kBf16PageHeadBytes);
+      bulk_g2s(&S.k[0][0], p.k_pool + off, kBf16PageHeadBytes, &S.bar);
+      bulk_g2s(&S.v[0][0], p.v_pool + off, kBf16PageHeadBytes, &S.bar);
+    }
+  }
+  __syncthreads();
+  if (S.bad) return;
+  const bool landed = mbar_wait(&S.bar, 0, p.status);
+  if (__syncthreads_or(!landed)) return;
+
+  uint8_t* rec = p.rec_pool + ((int64_t)p.dst[i] * p.H + h) * kRecordBytes;
+  const int64_t gidx = (int64_t)i * p.H + h;  // index into given-scale arrays
+  const int c = tid;
+
+  // ---- 2. per-channel statistics
+  {
+    float vmax = 0.f;
+    for (int t = 0; t < kPageTokens; ++t) vmax = fmaxf(vmax, fabsf(bf16_lo(S.v[t][c])));
+    S.u[c] = given ? p.g_vchan[gidx * kHeadDim + c] : __fdiv_rn(vmax, 127.f);
+  }
+  double mant = 1.0;
+  int expo = 0;
+  double ms = 0.0;
+  if (!given) {
+    int emax = 1;
+    for (int t = 0; t < kPageTokens; ++t) {
+      int e = (S.k[t][c] >> 7) & 0xff;
+      emax = max(emax, e);
+    }
+    // element = m * 2^(e - 134) (m with the hidden bit; subnormals use e = 1);
+    // square = m^2 * 2^(2e - 268); fixed point unit 2^(2 emax - 308)
+    unsigned long long acc = 0;
+    for (int t = 0; t < kPageTokens; ++t) {
+      uint32_t bits = S.k[t][c] & 0x7fffu;
+      int e = bits >> 7;
+      uint32_t m = bits & 0x7fu;
+      if (e) m |= 0x80u; else e = 1;
+      unsigned long long m2 = (unsigned long long)(m * m);
+      int sh = 2 * (emax - e);
+      if (sh <= 40) acc += m2 << (40 - sh);
+      else if (sh < 56) acc += m2 >> (sh - 40);
+    }
+    ms = acc ? ldexp((double)acc, 2 * emax - 308 - 6) : 0x1p-252;  // mean over 64 tokens
+    mant = frexp(ms, &expo);
+  }
+  // ---- 3. geometric mean of ms over channels: product of mantissas, sum of exponents
+  if (!given) {
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+      double mo = __shfl_xor_sync(0xffffffffu, mant, off);
+      int eo = __shfl_xor_sync(0xffffffffu, expo, off);
+      int t;
+      mant = frexp(mant * mo, &t);
+      expo += eo + t;
+    }
+    if ((tid & 31) == 0) {
+      S.red_m[tid >> 5] = mant;
+      S.red_e[tid >> 5] = expo;
+    }
+  }
+  __syncthreads();
+  if (!given && tid == 0) {
+    double m = S.red_m[0];
+    int e = S.red_e[0];
+    for (int w = 1; w < 8; ++w) {
+      int t;
+      m = frexp(m * S.red_m[w], &t);
+      e += S.red_e[w] + t;
+    }
+    double lnG = (log(m) + (double)e * 0.69314718055994530942) / kHeadDim;
+    S.invG = exp(-lnG);
+  }
+  __syncthreads();
+  // ---- 4. float32 neighbours of shat_c = (ms_c / G)^(1/4), clamped to 2^+-14
+  if (!given) {
+    double x = ms * S.invG;
+    float lo, hi, dl = 0.f, dh = 0.f;
+    int ex = 0;
+    if (x >= 0x1p56) {
+      lo = hi = 0x1p14f;
+      ex = 1;
+    } else if (x <= 0x1p-56) {
+      lo = hi = 0x1p-14f;
+      ex = 1;
+    } else {
+      float cc = sqrtf(sqrtf((float)x));
+      for (int it = 0; it < 4; ++it) {
+        if (pow4_minus(cc, x) > 0.0) cc = nextafterf(cc, 0.f);
+        else if (pow4_minus(nextafterf(cc, 0x1p127f), x) <= 0.0) cc = nextafterf(cc, 0x1p127f);
+        else break;
+      }
+      double df = pow4_minus(cc, x);
+      if (df == 0.0) {
+        lo = hi = cc;
+        ex = 1;
+      } else {
+        lo = cc;
+        hi = nextafterf(cc, 0x1p127f);
+        double rx = 1.0 / x;
+        double a = df * rx, b = pow4_minus(hi, x) * rx;  // relative error of the fourth power
+        dl = (float)(0.25 * a - 0.125 * a * a);           // ln(lo / shat)
+        dh = (float)(0.25 * b - 0.125 * b * b);           // ln(hi / shat)
+      }
+    }
+    S.slo[c] = lo;
+    S.shi[c] = hi;
+    S.dlo[c] = dl;
+    S.dhi[c] = dh;
+    S.exact[c] = ex;
+  }
+  __syncthreads();
+  if (given) {
+    S.s[c] = p.g_kchan[gidx * kHeadDim + c];
+  } else if (tid == 0) {
+    float E = 0.f;
+    for (int ch = 0; ch < kHeadDim; ++ch) {
+      if (S.exact[ch]) {
+        S.s[ch] = S.slo[ch];
+        continue;
+      }
+      float a = E + S.dlo[ch], b = E + S.dhi[ch];
+      if (fabsf(a) <= fabsf(b)) {
+        S.s[ch] = S.slo[ch];
+        E = a;
+      } else {
+        S.s[ch] = S.shi[ch];
+        E = b;
+      }
+    }
+  }
+  __syncthreads();
+  // ---- 5. codes: thread (token t, quarter q) handles 64 channels, chunks rotated
+  //         by lane so that shared-memory reads do not conflict
+  {
+    const int t = tid >> 2, q = tid & 3, lane = tid & 31;
+    float y[8][8];
+    float ymax = 0.f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int ch0 = q * 64 + ((k + lane) & 7) * 8;
+      uint4 w = *reinterpret_cast<const uint4*>(&S.k[t][ch0]);
+      float f[8] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y),
+                    bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w)};
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        y[k][e] = __fdiv_rn(f[e], S.s[ch0 + e]);
+        ymax = fmaxf(ymax, fabsf(y[k][e]));
+      }
+    }
+    ymax = fmaxf(ymax, __shfl_xor_sync(0xffffffffu, ymax, 1));
+    ymax = fmaxf(ymax, __shfl_xor_sync(0xffffffffu, ymax, 2));
+    const float r = given ? p.g_ktok[gidx * kPageTokens + t] : __fdiv_rn(ymax, 127.f);
+    int8_t* kc = reinterpret_cast<int8_t*>(rec + kOffKc) + t * kHeadDim;
+    int8_t* vc = reinterpret_cast<int8_t*>(rec + kOffVc) + t * kHeadDim;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int ch0 = q * 64 + ((k + lane) & 7) * 8;
+      uint32_t wk[2] = {0u, 0u}, wv[2] = {0u, 0u};
+      uint4 w = *reinterpret_cast<const uint4*>(&S.v[t][ch0]);
+      float f[8] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y),
+                    bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w)};
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        uint32_t ck = (uint8_t)code_of(y[k][e], r);
+        uint32_t cv = (uint8_t)code_of(f[e], S.u[ch0 + e]);
+        wk[e >> 2] |= ck << (8 * (e & 3));
+        wv[e >> 2] |= cv << (8 * (e & 3));
+      }
+      *reinterpret_cast<uint2*>(kc + ch0) = make_uint2(wk[0], wk[1]);
+      *reinterpret_cast<uint2*>(vc + ch0) = make_uint2(wv[0], wv[1]);
+    }
+    if (q == 0) reinterpret_cast<float*>(rec + kOffKsTok)[t] = r;
+  }
+  reinterpret_cast<float*>(rec + kOffKsChan)[c] = S.s[c];
+  reinterpret_cast<float*>(rec + kOffVsChan)[c] = S.u[c];
+}
+
+cudaError_t launch_quantize(const QuantParams& p, int n_pages, cudaStream_t stream) {
+  static bool configured = false;
+  const int smem = (int)sizeof(QSmem);
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(quantize_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  if (n_pages == 0) return cudaSuccess;
+  quantize_kernel<<<n_pages * p.H, 256, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace tpk
