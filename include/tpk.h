@@ -62,7 +62,7 @@ enum { TPK_IMPL_DEFAULT = 0, TPK_IMPL_SIMT = 1, TPK_IMPL_TENSOR = 2 };
 
 /* Bytes of one 8-bit page-head record:
  *   int8 kc[64][256]   key codes, token-major          offset 0
- *   int8 vc[64][256]   value codes, token-major        offset 16384
+ *   int8 vc[256][64]   value codes, channel-major      offset 16384
  *   f32  ks_chan[256]  key channel scale s_c           offset 32768
  *   f32  ks_tok[64]    key per-token factor r_t        offset 33792
  *   f32  vs_chan[256]  value channel scale u_c         offset 34048

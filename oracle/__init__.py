@@ -102,10 +102,13 @@ def quantize_pages(H, k_pool, v_pool, src_slots, dst_slots, rec_pool):
 
 
 def record_fields(rec):
-    """Split one 35,072-byte record into (kc[64][256], vc[64][256], s[256], r[64], u[256])."""
+    """Split one 35,072-byte record into (kc[64][256], vc[64][256], s[256], r[64], u[256]).
+
+    Value codes are stored channel-major (vc[256][64]); the returned vc is the
+    token-major view vc[t][c]."""
     rec = np.asarray(rec, np.uint8)
     kc = rec[OFF_KC:OFF_VC].view(np.int8).reshape(T_PAGE, D_HEAD)
-    vc = rec[OFF_VC:OFF_KS_CHAN].view(np.int8).reshape(T_PAGE, D_HEAD)
+    vc = rec[OFF_VC:OFF_KS_CHAN].view(np.int8).reshape(D_HEAD, T_PAGE).T
     s = rec[OFF_KS_CHAN:OFF_KS_TOK].view(np.float32)
     r = rec[OFF_KS_TOK:OFF_VS_CHAN].view(np.float32)
     u = rec[OFF_VS_CHAN:REC_BYTES].view(np.float32)

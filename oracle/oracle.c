@@ -35,7 +35,7 @@
  *
  * Record layout of one 8-bit page-head (35,072 bytes):
  *   int8  kc[64][256]      keys, token-major       offset 0
- *   int8  vc[64][256]      values, token-major     offset 16384
+ *   int8  vc[256][64]      values, channel-major   offset 16384
  *   f32   ks_chan[256]     key channel scale s_c   offset 32768
  *   f32   ks_tok[64]       key token factor r_t    offset 33792
  *   f32   vs_chan[256]     value channel scale u_c offset 34048
@@ -150,7 +150,7 @@ void orc_codes_given(const uint16_t* k, const uint16_t* v, const float* ks_chan,
     for (int c = 0; c < D_HEAD; ++c) {
       float y = bf16_float(k[t * D_HEAD + c]) / ks_chan[c];
       kc[t * D_HEAD + c] = code_of(y, ks_tok[t]);
-      vc[t * D_HEAD + c] = code_of(bf16_float(v[t * D_HEAD + c]), vs_chan[c]);
+      vc[c * T_PAGE + t] = code_of(bf16_float(v[t * D_HEAD + c]), vs_chan[c]);
     }
   memcpy(rec + OFF_KS_CHAN, ks_chan, 4 * D_HEAD);
   memcpy(rec + OFF_KS_TOK, ks_tok, 4 * T_PAGE);
@@ -280,7 +280,7 @@ static void partial_int8_head(int H, int G, int h, const uint16_t* q, const uint
       for (int c = 0; c < d; ++c) {
         int64_t i = ((int64_t)p * T_PAGE + t) * d + c;
         K[i] = (double)kc[t * d + c] * (double)s[c] * (double)r[t];
-        V[i] = (double)vc[t * d + c] * (double)u[c];
+        V[i] = (double)vc[c * T_PAGE + t] * (double)u[c];
       }
   }
   for (int g = 0; g < G; ++g)

@@ -76,8 +76,8 @@ def test_zero_rows_channels_and_clamp():
     for slot in w.int8_slots():
         k = w.k_pool[slot, 0]
         k[:, 5] = 0                                   # silent channel -> clamped 2^-14
-        k[9, :] = 0                                   # silent row -> r = 0
         k[:, 200] = synth.f32_to_bf16(np.full(64, 2.0 ** 60, np.float32))  # far above the clamp
+        k[9, :] = 0                                   # silent row -> r = 0
         w.v_pool[slot, 0][:, 7] = 0
     ref = oracle_records(w).reshape(w.n_slots, 1, oracle.REC_BYTES)
     d = DevWorkload(w)

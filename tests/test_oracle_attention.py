@@ -176,7 +176,7 @@ def representable_records(seed, n_pages, H):
         for h in range(H):
             rec = recs[p, h]
             rec[:16384] = kc[p, h].reshape(-1).view(np.uint8)
-            rec[16384:32768] = vc[p, h].reshape(-1).view(np.uint8)
+            rec[16384:32768] = np.ascontiguousarray(vc[p, h].T).reshape(-1).view(np.uint8)  # channel-major
             rec[32768:33792] = s[p, h].view(np.uint8)
             rec[33792:34048] = r[p, h].view(np.uint8)
             rec[34048:] = u[p, h].view(np.uint8)

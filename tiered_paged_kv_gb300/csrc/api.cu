@@ -15,6 +15,8 @@
 namespace tpk {
 cudaError_t launch_decode_simt(const DecodeParams& p, cudaStream_t stream);
 int decode_simt_blocks_per_sm();
+cudaError_t launch_decode_mma(const DecodeParams& p, cudaStream_t stream);
+int decode_mma_blocks_per_sm();
 cudaError_t launch_merge(int n_parts, int rows, const float* o_parts, const float* lse_parts, float* o_acc,
                          float* lse_acc, cudaStream_t stream);
 cudaError_t launch_quantize(const QuantParams& p, int n_pages, cudaStream_t stream);
@@ -90,9 +92,20 @@ void fill_common(DecodeParams& p, const tpk_shape* s, const void* q) {
   p.H = s->kv_heads;
 }
 
+bool use_simt(const tpk_shape* s) { return s->impl == TPK_IMPL_SIMT; }
+
+int blocks_per_sm(const tpk_shape* s) {
+  static int simt = 0, mma = 0;
+  if (use_simt(s)) {
+    if (!simt) simt = decode_simt_blocks_per_sm();
+    return simt;
+  }
+  if (!mma) mma = decode_mma_blocks_per_sm();
+  return mma;
+}
+
 tpk_status launch_decode(const tpk_shape* s, const DecodeParams& p, cudaStream_t st) {
-  (void)s;
-  cudaError_t e = launch_decode_simt(p, st);
+  cudaError_t e = use_simt(s) ? launch_decode_simt(p, st) : launch_decode_mma(p, st);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   return TPK_OK;
 }
@@ -277,9 +290,7 @@ tpk_status tpk_decode_hybrid_batched(const tpk_shape* shape, int n_req, const vo
   if (any_e && (!k_pool || !v_pool || !page_table)) return fail(TPK_ERR_INVALID, "null BF16 pool or page table");
   if (any_8 && (!rec_pool || !page_table8)) return fail(TPK_ERR_INVALID, "null 8-bit pool or page table");
   // ---- split plan: about one resident wave of equal-byte units
-  static int blocks_per_sm = 0;
-  if (!blocks_per_sm) blocks_per_sm = decode_simt_blocks_per_sm();
-  const int target = num_sms() * blocks_per_sm;
+  const int target = num_sms() * blocks_per_sm(shape);
   double chunk = std::max(total / target, 16384.0);
   DecodeParams p;
   fill_common(p, shape, q);

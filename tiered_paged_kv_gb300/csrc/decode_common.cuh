@@ -60,8 +60,9 @@ __device__ __forceinline__ int item_page(const UnitInfo& ui, const Items& it, in
 }
 
 // Stage the unit's page-table entries (first kPtCache of them).
+template <typename Smem>
 __device__ __forceinline__ void load_page_table(const DecodeParams& p, const UnitInfo& ui, const Items& it,
-                                                DecSmem& S) {
+                                                Smem& S) {
   const int32_t* pt = (ui.tier == 0 ? p.page_table : p.page_table8) + ui.pt_off + it.pg_first;
   int n = min(it.n_pages, kPtCache);
   for (int i = threadIdx.x; i < n; i += blockDim.x) S.pt[i] = __ldg(pt + i);
@@ -98,22 +99,25 @@ __device__ __forceinline__ void issue_item(const DecodeParams& p, const UnitInfo
 }
 
 // -------------------------------------------------------------- epilogue
-// Per-warp state on entry: m_run (base-2 running max, integer valued, per lane
-// for row lane & 7), l_lane (partial sum of weights over the lane's key slot),
-// and O[r][c] for rows r = 0..7, channels 8 * lane + c (SIMT) -- the caller
-// first writes its O into `ep_o` ([warp][row][256] floats aliasing the stages).
+// On entry every consumer warp w has stored its online-softmax state for the 8
+// query rows: ep_m[w][r] (base-2 running max, integer valued, or -inf),
+// ep_l[w][r] (sum of weights) and its unnormalised accumulator in
+// ep_o[w][r][256] (shared memory aliasing the idle stages).
 //
-// Combines the warps into the unit's partial and writes it, then (fold mode)
-// the last unit of a (request, head) folds all of that head's partials.
-__device__ __forceinline__ void write_and_fold(const DecodeParams& p, const UnitInfo& ui, DecSmem& S,
+// Threads 0..127 combine the kDecWarps warps into the unit's partial (o, lse)
+// and write it; in fold mode the last unit of a (request, KV head) then merges
+// all of that head's partials in unit order.  Every thread of the block must
+// call this (it contains block barriers); threads >= 128 only take part in them.
+template <typename Smem>
+__device__ __forceinline__ void write_and_fold(const DecodeParams& p, const UnitInfo& ui, Smem& S,
                                                const float* ep_o) {
   const int tid = threadIdx.x;
+  const bool worker = tid < 128;
   const int G = kGroup;
-  // destination rows of this unit's partial
   float* dst_o;
   float* dst_lse;
   bool fold = false;
-  int row0_final = (ui.b * p.H + ui.h) * G;
+  const int row0_final = (ui.b * p.H + ui.h) * G;
   if (p.mode == kModePrimitive) {
     int row0 = (ui.split * p.H + ui.h) * G;
     dst_o = p.part_o + (int64_t)row0 * kHeadDim;
@@ -122,15 +126,13 @@ __device__ __forceinline__ void write_and_fold(const DecodeParams& p, const Unit
     dst_o = p.out_o + (int64_t)row0_final * kHeadDim;
     dst_lse = p.out_lse + row0_final;
   } else {
-    int u = blockIdx.x;
-    dst_o = p.part_o + (int64_t)u * G * kHeadDim;
-    dst_lse = p.part_lse + u * G;
+    dst_o = p.part_o + (int64_t)blockIdx.x * G * kHeadDim;
+    dst_lse = p.part_lse + blockIdx.x * G;
     fold = true;
   }
-  // 2048 outputs, 16 per thread: row r = tid / 16, channels (tid % 16) * 16 ...
-  {
-    int r = tid >> 4;
-    int c0 = (tid & 15) * 16;
+  const int r = (tid >> 4) & 7;
+  const int c0 = (tid & 15) * 16;
+  if (worker) {
     float M = kNegInf;
 #pragma unroll
     for (int w = 0; w < kDecWarps; ++w) M = fmaxf(M, S.ep_m[w][r]);
@@ -142,8 +144,8 @@ __device__ __forceinline__ void write_and_fold(const DecodeParams& p, const Unit
       fw[w] = (mw == kNegInf) ? 0.f : ldexpf(1.f, (int)(mw - M));
       L += fw[w] * S.ep_l[w][r];
     }
-    bool empty = !(L > 0.f);
-    float inv = empty ? 0.f : 1.f / L;
+    const bool empty = !(L > 0.f);
+    const float inv = empty ? 0.f : 1.f / L;
 #pragma unroll
     for (int c = 0; c < 16; c += 4) {
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -174,11 +176,9 @@ __device__ __forceinline__ void write_and_fold(const DecodeParams& p, const Unit
     if (S.is_last) *ticket = 0;  // leave the workspace zeroed for the next launch
   }
   __syncthreads();
-  if (!S.is_last) return;
+  if (!S.is_last || !worker) return;
   __threadfence();
   const int first = blockIdx.x - ui.unit_in_head;
-  int r = tid >> 4;
-  int c0 = (tid & 15) * 16;
   float M = kNegInf;
   for (int i = 0; i < ui.per_head; ++i) M = fmaxf(M, __ldcg(p.part_lse + (first + i) * G + r));
   float* out_o = p.out_o + (int64_t)(row0_final + r) * kHeadDim + c0;
@@ -193,7 +193,7 @@ __device__ __forceinline__ void write_and_fold(const DecodeParams& p, const Unit
     float li = __ldcg(p.part_lse + (first + i) * G + r);
     if (li != kNegInf) L += expf(li - M);
   }
-  float LSE = M + logf(L);
+  const float LSE = M + logf(L);
   float acc[16];
 #pragma unroll
   for (int c = 0; c < 16; ++c) acc[c] = 0.f;

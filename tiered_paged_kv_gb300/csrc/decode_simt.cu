@@ -64,6 +64,34 @@ __device__ __forceinline__ void bf16x8_to_float(uint4 w, float (&f)[8]) {
   f[7] = bf16_hi(w.w);
 }
 
+// The 8-bit record stores value codes channel-major ([256][64]); the CUDA-core
+// path reads them token-major, so the block transposes them in place once the
+// record has landed (each thread moves a 4-channel x 32-token block, with 4x4
+// byte transposes in registers).
+__device__ __forceinline__ void transpose_value_codes(uint8_t* vc) {
+  const int a = threadIdx.x & 63, b = threadIdx.x >> 6;
+  uint32_t w[4][8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint4* src = reinterpret_cast<const uint4*>(vc + (4 * a + i) * kPageTokens + 32 * b);
+    uint4 x = src[0], y = src[1];
+    w[i][0] = x.x; w[i][1] = x.y; w[i][2] = x.z; w[i][3] = x.w;
+    w[i][4] = y.x; w[i][5] = y.y; w[i][6] = y.z; w[i][7] = y.w;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int kw = 0; kw < 8; ++kw) {
+    uint32_t t01lo = __byte_perm(w[0][kw], w[1][kw], 0x5140), t01hi = __byte_perm(w[0][kw], w[1][kw], 0x7362);
+    uint32_t t23lo = __byte_perm(w[2][kw], w[3][kw], 0x5140), t23hi = __byte_perm(w[2][kw], w[3][kw], 0x7362);
+    uint32_t o[4] = {__byte_perm(t01lo, t23lo, 0x5410), __byte_perm(t01lo, t23lo, 0x7632),
+                     __byte_perm(t01hi, t23hi, 0x5410), __byte_perm(t01hi, t23hi, 0x7632)};
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      *reinterpret_cast<uint32_t*>(vc + (32 * b + 4 * kw + e) * kHeadDim + 4 * a) = o[e];
+  }
+  __syncthreads();
+}
+
 // Online-softmax state of one warp.
 struct SoftmaxState {
   float m_run;   // base-2 running max of row (lane & 7), integer valued (or -inf)
@@ -134,8 +162,13 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_simt_kernel(const __gri
   for (int j = 0; j < it.n; ++j) {
     const int s = j % kStages;
     const bool landed = mbar_wait(&S.full[s], (j / kStages) & 1, p.status);
-    if (landed && S.valid[s]) {
-      const uint8_t* slot = S.slot[s];
+    if (!__syncthreads_and(landed)) {  // the block agrees on whether a wait gave up
+      stop = j;
+      break;
+    }
+    if (S.valid[s]) {
+      uint8_t* slot = S.slot[s];
+      if (ui.tier == 1) transpose_value_codes(slot + kOffVc);
       if (ui.tier == 0) {
         // ---------------- exact tier: 32 BF16 tokens, 8 per warp
         const uint16_t* Ks = reinterpret_cast<const uint16_t*>(slot);
@@ -189,7 +222,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_simt_kernel(const __gri
       } else {
         // ---------------- 8-bit tier: one 64-token record, 16 tokens per warp
         const int8_t* kc = reinterpret_cast<const int8_t*>(slot + kOffKc);
-        const int8_t* vc = reinterpret_cast<const int8_t*>(slot + kOffVc);
+        const int8_t* vc = reinterpret_cast<const int8_t*>(slot + kOffVc);  // token-major after the transpose
         const float* ks = reinterpret_cast<const float*>(slot + kOffKsChan);
         const float* kr = reinterpret_cast<const float*>(slot + kOffKsTok);
         const float* vs = reinterpret_cast<const float*>(slot + kOffVsChan);
@@ -247,11 +280,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_simt_kernel(const __gri
         }
       }
     }
-    // every warp is done with stage s; the block agrees on whether a wait gave up
-    if (__syncthreads_or(!landed)) {
-      stop = j;
-      break;
-    }
+    __syncthreads();  // every warp is done with stage s
     if (tid == 0 && j + kStages < it.n) issue_item(p, ui, it, S, j + kStages, s);
   }
 
