@@ -80,3 +80,29 @@ def test_full_hybrid_128k(impl):
 def test_full_batched_16(impl):
     w = synth.batched_hybrid(seed=3)
     check_hybrid(w, impl, gpu_records=True, what="batched 16")
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+def test_back_to_back_launches_share_a_workspace(impl):
+    """Twenty launches queued without synchronising, one workspace: every result
+    must equal the first bit for bit (catches pipeline and ticket races)."""
+    t = __import__("torch")
+    w = synth.hybrid_128k(seed=2, n_tokens=32768, recent=1024)
+    d = DevWorkload(w, impl)
+    d.quantize_gpu()
+    nbytes = tpk.hybrid_workspace_bytes(d.shape, w.B)
+    ws = t.empty(nbytes, dtype=t.uint8, device="cuda")
+    tpk.workspace_init(ws, nbytes)
+    outs = []
+    for _ in range(20):
+        o = t.empty(w.B, w.H * w.G, 256, dtype=t.float32, device="cuda")
+        lse = t.empty(w.B, w.H * w.G, dtype=t.float32, device="cuda")
+        tpk.decode_hybrid_batched(d.shape, w.B, d.q, d.k, d.v, d.rec, d.pt, d.off, w.n_ex, d.pt8, d.off8, w.n8, o,
+                                  lse, ws, nbytes)
+        outs.append((o, lse))
+    t.cuda.synchronize()
+    st, flags = tpk.get_device_status(reset=True)
+    assert st == 0, flags
+    for o, lse in outs[1:]:
+        assert t.equal(o, outs[0][0]) and t.equal(lse, outs[0][1])
+    assert int(ws[:w.B * w.H * 4].sum().item()) == 0  # tickets left at zero

@@ -289,12 +289,22 @@ tpk_status tpk_decode_hybrid_batched(const tpk_shape* shape, int n_req, const vo
   }
   if (any_e && (!k_pool || !v_pool || !page_table)) return fail(TPK_ERR_INVALID, "null BF16 pool or page table");
   if (any_8 && (!rec_pool || !page_table8)) return fail(TPK_ERR_INVALID, "null 8-bit pool or page table");
-  // ---- split plan: about one resident wave of equal-byte units
-  const int target = num_sms() * blocks_per_sm(shape);
-  double chunk = std::max(total / target, 16384.0);
+  // ---- split plan: equal-byte units filling whole waves of resident blocks.
+  // Every non-empty (request, head, tier) needs at least one unit; the number of
+  // waves is the fewest that hold those, and the chunk size grows until the
+  // units fit in them (a unit more would start a wave of its own).
+  const int per_wave = num_sms() * blocks_per_sm(shape);
+  int min_units = 0;
+  for (int b = 0; b < n_req; ++b)
+    min_units += H * std::max(1, (n_exact_tokens[b] > 0) + (n_int8_pages[b] > 0));
+  if (min_units > kMaxUnits) return fail(TPK_ERR_UNSUPPORTED, "%d (request, head, tier) segments exceed %d units", min_units, kMaxUnits);
+  const int waves = (min_units + per_wave - 1) / per_wave;
+  const int target = std::min(kMaxUnits, waves * per_wave);
+  double chunk = std::max(total / target, 4096.0);
   DecodeParams p;
   fill_common(p, shape, q);
-  for (int attempt = 0; attempt < 40; ++attempt, chunk *= 1.25) {
+  bool planned = false;
+  for (int attempt = 0; attempt < 2000 && !planned; ++attempt, chunk *= 1.01) {
     int units = 0;
     bool fits = true;
     for (int b = 0; b < n_req; ++b) {
@@ -306,14 +316,14 @@ tpk_status tpk_decode_hybrid_batched(const tpk_shape* shape, int n_req, const vo
       if (se > 32767 || s8 > 32767) { fits = false; break; }
       p.req[b] = ReqPlan{units, req_page_off[b], 0, ne, req_page_off8[b], 0, n8, (int16_t)se, (int16_t)s8};
       units += H * (se + s8);
-      if (units > kMaxUnits) { fits = false; break; }
+      if (units > target) { fits = false; break; }
     }
     if (fits) {
       p.n_units = units;
-      break;
+      planned = true;
     }
-    if (attempt == 39) return fail(TPK_ERR_UNSUPPORTED, "could not plan within %d units", kMaxUnits);
   }
+  if (!planned) return fail(TPK_ERR_UNSUPPORTED, "could not plan within %d units", target);
   p.k_pool = static_cast<const uint16_t*>(k_pool);
   p.v_pool = static_cast<const uint16_t*>(v_pool);
   p.rec_pool = static_cast<const uint8_t*>(rec_pool);

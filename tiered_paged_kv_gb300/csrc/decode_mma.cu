@@ -1,40 +1,51 @@
-// Split-tier paged decode attention on the tensor cores (mma.sync).
+// Split-tier paged decode attention on the tensor cores (mma.sync, f16/bf16 with
+// FP32 accumulation).
 //
 // One thread block = one unit (a range of pages of one tier for one (request,
 // KV head)).  A producer warp streams the unit's items into a ring of 6
-// shared-memory slots; 4 consumer warps each take whole items (item j goes to
-// warp j % 4) and keep their own online-softmax state and FP32 output for the 8
-// query rows of the GQA group.  Thread (g, t) = (lane / 4, lane % 4) of a
-// consumer warp owns query row g and output channels 8n + 2t + {0, 1}.
+// shared-memory slots.  8 consumer warps work in 4 pairs: item j goes to pair
+// j % 4, and the two warps of the pair split the item's tokens in halves.  Each
+// warp keeps its own online-softmax state and FP32 output for the 8 query rows
+// of the GQA group; the epilogue merges the 8 warps.
 //
-// 8-bit tier ("SYCL", "Attention that reads 8-bit history"): both products run on
-// the integer tensor path (mma m16n8k32 s8 x s8 -> s32), reading the page's codes
-// straight from shared memory:
-//   QK  A = the folded query q'_c = q_c s_c (per page) quantised per row to a
-//         high and a low int8 plane (rows 0-7 and 8-15 of the 16-row tile:
-//         q' ~ sigma (hi + lo / 254)), B = the key codes; the per-token factor
-//         r_t is applied after the dot product;
-//   PV  A = the probabilities as int8 high/low planes (p ~ (hi + lo / 254) / 127),
-//         B = the value codes (channel-major, four consecutive tokens per word);
-//         the page's integer result is rescaled by the value scale u_c and added
-//         to the FP32 accumulator once per page.
-// Exact tier: BF16 half-pages (32 tokens) staged with a padded row pitch so
-// ldmatrix reads are conflict-free; QK on bf16 mma with q exact; P enters PV as
-// bf16 high/low planes (rows 0-7 / 8-15), giving about 16 bits of P.
+// Thread (g, t) = (lane / 4, lane % 4) of a consumer warp:
+//   - in QK (S = Q K^T, M = 16 query-row slots, N = 8 tokens per tile) it owns
+//     query row g and receives the scores of 2 tokens per tile;
+//   - in PV the output is computed transposed, O^T = V^T P^T (M = 16 channels,
+//     N = 8 query rows, K = tokens), so the accumulator is exactly the output:
+//     thread (g, t) holds channels 16m + g and 16m + g + 8 of rows 2t, 2t + 1.
+//
+// 8-bit tier ("SYCL", "Attention that reads 8-bit history").  The codes are exact
+// in f16, so both products run on f16 tensor cores:
+//   QK  A = the folded query q'_c = q_c s_c, split into f16 high and low planes
+//         (rows 0-7 and 8-15 of the tile), B = key codes; the per-token factor r_t
+//         is applied to the scores after the dot product;
+//   PV  A = value codes (channel-major, so four consecutive tokens of a channel
+//         are one word), B = the probabilities as f16 high and low planes (two
+//         products); each page's result is rescaled by its value scale u_c and
+//         added to the FP32 accumulator -- PV runs on raw codes and is rescaled
+//         per page.
+// The integer tensor path (s8 x s8) is not used: on this GPU it runs at about a
+// quarter of the f16 rate.
+//
+// Exact tier: BF16 half-pages (32 tokens) staged with a padded row pitch so that
+// ldmatrix reads are conflict-free; q is exact in bf16; P enters as bf16 high and
+// low planes.
 //
 // Online softmax ("SYCL", "Exact tricks and a two-owner decoder"): the running
 // maximum is an integer in base 2, every rescale is a power of two built by
-// exponent arithmetic, and the rescale is skipped when all eight rows' factors
-// are 1 (a warp vote).
+// exponent arithmetic, and the rescale is skipped when no row's maximum moved
+// (a warp vote).
+#include <cuda_fp16.h>
+
 #include "decode_common.cuh"
 
 namespace tpk {
 
-constexpr int kMmaCons = kDecWarps;              // consumer warps
-constexpr int kMmaThreads = (kMmaCons + 1) * 32;  // + one producer warp
+constexpr int kCons = 8;                       // consumer warps (4 pairs)
+constexpr int kMmaThreads = (kCons + 1) * 32;  // + one producer warp
 constexpr int kMmaSlots = 6;
 constexpr int kPad = 528;  // BF16 row pitch in shared memory (512 B + 16 B)
-constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23: float + kMagic rounds to an integer in the low bits
 constexpr unsigned kAll = 0xffffffffu;
 
 struct MmaSmem {
@@ -43,24 +54,29 @@ struct MmaSmem {
   uint64_t empty[kMmaSlots];
   int valid[kMmaSlots];
   int pt[kPtCache];
-  alignas(16) uint32_t q[kGroup][kHeadDim / 2];  // the unit's query rows (bf16 pairs)
-  float ep_m[kDecWarps][kGroup];
-  float ep_l[kDecWarps][kGroup];
+  alignas(16) uint32_t q[kGroup][kHeadDim / 2];  // the unit's query rows, bf16 pairs
+  alignas(16) float qs[kGroup][kHeadDim];        // the same rows as float, times a power of two
+  float ep_m[kCons][kGroup];
+  float ep_l[kCons][kGroup];
   int is_last;
   int abort;
 };
+static_assert(sizeof(MmaSmem) <= 227 * 1024, "shared memory per block");
 
 // ----------------------------------------------------------------- PTX
-__device__ __forceinline__ void mma_s8(int (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm("mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                        uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
       "{%0,%1,%2,%3};"
-      : "+r"(d[0]), "+r"(d[1]), "+r"(d[2]), "+r"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
 __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1) {
-  asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
       "{%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
@@ -80,15 +96,34 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], const void* p) {
                : "memory");
 }
 
-// low bytes of four words -> one word
-__device__ __forceinline__ uint32_t pack4(uint32_t b0, uint32_t b1, uint32_t b2, uint32_t b3) {
-  return __byte_perm(__byte_perm(b0, b1, 0x0040), __byte_perm(b2, b3, 0x0040), 0x5410);
+// (lo, hi) -> packed pair, lo in the low half
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
 }
-
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
+}
+__device__ __forceinline__ float f16_lo(uint32_t w) {
+  return __half2float(__ushort_as_half((unsigned short)(w & 0xffffu)));
+}
+__device__ __forceinline__ float f16_hi(uint32_t w) { return __half2float(__ushort_as_half((unsigned short)(w >> 16))); }
+
+// Four signed 8-bit codes -> two f16 pairs, exactly: each byte biased by 128
+// becomes the mantissa of 1024 (f16 0x6400 | u = 1024 + u), then 1152 is
+// subtracted.  lo = bytes 0, 1; hi = bytes 2, 3.
+__device__ __forceinline__ void codes_to_f16(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t x = w ^ 0x80808080u;
+  const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));  // 1152
+  uint32_t a = __byte_perm(x, 0x64646464u, 0x5140);
+  uint32_t b = __byte_perm(x, 0x64646464u, 0x5342);
+  __half2 ha = __hsub2(*reinterpret_cast<__half2*>(&a), bias);
+  __half2 hb = __hsub2(*reinterpret_cast<__half2*>(&b), bias);
+  lo = *reinterpret_cast<uint32_t*>(&ha);
+  hi = *reinterpret_cast<uint32_t*>(&hb);
 }
 
 // ----------------------------------------------------------------- producer
@@ -121,11 +156,12 @@ __device__ __forceinline__ void mma_issue(const DecodeParams& p, const UnitInfo&
   }
 }
 
-// Online-softmax update for one item: x[] are this thread's base-2 scores (row
-// g), -inf where masked.  Rescales O when the row maximum moved (skipped when
-// all rows keep their maximum) and turns x[] into weights.
+// Online-softmax update for this thread's base-2 scores x[] of query row g (-inf
+// where masked).  Rescales O (rows 2t, 2t + 1) when a row maximum moved and
+// turns x[] into weights.
 template <int N>
-__device__ __forceinline__ void softmax_update(float (&x)[N], float& m_run, float& l_run, float (&O)[32][2]) {
+__device__ __forceinline__ void softmax_update(float (&x)[N], float& m_run, float& l_run, float (&O)[16][4]) {
+  const int lane = threadIdx.x & 31, t = lane & 3;
   float mx = kNegInf;
 #pragma unroll
   for (int i = 0; i < N; ++i) mx = fmaxf(mx, x[i]);
@@ -134,10 +170,14 @@ __device__ __forceinline__ void softmax_update(float (&x)[N], float& m_run, floa
   const float m_new = (mx == kNegInf) ? m_run : fmaxf(m_run, ceilf(mx));
   const float alpha = (m_new == m_run) ? 1.f : (m_run == kNegInf ? 0.f : ldexpf(1.f, (int)(m_run - m_new)));
   if (!__all_sync(kAll, alpha == 1.f)) {
+    const float a0 = __shfl_sync(kAll, alpha, 8 * t);      // row 2t is held by lanes 4 * (2t) ..
+    const float a1 = __shfl_sync(kAll, alpha, 8 * t + 4);  // row 2t + 1
 #pragma unroll
-    for (int n = 0; n < 32; ++n) {
-      O[n][0] *= alpha;
-      O[n][1] *= alpha;
+    for (int m = 0; m < 16; ++m) {
+      O[m][0] *= a0;
+      O[m][1] *= a1;
+      O[m][2] *= a0;
+      O[m][3] *= a1;
     }
   }
   float l = l_run * alpha;
@@ -150,196 +190,144 @@ __device__ __forceinline__ void softmax_update(float (&x)[N], float& m_run, floa
   m_run = m_new;
 }
 
-// ---------------------------------------------------------------- 8-bit page
-__device__ __forceinline__ void process_int8_page(const uint8_t* rec, const uint32_t* qrow, float qscale,
-                                                  float& m_run, float& l_run, float (&O)[32][2]) {
+// ------------------------------------------------------- 8-bit half page
+// Warp half h (0 or 1) of a record: tokens 32h .. 32h + 31.  Within the half,
+// thread t owns tokens 8t .. 8t + 7: QK tile j column 2t + e is token
+// 8t + 2j + e, and PV k-step i covers tokens 8t + 4i + {0..3} of every thread t.
+__device__ __forceinline__ void process_int8_half(const uint8_t* rec, int h, const MmaSmem& S, float qk_scale,
+                                                  float& m_run, float& l_run, float (&O)[16][4]) {
   const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
   const float* ks = reinterpret_cast<const float*>(rec + kOffKsChan);
-  const float* kr = reinterpret_cast<const float*>(rec + kOffKsTok);
+  const float* kr = reinterpret_cast<const float*>(rec + kOffKsTok) + 32 * h;
   const float* vs = reinterpret_cast<const float*>(rec + kOffVsChan);
+  const uint8_t* kc = rec + kOffKc + 32 * h * kHeadDim;
+  const uint8_t* vc = rec + kOffVc + 32 * h;
+  const float* qrow = S.qs[g];
 
-  // q'_c = q_c s_c for this thread's 64 channels 64J + 16t + i of row g
-  float amax = 0.f;
+  // ---- QK: 4 tiles of 8 tokens, 16 k-steps of 16 channels.  k-step 4J + i uses
+  // channels 64J + 16t + 4i + {0, 1} (k = 2t, 2t+1) and + {2, 3} (k = 2t+8, 2t+9).
+  float acc[4][4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
 #pragma unroll
   for (int J = 0; J < 4; ++J) {
-    uint32_t qb[8];
-    {
-      uint4 a = *reinterpret_cast<const uint4*>(qrow + 32 * J + 8 * t);
-      uint4 b = *reinterpret_cast<const uint4*>(qrow + 32 * J + 8 * t + 4);
-      qb[0] = a.x; qb[1] = a.y; qb[2] = a.z; qb[3] = a.w; qb[4] = b.x; qb[5] = b.y; qb[6] = b.z; qb[7] = b.w;
-    }
+    uint4 kw[4];
 #pragma unroll
-    for (int v = 0; v < 4; ++v) {
-      float4 s4 = *reinterpret_cast<const float4*>(ks + 64 * J + 16 * t + 4 * v);
-      uint32_t w0 = qb[2 * v], w1 = qb[2 * v + 1];
-      amax = fmaxf(amax, fabsf(bf16_lo(w0) * s4.x));
-      amax = fmaxf(amax, fabsf(bf16_hi(w0) * s4.y));
-      amax = fmaxf(amax, fabsf(bf16_lo(w1) * s4.z));
-      amax = fmaxf(amax, fabsf(bf16_hi(w1) * s4.w));
-    }
-  }
-  amax = fmaxf(amax, __shfl_xor_sync(kAll, amax, 1));
-  amax = fmaxf(amax, __shfl_xor_sync(kAll, amax, 2));
-  const float inv = amax > 0.f ? 127.f / amax : 0.f;
-  const float arow = amax > 0.f ? qscale * (amax * (1.f / 127.f)) * (1.f / 254.f) : 0.f;
-
-  // int8 planes of q': A fragments for the 8 k-steps of 32 channels
-  uint32_t qa[8][4];
+    for (int j = 0; j < 4; ++j)
+      kw[j] = *reinterpret_cast<const uint4*>(kc + (8 * (g >> 1) + 2 * j + (g & 1)) * kHeadDim + 64 * J + 16 * t);
 #pragma unroll
-  for (int J = 0; J < 4; ++J) {
+    for (int i = 0; i < 4; ++i) {
+      const int ch = 64 * J + 16 * t + 4 * i;
+      const float4 s4 = *reinterpret_cast<const float4*>(ks + ch);
+      const float4 q4 = *reinterpret_cast<const float4*>(qrow + ch);
+      const float x0 = q4.x * s4.x, x1 = q4.y * s4.y, x2 = q4.z * s4.z, x3 = q4.w * s4.w;
+      const uint32_t h01 = pack_f16(x0, x1), h23 = pack_f16(x2, x3);
+      const uint32_t l01 = pack_f16(x0 - f16_lo(h01), x1 - f16_hi(h01));
+      const uint32_t l23 = pack_f16(x2 - f16_lo(h23), x3 - f16_hi(h23));
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      uint32_t hi[8], lo[8];
-      const uint4 qv = *reinterpret_cast<const uint4*>(qrow + 32 * J + 8 * t + 4 * h);
-      const uint32_t qh[4] = {qv.x, qv.y, qv.z, qv.w};
-#pragma unroll
-      for (int v = 0; v < 2; ++v) {
-        float4 s4 = *reinterpret_cast<const float4*>(ks + 64 * J + 16 * t + 8 * h + 4 * v);
-        uint32_t w0 = qh[2 * v], w1 = qh[2 * v + 1];
-        float x[4] = {bf16_lo(w0) * s4.x, bf16_hi(w0) * s4.y, bf16_lo(w1) * s4.z, bf16_hi(w1) * s4.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          float t1 = fmaf(x[e], inv, kMagic);
-          float hf = t1 - kMagic;
-          float res = fmaf(x[e], inv, -hf);
-          float t2 = fmaf(res, 254.f, kMagic);
-          hi[4 * v + e] = __float_as_uint(t1);
-          lo[4 * v + e] = __float_as_uint(t2);
-        }
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t w = i == 0 ? kw[j].x : i == 1 ? kw[j].y : i == 2 ? kw[j].z : kw[j].w;
+        uint32_t b0, b1;
+        codes_to_f16(w, b0, b1);
+        mma_f16(acc[j], h01, l01, h23, l23, b0, b1);
       }
-      qa[2 * J + h][0] = pack4(hi[0], hi[1], hi[2], hi[3]);
-      qa[2 * J + h][1] = pack4(lo[0], lo[1], lo[2], lo[3]);
-      qa[2 * J + h][2] = pack4(hi[4], hi[5], hi[6], hi[7]);
-      qa[2 * J + h][3] = pack4(lo[4], lo[5], lo[6], lo[7]);
     }
   }
-
-  // QK: n-tile j holds keys 16 (n / 2) + 2 j + (n & 1) in column n, so thread t
-  // receives the scores of keys 16 t + 2 j + {0, 1}.
-  float x[16];
+  // scores (base 2): high + low planes, times r_t of each token
+  float x[8];
+  {
+    const float4 r0 = *reinterpret_cast<const float4*>(kr + 8 * t);
+    const float4 r1 = *reinterpret_cast<const float4*>(kr + 8 * t + 4);
+    const float rr[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const uint8_t* krow = rec + kOffKc + (16 * (g >> 1) + 2 * j + (g & 1)) * kHeadDim + 16 * t;
-    int c[4] = {0, 0, 0, 0};
-#pragma unroll
-    for (int J = 0; J < 4; ++J) {
-      uint4 w = *reinterpret_cast<const uint4*>(krow + 64 * J);
-      mma_s8(c, qa[2 * J], w.x, w.y);
-      mma_s8(c, qa[2 * J + 1], w.z, w.w);
+    for (int j = 0; j < 4; ++j) {
+      x[2 * j] = (acc[j][0] + acc[j][2]) * qk_scale * rr[2 * j];
+      x[2 * j + 1] = (acc[j][1] + acc[j][3]) * qk_scale * rr[2 * j + 1];
     }
-    x[2 * j] = (float)(c[0] * 254 + c[2]);
-    x[2 * j + 1] = (float)(c[1] * 254 + c[3]);
   }
-  // per-token factor r_t after the dot product (keys 16t .. 16t+15 of this thread)
+  softmax_update<8>(x, m_run, l_run, O);
+  // P^T as f16 high / low planes for the two k-steps
+  uint32_t ph[2][2], pl[2][2];
 #pragma unroll
-  for (int v = 0; v < 4; ++v) {
-    float4 r4 = *reinterpret_cast<const float4*>(kr + 16 * t + 4 * v);
-    x[4 * v] *= arow * r4.x;
-    x[4 * v + 1] *= arow * r4.y;
-    x[4 * v + 2] *= arow * r4.z;
-    x[4 * v + 3] *= arow * r4.w;
-  }
-  softmax_update<16>(x, m_run, l_run, O);
-
-  // P as int8 planes: k-step s covers keys 16 t + 8 s + (0..7) of thread t
-  uint32_t pa[2][4];
+  for (int i = 0; i < 2; ++i)
 #pragma unroll
-  for (int s = 0; s < 2; ++s) {
-    uint32_t hi[8], lo[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      float v = 127.f * x[8 * s + e];
-      float t1 = v + kMagic;
-      float hf = t1 - kMagic;
-      float t2 = fmaf(v - hf, 254.f, kMagic);
-      hi[e] = __float_as_uint(t1);
-      lo[e] = __float_as_uint(t2);
+    for (int hh = 0; hh < 2; ++hh) {
+      const float p0 = x[2 * (2 * i + hh)], p1 = x[2 * (2 * i + hh) + 1];
+      const uint32_t hi = pack_f16(p0, p1);
+      ph[i][hh] = hi;
+      pl[i][hh] = pack_f16(p0 - f16_lo(hi), p1 - f16_hi(hi));
     }
-    pa[s][0] = pack4(hi[0], hi[1], hi[2], hi[3]);
-    pa[s][1] = pack4(lo[0], lo[1], lo[2], lo[3]);
-    pa[s][2] = pack4(hi[4], hi[5], hi[6], hi[7]);
-    pa[s][3] = pack4(lo[4], lo[5], lo[6], lo[7]);
-  }
-
-  // PV: n-tile n covers channels 8n .. 8n+7; column g reads channel 8n + g's
-  // 16 codes of tokens 16t .. 16t+15 (one 16-byte word, both k-steps).
+  // ---- PV: 16 channel tiles; each page result times u_c into the accumulator
 #pragma unroll
-  for (int n = 0; n < 32; ++n) {
-    uint4 w = *reinterpret_cast<const uint4*>(rec + kOffVc + (8 * n + g) * kPageTokens + 16 * t);
-    int d[4] = {0, 0, 0, 0};
-    mma_s8(d, pa[0], w.x, w.y);
-    mma_s8(d, pa[1], w.z, w.w);
-    float2 u2 = *reinterpret_cast<const float2*>(vs + 8 * n + 2 * t);
-    O[n][0] = fmaf(u2.x, (float)(d[0] * 254 + d[2]), O[n][0]);
-    O[n][1] = fmaf(u2.y, (float)(d[1] * 254 + d[3]), O[n][1]);
+  for (int m = 0; m < 16; ++m) {
+    const uint2 va = *reinterpret_cast<const uint2*>(vc + (16 * m + g) * kPageTokens + 8 * t);
+    const uint2 vb = *reinterpret_cast<const uint2*>(vc + (16 * m + g + 8) * kPageTokens + 8 * t);
+    float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      uint32_t a0, a2, a1, a3;
+      codes_to_f16(i == 0 ? va.x : va.y, a0, a2);
+      codes_to_f16(i == 0 ? vb.x : vb.y, a1, a3);
+      mma_f16(c, a0, a1, a2, a3, ph[i][0], ph[i][1]);
+      mma_f16(c, a0, a1, a2, a3, pl[i][0], pl[i][1]);
+    }
+    const float ua = vs[16 * m + g], ub = vs[16 * m + g + 8];
+    O[m][0] = fmaf(ua, c[0], O[m][0]);
+    O[m][1] = fmaf(ua, c[1], O[m][1]);
+    O[m][2] = fmaf(ub, c[2], O[m][2]);
+    O[m][3] = fmaf(ub, c[3], O[m][3]);
   }
 }
 
-// -------------------------------------------------------- BF16 half-page
-__device__ __forceinline__ void process_bf16_half(uint8_t* slot, int tok0, int tb, int te, const uint32_t* qrow,
-                                                  float qscale, float& m_run, float& l_run, float (&O)[32][2]) {
-  const int lane = threadIdx.x & 31, t = lane & 3;
-  const uint8_t* K = slot;
-  uint8_t* V = slot + 32 * kPad;
-  // zero the value rows of tokens outside the range (they may hold anything)
-  if (tok0 < tb || tok0 + 32 > te) {
-    for (int k = 0; k < 32; ++k) {
-      int tok = tok0 + k;
+// ------------------------------------------------------ BF16 quarter page
+// Warp half h of a BF16 half-page item: tokens 16h .. 16h + 15 of the item.
+__device__ __forceinline__ void process_bf16_quarter(uint8_t* slot, int h, int tok0, int tb, int te,
+                                                     const MmaSmem& S, float qscale, float& m_run, float& l_run,
+                                                     float (&O)[16][4]) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+  const uint8_t* K = slot + 16 * h * kPad;
+  uint8_t* V = slot + (32 + 16 * h) * kPad;
+  const int base = tok0 + 16 * h;
+  if (base < tb || base + 16 > te) {  // zero value rows of tokens outside the range
+    for (int k = 0; k < 16; ++k) {
+      const int tok = base + k;
       if (tok < tb || tok >= te) *reinterpret_cast<uint4*>(V + k * kPad + 16 * lane) = make_uint4(0, 0, 0, 0);
     }
     __syncwarp();
   }
-  // QK: n-tile j = keys 8j .. 8j+7
-  float x[8];
+  const uint32_t* qrow = S.q[g];
+  float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll 4
+  for (int kk = 0; kk < 8; ++kk) {
+    const uint32_t qa0 = qrow[16 * kk + t], qa1 = qrow[16 * kk + 4 + t];
+    const uint32_t qa2 = qrow[16 * kk + 8 + t], qa3 = qrow[16 * kk + 12 + t];
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    float c[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 2
-    for (int kk = 0; kk < 8; ++kk) {
-      // A: q[g][16 ks + 2t, +1] and q[g][16 ks + 8 + 2t, +1] for k-steps ks = 2kk, 2kk+1
-      const uint32_t qa0 = qrow[16 * kk + t], qa1 = qrow[16 * kk + 4 + t];
-      const uint32_t qa2 = qrow[16 * kk + 8 + t], qa3 = qrow[16 * kk + 12 + t];
-      uint32_t m[4];
-      ldsm_x4(m, K + (8 * j + (lane & 7)) * kPad + (4 * kk + (lane >> 3)) * 16);
-      mma_bf16(c, qa0, 0u, qa1, 0u, m[0], m[1]);
-      mma_bf16(c, qa2, 0u, qa3, 0u, m[2], m[3]);
+    for (int j = 0; j < 2; ++j) {
+      uint32_t m4[4];
+      ldsm_x4(m4, K + (8 * j + (lane & 7)) * kPad + (4 * kk + (lane >> 3)) * 16);
+      mma_bf16(acc[j], qa0, 0u, qa1, 0u, m4[0], m4[1]);
+      mma_bf16(acc[j], qa2, 0u, qa3, 0u, m4[2], m4[3]);
     }
+  }
+  float x[4];
+#pragma unroll
+  for (int j = 0; j < 2; ++j)
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
-      int tok = tok0 + 8 * j + 2 * t + e;
-      x[2 * j + e] = (tok >= tb && tok < te) ? c[e] * qscale : kNegInf;
+      const int tok = base + 8 * j + 2 * t + e;
+      x[2 * j + e] = (tok >= tb && tok < te) ? acc[j][e] * qscale : kNegInf;
     }
-  }
-  softmax_update<8>(x, m_run, l_run, O);
-  // P as bf16 high/low planes; k-step ks = keys 16 ks .. 16 ks + 15
-  uint32_t pa[2][4];
+  softmax_update<4>(x, m_run, l_run, O);
+  const uint32_t ph0 = pack_bf16(x[0], x[1]), ph1 = pack_bf16(x[2], x[3]);
+  const uint32_t pl0 = pack_bf16(x[0] - bf16_lo(ph0), x[1] - bf16_hi(ph0));
+  const uint32_t pl1 = pack_bf16(x[2] - bf16_lo(ph1), x[3] - bf16_hi(ph1));
+  const int i = lane >> 3;
 #pragma unroll
-  for (int ks = 0; ks < 2; ++ks) {
-#pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      float p0 = x[2 * (2 * ks + hh)], p1 = x[2 * (2 * ks + hh) + 1];
-      uint32_t hi = pack_bf16(p0, p1);
-      float r0 = p0 - bf16_lo(hi), r1 = p1 - bf16_hi(hi);
-      pa[ks][2 * hh] = hi;
-      pa[ks][2 * hh + 1] = pack_bf16(r0, r1);
-    }
-  }
-  // PV: pairs of n-tiles (16 channels) per ldmatrix.x4.trans
-#pragma unroll
-  for (int np = 0; np < 16; ++np) {
-    float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int ks = 0; ks < 2; ++ks) {
-      const int i = lane >> 3;
-      uint32_t m[4];
-      ldsm_x4_t(m, V + (16 * ks + (i & 1) * 8 + (lane & 7)) * kPad + (2 * np + (i >> 1)) * 16);
-      mma_bf16(d0, pa[ks][0], pa[ks][1], pa[ks][2], pa[ks][3], m[0], m[1]);
-      mma_bf16(d1, pa[ks][0], pa[ks][1], pa[ks][2], pa[ks][3], m[2], m[3]);
-    }
-    O[2 * np][0] += d0[0] + d0[2];
-    O[2 * np][1] += d0[1] + d0[3];
-    O[2 * np + 1][0] += d1[0] + d1[2];
-    O[2 * np + 1][1] += d1[1] + d1[3];
+  for (int m = 0; m < 16; ++m) {
+    uint32_t a[4];
+    ldsm_x4_t(a, V + ((i >> 1) * 8 + (lane & 7)) * kPad + (2 * m + (i & 1)) * 16);
+    mma_bf16(O[m], a[0], a[1], a[2], a[3], ph0, ph1);
+    mma_bf16(O[m], a[0], a[1], a[2], a[3], pl0, pl1);
   }
 }
 
@@ -355,7 +343,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) decode_mma_kernel(const __grid
   if (tid == 0) {
     for (int s = 0; s < kMmaSlots; ++s) {
       mbar_init(&S.full[s], 1);
-      mbar_init(&S.empty[s], 1);
+      mbar_init(&S.empty[s], 2);
     }
     S.abort = 0;
     fence_mbar_init();
@@ -366,14 +354,38 @@ __global__ void __launch_bounds__(kMmaThreads, 1) decode_mma_kernel(const __grid
     for (int i = tid; i < kGroup * kHeadDim / 2; i += blockDim.x) (&S.q[0][0])[i] = __ldg(q32 + i);
   }
   __syncthreads();
+  // Float copy of q times 2^-(e+1), e the exponent of the row's max |q|: with
+  // s_c <= 2^14 every q'_c = q_c s_c of this row then stays below 2^13, inside
+  // f16 range, whatever the page.
+  float qk_scale = p.qscale;
+  if (warp < kCons) {
+    float qmax = 0.f;
+    for (int c = t; c < kHeadDim / 2; c += 4) {
+      const uint32_t w = S.q[g][c];
+      qmax = fmaxf(qmax, fmaxf(fabsf(bf16_lo(w)), fabsf(bf16_hi(w))));
+    }
+    qmax = fmaxf(qmax, __shfl_xor_sync(kAll, qmax, 1));
+    qmax = fmaxf(qmax, __shfl_xor_sync(kAll, qmax, 2));
+    int e = 0;
+    frexpf(qmax, &e);
+    const float sc = qmax > 0.f ? ldexpf(1.f, -(e + 1)) : 1.f;
+    qk_scale = p.qscale / sc;
+    if (warp == 0)
+      for (int c = t; c < kHeadDim / 2; c += 4) {
+        const uint32_t w = S.q[g][c];
+        S.qs[g][2 * c] = bf16_lo(w) * sc;
+        S.qs[g][2 * c + 1] = bf16_hi(w) * sc;
+      }
+  }
+  __syncthreads();
 
   int issued = 0;
-  float O[32][2];
+  float O[16][4];
 #pragma unroll
-  for (int n = 0; n < 32; ++n) O[n][0] = O[n][1] = 0.f;
+  for (int m = 0; m < 16; ++m) O[m][0] = O[m][1] = O[m][2] = O[m][3] = 0.f;
   float m_run = kNegInf, l_run = 0.f;
 
-  if (warp == kMmaCons) {
+  if (warp == kCons) {
     // ---------------------------------------------------------- producer
     if (lane == 0) {
       for (int j = 0; j < it.n; ++j) {
@@ -388,47 +400,45 @@ __global__ void __launch_bounds__(kMmaThreads, 1) decode_mma_kernel(const __grid
     }
   } else {
     // ---------------------------------------------------------- consumers
-    if (ui.tier == 1) {
-      const uint32_t* qrow_s = S.q[g];
-      for (int j = warp; j < it.n; j += kMmaCons) {
-        const int s = j % kMmaSlots;
-        if (!mbar_wait(&S.full[s], (j / kMmaSlots) & 1, p.status)) {
-          S.abort = 1;
-          break;
-        }
-        if (S.valid[s]) process_int8_page(S.slot[s], qrow_s, p.qscale, m_run, l_run, O);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&S.empty[s]);
+    const int pair = warp >> 1, half = warp & 1;
+    for (int j = pair; j < it.n; j += kCons / 2) {
+      const int s = j % kMmaSlots;
+      // Slot s last held item j - 6, which another pair may still own.  A parity
+      // wait on full[s] would then match that item's phase, so first wait for its
+      // release (empty[s] is at most one phase behind here: item j - 12 belonged
+      // to this pair), after which full[s]'s pending phase is item j's.
+      if (j >= kMmaSlots && !mbar_wait(&S.empty[s], ((j / kMmaSlots) - 1) & 1, p.status)) {
+        S.abort = 1;
+        break;
       }
-    } else {
-      const uint32_t* qrow_s = S.q[g];
-      for (int j = warp; j < it.n; j += kMmaCons) {
-        const int s = j % kMmaSlots;
-        if (!mbar_wait(&S.full[s], (j / kMmaSlots) & 1, p.status)) {
-          S.abort = 1;
-          break;
-        }
-        if (S.valid[s])
-          process_bf16_half(S.slot[s], (it.first + j) * 32, ui.tok_begin, ui.tok_end, qrow_s, p.qscale, m_run,
-                            l_run, O);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&S.empty[s]);
+      if (!mbar_wait(&S.full[s], (j / kMmaSlots) & 1, p.status)) {
+        S.abort = 1;
+        break;
       }
+      if (S.valid[s]) {
+        if (ui.tier == 1)
+          process_int8_half(S.slot[s], half, S, qk_scale, m_run, l_run, O);
+        else
+          process_bf16_quarter(S.slot[s], half, (it.first + j) * 32, ui.tok_begin, ui.tok_end, S, p.qscale, m_run,
+                               l_run, O);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.empty[s]);
     }
   }
   __syncthreads();
   if (S.abort) {
     // A wait gave up: let the copies this block issued land (bounded), then leave
     // without a result; the status word reports the timeout.
-    if (warp == kMmaCons && lane == 0)
+    if (warp == kCons && lane == 0)
       for (int j = max(0, issued - kMmaSlots); j < issued; ++j)
         mbar_wait(&S.full[j % kMmaSlots], (j / kMmaSlots) & 1, p.status);
     __syncthreads();
     return;
   }
-  // ---- per-warp states into shared memory (stages are idle now)
-  float* ep_o = reinterpret_cast<float*>(S.slot[0]);
-  if (warp < kMmaCons) {
+  // ---- per-warp states into shared memory (the stages are idle now)
+  float* ep_o = reinterpret_cast<float*>(S.slot[0]);  // [8 warps][8 rows][256], spans slots 0-1
+  if (warp < kCons) {
     float L = l_run;
     L += __shfl_xor_sync(kAll, L, 1);
     L += __shfl_xor_sync(kAll, L, 2);
@@ -436,14 +446,17 @@ __global__ void __launch_bounds__(kMmaThreads, 1) decode_mma_kernel(const __grid
       S.ep_m[warp][g] = m_run;
       S.ep_l[warp][g] = L;
     }
-    const float osc = ui.tier == 1 ? 1.f / (127.f * 254.f) : 1.f;
-    float* dst = ep_o + (warp * kGroup + g) * kHeadDim + 2 * t;
+    float* base = ep_o + warp * kGroup * kHeadDim;
 #pragma unroll
-    for (int n = 0; n < 32; ++n)
-      *reinterpret_cast<float2*>(dst + 8 * n) = make_float2(O[n][0] * osc, O[n][1] * osc);
+    for (int m = 0; m < 16; ++m) {
+      base[(2 * t) * kHeadDim + 16 * m + g] = O[m][0];
+      base[(2 * t + 1) * kHeadDim + 16 * m + g] = O[m][1];
+      base[(2 * t) * kHeadDim + 16 * m + g + 8] = O[m][2];
+      base[(2 * t + 1) * kHeadDim + 16 * m + g + 8] = O[m][3];
+    }
   }
   __syncthreads();
-  write_and_fold(p, ui, S, ep_o);
+  write_and_fold<kCons>(p, ui, S, ep_o, reinterpret_cast<float*>(S.slot[2]), kSlotBytes / 4);
 }
 
 cudaError_t launch_decode_mma(const DecodeParams& p, cudaStream_t stream) {
