@@ -76,7 +76,9 @@ typedef struct {
   int page_tokens;   /* must be 64 */
   float sm_scale;    /* softmax scale; 0 selects 1/sqrt(head_dim) (the only value supported) */
   int impl;          /* TPK_IMPL_* */
-  int64_t kv_slots;  /* slots in the BF16 pools (bounds for page_table entries); 0 = unchecked */
+  int64_t kv_slots;  /* slots in the BF16 pools (bounds for page_table entries); 0 = unchecked,
+                        allowed only with TPK_IMPL_SIMT: the tensor-core kernel reads the BF16
+                        pools through TMA tensor maps that need the pool size */
   int64_t rec_slots; /* slots in the 8-bit pool (bounds for page_table8 entries); 0 = unchecked */
 } tpk_shape;
 
@@ -156,21 +158,22 @@ tpk_status tpk_merge_lse(int n_parts, int rows, int head_dim, const float* o_par
                          float* o_acc, float* lse_acc, tpk_stream_t stream);
 
 /*
- * Workspace bytes tpk_decode_hybrid_batched needs for n_req requests (an upper
- * bound independent of the lengths).  The workspace must be zeroed once before
- * first use (tpk_workspace_init); the kernels leave it zeroed again.
+ * Workspace bytes tpk_decode_hybrid_batched needs (partial results of the split
+ * units, about 16 MiB; independent of the lengths).  The contents need no
+ * initialisation.  tpk_workspace_init zero-fills a buffer (a convenience only).
  */
 size_t tpk_hybrid_workspace_bytes(const tpk_shape* shape, int n_req);
 tpk_status tpk_workspace_init(void* ws, size_t ws_bytes, tpk_stream_t stream);
 
 /*
- * Multi-request hybrid decode in one launch ("SYCL", section "Exact tricks and a
- * two-owner decoder": requests in one launch, each with its own page metadata and
- * its own merge accumulator).  For each request b and KV head h: the exact partial
- * over its BF16 tokens [0, n_exact_tokens[b]) and the 8-bit partial over its pages
- * [0, n_int8_pages[b]), split across thread blocks and folded, in a fixed order,
- * into o[b] (dev float32 [n_req][H*G][256]) and lse[b] (dev float32 [n_req][H*G]),
- * which are overwritten.
+ * Multi-request hybrid decode ("SYCL", section "Exact tricks and a two-owner
+ * decoder": requests in one launch, each with its own page metadata and its own
+ * merge accumulator).  For each request b and KV head h: the exact partial over
+ * its BF16 tokens [0, n_exact_tokens[b]) and the 8-bit partial over its pages
+ * [0, n_int8_pages[b]), split across thread blocks of one decode launch, then
+ * folded, in a fixed order, by a second small launch into o[b] (dev float32
+ * [n_req][H*G][256]) and lse[b] (dev float32 [n_req][H*G]), which are
+ * overwritten.
  *   q           dev bf16 [n_req][H*G][256]
  *   page_table  dev int32, flat; request b's exact-tier slots start at
  *               req_page_off[b] (host int32 [n_req + 1])
@@ -178,9 +181,10 @@ tpk_status tpk_workspace_init(void* ws, size_t ws_bytes, tpk_stream_t stream);
  *               (host int32 [n_req + 1])
  *   n_exact_tokens, n_int8_pages: host int32 [n_req]
  * The host arrays are read during the call (the split plan is built on the host
- * and passed by value to the kernel, so the call can be captured in a CUDA graph).
- * ws: dev workspace of at least tpk_hybrid_workspace_bytes(shape, n_req) bytes,
- * zeroed before first use.  Calls sharing a workspace must not overlap on the GPU.
+ * and passed by value to the kernels, so the call can be captured in a CUDA graph
+ * once each device has seen one uncaptured call).
+ * ws: dev workspace of at least tpk_hybrid_workspace_bytes(shape, n_req) bytes.
+ * Calls sharing a workspace must not overlap on the GPU.
  */
 tpk_status tpk_decode_hybrid_batched(const tpk_shape* shape, int n_req, const void* q, const void* k_pool,
                                      const void* v_pool, const void* rec_pool, const int32_t* page_table,

@@ -85,7 +85,7 @@ def test_full_batched_16(impl):
 @pytest.mark.parametrize("impl", IMPLS)
 def test_back_to_back_launches_share_a_workspace(impl):
     """Twenty launches queued without synchronising, one workspace: every result
-    must equal the first bit for bit (catches pipeline and ticket races)."""
+    must equal the first bit for bit (catches pipeline and workspace races)."""
     t = __import__("torch")
     w = synth.hybrid_128k(seed=2, n_tokens=32768, recent=1024)
     d = DevWorkload(w, impl)
@@ -105,4 +105,3 @@ def test_back_to_back_launches_share_a_workspace(impl):
     assert st == 0, flags
     for o, lse in outs[1:]:
         assert t.equal(o, outs[0][0]) and t.equal(lse, outs[0][1])
-    assert int(ws[:w.B * w.H * 4].sum().item()) == 0  # tickets left at zero

@@ -20,6 +20,7 @@ int decode_mma_blocks_per_sm();
 cudaError_t launch_merge(int n_parts, int rows, const float* o_parts, const float* lse_parts, float* o_acc,
                          float* lse_acc, cudaStream_t stream);
 cudaError_t launch_quantize(const QuantParams& p, int n_pages, cudaStream_t stream);
+cudaError_t launch_fold(const DecodeParams& p, cudaStream_t stream);
 }  // namespace tpk
 
 using namespace tpk;
@@ -28,7 +29,7 @@ __device__ int g_tpk_status;
 
 namespace {
 
-constexpr int kMaxUnits = 4096;       // partial slots in the hybrid workspace
+constexpr int kMaxUnits = 2048;       // partial slots in the hybrid workspace (256 requests x 4 heads x 2 tiers)
 constexpr int kMaxSplits = 4096;      // primitive calls
 constexpr int kMaxHeads = 1024;
 
@@ -77,10 +78,16 @@ int* status_ptr() {
 }
 
 int num_sms() {
-  int dev = 0, n = 0;
+  static int cached[64] = {0};
+  int dev = 0;
   cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-  return n > 0 ? n : 1;
+  if (dev < 0 || dev >= 64) dev = 0;
+  if (!cached[dev]) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cached[dev] = n > 0 ? n : 1;
+  }
+  return cached[dev];
 }
 
 void fill_common(DecodeParams& p, const tpk_shape* s, const void* q) {
@@ -93,6 +100,51 @@ void fill_common(DecodeParams& p, const tpk_shape* s, const void* q) {
 }
 
 bool use_simt(const tpk_shape* s) { return s->impl == TPK_IMPL_SIMT; }
+
+// cuTensorMapEncodeTiled, fetched from the driver at run time (no link-time
+// dependency on libcuda).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  }
+  return fn;
+}
+
+// The tensor-core kernel reads BF16 half-pages with TMA: each pool is a 2-D
+// tensor of [kv_slots * H * 64 rows][256 bf16] with 32-row x 64-column boxes and
+// the 128-byte swizzle.
+tpk_status make_pool_maps(DecodeParams& p, const tpk_shape* s, const void* k_pool, const void* v_pool) {
+  if (use_simt(s)) return TPK_OK;
+  if (s->kv_slots <= 0)
+    return fail(TPK_ERR_INVALID, "kv_slots must be set: the tensor-core kernel reads the BF16 pools with TMA");
+  const uint64_t rows = (uint64_t)s->kv_slots * s->kv_heads * kPageTokens;
+  if (rows >= (1ull << 31)) return fail(TPK_ERR_UNSUPPORTED, "BF16 pool too large for one tensor map");
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return fail(TPK_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)kHeadDim * 2};
+  cuuint32_t box[2] = {64, 32};
+  cuuint32_t estr[2] = {1, 1};
+  const void* pools[2] = {k_pool, v_pool};
+  CUtensorMap* maps[2] = {&p.kmap, &p.vmap};
+  for (int i = 0; i < 2; ++i) {
+    CUresult r = fn(maps[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(pools[i]), dims, strides, box,
+                    estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(TPK_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  }
+  return TPK_OK;
+}
 
 int blocks_per_sm(const tpk_shape* s) {
   static int simt = 0, mma = 0;
@@ -195,6 +247,10 @@ tpk_status tpk_decode_attn_exact(const tpk_shape* shape, const void* q, const vo
   if (num_splits > 32767) return fail(TPK_ERR_INVALID, "num_splits too large");
   p.req[0].splits_e = (int16_t)num_splits;
   p.n_units = num_splits * shape->kv_heads;
+  if (tok_end > tok_begin) {
+    st = make_pool_maps(p, shape, k_pool, v_pool);
+    if (st != TPK_OK) return st;
+  }
   return launch_decode(shape, p, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -242,8 +298,7 @@ static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 size_t tpk_hybrid_workspace_bytes(const tpk_shape* shape, int n_req) {
   if (!shape || n_req < 1 || shape->kv_heads < 1) return 0;
-  return align256((size_t)n_req * shape->kv_heads * sizeof(int)) + align256((size_t)kMaxUnits * kGroup * 4) +
-         (size_t)kMaxUnits * kGroup * kHeadDim * 4;
+  return align256((size_t)kMaxUnits * kGroup * 4) + (size_t)kMaxUnits * kGroup * kHeadDim * 4;
 }
 
 tpk_status tpk_workspace_init(void* ws, size_t ws_bytes, tpk_stream_t stream) {
@@ -330,8 +385,6 @@ tpk_status tpk_decode_hybrid_batched(const tpk_shape* shape, int n_req, const vo
   p.page_table = page_table;
   p.page_table8 = page_table8;
   uint8_t* w = static_cast<uint8_t*>(ws);
-  p.tickets = reinterpret_cast<int*>(w);
-  w += align256((size_t)n_req * H * sizeof(int));
   p.part_lse = reinterpret_cast<float*>(w);
   w += align256((size_t)kMaxUnits * kGroup * 4);
   p.part_o = reinterpret_cast<float*>(w);
@@ -341,7 +394,19 @@ tpk_status tpk_decode_hybrid_batched(const tpk_shape* shape, int n_req, const vo
   p.n_req = n_req;
   p.status = status_ptr();
   if (!p.status) return fail(TPK_ERR_CUDA, "cannot resolve the device status word");
-  return launch_decode(shape, p, reinterpret_cast<cudaStream_t>(stream));
+  if (any_e) {
+    st = make_pool_maps(p, shape, k_pool, v_pool);
+    if (st != TPK_OK) return st;
+  }
+  st = launch_decode(shape, p, reinterpret_cast<cudaStream_t>(stream));
+  if (st != TPK_OK) return st;
+  bool any_split = false;
+  for (int b = 0; b < n_req; ++b) any_split |= p.req[b].splits_e + p.req[b].splits_8 > 1;
+  if (any_split) {
+    cudaError_t e = launch_fold(p, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "fold launch");
+  }
+  return TPK_OK;
 }
 
 tpk_status tpk_get_device_status(int* flags, int reset, tpk_stream_t stream) {

@@ -2,8 +2,10 @@
 // mbarrier and bulk-copy (cp.async.bulk) wrappers written as inline PTX for
 // sm_103a, and the per-launch split plan passed by value to the decode kernels.
 #pragma once
-#include <cstdint>
+#include <cuda.h>  // CUtensorMap (type only; the encode entry point is fetched at run time)
 #include <cuda_runtime.h>
+
+#include <cstdint>
 
 namespace tpk {
 
@@ -46,6 +48,8 @@ constexpr int kMaxReqPerLaunch = 256;
 enum : int { kModePrimitive = 0, kModeFold = 1 };
 
 struct DecodeParams {
+  CUtensorMap kmap;         // BF16 pools as 2-D tensors [slot * H * 64][256], 32 x 64 boxes,
+  CUtensorMap vmap;         // 128-byte swizzle (tensor-core kernel only)
   const uint16_t* q;        // bf16 [n_req][H*G][256]
   const uint16_t* k_pool;   // bf16 [slot][H][64][256]
   const uint16_t* v_pool;
@@ -54,11 +58,10 @@ struct DecodeParams {
   const int32_t* page_table8;
   int64_t kv_slots;         // 0 = unchecked
   int64_t rec_slots;
-  float* part_o;            // primitive: o_part [split][H*G][256]; fold: workspace [unit][G][256]
+  float* part_o;            // primitive: o_part [split][H*G][256]; multi-request: workspace [unit][G][256]
   float* part_lse;
-  float* out_o;             // fold: final o [n_req][H*G][256]
+  float* out_o;             // multi-request: final o [n_req][H*G][256]
   float* out_lse;
-  int* tickets;             // fold: [n_req][H], zero between launches
   int* status;              // device status word
   float qscale;             // sm_scale * log2(e)
   int H;
@@ -188,6 +191,16 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* s
       return false;
     }
   }
+}
+
+// 2-D tensor copy global -> shared (TMA), completion counted on an mbarrier.
+// x is the innermost coordinate (elements), y the row.
+__device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          smem_u32(smem_dst)),
+      "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
 }
 
 // 1-D bulk copy global -> shared, completion counted on an mbarrier (bytes and

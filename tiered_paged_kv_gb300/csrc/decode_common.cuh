@@ -104,14 +104,14 @@ __device__ __forceinline__ void issue_item(const DecodeParams& p, const UnitInfo
 // ep_l[w][r] (sum of weights) and its unnormalised accumulator in
 // ep_o[w][r][256] (shared memory aliasing the idle stages).
 //
-// Threads 0..127 combine the NW warps into the unit's partial (o, lse)
-// and write it; in fold mode the last unit of a (request, KV head) then merges
-// all of that head's partials in unit order (a fixed order, so the result does
-// not depend on which unit finished last).  `scratch` is idle shared memory.  Every thread of the block must
+// Threads 0..127 combine the NW warps into the unit's partial (o, lse) and
+// write it: to the caller's partial arrays (primitive calls), straight to the
+// output when the head has a single unit, or to the workspace, where the fold
+// kernel merges the head's partials.  Every thread of the block must
 // call this (it contains block barriers); threads >= 128 only take part in them.
 template <int NW, typename Smem>
 __device__ __forceinline__ void write_and_fold(const DecodeParams& p, const UnitInfo& ui, Smem& S,
-                                               const float* ep_o, float* scratch, int scratch_floats) {
+                                               const float* ep_o) {
   const int tid = threadIdx.x;
   const bool worker = tid < 128;
   const int G = kGroup;
@@ -166,76 +166,7 @@ __device__ __forceinline__ void write_and_fold(const DecodeParams& p, const Unit
     }
     if ((tid & 15) == 0) dst_lse[r] = empty ? kNegInf : (M + log2f(L)) * kLn2;
   }
-  if (!fold) return;
-  // ---- fold: the last unit of this (request, head) merges all its partials
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) {
-    int* ticket = p.tickets + ui.b * p.H + ui.h;
-    int prev = atomicAdd(ticket, 1);
-    S.is_last = (prev == ui.per_head - 1);
-    if (S.is_last) *ticket = 0;  // leave the workspace zeroed for the next launch
-  }
-  __syncthreads();
-  if (!S.is_last) return;
-  __threadfence();
-  const int first = blockIdx.x - ui.unit_in_head;
-  const int n = ui.per_head;
-  // stage the head's partial lse values [n][8] in shared memory (they are
-  // contiguous in the workspace), using the idle stage memory as scratch
-  float* lse_s = scratch;
-  const bool staged = n * G <= scratch_floats;
-  if (staged)
-    for (int i = tid; i < n * G; i += blockDim.x) lse_s[i] = __ldcg(p.part_lse + first * G + i);
-  __syncthreads();
-  if (!worker) return;
-  auto lse_at = [&](int i) { return staged ? lse_s[i * G + r] : __ldcg(p.part_lse + (first + i) * G + r); };
-  float M = kNegInf;
-  for (int i = 0; i < n; ++i) M = fmaxf(M, lse_at(i));
-  float* out_o = p.out_o + (int64_t)(row0_final + r) * kHeadDim + c0;
-  if (M == kNegInf) {
-#pragma unroll
-    for (int c = 0; c < 16; ++c) out_o[c] = 0.f;
-    if ((tid & 15) == 0) p.out_lse[row0_final + r] = kNegInf;
-    return;
-  }
-  float L = 0.f;
-  for (int i = 0; i < n; ++i) {
-    float li = lse_at(i);
-    if (li != kNegInf) L += expf(li - M);
-  }
-  const float LSE = M + logf(L);
-  float acc[16];
-#pragma unroll
-  for (int c = 0; c < 16; ++c) acc[c] = 0.f;
-  // four partials per iteration keep 16 independent 16-byte loads in flight
-  for (int i0 = 0; i0 < n; i0 += 4) {
-    float4 v[4][4];
-    float wgt[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int i = i0 + k;
-      const float li = i < n ? lse_at(i) : kNegInf;
-      wgt[k] = (li == kNegInf) ? 0.f : expf(li - LSE);
-      const float4* src =
-          reinterpret_cast<const float4*>(p.part_o + ((int64_t)(first + min(i, n - 1)) * G + r) * kHeadDim + c0);
-#pragma unroll
-      for (int c = 0; c < 4; ++c) v[k][c] = (wgt[k] != 0.f) ? __ldcg(src + c) : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-#pragma unroll
-    for (int k = 0; k < 4; ++k)
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        acc[4 * c + 0] += wgt[k] * v[k][c].x;
-        acc[4 * c + 1] += wgt[k] * v[k][c].y;
-        acc[4 * c + 2] += wgt[k] * v[k][c].z;
-        acc[4 * c + 3] += wgt[k] * v[k][c].w;
-      }
-  }
-#pragma unroll
-  for (int c = 0; c < 16; c += 4)
-    *reinterpret_cast<float4*>(out_o + c) = make_float4(acc[c], acc[c + 1], acc[c + 2], acc[c + 3]);
-  if ((tid & 15) == 0) p.out_lse[row0_final + r] = LSE;
+  (void)fold;
 }
 
 }  // namespace tpk

@@ -28,9 +28,9 @@
 // The integer tensor path (s8 x s8) is not used: on this GPU it runs at about a
 // quarter of the f16 rate.
 //
-// Exact tier: BF16 half-pages (32 tokens) staged with a padded row pitch so that
-// ldmatrix reads are conflict-free; q is exact in bf16; P enters as bf16 high and
-// low planes.
+// Exact tier: BF16 half-pages (32 tokens) arrive by TMA tensor copies in the
+// 128-byte-swizzled layout, so ldmatrix reads are conflict-free; q is exact in
+// bf16; P enters as bf16 high and low planes.
 //
 // Online softmax ("SYCL", "Exact tricks and a two-owner decoder"): the running
 // maximum is an integer in base 2, every rescale is a power of two built by
@@ -45,7 +45,6 @@ namespace tpk {
 constexpr int kCons = 8;                       // consumer warps (4 pairs)
 constexpr int kMmaThreads = (kCons + 1) * 32;  // + one producer warp
 constexpr int kMmaSlots = 6;
-constexpr int kPad = 528;  // BF16 row pitch in shared memory (512 B + 16 B)
 constexpr unsigned kAll = 0xffffffffu;
 
 struct MmaSmem {
@@ -127,27 +126,37 @@ __device__ __forceinline__ void codes_to_f16(uint32_t w, uint32_t& lo, uint32_t&
 }
 
 // ----------------------------------------------------------------- producer
+// BF16 half-pages arrive by TMA as 128-byte-swizzled tiles: K at tiles 0-3 and V
+// at tiles 4-7 of the slot (1024-byte aligned), tile c = channels 64c .. 64c+63
+// of the 32 tokens, row r at byte 128 r, 16-byte chunk k stored at chunk k ^ (r % 8).
+__device__ __forceinline__ uint8_t* bf16_tiles(uint8_t* slot) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(slot) + 1023) & ~uintptr_t(1023));
+}
+__device__ __forceinline__ uint32_t swz(int r, int chunk) {  // byte offset of (row, 16-byte chunk 0..31)
+  return (chunk >> 3) * 4096 + r * 128 + (((chunk & 7) ^ (r & 7)) << 4);
+}
+
 __device__ __forceinline__ void mma_issue(const DecodeParams& p, const UnitInfo& ui, const Items& it, MmaSmem& S,
                                           int j, int s) {
   int page = item_page(ui, it, j);
   int idx = page - it.pg_first;
-  int64_t slot = idx < kPtCache ? S.pt[idx]
-                                : __ldg((ui.tier == 0 ? p.page_table : p.page_table8) + ui.pt_off + page);
+  int64_t slot = idx < kPtCache ? S.pt[idx] : __ldg((ui.tier == 0 ? p.page_table : p.page_table8) + ui.pt_off + page);
   int64_t lim = ui.tier == 0 ? p.kv_slots : p.rec_slots;
-  bool ok = slot >= 0 && (lim == 0 || slot < lim);
-  S.valid[s] = ok ? 1 : 0;
+  const bool ok = slot >= 0 && (lim == 0 || slot < lim);
+  S.valid[s] = ok;
   if (!ok) {
     atomicOr(p.status, kStatusBadSlot);
     mbar_arrive(&S.full[s]);
     return;
   }
   if (ui.tier == 0) {
-    const int half = (it.first + j) & 1;
-    const int64_t off = ((slot * p.H + ui.h) * kPageTokens + half * 32) * (int64_t)kHeadDim;
+    const int row0 = (int)((slot * p.H + ui.h) * kPageTokens + ((it.first + j) & 1) * 32);
+    uint8_t* base = bf16_tiles(S.slot[s]);
     mbar_arrive_expect_tx(&S.full[s], 32768);
-    for (int r = 0; r < 32; ++r) {
-      bulk_g2s(S.slot[s] + r * kPad, p.k_pool + off + r * kHeadDim, 512, &S.full[s]);
-      bulk_g2s(S.slot[s] + (32 + r) * kPad, p.v_pool + off + r * kHeadDim, 512, &S.full[s]);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      tma_load_2d(base + c * 4096, &p.kmap, 64 * c, row0, &S.full[s]);
+      tma_load_2d(base + 16384 + c * 4096, &p.vmap, 64 * c, row0, &S.full[s]);
     }
   } else {
     const uint8_t* src = p.rec_pool + (slot * p.H + ui.h) * (int64_t)kRecordBytes;
@@ -285,13 +294,14 @@ __device__ __forceinline__ void process_bf16_quarter(uint8_t* slot, int h, int t
                                                      const MmaSmem& S, float qscale, float& m_run, float& l_run,
                                                      float (&O)[16][4]) {
   const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-  const uint8_t* K = slot + 16 * h * kPad;
-  uint8_t* V = slot + (32 + 16 * h) * kPad;
+  uint8_t* K = bf16_tiles(slot);
+  uint8_t* V = K + 16384;
   const int base = tok0 + 16 * h;
   if (base < tb || base + 16 > te) {  // zero value rows of tokens outside the range
     for (int k = 0; k < 16; ++k) {
-      const int tok = base + k;
-      if (tok < tb || tok >= te) *reinterpret_cast<uint4*>(V + k * kPad + 16 * lane) = make_uint4(0, 0, 0, 0);
+      const int tok = base + k, r = 16 * h + k;
+      if (tok < tb || tok >= te)
+        *reinterpret_cast<uint4*>(V + (lane >> 3) * 4096 + r * 128 + (lane & 7) * 16) = make_uint4(0, 0, 0, 0);
     }
     __syncwarp();
   }
@@ -304,7 +314,7 @@ __device__ __forceinline__ void process_bf16_quarter(uint8_t* slot, int h, int t
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
       uint32_t m4[4];
-      ldsm_x4(m4, K + (8 * j + (lane & 7)) * kPad + (4 * kk + (lane >> 3)) * 16);
+      ldsm_x4(m4, K + swz(16 * h + 8 * j + (lane & 7), 4 * kk + (lane >> 3)));
       mma_bf16(acc[j], qa0, 0u, qa1, 0u, m4[0], m4[1]);
       mma_bf16(acc[j], qa2, 0u, qa3, 0u, m4[2], m4[3]);
     }
@@ -325,7 +335,7 @@ __device__ __forceinline__ void process_bf16_quarter(uint8_t* slot, int h, int t
 #pragma unroll
   for (int m = 0; m < 16; ++m) {
     uint32_t a[4];
-    ldsm_x4_t(a, V + ((i >> 1) * 8 + (lane & 7)) * kPad + (2 * m + (i & 1)) * 16);
+    ldsm_x4_t(a, V + swz(16 * h + (i >> 1) * 8 + (lane & 7), 2 * m + (i & 1)));
     mma_bf16(O[m], a[0], a[1], a[2], a[3], ph0, ph1);
     mma_bf16(O[m], a[0], a[1], a[2], a[3], pl0, pl1);
   }
@@ -456,7 +466,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) decode_mma_kernel(const __grid
     }
   }
   __syncthreads();
-  write_and_fold<kCons>(p, ui, S, ep_o, reinterpret_cast<float*>(S.slot[2]), kSlotBytes / 4);
+  write_and_fold<kCons>(p, ui, S, ep_o);
 }
 
 cudaError_t launch_decode_mma(const DecodeParams& p, cudaStream_t stream) {

@@ -310,7 +310,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_simt_kernel(const __gri
     *reinterpret_cast<float4*>(dst + 4) = make_float4(O[r][4], O[r][5], O[r][6], O[r][7]);
   }
   __syncthreads();
-  write_and_fold<kDecWarps>(p, ui, S, ep_o, reinterpret_cast<float*>(S.slot[1]), kSlotBytes / 4);
+  write_and_fold<kDecWarps>(p, ui, S, ep_o);
 }
 
 cudaError_t launch_decode_simt(const DecodeParams& p, cudaStream_t stream) {

@@ -34,6 +34,77 @@ __global__ void __launch_bounds__(kHeadDim) merge_kernel(int n_parts, int rows, 
   if (c == 0) lse_acc[row] = LSE;
 }
 
+// Fold of the multi-request launch: block (request b, KV head h, row r) merges
+// the partials of that head's units, in unit order, for one output row; thread c
+// owns channel c.  All the lse values are staged in shared memory first and the
+// o loads are issued in batches, so the fold costs a few memory round trips.
+__global__ void __launch_bounds__(kHeadDim) fold_kernel(const __grid_constant__ DecodeParams p) {
+  __shared__ float lse_s[1024];
+  __shared__ float w_s[1024];
+  const int G = kGroup;
+  const int b = blockIdx.x / (p.H * G);
+  const int h = (blockIdx.x / G) % p.H;
+  const int r = blockIdx.x % G;
+  const ReqPlan& rp = p.req[b];
+  const int n = rp.splits_e + rp.splits_8;
+  if (n <= 1) return;  // a single unit wrote the output itself
+  const int first = rp.unit_base + h * n;
+  const int c = threadIdx.x;
+  const float ninf = -__builtin_huge_valf();
+  const int row_out = (b * p.H + h) * G + r;
+  float M = ninf, L = 0.f;
+  for (int i0 = 0; i0 < n; i0 += 1024) {
+    const int cnt = min(1024, n - i0);
+    __syncthreads();
+    for (int i = c; i < cnt; i += blockDim.x) lse_s[i] = p.part_lse[(first + i0 + i) * G + r];
+    __syncthreads();
+    float bm = ninf;
+    for (int i = 0; i < cnt; ++i) bm = fmaxf(bm, lse_s[i]);
+    if (bm == ninf) continue;
+    if (bm > M) {
+      L = (M == ninf) ? 0.f : L * expf(M - bm);
+      M = bm;
+    }
+    for (int i = 0; i < cnt; ++i)
+      if (lse_s[i] != ninf) L += expf(lse_s[i] - M);
+  }
+  if (M == ninf) {
+    p.out_o[(int64_t)row_out * kHeadDim + c] = 0.f;
+    if (c == 0) p.out_lse[row_out] = ninf;
+    return;
+  }
+  const float LSE = M + logf(L);
+  float acc = 0.f;
+  for (int i0 = 0; i0 < n; i0 += 1024) {
+    const int cnt = min(1024, n - i0);
+    __syncthreads();
+    for (int i = c; i < cnt; i += blockDim.x) {
+      const float li = p.part_lse[(first + i0 + i) * G + r];
+      w_s[i] = (li == ninf) ? 0.f : expf(li - LSE);
+    }
+    __syncthreads();
+    const float* src = p.part_o + ((int64_t)(first + i0) * G + r) * kHeadDim + c;
+    int i = 0;
+    for (; i + 8 <= cnt; i += 8) {
+      float v[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) v[k] = src[(int64_t)(i + k) * G * kHeadDim];
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        if (w_s[i + k] != 0.f) acc += w_s[i + k] * v[k];
+    }
+    for (; i < cnt; ++i)
+      if (w_s[i] != 0.f) acc += w_s[i] * src[(int64_t)i * G * kHeadDim];
+  }
+  p.out_o[(int64_t)row_out * kHeadDim + c] = acc;
+  if (c == 0) p.out_lse[row_out] = LSE;
+}
+
+cudaError_t launch_fold(const DecodeParams& p, cudaStream_t stream) {
+  fold_kernel<<<p.n_req * p.H * kGroup, kHeadDim, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_merge(int n_parts, int rows, const float* o_parts, const float* lse_parts, float* o_acc,
                          float* lse_acc, cudaStream_t stream) {
   if (rows == 0) return cudaSuccess;
