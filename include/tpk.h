@@ -194,6 +194,31 @@ tpk_status tpk_decode_hybrid_batched(const tpk_shape* shape, int n_req, const vo
                                      tpk_stream_t stream);
 
 /*
+ * Multi-request hybrid decode that allocates nothing and takes no workspace.
+ * There is no counterpart in the pages this library follows: it exists for
+ * callers that cannot hand the library device memory -- a plugin whose host
+ * engine owns every device allocation and offers no way to ask for more, or a
+ * runtime whose memory budget is fixed once serving starts.
+ * Same arguments and results as tpk_decode_hybrid_batched, minus ws/ws_bytes.
+ * Scratch: a file-scope device array of tpk_static_scratch_bytes() bytes
+ * (16,842,752: the partials of the largest split plan, 2048 units), held by every
+ * GPU that loads the library until the process exits.  A call whose plan needs
+ * more fails with TPK_ERR_NOMEM.
+ * The first call on a device resolves the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  Every call shares the one array and no state carries over between
+ * calls that needs clearing, but calls that overlap on the GPU (for example on two
+ * streams) race on it: serialise them.
+ */
+size_t tpk_static_scratch_bytes(void);
+tpk_status tpk_decode_hybrid_batched_static(const tpk_shape* shape, int n_req, const void* q, const void* k_pool,
+                                            const void* v_pool, const void* rec_pool, const int32_t* page_table,
+                                            const int32_t* req_page_off, const int32_t* n_exact_tokens,
+                                            const int32_t* page_table8, const int32_t* req_page_off8,
+                                            const int32_t* n_int8_pages, float* o, float* lse,
+                                            tpk_stream_t stream);
+
+/*
  * Device status word: bit 0 = a page-table entry outside the pool was skipped.
  * Synchronises `stream`, stores the word in *flags and, if reset != 0, clears it.
  */

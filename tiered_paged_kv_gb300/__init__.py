@@ -20,6 +20,7 @@ __all__ = [
     "Shape", "TpkError", "lib", "RECORD_BYTES", "IMPL_DEFAULT", "IMPL_SIMT", "IMPL_TENSOR",
     "kv_quantize_pages", "kv_quantize_pages_given_scales", "decode_attn_exact", "decode_attn_int8",
     "merge_lse", "hybrid_workspace_bytes", "workspace_init", "decode_hybrid_batched", "get_device_status",
+    "static_scratch_bytes", "decode_hybrid_batched_static",
 ]
 
 RECORD_BYTES = 35072
@@ -69,9 +70,12 @@ def lib():
         L.tpk_workspace_init.argtypes = [vp, sz, vp]
         L.tpk_decode_hybrid_batched.argtypes = [sp, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         L.tpk_get_device_status.argtypes = [ctypes.POINTER(ctypes.c_int), i32, vp]
+        L.tpk_static_scratch_bytes.argtypes = []
+        L.tpk_static_scratch_bytes.restype = sz
+        L.tpk_decode_hybrid_batched_static.argtypes = [sp, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
         for name in ("tpk_kv_quantize_pages", "tpk_kv_quantize_pages_given_scales", "tpk_decode_attn_exact",
                      "tpk_decode_attn_int8", "tpk_merge_lse", "tpk_workspace_init", "tpk_decode_hybrid_batched",
-                     "tpk_get_device_status"):
+                     "tpk_get_device_status", "tpk_decode_hybrid_batched_static"):
             getattr(L, name).restype = i32
         _lib = L
     return _lib
@@ -154,6 +158,23 @@ def decode_hybrid_batched(shape, n_req, q, k_pool, v_pool, rec_pool, page_table,
     _check(lib().tpk_decode_hybrid_batched(ctypes.byref(shape), int(n_req), _ptr(q), _ptr(k_pool), _ptr(v_pool),
                                            _ptr(rec_pool), _ptr(page_table), pa, pb, _ptr(page_table8), pc, pd,
                                            _ptr(o), _ptr(lse), _ptr(ws), int(ws_bytes), _stream(stream)))
+
+
+def static_scratch_bytes():
+    return int(lib().tpk_static_scratch_bytes())
+
+
+def decode_hybrid_batched_static(shape, n_req, q, k_pool, v_pool, rec_pool, page_table, req_page_off,
+                                 n_exact_tokens, page_table8, req_page_off8, n_int8_pages, o, lse, stream=None):
+    """As decode_hybrid_batched, with the library's fixed device scratch instead of
+    a caller workspace (for callers that cannot allocate device memory)."""
+    a, pa = _host_i32(req_page_off)
+    b, pb = _host_i32(n_exact_tokens)
+    c, pc = _host_i32(req_page_off8)
+    d, pd = _host_i32(n_int8_pages)
+    _check(lib().tpk_decode_hybrid_batched_static(ctypes.byref(shape), int(n_req), _ptr(q), _ptr(k_pool),
+                                                  _ptr(v_pool), _ptr(rec_pool), _ptr(page_table), pa, pb,
+                                                  _ptr(page_table8), pc, pd, _ptr(o), _ptr(lse), _stream(stream)))
 
 
 def get_device_status(reset=True, stream=None):

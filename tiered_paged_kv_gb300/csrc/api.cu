@@ -27,6 +27,10 @@ using namespace tpk;
 
 __device__ int g_tpk_status;
 
+namespace tpk {
+void set_error(const char* msg);
+}
+
 namespace {
 
 constexpr int kMaxUnits = 2048;       // partial slots in the hybrid workspace (256 requests x 4 heads x 2 tiers)
@@ -163,6 +167,8 @@ tpk_status launch_decode(const tpk_shape* s, const DecodeParams& p, cudaStream_t
 }
 
 }  // namespace
+
+void tpk::set_error(const char* msg) { g_err = msg; }
 
 extern "C" {
 
