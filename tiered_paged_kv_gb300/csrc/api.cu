@@ -350,41 +350,63 @@ tpk_status tpk_decode_hybrid_batched(const tpk_shape* shape, int n_req, const vo
   }
   if (any_e && (!k_pool || !v_pool || !page_table)) return fail(TPK_ERR_INVALID, "null BF16 pool or page table");
   if (any_8 && (!rec_pool || !page_table8)) return fail(TPK_ERR_INVALID, "null 8-bit pool or page table");
-  // ---- split plan: equal-byte units filling whole waves of resident blocks.
-  // Every non-empty (request, head, tier) needs at least one unit; the number of
-  // waves is the fewest that hold those, and the chunk size grows until the
-  // units fit in them (a unit more would start a wave of its own).
+  // ---- split plan.  Every request's heads share one split of each tier.  The
+  // U = waves * per_wave / H unit budget per head (waves: the fewest whole
+  // waves of resident blocks giving every segment about 4 units) is shared among the
+  // (request, tier) segments in proportion to their bytes (largest remainder,
+  // at least one unit per non-empty segment, at most one per page), so units
+  // carry about equal bytes and whole waves of resident blocks are filled.
   const int per_wave = num_sms() * blocks_per_sm(shape);
   int min_units = 0;
-  for (int b = 0; b < n_req; ++b)
-    min_units += H * std::max(1, (n_exact_tokens[b] > 0) + (n_int8_pages[b] > 0));
-  if (min_units > kMaxUnits) return fail(TPK_ERR_UNSUPPORTED, "%d (request, head, tier) segments exceed %d units", min_units, kMaxUnits);
-  const int waves = (min_units + per_wave - 1) / per_wave;
-  const int target = std::min(kMaxUnits, waves * per_wave);
-  double chunk = std::max(total / target, 4096.0);
+  for (int b = 0; b < n_req; ++b) min_units += std::max(1, (n_exact_tokens[b] > 0) + (n_int8_pages[b] > 0));
+  if (min_units * H > kMaxUnits)
+    return fail(TPK_ERR_UNSUPPORTED, "%d (request, head, tier) segments exceed %d units", min_units * H, kMaxUnits);
+  // enough waves that segments average at least 4 units (balance across requests)
+  const int want = std::max((per_wave + H - 1) / H, 4 * min_units) * H;
+  const int waves = std::max(1, (want + per_wave - 1) / per_wave);
+  const int U = std::max(min_units, std::min(kMaxUnits, waves * per_wave) / H);
+  std::vector<double> wgt(2 * n_req);
+  std::vector<int> cap(2 * n_req), cnt(2 * n_req);
+  double W = 0.0;
+  for (int b = 0; b < n_req; ++b) {
+    const int ne = n_exact_tokens[b], n8 = n_int8_pages[b];
+    wgt[2 * b] = 1024.0 * ne;
+    wgt[2 * b + 1] = (double)kRecordBytes * n8;
+    cap[2 * b] = ne > 0 ? (ne + kPageTokens - 1) / kPageTokens : (n8 > 0 ? 0 : 1);  // empty request: one empty unit
+    cap[2 * b + 1] = n8;
+    W += wgt[2 * b] + wgt[2 * b + 1];
+  }
+  int used = 0;
+  std::vector<std::pair<double, int>> rem;
+  for (int x = 0; x < 2 * n_req; ++x) {
+    if (cap[x] == 0) {
+      cnt[x] = 0;
+      continue;
+    }
+    const double ideal = W > 0 ? U * wgt[x] / W : 0.0;
+    cnt[x] = std::min(cap[x], std::max(1, (int)std::floor(ideal)));
+    used += cnt[x];
+    if (cnt[x] < cap[x]) rem.push_back({ideal - std::floor(ideal), x});
+  }
+  std::sort(rem.begin(), rem.end(), [](const std::pair<double, int>& a, const std::pair<double, int>& c) {
+    return a.first > c.first || (a.first == c.first && a.second < c.second);
+  });
+  for (size_t k = 0; used < U && k < rem.size(); ++k) {
+    cnt[rem[k].second] += 1;
+    used += 1;
+  }
   DecodeParams p;
   fill_common(p, shape, q);
-  bool planned = false;
-  for (int attempt = 0; attempt < 2000 && !planned; ++attempt, chunk *= 1.01) {
-    int units = 0;
-    bool fits = true;
-    for (int b = 0; b < n_req; ++b) {
-      int ne = n_exact_tokens[b], n8 = n_int8_pages[b];
-      int pe = (ne + kPageTokens - 1) / kPageTokens;
-      int se = ne > 0 ? (int)std::min<double>(pe, std::ceil(1024.0 * ne / chunk)) : 0;
-      int s8 = n8 > 0 ? (int)std::min<double>(n8, std::ceil((double)kRecordBytes * n8 / chunk)) : 0;
-      if (se == 0 && s8 == 0) se = 1;  // an empty unit writes the empty result
-      if (se > 32767 || s8 > 32767) { fits = false; break; }
-      p.req[b] = ReqPlan{units, req_page_off[b], 0, ne, req_page_off8[b], 0, n8, (int16_t)se, (int16_t)s8};
-      units += H * (se + s8);
-      if (units > target) { fits = false; break; }
-    }
-    if (fits) {
-      p.n_units = units;
-      planned = true;
-    }
+  int units = 0;
+  for (int b = 0; b < n_req; ++b) {
+    const int se = cnt[2 * b], s8 = cnt[2 * b + 1];
+    if (se > 32767 || s8 > 32767) return fail(TPK_ERR_UNSUPPORTED, "request %d: too many splits", b);
+    p.req[b] = ReqPlan{units, req_page_off[b], 0, n_exact_tokens[b], req_page_off8[b], 0, n_int8_pages[b],
+                       (int16_t)se, (int16_t)s8};
+    units += H * (se + s8);
   }
-  if (!planned) return fail(TPK_ERR_UNSUPPORTED, "could not plan within %d units", target);
+  if (units > kMaxUnits) return fail(TPK_ERR_UNSUPPORTED, "could not plan within %d units", kMaxUnits);
+  p.n_units = units;
   p.k_pool = static_cast<const uint16_t*>(k_pool);
   p.v_pool = static_cast<const uint16_t*>(v_pool);
   p.rec_pool = static_cast<const uint8_t*>(rec_pool);

@@ -34,29 +34,75 @@ __global__ void __launch_bounds__(kHeadDim) merge_kernel(int n_parts, int rows, 
   if (c == 0) lse_acc[row] = LSE;
 }
 
-// Fold of the multi-request launch: block (request b, KV head h, row r) merges
-// the partials of that head's units, in unit order, for one output row; thread c
-// owns channel c.  All the lse values are staged in shared memory first and the
-// o loads are issued in batches, so the fold costs a few memory round trips.
-__global__ void __launch_bounds__(kHeadDim) fold_kernel(const __grid_constant__ DecodeParams p) {
-  __shared__ float lse_s[1024];
-  __shared__ float w_s[1024];
+// Fold of the multi-request launch: block (request b, KV head h, row r,
+// channel quarter) merges the partials of that head's units, in unit order, for
+// 64 channels of one output row; thread c owns one channel.  The lse values are
+// staged in shared memory with their merge weights, then every partial's value
+// for the thread's channel is loaded in batches of 16 independent loads.
+constexpr int kFoldQuarters = 4;
+constexpr int kFoldFast = 64;  // heads with at most this many units (= threads per block) fold in one round trip
+__global__ void __launch_bounds__(64) fold_kernel(const __grid_constant__ DecodeParams p) {
+  constexpr int kChunk = 2048;  // partials per shared-memory pass
+  __shared__ float lse_s[kChunk];
+  __shared__ float w_s[kChunk];
+  __shared__ float red_s[2];
   const int G = kGroup;
-  const int b = blockIdx.x / (p.H * G);
-  const int h = (blockIdx.x / G) % p.H;
-  const int r = blockIdx.x % G;
+  const int qtr = blockIdx.x % kFoldQuarters;
+  const int row = blockIdx.x / kFoldQuarters;  // (b * H + h) * G + r
+  const int b = row / (p.H * G);
+  const int h = (row / G) % p.H;
+  const int r = row % G;
   const ReqPlan& rp = p.req[b];
   const int n = rp.splits_e + rp.splits_8;
   if (n <= 1) return;  // a single unit wrote the output itself
+  wait_for_primary_grid();
   const int first = rp.unit_base + h * n;
-  const int c = threadIdx.x;
+  const int c = qtr * 64 + threadIdx.x;
   const float ninf = -__builtin_huge_valf();
-  const int row_out = (b * p.H + h) * G + r;
-  float M = ninf, L = 0.f;
-  for (int i0 = 0; i0 < n; i0 += 1024) {
-    const int cnt = min(1024, n - i0);
+  if (n <= kFoldFast) {
+    // One memory round trip.  Thread i (< n) owns partial i's lse; the block
+    // reduces max and sum with a fixed tree (deterministic), and each thread then
+    // combines its channel from values requested right after the wait.
+    float v[kFoldFast];
+    const float* src = p.part_o + ((int64_t)first * G + r) * kHeadDim + c;
+#pragma unroll
+    for (int i = 0; i < kFoldFast; ++i) v[i] = i < n ? src[(int64_t)i * G * kHeadDim] : 0.f;
+    const int t = threadIdx.x;
+    const float li = t < n ? p.part_lse[(first + t) * G + r] : ninf;
+    float m = li;
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    if ((t & 31) == 0) red_s[t >> 5] = m;
     __syncthreads();
-    for (int i = c; i < cnt; i += blockDim.x) lse_s[i] = p.part_lse[(first + i0 + i) * G + r];
+    const float M = fmaxf(red_s[0], red_s[1]);
+    if (M == ninf) {
+      p.out_o[(int64_t)row * kHeadDim + c] = 0.f;
+      if (c == 0) p.out_lse[row] = ninf;
+      return;
+    }
+    const float wi = (li == ninf) ? 0.f : expf(li - M);
+    float sum = wi;
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    __syncthreads();
+    if ((t & 31) == 0) red_s[t >> 5] = sum;
+    __syncthreads();
+    const float L = red_s[0] + red_s[1];
+    if (t < n) w_s[t] = wi / L;
+    __syncthreads();
+    float acc = 0.f;
+#pragma unroll
+    for (int i = 0; i < kFoldFast; ++i)
+      if (i < n) acc += w_s[i] * v[i];
+    p.out_o[(int64_t)row * kHeadDim + c] = acc;
+    if (c == 0) p.out_lse[row] = M + logf(L);
+    return;
+  }
+  float M = ninf, L = 0.f;
+  for (int i0 = 0; i0 < n; i0 += kChunk) {
+    const int cnt = min(kChunk, n - i0);
+    __syncthreads();
+    for (int i = threadIdx.x; i < cnt; i += blockDim.x) lse_s[i] = p.part_lse[(first + i0 + i) * G + r];
     __syncthreads();
     float bm = ninf;
     for (int i = 0; i < cnt; ++i) bm = fmaxf(bm, lse_s[i]);
@@ -69,40 +115,46 @@ __global__ void __launch_bounds__(kHeadDim) fold_kernel(const __grid_constant__ 
       if (lse_s[i] != ninf) L += expf(lse_s[i] - M);
   }
   if (M == ninf) {
-    p.out_o[(int64_t)row_out * kHeadDim + c] = 0.f;
-    if (c == 0) p.out_lse[row_out] = ninf;
+    p.out_o[(int64_t)row * kHeadDim + c] = 0.f;
+    if (c == 0) p.out_lse[row] = ninf;
     return;
   }
   const float LSE = M + logf(L);
   float acc = 0.f;
-  for (int i0 = 0; i0 < n; i0 += 1024) {
-    const int cnt = min(1024, n - i0);
+  for (int i0 = 0; i0 < n; i0 += kChunk) {
+    const int cnt = min(kChunk, n - i0);
     __syncthreads();
-    for (int i = c; i < cnt; i += blockDim.x) {
+    for (int i = threadIdx.x; i < cnt; i += blockDim.x) {
       const float li = p.part_lse[(first + i0 + i) * G + r];
       w_s[i] = (li == ninf) ? 0.f : expf(li - LSE);
     }
     __syncthreads();
     const float* src = p.part_o + ((int64_t)(first + i0) * G + r) * kHeadDim + c;
-    int i = 0;
-    for (; i + 8 <= cnt; i += 8) {
-      float v[8];
+    for (int j0 = 0; j0 < cnt; j0 += 16) {
+      float v[16];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) v[k] = src[(int64_t)(i + k) * G * kHeadDim];
+      for (int k = 0; k < 16; ++k) v[k] = (j0 + k < cnt) ? src[(int64_t)(j0 + k) * G * kHeadDim] : 0.f;
 #pragma unroll
-      for (int k = 0; k < 8; ++k)
-        if (w_s[i + k] != 0.f) acc += w_s[i + k] * v[k];
+      for (int k = 0; k < 16; ++k)
+        if (j0 + k < cnt && w_s[j0 + k] != 0.f) acc += w_s[j0 + k] * v[k];
     }
-    for (; i < cnt; ++i)
-      if (w_s[i] != 0.f) acc += w_s[i] * src[(int64_t)i * G * kHeadDim];
   }
-  p.out_o[(int64_t)row_out * kHeadDim + c] = acc;
-  if (c == 0) p.out_lse[row_out] = LSE;
+  p.out_o[(int64_t)row * kHeadDim + c] = acc;
+  if (c == 0) p.out_lse[row] = LSE;
 }
 
 cudaError_t launch_fold(const DecodeParams& p, cudaStream_t stream) {
-  fold_kernel<<<p.n_req * p.H * kGroup, kHeadDim, 0, stream>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.n_req * p.H * kGroup * kFoldQuarters);
+  cfg.blockDim = dim3(64);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, fold_kernel, p);
 }
 
 cudaError_t launch_merge(int n_parts, int rows, const float* o_parts, const float* lse_parts, float* o_acc,
