@@ -66,6 +66,10 @@ enum { TPK_IMPL_DEFAULT = 0, TPK_IMPL_SIMT = 1, TPK_IMPL_TENSOR = 2 };
  *   f32  ks_chan[256]  key channel scale s_c           offset 32768
  *   f32  ks_tok[64]    key per-token factor r_t        offset 33792
  *   f32  vs_chan[256]  value channel scale u_c         offset 34048
+ * Position swizzles (the format is shaped for the kernel that reads it):
+ *   key code (t, c)   at byte t*256 + (c XOR 64*(t mod 2))
+ *   value code (c, t) at byte c*64 + (t XOR 32*((c/2) mod 2))
+ *   s_c               at float (c XOR 8*((c/32) mod 2))
  * Dequantised: k_tc = kc_tc * s_c * r_t and v_tc = vc_tc * u_c. */
 #define TPK_RECORD_BYTES 35072
 

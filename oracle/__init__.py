@@ -101,18 +101,41 @@ def quantize_pages(H, k_pool, v_pool, src_slots, dst_slots, rec_pool):
                              len(src), _p(rec_pool))
 
 
-def record_fields(rec):
-    """Split one 35,072-byte record into (kc[64][256], vc[64][256], s[256], r[64], u[256]).
+_T = np.arange(T_PAGE)[:, None]
+_C = np.arange(D_HEAD)[None, :]
+# byte / float positions of the swizzled record fields (see oracle.c)
+KC_POS = _T * D_HEAD + (_C ^ (64 * (_T & 1)))                    # [t][c]
+VC_POS = (_C * T_PAGE + (_T ^ (32 * ((_C >> 1) & 1))))          # [t][c] -> position in vc[256][64]
+KS_POS = np.arange(D_HEAD) ^ (8 * ((np.arange(D_HEAD) >> 5) & 1))
 
-    Value codes are stored channel-major (vc[256][64]); the returned vc is the
-    token-major view vc[t][c]."""
+
+def record_fields(rec):
+    """Split one 35,072-byte record into logical (kc[64][256], vc[64][256] (token
+    by channel), s[256], r[64], u[256]), undoing the position swizzles."""
     rec = np.asarray(rec, np.uint8)
-    kc = rec[OFF_KC:OFF_VC].view(np.int8).reshape(T_PAGE, D_HEAD)
-    vc = rec[OFF_VC:OFF_KS_CHAN].view(np.int8).reshape(D_HEAD, T_PAGE).T
-    s = rec[OFF_KS_CHAN:OFF_KS_TOK].view(np.float32)
+    kc = rec[OFF_KC:OFF_VC].view(np.int8)[KC_POS]
+    vc = rec[OFF_VC:OFF_KS_CHAN].view(np.int8)[VC_POS]
+    s = rec[OFF_KS_CHAN:OFF_KS_TOK].view(np.float32)[KS_POS]
     r = rec[OFF_KS_TOK:OFF_VS_CHAN].view(np.float32)
     u = rec[OFF_VS_CHAN:REC_BYTES].view(np.float32)
     return kc, vc, s, r, u
+
+
+def pack_record(kc, vc, s, r, u):
+    """Inverse of record_fields: logical fields -> 35,072-byte record."""
+    rec = np.zeros(REC_BYTES, np.uint8)
+    kcb = np.zeros(T_PAGE * D_HEAD, np.int8)
+    kcb[KC_POS] = kc
+    vcb = np.zeros(T_PAGE * D_HEAD, np.int8)
+    vcb[VC_POS] = vc
+    ks = np.zeros(D_HEAD, np.float32)
+    ks[KS_POS] = s
+    rec[OFF_KC:OFF_VC] = kcb.view(np.uint8)
+    rec[OFF_VC:OFF_KS_CHAN] = vcb.view(np.uint8)
+    rec[OFF_KS_CHAN:OFF_KS_TOK] = ks.view(np.uint8)
+    rec[OFF_KS_TOK:OFF_VS_CHAN] = np.asarray(r, np.float32).view(np.uint8)
+    rec[OFF_VS_CHAN:REC_BYTES] = np.asarray(u, np.float32).view(np.uint8)
+    return rec
 
 
 # ------------------------------------------------------------------ attention

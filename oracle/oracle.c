@@ -39,6 +39,10 @@
  *   f32   ks_chan[256]     key channel scale s_c   offset 32768
  *   f32   ks_tok[64]       key token factor r_t    offset 33792
  *   f32   vs_chan[256]     value channel scale u_c offset 34048
+ * with three position swizzles (the format is shaped for the kernel that reads it):
+ *   key code (t, c)   at byte t*256 + (c XOR 64 * (t mod 2))
+ *   value code (c, t) at byte c*64 + (t XOR 32 * ((c / 2) mod 2))
+ *   s_c               at float (c XOR 8 * ((c / 32) mod 2))
  * Dequantised: k_tc = kc_tc * s_c * r_t,  v_tc = vc_tc * u_c.
  */
 #include <math.h>
@@ -55,6 +59,11 @@
 #define OFF_KS_CHAN 32768
 #define OFF_KS_TOK 33792
 #define OFF_VS_CHAN 34048
+
+/* positions inside a record (see the layout above) */
+static int kc_pos(int t, int c) { return t * D_HEAD + (c ^ (64 * (t & 1))); }
+static int vc_pos(int c, int t) { return c * T_PAGE + (t ^ (32 * ((c >> 1) & 1))); }
+static int ks_pos(int c) { return c ^ (8 * ((c >> 5) & 1)); }
 
 static double bf16_value(uint16_t b) {
   uint32_t u = (uint32_t)b << 16;
@@ -149,10 +158,11 @@ void orc_codes_given(const uint16_t* k, const uint16_t* v, const float* ks_chan,
   for (int t = 0; t < T_PAGE; ++t)
     for (int c = 0; c < D_HEAD; ++c) {
       float y = bf16_float(k[t * D_HEAD + c]) / ks_chan[c];
-      kc[t * D_HEAD + c] = code_of(y, ks_tok[t]);
-      vc[c * T_PAGE + t] = code_of(bf16_float(v[t * D_HEAD + c]), vs_chan[c]);
+      kc[kc_pos(t, c)] = code_of(y, ks_tok[t]);
+      vc[vc_pos(c, t)] = code_of(bf16_float(v[t * D_HEAD + c]), vs_chan[c]);
     }
-  memcpy(rec + OFF_KS_CHAN, ks_chan, 4 * D_HEAD);
+  float* ks = (float*)(rec + OFF_KS_CHAN);
+  for (int c = 0; c < D_HEAD; ++c) ks[ks_pos(c)] = ks_chan[c];
   memcpy(rec + OFF_KS_TOK, ks_tok, 4 * T_PAGE);
   memcpy(rec + OFF_VS_CHAN, vs_chan, 4 * D_HEAD);
 }
@@ -272,15 +282,16 @@ static void partial_int8_head(int H, int G, int h, const uint16_t* q, const uint
     const uint8_t* rec = rec_pool + ((int64_t)page_table8[page_begin + p] * H + h) * REC_BYTES;
     const int8_t* kc = (const int8_t*)(rec + OFF_KC);
     const int8_t* vc = (const int8_t*)(rec + OFF_VC);
-    float s[D_HEAD], r[T_PAGE], u[D_HEAD];
-    memcpy(s, rec + OFF_KS_CHAN, sizeof s);
+    float s[D_HEAD], r[T_PAGE], u[D_HEAD], s_stored[D_HEAD];
+    memcpy(s_stored, rec + OFF_KS_CHAN, sizeof s_stored);
+    for (int c = 0; c < D_HEAD; ++c) s[c] = s_stored[ks_pos(c)];
     memcpy(r, rec + OFF_KS_TOK, sizeof r);
     memcpy(u, rec + OFF_VS_CHAN, sizeof u);
     for (int t = 0; t < T_PAGE; ++t)
       for (int c = 0; c < d; ++c) {
         int64_t i = ((int64_t)p * T_PAGE + t) * d + c;
-        K[i] = (double)kc[t * d + c] * (double)s[c] * (double)r[t];
-        V[i] = (double)vc[c * T_PAGE + t] * (double)u[c];
+        K[i] = (double)kc[kc_pos(t, c)] * (double)s[c] * (double)r[t];
+        V[i] = (double)vc[vc_pos(c, t)] * (double)u[c];
       }
   }
   for (int g = 0; g < G; ++g)

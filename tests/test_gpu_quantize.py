@@ -32,9 +32,10 @@ def test_codes_bit_exact_given_oracle_scales(name):
     slots = w.int8_slots()
     H = w.H
     recs = ref.reshape(w.n_slots, H, oracle.REC_BYTES)[slots]  # [n][H][rec]
-    ks = recs[:, :, oracle.OFF_KS_CHAN:oracle.OFF_KS_TOK].copy().view(np.float32)
-    kt = recs[:, :, oracle.OFF_KS_TOK:oracle.OFF_VS_CHAN].copy().view(np.float32)
-    vs = recs[:, :, oracle.OFF_VS_CHAN:].copy().view(np.float32)
+    fields = [[oracle.record_fields(recs[i, h]) for h in range(H)] for i in range(len(slots))]
+    ks = np.array([[f[2] for f in row] for row in fields], np.float32)   # logical channel order
+    kt = np.array([[f[3] for f in row] for row in fields], np.float32)
+    vs = np.array([[f[4] for f in row] for row in fields], np.float32)
     d = DevWorkload(w)
     s = dev_i32(slots)
     tpk.kv_quantize_pages_given_scales(d.shape, d.k, d.v, s, s, len(slots), dev_f32(ks), dev_f32(kt), dev_f32(vs),

@@ -174,12 +174,7 @@ def representable_records(seed, n_pages, H):
     vp = np.zeros((n_pages, H, 64, D), np.uint16)
     for p in range(n_pages):
         for h in range(H):
-            rec = recs[p, h]
-            rec[:16384] = kc[p, h].reshape(-1).view(np.uint8)
-            rec[16384:32768] = np.ascontiguousarray(vc[p, h].T).reshape(-1).view(np.uint8)  # channel-major
-            rec[32768:33792] = s[p, h].view(np.uint8)
-            rec[33792:34048] = r[p, h].view(np.uint8)
-            rec[34048:] = u[p, h].view(np.uint8)
+            recs[p, h] = oracle.pack_record(kc[p, h], vc[p, h], s[p, h], r[p, h], u[p, h])
             kv = kc[p, h].astype(np.float32) * s[p, h][None, :] * r[p, h][:, None]
             vv = vc[p, h].astype(np.float32) * u[p, h][None, :]
             kp[p, h] = synth.f32_to_bf16(kv)

@@ -20,6 +20,15 @@ constexpr int kOffKsTok = 33792;
 constexpr int kOffVsChan = 34048;
 constexpr int kBf16PageHeadBytes = kPageTokens * kHeadDim * 2;  // 32 KB (K or V)
 
+// Position swizzles of the record fields (they spread the tensor-core kernel's
+// shared-memory reads over all banks):
+//   key code (t, c)   at byte t*256 + (c ^ 64 (t & 1))
+//   value code (c, t) at byte c*64 + (t ^ 32 ((c >> 1) & 1))
+//   s_c               at float c ^ 8 ((c >> 5) & 1)
+__host__ __device__ __forceinline__ int kc_byte(int t, int c) { return t * kHeadDim + (c ^ ((t & 1) << 6)); }
+__host__ __device__ __forceinline__ int vc_byte(int c, int t) { return c * kPageTokens + (t ^ (((c >> 1) & 1) << 5)); }
+__host__ __device__ __forceinline__ int ks_index(int c) { return c ^ (((c >> 5) & 1) << 3); }
+
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 

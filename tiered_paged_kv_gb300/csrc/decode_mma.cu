@@ -210,7 +210,7 @@ __device__ __forceinline__ void process_int8_half(const uint8_t* rec, int h, con
   const float* kr = reinterpret_cast<const float*>(rec + kOffKsTok) + 32 * h;
   const float* vs = reinterpret_cast<const float*>(rec + kOffVsChan);
   const uint8_t* kc = rec + kOffKc + 32 * h * kHeadDim;
-  const uint8_t* vc = rec + kOffVc + 32 * h;
+  const uint8_t* vc = rec + kOffVc;
   const float* qrow = S.qs[g];
 
   // ---- QK: 4 tiles of 8 tokens, 16 k-steps of 16 channels.  k-step 4J + i uses
@@ -222,13 +222,14 @@ __device__ __forceinline__ void process_int8_half(const uint8_t* rec, int h, con
   for (int J = 0; J < 4; ++J) {
     uint4 kw[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
-      kw[j] = *reinterpret_cast<const uint4*>(kc + (8 * (g >> 1) + 2 * j + (g & 1)) * kHeadDim + 64 * J + 16 * t);
+    for (int j = 0; j < 4; ++j)  // token 8 (g >> 1) + 2j + (g & 1) of the half (odd tokens: 64-byte halves swapped)
+      kw[j] = *reinterpret_cast<const uint4*>(kc + (8 * (g >> 1) + 2 * j + (g & 1)) * kHeadDim +
+                                              ((64 * J + 16 * t) ^ ((g & 1) << 6)));
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int ch = 64 * J + 16 * t + 4 * i;
-      const float4 s4 = *reinterpret_cast<const float4*>(ks + ch);
-      const float4 q4 = *reinterpret_cast<const float4*>(qrow + ch);
+      const float4 s4 = *reinterpret_cast<const float4*>(ks + ks_index(ch));
+      const float4 q4 = *reinterpret_cast<const float4*>(qrow + ks_index(ch));
       const float x0 = q4.x * s4.x, x1 = q4.y * s4.y, x2 = q4.z * s4.z, x3 = q4.w * s4.w;
       const uint32_t h01 = pack_f16(x0, x1), h23 = pack_f16(x2, x3);
       const uint32_t l01 = pack_f16(x0 - f16_lo(h01), x1 - f16_hi(h01));
@@ -269,8 +270,8 @@ __device__ __forceinline__ void process_int8_half(const uint8_t* rec, int h, con
   // ---- PV: 16 channel tiles; each page result times u_c into the accumulator
 #pragma unroll
   for (int m = 0; m < 16; ++m) {
-    const uint2 va = *reinterpret_cast<const uint2*>(vc + (16 * m + g) * kPageTokens + 8 * t);
-    const uint2 vb = *reinterpret_cast<const uint2*>(vc + (16 * m + g + 8) * kPageTokens + 8 * t);
+    const uint2 va = *reinterpret_cast<const uint2*>(vc + vc_byte(16 * m + g, 32 * h + 8 * t));
+    const uint2 vb = *reinterpret_cast<const uint2*>(vc + vc_byte(16 * m + g + 8, 32 * h + 8 * t));
     float c[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
@@ -384,8 +385,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1) decode_mma_kernel(const __grid
     if (warp == 0)
       for (int c = t; c < kHeadDim / 2; c += 4) {
         const uint32_t w = S.q[g][c];
-        S.qs[g][2 * c] = bf16_lo(w) * sc;
-        S.qs[g][2 * c + 1] = bf16_hi(w) * sc;
+        S.qs[g][ks_index(2 * c)] = bf16_lo(w) * sc;  // same channel permutation as the record's s_c
+        S.qs[g][ks_index(2 * c + 1)] = bf16_hi(w) * sc;
       }
   }
   __syncthreads();

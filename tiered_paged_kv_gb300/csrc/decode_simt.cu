@@ -73,7 +73,7 @@ __device__ __forceinline__ void transpose_value_codes(uint8_t* vc) {
   uint32_t w[4][8];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const uint4* src = reinterpret_cast<const uint4*>(vc + (4 * a + i) * kPageTokens + 32 * b);
+    const uint4* src = reinterpret_cast<const uint4*>(vc + vc_byte(4 * a + i, 32 * b));
     uint4 x = src[0], y = src[1];
     w[i][0] = x.x; w[i][1] = x.y; w[i][2] = x.z; w[i][3] = x.w;
     w[i][4] = y.x; w[i][5] = y.y; w[i][6] = y.z; w[i][7] = y.w;
@@ -229,8 +229,8 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_simt_kernel(const __gri
         const float* vs = reinterpret_cast<const float*>(slot + kOffVsChan);
         float sc[8], uc[8];
         {
-          float4 a = *reinterpret_cast<const float4*>(ks + lane * 8);
-          float4 b = *reinterpret_cast<const float4*>(ks + lane * 8 + 4);
+          float4 a = *reinterpret_cast<const float4*>(ks + ks_index(lane * 8));
+          float4 b = *reinterpret_cast<const float4*>(ks + ks_index(lane * 8 + 4));
           float4 c = *reinterpret_cast<const float4*>(vs + lane * 8);
           float4 d = *reinterpret_cast<const float4*>(vs + lane * 8 + 4);
           sc[0] = a.x; sc[1] = a.y; sc[2] = a.z; sc[3] = a.w;
@@ -246,7 +246,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_simt_kernel(const __gri
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             float k[8];
-            codes8_to_float(*reinterpret_cast<const uint2*>(kc + (key0 + i) * kHeadDim + lane * 8), k);
+            codes8_to_float(*reinterpret_cast<const uint2*>(kc + kc_byte(key0 + i, lane * 8)), k);
 #pragma unroll
             for (int c = 0; c < 8; ++c) k[c] *= sc[c];
 #pragma unroll

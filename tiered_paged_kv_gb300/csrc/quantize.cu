@@ -20,7 +20,8 @@
 //   5. threads (token, quarter row) divide keys by s_c, take the per-token
 //      absolute maximum r_t = max|y| / 127 and form the codes with IEEE float32
 //      divisions and half-to-even rint; thread c also codes value channel c
-//      (stored channel-major, one 64-byte row per channel).
+//      (stored channel-major, one 64-byte row per channel).  Fields are written
+//      at their swizzled positions (kc_byte, vc_byte, ks_index).
 #include "common.cuh"
 
 namespace tpk {
@@ -91,14 +92,13 @@ __global__ void __launch_bounds__(256) quantize_kernel(const __grid_constant__ Q
     const float u = given ? p.g_vchan[gidx * kHeadDim + c] : __fdiv_rn(vmax, 127.f);
     S.u[c] = u;
     // value codes of channel c: one contiguous 64-byte row (channel-major layout)
-    uint4* dst = reinterpret_cast<uint4*>(rec + kOffVc + c * kPageTokens);
 #pragma unroll
     for (int t0 = 0; t0 < kPageTokens; t0 += 16) {
       uint32_t wv[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
       for (int e = 0; e < 16; ++e)
         wv[e >> 2] |= (uint32_t)(uint8_t)code_of(bf16_lo(S.v[t0 + e][c]), u) << (8 * (e & 3));
-      dst[t0 >> 4] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+      *reinterpret_cast<uint4*>(rec + kOffVc + vc_byte(c, t0)) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
     }
   }
   double mant = 1.0;
@@ -233,18 +233,18 @@ __global__ void __launch_bounds__(256) quantize_kernel(const __grid_constant__ Q
     ymax = fmaxf(ymax, __shfl_xor_sync(0xffffffffu, ymax, 1));
     ymax = fmaxf(ymax, __shfl_xor_sync(0xffffffffu, ymax, 2));
     const float r = given ? p.g_ktok[gidx * kPageTokens + t] : __fdiv_rn(ymax, 127.f);
-    int8_t* kc = reinterpret_cast<int8_t*>(rec + kOffKc) + t * kHeadDim;
+    uint8_t* kc = rec + kOffKc;
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
       const int ch0 = q * 64 + ((k + lane) & 7) * 8;
       uint32_t wk[2] = {0u, 0u};
 #pragma unroll
       for (int e = 0; e < 8; ++e) wk[e >> 2] |= (uint32_t)(uint8_t)code_of(y[k][e], r) << (8 * (e & 3));
-      *reinterpret_cast<uint2*>(kc + ch0) = make_uint2(wk[0], wk[1]);
+      *reinterpret_cast<uint2*>(kc + kc_byte(t, ch0)) = make_uint2(wk[0], wk[1]);
     }
     if (q == 0) reinterpret_cast<float*>(rec + kOffKsTok)[t] = r;
   }
-  reinterpret_cast<float*>(rec + kOffKsChan)[c] = S.s[c];
+  reinterpret_cast<float*>(rec + kOffKsChan)[ks_index(c)] = S.s[c];
   reinterpret_cast<float*>(rec + kOffVsChan)[c] = S.u[c];
 }
 
