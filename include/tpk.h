@@ -61,8 +61,8 @@ typedef enum {
 enum { TPK_IMPL_DEFAULT = 0, TPK_IMPL_SIMT = 1, TPK_IMPL_TENSOR = 2 };
 
 /* Bytes of one 8-bit page-head record:
- *   int8 kc[64][256]   key codes, token-major          offset 0
- *   int8 vc[256][64]   value codes, channel-major      offset 16384
+ *   u8   kc[64][256]   key codes, token-major          offset 0
+ *   u8   vc[256][64]   value codes, channel-major      offset 16384
  *   f32  ks_chan[256]  key channel scale s_c           offset 32768
  *   f32  ks_tok[64]    key per-token factor r_t        offset 33792
  *   f32  vs_chan[256]  value channel scale u_c         offset 34048
@@ -70,6 +70,8 @@ enum { TPK_IMPL_DEFAULT = 0, TPK_IMPL_SIMT = 1, TPK_IMPL_TENSOR = 2 };
  *   key code (t, c)   at byte t*256 + (c XOR 64*(t mod 2))
  *   value code (c, t) at byte c*64 + (t XOR 32*((c/2) mod 2))
  *   s_c               at float (c XOR 8*((c/32) mod 2))
+ * A code c in [-127, 127] is stored as the byte c + 128 (offset binary), so
+ * the tensor-core kernel widens it to f16 with one byte permute.
  * Dequantised: k_tc = kc_tc * s_c * r_t and v_tc = vc_tc * u_c. */
 #define TPK_RECORD_BYTES 35072
 

@@ -111,10 +111,11 @@ KS_POS = np.arange(D_HEAD) ^ (8 * ((np.arange(D_HEAD) >> 5) & 1))
 
 def record_fields(rec):
     """Split one 35,072-byte record into logical (kc[64][256], vc[64][256] (token
-    by channel), s[256], r[64], u[256]), undoing the position swizzles."""
+    by channel), s[256], r[64], u[256]), undoing the position swizzles and the
+    code bias (a code c is stored as the byte c + 128)."""
     rec = np.asarray(rec, np.uint8)
-    kc = rec[OFF_KC:OFF_VC].view(np.int8)[KC_POS]
-    vc = rec[OFF_VC:OFF_KS_CHAN].view(np.int8)[VC_POS]
+    kc = (rec[OFF_KC:OFF_VC][KC_POS].astype(np.int16) - 128).astype(np.int8)
+    vc = (rec[OFF_VC:OFF_KS_CHAN][VC_POS].astype(np.int16) - 128).astype(np.int8)
     s = rec[OFF_KS_CHAN:OFF_KS_TOK].view(np.float32)[KS_POS]
     r = rec[OFF_KS_TOK:OFF_VS_CHAN].view(np.float32)
     u = rec[OFF_VS_CHAN:REC_BYTES].view(np.float32)
@@ -124,14 +125,14 @@ def record_fields(rec):
 def pack_record(kc, vc, s, r, u):
     """Inverse of record_fields: logical fields -> 35,072-byte record."""
     rec = np.zeros(REC_BYTES, np.uint8)
-    kcb = np.zeros(T_PAGE * D_HEAD, np.int8)
-    kcb[KC_POS] = kc
-    vcb = np.zeros(T_PAGE * D_HEAD, np.int8)
-    vcb[VC_POS] = vc
+    kcb = np.zeros(T_PAGE * D_HEAD, np.uint8)
+    kcb[KC_POS] = (np.asarray(kc, np.int16) + 128).astype(np.uint8)
+    vcb = np.zeros(T_PAGE * D_HEAD, np.uint8)
+    vcb[VC_POS] = (np.asarray(vc, np.int16) + 128).astype(np.uint8)
     ks = np.zeros(D_HEAD, np.float32)
     ks[KS_POS] = s
-    rec[OFF_KC:OFF_VC] = kcb.view(np.uint8)
-    rec[OFF_VC:OFF_KS_CHAN] = vcb.view(np.uint8)
+    rec[OFF_KC:OFF_VC] = kcb
+    rec[OFF_VC:OFF_KS_CHAN] = vcb
     rec[OFF_KS_CHAN:OFF_KS_TOK] = ks.view(np.uint8)
     rec[OFF_KS_TOK:OFF_VS_CHAN] = np.asarray(r, np.float32).view(np.uint8)
     rec[OFF_VS_CHAN:REC_BYTES] = np.asarray(u, np.float32).view(np.uint8)

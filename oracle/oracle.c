@@ -34,8 +34,8 @@
  *     gives o = 0, lse = -inf.
  *
  * Record layout of one 8-bit page-head (35,072 bytes):
- *   int8  kc[64][256]      keys, token-major       offset 0
- *   int8  vc[256][64]      values, channel-major   offset 16384
+ *   u8    kc[64][256]      keys, token-major       offset 0
+ *   u8    vc[256][64]      values, channel-major   offset 16384
  *   f32   ks_chan[256]     key channel scale s_c   offset 32768
  *   f32   ks_tok[64]       key token factor r_t    offset 33792
  *   f32   vs_chan[256]     value channel scale u_c offset 34048
@@ -43,6 +43,7 @@
  *   key code (t, c)   at byte t*256 + (c XOR 64 * (t mod 2))
  *   value code (c, t) at byte c*64 + (t XOR 32 * ((c / 2) mod 2))
  *   s_c               at float (c XOR 8 * ((c / 32) mod 2))
+ * and each code c in [-127, 127] stored as the byte c + 128 (offset binary).
  * Dequantised: k_tc = kc_tc * s_c * r_t,  v_tc = vc_tc * u_c.
  */
 #include <math.h>
@@ -153,13 +154,13 @@ static int8_t code_of(float x, float scale) {
  */
 void orc_codes_given(const uint16_t* k, const uint16_t* v, const float* ks_chan, const float* ks_tok,
                      const float* vs_chan, uint8_t* rec) {
-  int8_t* kc = (int8_t*)(rec + OFF_KC);
-  int8_t* vc = (int8_t*)(rec + OFF_VC);
+  uint8_t* kc = rec + OFF_KC;
+  uint8_t* vc = rec + OFF_VC;
   for (int t = 0; t < T_PAGE; ++t)
     for (int c = 0; c < D_HEAD; ++c) {
       float y = bf16_float(k[t * D_HEAD + c]) / ks_chan[c];
-      kc[kc_pos(t, c)] = code_of(y, ks_tok[t]);
-      vc[vc_pos(c, t)] = code_of(bf16_float(v[t * D_HEAD + c]), vs_chan[c]);
+      kc[kc_pos(t, c)] = (uint8_t)(code_of(y, ks_tok[t]) + 128);
+      vc[vc_pos(c, t)] = (uint8_t)(code_of(bf16_float(v[t * D_HEAD + c]), vs_chan[c]) + 128);
     }
   float* ks = (float*)(rec + OFF_KS_CHAN);
   for (int c = 0; c < D_HEAD; ++c) ks[ks_pos(c)] = ks_chan[c];
@@ -280,8 +281,8 @@ static void partial_int8_head(int H, int G, int h, const uint16_t* q, const uint
   double* qd = (double*)malloc(sizeof(double) * (size_t)G * d);
   for (int p = 0; p < np; ++p) {
     const uint8_t* rec = rec_pool + ((int64_t)page_table8[page_begin + p] * H + h) * REC_BYTES;
-    const int8_t* kc = (const int8_t*)(rec + OFF_KC);
-    const int8_t* vc = (const int8_t*)(rec + OFF_VC);
+    const uint8_t* kc = rec + OFF_KC;
+    const uint8_t* vc = rec + OFF_VC;
     float s[D_HEAD], r[T_PAGE], u[D_HEAD], s_stored[D_HEAD];
     memcpy(s_stored, rec + OFF_KS_CHAN, sizeof s_stored);
     for (int c = 0; c < D_HEAD; ++c) s[c] = s_stored[ks_pos(c)];
@@ -290,8 +291,8 @@ static void partial_int8_head(int H, int G, int h, const uint16_t* q, const uint
     for (int t = 0; t < T_PAGE; ++t)
       for (int c = 0; c < d; ++c) {
         int64_t i = ((int64_t)p * T_PAGE + t) * d + c;
-        K[i] = (double)kc[kc_pos(t, c)] * (double)s[c] * (double)r[t];
-        V[i] = (double)vc[vc_pos(c, t)] * (double)u[c];
+        K[i] = (double)((int)kc[kc_pos(t, c)] - 128) * (double)s[c] * (double)r[t];
+        V[i] = (double)((int)vc[vc_pos(c, t)] - 128) * (double)u[c];
       }
   }
   for (int g = 0; g < G; ++g)

@@ -202,3 +202,19 @@ def test_pool_conversion_places_records():
             one, _ = oracle.quantize_page_head(w.k_pool[slot, h], w.v_pool[slot, h])
             at = (slot * w.H + h) * oracle.REC_BYTES
             assert np.array_equal(rec_pool[at:at + oracle.REC_BYTES], one)
+
+
+def test_code_bytes_are_offset_binary():
+    """A code c is stored as the byte c + 128: an all-zero page stores 0x80 in
+    every code byte, and a page whose codes reach +-127 stores 0xff and 0x01."""
+    z = np.zeros((64, 256), np.uint16)
+    rec = oracle.quantize_page_head(z, z)[0]
+    assert np.all(rec[oracle.OFF_KC:oracle.OFF_KS_CHAN] == 0x80)
+    k, v = random_page(0, "unit")
+    rec = oracle.quantize_page_head(k, v)[0]
+    kc, vc = oracle.record_fields(rec)[:2]
+    raw = rec[oracle.OFF_KC:oracle.OFF_KS_CHAN]
+    assert raw.min() >= 1 and raw.max() <= 255
+    assert 127 in np.abs(kc) and 127 in np.abs(vc)
+    assert np.array_equal(np.sort(raw.astype(np.int16) - 128),
+                          np.sort(np.concatenate([kc.ravel(), vc.ravel()]).astype(np.int16)))

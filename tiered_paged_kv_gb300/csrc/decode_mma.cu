@@ -21,10 +21,14 @@
 //         (rows 0-7 and 8-15 of the tile), B = key codes; the per-token factor r_t
 //         is applied to the scores after the dot product;
 //   PV  A = value codes (channel-major, so four consecutive tokens of a channel
-//         are one word), B = the probabilities as f16 high and low planes (two
-//         products); each page's result is rescaled by its value scale u_c and
-//         added to the FP32 accumulator -- PV runs on raw codes and is rescaled
-//         per page.
+//         are one word), B = the probabilities as one f16 plane (the weights are
+//         rounded to f16 before they enter the row sums too); each page's result
+//         is rescaled by its value scale u_c and added to the FP32 accumulator --
+//         PV runs on raw codes and is rescaled per page.
+// The stored code bytes (code + 128) widen to f16 as 1152 + code with one byte
+// permute per two codes; the 1152 offset is removed once per page and row: from
+// the scores as 1152 * sum_c q'_c, and from the PV accumulator, which starts at
+// -1152 * sum_t p_t.
 // The integer tensor path (s8 x s8) is not used: on this GPU it runs at about a
 // quarter of the f16 rate.
 //
@@ -111,18 +115,13 @@ __device__ __forceinline__ float f16_lo(uint32_t w) {
 }
 __device__ __forceinline__ float f16_hi(uint32_t w) { return __half2float(__ushort_as_half((unsigned short)(w >> 16))); }
 
-// Four signed 8-bit codes -> two f16 pairs, exactly: each byte biased by 128
-// becomes the mantissa of 1024 (f16 0x6400 | u = 1024 + u), then 1152 is
-// subtracted.  lo = bytes 0, 1; hi = bytes 2, 3.
+// Four stored code bytes (code + 128) -> two f16 pairs holding 1152 + code,
+// exactly: each byte becomes the low mantissa byte of f16 1024 (0x6400 | b =
+// 1024 + b).  lo = bytes 0, 1; hi = bytes 2, 3.
+constexpr float kCodeOffset = 1152.f;
 __device__ __forceinline__ void codes_to_f16(uint32_t w, uint32_t& lo, uint32_t& hi) {
-  const uint32_t x = w ^ 0x80808080u;
-  const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));  // 1152
-  uint32_t a = __byte_perm(x, 0x64646464u, 0x5140);
-  uint32_t b = __byte_perm(x, 0x64646464u, 0x5342);
-  __half2 ha = __hsub2(*reinterpret_cast<__half2*>(&a), bias);
-  __half2 hb = __hsub2(*reinterpret_cast<__half2*>(&b), bias);
-  lo = *reinterpret_cast<uint32_t*>(&ha);
-  hi = *reinterpret_cast<uint32_t*>(&hb);
+  lo = __byte_perm(w, 0x64646464u, 0x5140);
+  hi = __byte_perm(w, 0x64646464u, 0x5342);
 }
 
 // ----------------------------------------------------------------- producer
@@ -166,10 +165,10 @@ __device__ __forceinline__ void mma_issue(const DecodeParams& p, const UnitInfo&
 }
 
 // Online-softmax update for this thread's base-2 scores x[] of query row g (-inf
-// where masked).  Rescales O (rows 2t, 2t + 1) when a row maximum moved and
-// turns x[] into weights.
+// where masked).  Rescales O (rows 2t, 2t + 1) when a row maximum moved, turns
+// x[] into weights and returns the factor alpha the row sum must be scaled by.
 template <int N>
-__device__ __forceinline__ void softmax_update(float (&x)[N], float& m_run, float& l_run, float (&O)[16][4]) {
+__device__ __forceinline__ float softmax_rescale(float (&x)[N], float& m_run, float (&O)[16][4]) {
   const int lane = threadIdx.x & 31, t = lane & 3;
   float mx = kNegInf;
 #pragma unroll
@@ -189,14 +188,10 @@ __device__ __forceinline__ void softmax_update(float (&x)[N], float& m_run, floa
       O[m][3] *= a1;
     }
   }
-  float l = l_run * alpha;
 #pragma unroll
-  for (int i = 0; i < N; ++i) {
-    x[i] = (x[i] == kNegInf) ? 0.f : exp2f(x[i] - m_new);
-    l += x[i];
-  }
-  l_run = l;
+  for (int i = 0; i < N; ++i) x[i] = (x[i] == kNegInf) ? 0.f : exp2f(x[i] - m_new);
   m_run = m_new;
+  return alpha;
 }
 
 // ------------------------------------------------------- 8-bit half page
@@ -218,6 +213,7 @@ __device__ __forceinline__ void process_int8_half(const uint8_t* rec, int h, con
   float acc[4][4];
 #pragma unroll
   for (int j = 0; j < 4; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+  float qsum = 0.f;  // sum of this thread's 64 folded-query values of row g
 #pragma unroll
   for (int J = 0; J < 4; ++J) {
     uint4 kw[4];
@@ -231,6 +227,7 @@ __device__ __forceinline__ void process_int8_half(const uint8_t* rec, int h, con
       const float4 s4 = *reinterpret_cast<const float4*>(ks + ks_index(ch));
       const float4 q4 = *reinterpret_cast<const float4*>(qrow + ks_index(ch));
       const float x0 = q4.x * s4.x, x1 = q4.y * s4.y, x2 = q4.z * s4.z, x3 = q4.w * s4.w;
+      qsum += (x0 + x1) + (x2 + x3);
       const uint32_t h01 = pack_f16(x0, x1), h23 = pack_f16(x2, x3);
       const uint32_t l01 = pack_f16(x0 - f16_lo(h01), x1 - f16_hi(h01));
       const uint32_t l23 = pack_f16(x2 - f16_lo(h23), x3 - f16_hi(h23));
@@ -243,6 +240,10 @@ __device__ __forceinline__ void process_int8_half(const uint8_t* rec, int h, con
       }
     }
   }
+  // The products ran on 1152 + code: remove 1152 * sum_c q'_c (row g, all 256
+  // channels) from the high plane's dot before the low plane's is added.
+  qsum += __shfl_xor_sync(kAll, qsum, 1);
+  qsum += __shfl_xor_sync(kAll, qsum, 2);
   // scores (base 2): high + low planes, times r_t of each token
   float x[8];
   {
@@ -251,35 +252,40 @@ __device__ __forceinline__ void process_int8_half(const uint8_t* rec, int h, con
     const float rr[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      x[2 * j] = (acc[j][0] + acc[j][2]) * qk_scale * rr[2 * j];
-      x[2 * j + 1] = (acc[j][1] + acc[j][3]) * qk_scale * rr[2 * j + 1];
+      x[2 * j] = (fmaf(-kCodeOffset, qsum, acc[j][0]) + acc[j][2]) * qk_scale * rr[2 * j];
+      x[2 * j + 1] = (fmaf(-kCodeOffset, qsum, acc[j][1]) + acc[j][3]) * qk_scale * rr[2 * j + 1];
     }
   }
-  softmax_update<8>(x, m_run, l_run, O);
-  // P^T as f16 high / low planes for the two k-steps
-  uint32_t ph[2][2], pl[2][2];
+  const float alpha = softmax_rescale<8>(x, m_run, O);
+  // P^T as one f16 plane: pw[k] = tokens 8t + 2k, 8t + 2k + 1 of row g.  The
+  // rounded weights are the ones summed into l, so numerator and denominator
+  // use the same probabilities.
+  uint32_t pw[4];
+  float lp = 0.f;
 #pragma unroll
-  for (int i = 0; i < 2; ++i)
-#pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      const float p0 = x[2 * (2 * i + hh)], p1 = x[2 * (2 * i + hh) + 1];
-      const uint32_t hi = pack_f16(p0, p1);
-      ph[i][hh] = hi;
-      pl[i][hh] = pack_f16(p0 - f16_lo(hi), p1 - f16_hi(hi));
-    }
+  for (int k = 0; k < 4; ++k) {
+    pw[k] = pack_f16(x[2 * k], x[2 * k + 1]);
+    lp += f16_lo(pw[k]) + f16_hi(pw[k]);
+  }
+  l_run = l_run * alpha + lp;
+  // sum of the half's 32 weights of each row; the PV accumulator of rows 2t and
+  // 2t + 1 starts at -1152 times it, cancelling the code offset
+  float ps = lp + __shfl_xor_sync(kAll, lp, 1);
+  ps += __shfl_xor_sync(kAll, ps, 2);
+  const float c0 = -kCodeOffset * __shfl_sync(kAll, ps, 8 * t);
+  const float c1 = -kCodeOffset * __shfl_sync(kAll, ps, 8 * t + 4);
   // ---- PV: 16 channel tiles; each page result times u_c into the accumulator
 #pragma unroll
   for (int m = 0; m < 16; ++m) {
     const uint2 va = *reinterpret_cast<const uint2*>(vc + vc_byte(16 * m + g, 32 * h + 8 * t));
     const uint2 vb = *reinterpret_cast<const uint2*>(vc + vc_byte(16 * m + g + 8, 32 * h + 8 * t));
-    float c[4] = {0.f, 0.f, 0.f, 0.f};
+    float c[4] = {c0, c1, c0, c1};
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
       uint32_t a0, a2, a1, a3;
       codes_to_f16(i == 0 ? va.x : va.y, a0, a2);
       codes_to_f16(i == 0 ? vb.x : vb.y, a1, a3);
-      mma_f16(c, a0, a1, a2, a3, ph[i][0], ph[i][1]);
-      mma_f16(c, a0, a1, a2, a3, pl[i][0], pl[i][1]);
+      mma_f16(c, a0, a1, a2, a3, pw[2 * i], pw[2 * i + 1]);
     }
     const float ua = vs[16 * m + g], ub = vs[16 * m + g + 8];
     O[m][0] = fmaf(ua, c[0], O[m][0]);
@@ -328,7 +334,10 @@ __device__ __forceinline__ void process_bf16_quarter(uint8_t* slot, int h, int t
       const int tok = base + 8 * j + 2 * t + e;
       x[2 * j + e] = (tok >= tb && tok < te) ? acc[j][e] * qscale : kNegInf;
     }
-  softmax_update<4>(x, m_run, l_run, O);
+  {
+    const float alpha = softmax_rescale<4>(x, m_run, O);
+    l_run = l_run * alpha + ((x[0] + x[1]) + (x[2] + x[3]));
+  }
   const uint32_t ph0 = pack_bf16(x[0], x[1]), ph1 = pack_bf16(x[2], x[3]);
   const uint32_t pl0 = pack_bf16(x[0] - bf16_lo(ph0), x[1] - bf16_hi(ph0));
   const uint32_t pl1 = pack_bf16(x[2] - bf16_lo(ph1), x[3] - bf16_hi(ph1));

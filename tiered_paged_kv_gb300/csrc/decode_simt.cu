@@ -41,10 +41,10 @@ __device__ __forceinline__ float reduce_scatter32(float (&v)[32]) {
   return v[0];
 }
 
-// 8 signed 8-bit codes (two words) -> floats, exactly: each byte (biased by 128)
-// is placed in the mantissa of 2^23 and the bias 2^23 + 128 is subtracted.
+// 8 stored code bytes (two words) -> the codes as floats, exactly: each byte
+// (the code plus 128) is placed in the mantissa of 2^23 and 2^23 + 128 is subtracted.
 __device__ __forceinline__ void codes8_to_float(uint2 w, float (&f)[8]) {
-  uint32_t a = w.x ^ 0x80808080u, b = w.y ^ 0x80808080u;
+  const uint32_t a = w.x, b = w.y;
   const float bias = 8388736.0f;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
@@ -222,8 +222,8 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_simt_kernel(const __gri
         }
       } else {
         // ---------------- 8-bit tier: one 64-token record, 16 tokens per warp
-        const int8_t* kc = reinterpret_cast<const int8_t*>(slot + kOffKc);
-        const int8_t* vc = reinterpret_cast<const int8_t*>(slot + kOffVc);  // token-major after the transpose
+        const uint8_t* kc = slot + kOffKc;
+        const uint8_t* vc = slot + kOffVc;  // token-major after the transpose
         const float* ks = reinterpret_cast<const float*>(slot + kOffKsChan);
         const float* kr = reinterpret_cast<const float*>(slot + kOffKsTok);
         const float* vs = reinterpret_cast<const float*>(slot + kOffVsChan);

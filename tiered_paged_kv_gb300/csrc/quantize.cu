@@ -48,11 +48,12 @@ __device__ __forceinline__ double pow4_minus(float c, double x) {
   return (hi - x) + lo;
 }
 
-__device__ __forceinline__ int8_t code_of(float x, float scale) {
-  if (!(scale > 0.f)) return 0;
+// The stored byte of a code: clamp(rint(x / scale), -127, 127) + 128 (offset binary).
+__device__ __forceinline__ uint32_t code_byte(float x, float scale) {
+  if (!(scale > 0.f)) return 128u;
   float z = rintf(__fdiv_rn(x, scale));
   z = fminf(fmaxf(z, -127.f), 127.f);
-  return (int8_t)(int)z;
+  return (uint32_t)((int)z + 128);
 }
 
 __global__ void __launch_bounds__(256) quantize_kernel(const __grid_constant__ QuantParams p) {
@@ -97,7 +98,7 @@ __global__ void __launch_bounds__(256) quantize_kernel(const __grid_constant__ Q
       uint32_t wv[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
       for (int e = 0; e < 16; ++e)
-        wv[e >> 2] |= (uint32_t)(uint8_t)code_of(bf16_lo(S.v[t0 + e][c]), u) << (8 * (e & 3));
+        wv[e >> 2] |= code_byte(bf16_lo(S.v[t0 + e][c]), u) << (8 * (e & 3));
       *reinterpret_cast<uint4*>(rec + kOffVc + vc_byte(c, t0)) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
     }
   }
@@ -239,7 +240,7 @@ __global__ void __launch_bounds__(256) quantize_kernel(const __grid_constant__ Q
       const int ch0 = q * 64 + ((k + lane) & 7) * 8;
       uint32_t wk[2] = {0u, 0u};
 #pragma unroll
-      for (int e = 0; e < 8; ++e) wk[e >> 2] |= (uint32_t)(uint8_t)code_of(y[k][e], r) << (8 * (e & 3));
+      for (int e = 0; e < 8; ++e) wk[e >> 2] |= code_byte(y[k][e], r) << (8 * (e & 3));
       *reinterpret_cast<uint2*>(kc + kc_byte(t, ch0)) = make_uint2(wk[0], wk[1]);
     }
     if (q == 0) reinterpret_cast<float*>(rec + kOffKsTok)[t] = r;
