@@ -40,6 +40,16 @@ def test_ragged_batch(impl, gpu_records):
 
 
 @pytest.mark.parametrize("impl", IMPLS)
+@pytest.mark.parametrize("n_req", [4, 5])
+def test_plan_sizes(impl, n_req):
+    """Launches of up to four requests take the short plan parameter, longer
+    ones the full one: both sides of the boundary."""
+    lengths = [300 + 517 * i for i in range(n_req)]
+    w = synth.make_workload(lengths, 128, H=2, seed=30 + n_req, key_sigma="outliers")
+    check_hybrid(w, impl, what=f"{n_req} requests")
+
+
+@pytest.mark.parametrize("impl", IMPLS)
 def test_only_one_tier(impl):
     check_hybrid(synth.make_workload([5000, 77], None, H=2, seed=22), impl, what="all exact")
     w = synth.make_workload([64 * 30, 64 * 3], 0, H=2, seed=23)

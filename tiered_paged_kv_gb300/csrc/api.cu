@@ -13,14 +13,14 @@
 #include "tpk.h"
 
 namespace tpk {
-cudaError_t launch_decode_simt(const DecodeParams& p, cudaStream_t stream);
+cudaError_t launch_decode_simt(const DecodeParams& p, const ReqPlan* req, cudaStream_t stream);
 int decode_simt_blocks_per_sm();
-cudaError_t launch_decode_mma(const DecodeParams& p, cudaStream_t stream);
+cudaError_t launch_decode_mma(const DecodeParams& p, const ReqPlan* req, cudaStream_t stream);
 int decode_mma_blocks_per_sm();
 cudaError_t launch_merge(int n_parts, int rows, const float* o_parts, const float* lse_parts, float* o_acc,
                          float* lse_acc, cudaStream_t stream);
 cudaError_t launch_quantize(const QuantParams& p, int n_pages, cudaStream_t stream);
-cudaError_t launch_fold(const DecodeParams& p, cudaStream_t stream);
+cudaError_t launch_fold(const DecodeParams& p, const ReqPlan* req, cudaStream_t stream);
 }  // namespace tpk
 
 using namespace tpk;
@@ -160,8 +160,8 @@ int blocks_per_sm(const tpk_shape* s) {
   return mma;
 }
 
-tpk_status launch_decode(const tpk_shape* s, const DecodeParams& p, cudaStream_t st) {
-  cudaError_t e = use_simt(s) ? launch_decode_simt(p, st) : launch_decode_mma(p, st);
+tpk_status launch_decode(const tpk_shape* s, const DecodeParams& p, const ReqPlan* req, cudaStream_t st) {
+  cudaError_t e = use_simt(s) ? launch_decode_simt(p, req, st) : launch_decode_mma(p, req, st);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   return TPK_OK;
 }
@@ -248,16 +248,16 @@ tpk_status tpk_decode_attn_exact(const tpk_shape* shape, const void* q, const vo
   if (!p.status) return fail(TPK_ERR_CUDA, "cannot resolve the device status word");
   p.mode = kModePrimitive;
   p.n_req = 1;
-  p.req[0] = ReqPlan{0, 0, tok_begin, tok_end, 0, 0, 0, (int16_t)0, (int16_t)0};
+  ReqPlan req = ReqPlan{0, 0, tok_begin, tok_end, 0, 0, 0, (int16_t)0, (int16_t)0};
   // int16 split counts: fold larger counts through the unit decode's int arithmetic
   if (num_splits > 32767) return fail(TPK_ERR_INVALID, "num_splits too large");
-  p.req[0].splits_e = (int16_t)num_splits;
+  req.splits_e = (int16_t)num_splits;
   p.n_units = num_splits * shape->kv_heads;
   if (tok_end > tok_begin) {
     st = make_pool_maps(p, shape, k_pool, v_pool);
     if (st != TPK_OK) return st;
   }
-  return launch_decode(shape, p, reinterpret_cast<cudaStream_t>(stream));
+  return launch_decode(shape, p, &req, reinterpret_cast<cudaStream_t>(stream));
 }
 
 tpk_status tpk_decode_attn_int8(const tpk_shape* shape, const void* q, const void* rec_pool,
@@ -282,9 +282,9 @@ tpk_status tpk_decode_attn_int8(const tpk_shape* shape, const void* q, const voi
   if (!p.status) return fail(TPK_ERR_CUDA, "cannot resolve the device status word");
   p.mode = kModePrimitive;
   p.n_req = 1;
-  p.req[0] = ReqPlan{0, 0, 0, 0, 0, page_begin, page_end, (int16_t)0, (int16_t)num_splits};
+  const ReqPlan req = ReqPlan{0, 0, 0, 0, 0, page_begin, page_end, (int16_t)0, (int16_t)num_splits};
   p.n_units = num_splits * shape->kv_heads;
-  return launch_decode(shape, p, reinterpret_cast<cudaStream_t>(stream));
+  return launch_decode(shape, p, &req, reinterpret_cast<cudaStream_t>(stream));
 }
 
 tpk_status tpk_merge_lse(int n_parts, int rows, int head_dim, const float* o_parts, const float* lse_parts,
@@ -397,11 +397,12 @@ tpk_status tpk_decode_hybrid_batched(const tpk_shape* shape, int n_req, const vo
   }
   DecodeParams p;
   fill_common(p, shape, q);
+  std::vector<ReqPlan> req(n_req);
   int units = 0;
   for (int b = 0; b < n_req; ++b) {
     const int se = cnt[2 * b], s8 = cnt[2 * b + 1];
     if (se > 32767 || s8 > 32767) return fail(TPK_ERR_UNSUPPORTED, "request %d: too many splits", b);
-    p.req[b] = ReqPlan{units, req_page_off[b], 0, n_exact_tokens[b], req_page_off8[b], 0, n_int8_pages[b],
+    req[b] = ReqPlan{units, req_page_off[b], 0, n_exact_tokens[b], req_page_off8[b], 0, n_int8_pages[b],
                        (int16_t)se, (int16_t)s8};
     units += H * (se + s8);
   }
@@ -426,12 +427,12 @@ tpk_status tpk_decode_hybrid_batched(const tpk_shape* shape, int n_req, const vo
     st = make_pool_maps(p, shape, k_pool, v_pool);
     if (st != TPK_OK) return st;
   }
-  st = launch_decode(shape, p, reinterpret_cast<cudaStream_t>(stream));
+  st = launch_decode(shape, p, req.data(), reinterpret_cast<cudaStream_t>(stream));
   if (st != TPK_OK) return st;
   bool any_split = false;
-  for (int b = 0; b < n_req; ++b) any_split |= p.req[b].splits_e + p.req[b].splits_8 > 1;
+  for (int b = 0; b < n_req; ++b) any_split |= req[b].splits_e + req[b].splits_8 > 1;
   if (any_split) {
-    cudaError_t e = launch_fold(p, reinterpret_cast<cudaStream_t>(stream));
+    cudaError_t e = launch_fold(p, req.data(), reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "fold launch");
   }
   return TPK_OK;

@@ -53,6 +53,14 @@ struct ReqPlan {
 };
 
 constexpr int kMaxReqPerLaunch = 256;
+// Launches of at most kShortPlan requests pass a short plan: the kernels take
+// the plan as a parameter, and a smaller parameter block is set up faster at
+// every launch.
+constexpr int kShortPlan = 4;
+template <int R>
+struct Plan {
+  ReqPlan req[R];
+};
 
 enum : int { kModePrimitive = 0, kModeFold = 1 };
 
@@ -77,7 +85,6 @@ struct DecodeParams {
   int mode;
   int n_req;
   int n_units;
-  ReqPlan req[kMaxReqPerLaunch];
 };
 
 struct UnitInfo {
@@ -86,13 +93,13 @@ struct UnitInfo {
   int pt_off;
 };
 
-__device__ __forceinline__ UnitInfo decode_unit(const DecodeParams& p, int u) {
+__device__ __forceinline__ UnitInfo decode_unit(const DecodeParams& p, const ReqPlan* req, int u) {
   int lo = 0, hi = p.n_req - 1;
   while (lo < hi) {
     int mid = (lo + hi + 1) >> 1;
-    if (p.req[mid].unit_base <= u) lo = mid; else hi = mid - 1;
+    if (req[mid].unit_base <= u) lo = mid; else hi = mid - 1;
   }
-  const ReqPlan& r = p.req[lo];
+  const ReqPlan& r = req[lo];
   UnitInfo ui;
   ui.b = lo;
   int local = u - r.unit_base;

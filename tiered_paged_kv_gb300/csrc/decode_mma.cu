@@ -352,14 +352,16 @@ __device__ __forceinline__ void process_bf16_quarter(uint8_t* slot, int h, int t
 }
 
 // ------------------------------------------------------------------ kernel
-__global__ void __launch_bounds__(kMmaThreads, 1) decode_mma_kernel(const __grid_constant__ DecodeParams p) {
+template <int R>
+__global__ void __launch_bounds__(kMmaThreads, 1) decode_mma_kernel(const __grid_constant__ DecodeParams p,
+                                                                  const __grid_constant__ Plan<R> plan) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   MmaSmem& S = *reinterpret_cast<MmaSmem*>(smem_raw);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, t = lane & 3;
 
   allow_dependent_launch();
-  const UnitInfo ui = decode_unit(p, blockIdx.x);
+  const UnitInfo ui = decode_unit(p, plan.req, blockIdx.x);
   const Items it = unit_items(ui);
   if (tid == 0) {
     for (int s = 0; s < kMmaSlots; ++s) {
@@ -480,24 +482,33 @@ __global__ void __launch_bounds__(kMmaThreads, 1) decode_mma_kernel(const __grid
   write_and_fold<kCons>(p, ui, S, ep_o);
 }
 
-cudaError_t launch_decode_mma(const DecodeParams& p, cudaStream_t stream) {
+template <int R>
+static cudaError_t launch_mma(const DecodeParams& p, const ReqPlan* req, cudaStream_t stream) {
   static bool configured = false;
   const int smem = (int)sizeof(MmaSmem);
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<R>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  if (p.n_units == 0) return cudaSuccess;
-  decode_mma_kernel<<<p.n_units, kMmaThreads, smem, stream>>>(p);
+  Plan<R> plan = {};
+  for (int b = 0; b < p.n_req; ++b) plan.req[b] = req[b];
+  decode_mma_kernel<R><<<p.n_units, kMmaThreads, smem, stream>>>(p, plan);
   return cudaGetLastError();
+}
+
+cudaError_t launch_decode_mma(const DecodeParams& p, const ReqPlan* req, cudaStream_t stream) {
+  if (p.n_units == 0) return cudaSuccess;
+  return p.n_req <= kShortPlan ? launch_mma<kShortPlan>(p, req, stream)
+                               : launch_mma<kMaxReqPerLaunch>(p, req, stream);
 }
 
 int decode_mma_blocks_per_sm() {
   int n = 0;
   const int smem = (int)sizeof(MmaSmem);
-  cudaFuncSetAttribute(decode_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_mma_kernel, kMmaThreads, smem) != cudaSuccess)
+  cudaFuncSetAttribute(decode_mma_kernel<kMaxReqPerLaunch>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_mma_kernel<kMaxReqPerLaunch>, kMmaThreads, smem) !=
+      cudaSuccess)
     return 1;
   return n > 0 ? n : 1;
 }

@@ -122,13 +122,15 @@ __device__ __forceinline__ float softmax_step(SoftmaxState& st, float x, float (
   return p;
 }
 
-__global__ void __launch_bounds__(kDecThreads, 2) decode_simt_kernel(const __grid_constant__ DecodeParams p) {
+template <int R>
+__global__ void __launch_bounds__(kDecThreads, 2) decode_simt_kernel(const __grid_constant__ DecodeParams p,
+                                                                   const __grid_constant__ Plan<R> plan) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   DecSmem& S = *reinterpret_cast<DecSmem*>(smem_raw);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
   allow_dependent_launch();
-  const UnitInfo ui = decode_unit(p, blockIdx.x);
+  const UnitInfo ui = decode_unit(p, plan.req, blockIdx.x);
   const Items it = unit_items(ui);
 
   if (tid == 0) {
@@ -314,24 +316,33 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_simt_kernel(const __gri
   write_and_fold<kDecWarps>(p, ui, S, ep_o);
 }
 
-cudaError_t launch_decode_simt(const DecodeParams& p, cudaStream_t stream) {
+template <int R>
+static cudaError_t launch_simt(const DecodeParams& p, const ReqPlan* req, cudaStream_t stream) {
   static bool configured = false;
   const int smem = (int)sizeof(DecSmem);
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(decode_simt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = cudaFuncSetAttribute(decode_simt_kernel<R>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  if (p.n_units == 0) return cudaSuccess;
-  decode_simt_kernel<<<p.n_units, kDecThreads, smem, stream>>>(p);
+  Plan<R> plan = {};
+  for (int b = 0; b < p.n_req; ++b) plan.req[b] = req[b];
+  decode_simt_kernel<R><<<p.n_units, kDecThreads, smem, stream>>>(p, plan);
   return cudaGetLastError();
+}
+
+cudaError_t launch_decode_simt(const DecodeParams& p, const ReqPlan* req, cudaStream_t stream) {
+  if (p.n_units == 0) return cudaSuccess;
+  return p.n_req <= kShortPlan ? launch_simt<kShortPlan>(p, req, stream)
+                               : launch_simt<kMaxReqPerLaunch>(p, req, stream);
 }
 
 int decode_simt_blocks_per_sm() {
   int n = 0;
   const int smem = (int)sizeof(DecSmem);
-  cudaFuncSetAttribute(decode_simt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_simt_kernel, kDecThreads, smem) != cudaSuccess)
+  cudaFuncSetAttribute(decode_simt_kernel<kMaxReqPerLaunch>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_simt_kernel<kMaxReqPerLaunch>, kDecThreads, smem) !=
+      cudaSuccess)
     return 1;
   return n > 0 ? n : 1;
 }

@@ -41,7 +41,9 @@ __global__ void __launch_bounds__(kHeadDim) merge_kernel(int n_parts, int rows, 
 // for the thread's channel is loaded in batches of 16 independent loads.
 constexpr int kFoldQuarters = 4;
 constexpr int kFoldFast = 64;  // heads with at most this many units (= threads per block) fold in one round trip
-__global__ void __launch_bounds__(64) fold_kernel(const __grid_constant__ DecodeParams p) {
+template <int R>
+__global__ void __launch_bounds__(64) fold_kernel(const __grid_constant__ DecodeParams p,
+                                                  const __grid_constant__ Plan<R> plan) {
   constexpr int kChunk = 2048;  // partials per shared-memory pass
   __shared__ float lse_s[kChunk];
   __shared__ float w_s[kChunk];
@@ -52,7 +54,7 @@ __global__ void __launch_bounds__(64) fold_kernel(const __grid_constant__ Decode
   const int b = row / (p.H * G);
   const int h = (row / G) % p.H;
   const int r = row % G;
-  const ReqPlan& rp = p.req[b];
+  const ReqPlan& rp = plan.req[b];
   const int n = rp.splits_e + rp.splits_8;
   if (n <= 1) return;  // a single unit wrote the output itself
   wait_for_primary_grid();
@@ -143,7 +145,10 @@ __global__ void __launch_bounds__(64) fold_kernel(const __grid_constant__ Decode
   if (c == 0) p.out_lse[row] = LSE;
 }
 
-cudaError_t launch_fold(const DecodeParams& p, cudaStream_t stream) {
+template <int R>
+static cudaError_t launch_fold_t(const DecodeParams& p, const ReqPlan* req, cudaStream_t stream) {
+  Plan<R> plan = {};
+  for (int b = 0; b < p.n_req; ++b) plan.req[b] = req[b];
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.n_req * p.H * kGroup * kFoldQuarters);
   cfg.blockDim = dim3(64);
@@ -154,7 +159,12 @@ cudaError_t launch_fold(const DecodeParams& p, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, fold_kernel, p);
+  return cudaLaunchKernelEx(&cfg, fold_kernel<R>, p, plan);
+}
+
+cudaError_t launch_fold(const DecodeParams& p, const ReqPlan* req, cudaStream_t stream) {
+  return p.n_req <= kShortPlan ? launch_fold_t<kShortPlan>(p, req, stream)
+                               : launch_fold_t<kMaxReqPerLaunch>(p, req, stream);
 }
 
 cudaError_t launch_merge(int n_parts, int rows, const float* o_parts, const float* lse_parts, float* o_acc,
