@@ -229,11 +229,6 @@ __device__ __forceinline__ void bulk_g2s(void* smem_dst, const void* gmem_src, u
       : "memory");
 }
 
-// Programmatic dependent launch: a decode block lets the dependent (fold) grid
-// launch once every block of the decode grid has started; the fold grid waits
-// for the decode grid to complete and its writes to be visible.
-__device__ __forceinline__ void allow_dependent_launch() { asm volatile("griddepcontrol.launch_dependents;"); }
-__device__ __forceinline__ void wait_for_primary_grid() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }

@@ -360,7 +360,6 @@ __global__ void __launch_bounds__(kMmaThreads, 1) decode_mma_kernel(const __grid
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, t = lane & 3;
 
-  allow_dependent_launch();
   const UnitInfo ui = decode_unit(p, plan.req, blockIdx.x);
   const Items it = unit_items(ui);
   if (tid == 0) {

@@ -129,7 +129,6 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_simt_kernel(const __gri
   DecSmem& S = *reinterpret_cast<DecSmem*>(smem_raw);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
-  allow_dependent_launch();
   const UnitInfo ui = decode_unit(p, plan.req, blockIdx.x);
   const Items it = unit_items(ui);
 

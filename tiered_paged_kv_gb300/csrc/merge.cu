@@ -57,7 +57,6 @@ __global__ void __launch_bounds__(64) fold_kernel(const __grid_constant__ Decode
   const ReqPlan& rp = plan.req[b];
   const int n = rp.splits_e + rp.splits_8;
   if (n <= 1) return;  // a single unit wrote the output itself
-  wait_for_primary_grid();
   const int first = rp.unit_base + h * n;
   const int c = qtr * 64 + threadIdx.x;
   const float ninf = -__builtin_huge_valf();
@@ -149,17 +148,8 @@ template <int R>
 static cudaError_t launch_fold_t(const DecodeParams& p, const ReqPlan* req, cudaStream_t stream) {
   Plan<R> plan = {};
   for (int b = 0; b < p.n_req; ++b) plan.req[b] = req[b];
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.n_req * p.H * kGroup * kFoldQuarters);
-  cfg.blockDim = dim3(64);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, fold_kernel<R>, p, plan);
+  fold_kernel<R><<<p.n_req * p.H * kGroup * kFoldQuarters, 64, 0, stream>>>(p, plan);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_fold(const DecodeParams& p, const ReqPlan* req, cudaStream_t stream) {
