@@ -9,10 +9,14 @@ same launch).
 
 value  = algorithmic history bytes / device time per step, inputs resident in
          HBM, L2 flushed between timed steps (256 MB written, then 256 MB read).
-e2e    = the same metric through the same C-ABI call with the history in pinned
-         host memory: each step copies the step's 8-bit records, recent BF16
-         pages, q and page tables host->device, runs the call, and reads o and
+e2e    = the same metric through the library's host-resident path: the step's
+         history image (8-bit records, recent BF16 pages, q, page tables) sits in
+         pinned host memory; each step stages it into a device slot through the
+         stager (tpk_stager_*), runs the decode call on the slot and reads o and
          lse back.
+host_resident = 16 layers of such history images in pinned host memory through
+         two device slots, each layer staged while the previous one decodes;
+         link GB/s against a plain pinned copy measured in the same run.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl {tpk,reference}]
 Under torchrun (N > 1) every rank runs an independent replica on its GPU.
@@ -281,6 +285,7 @@ def run_gpu(args, dist, rank, world):
 
     # ---- end to end from pinned host memory (packed history, identity page tables)
     e2e = run_e2e(args, w, rec, shape, stream, dev, dist)
+    host_res = run_host_resident(args, w, rec, shape, stream, dev, dist) if args.layers > 0 else None
 
     # ---- CPU oracle baseline (rank 0, N = 1)
     cpu = None
@@ -306,7 +311,7 @@ def run_gpu(args, dist, rank, world):
         "config": {"workload": WORKLOAD, "history_bytes_per_step": hist_bytes, "kernel": args.kernel,
                    "l2": "flushed between timed steps (256 MB written, then 256 MB read so dirty lines are written back outside the timed step); inputs 295 MB also exceed L2",
                    "clocks_sampled": "nvidia-smi every 100 ms over a soak of back-to-back steps and the timed steps",
-                   "launch": "device time of CUDA-graph replays of the step (one kernel); e2e calls the C ABI directly",
+                   "launch": "device time of CUDA-graph replays of the step (decode + fold kernels); e2e calls the C ABI directly",
                    "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
                    "page_conversion_us": round(quant_ms * 1e3, 1),
                    "page_conversion_GBps": round((w.H * int(w.n8.sum()) * (65536 + 35072)) / (quant_ms * 1e-3) / 1e9, 1)},
@@ -316,6 +321,7 @@ def run_gpu(args, dist, rank, world):
                      "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)" if peak_kind == "measured"
                      else "fallback 6.8 TB/s"},
         "e2e": e2e,
+        "host_resident": host_res,
         "gpu_launches": args.steps * launches_per_step,
         "clocks": clk.summary(),
         "cpu_baseline": cpu,
@@ -325,71 +331,165 @@ def run_gpu(args, dist, rank, world):
 
 
 def run_e2e(args, w, rec_dev, shape, stream, dev, dist):
+    """The step end to end through the library's host-resident path: the step's
+    history image (8-bit records, recent BF16 pages, q, page tables) sits in pinned
+    host memory; each step stages it into a device slot (tpk_stager_*), decodes
+    from the slot and reads o and lse back."""
     import torch
 
     import tiered_paged_kv_gb300 as tpk
 
     H, G = w.H, w.G
-    slots8 = w.int8_slots()
-    n8 = len(slots8)
-    rec_view = rec_dev.view(w.n_slots, H * tpk.RECORD_BYTES)
-    # packed host copies: the step's 8-bit records and recent BF16 pages, in page order
-    rec_h = torch.empty(n8, H * tpk.RECORD_BYTES, dtype=torch.uint8).pin_memory()
-    rec_h.copy_(rec_view[torch.from_numpy(slots8).to(dev)].cpu())
-    ex_slots = np.asarray(w.pages[0][w.n8[0]:])
-    ne = len(ex_slots)
-    k_h = torch.from_numpy(w.k_pool[ex_slots].view(np.int16)).pin_memory()
-    v_h = torch.from_numpy(w.v_pool[ex_slots].view(np.int16)).pin_memory()
-    q_h = torch.from_numpy(w.q.view(np.int16)).pin_memory()
-    pt_h = torch.arange(ne, dtype=torch.int32).pin_memory()
-    pt8_h = torch.arange(n8, dtype=torch.int32).pin_memory()
+    img, off = w.packed_image(rec_dev.cpu().numpy())
+    img_h = torch.from_numpy(img).pin_memory()
+    slots = [torch.empty(off["nbytes"], dtype=torch.uint8, device=dev) for _ in range(2)]
+    o_d = torch.empty(1, H * G, 256, dtype=torch.float32, device=dev)
+    lse_d = torch.empty(1, H * G, dtype=torch.float32, device=dev)
     o_h = torch.empty(1, H * G, 256, dtype=torch.float32).pin_memory()
     lse_h = torch.empty(1, H * G, dtype=torch.float32).pin_memory()
-    rec_d = torch.empty_like(rec_h, device=dev)
-    k_d = torch.empty_like(k_h, device=dev)
-    v_d = torch.empty_like(v_h, device=dev)
-    q_d = torch.empty_like(q_h, device=dev)
-    pt_d = torch.empty_like(pt_h, device=dev)
-    pt8_d = torch.empty_like(pt8_h, device=dev)
-    o_d = torch.empty_like(o_h, device=dev)
-    lse_d = torch.empty_like(lse_h, device=dev)
-    shape2 = tpk.Shape(H, impl=shape.impl, kv_slots=ne, rec_slots=n8)
+    shape2 = tpk.Shape(H, impl=shape.impl, kv_slots=off["n_exact_pages"], rec_slots=off["n_int8_pages"])
     nbytes = tpk.hybrid_workspace_bytes(shape2, 1)
     ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
-    off = np.array([0, ne], np.int32)
-    off8 = np.array([0, n8], np.int32)
-    h2d = [(rec_d, rec_h), (k_d, k_h), (v_d, v_h), (q_d, q_h), (pt_d, pt_h), (pt8_d, pt8_h)]
-    h2d_bytes = sum(h.numel() * h.element_size() for _, h in h2d)
+    views = [slot_views(s, off, w) for s in slots]
     d2h_bytes = o_h.numel() * 4 + lse_h.numel() * 4
+    st = tpk.Stager(slots, off["nbytes"])
 
     def step():
-        for d, h in h2d:
-            d.copy_(h, non_blocking=True)
-        tpk.decode_hybrid_batched(shape2, 1, q_d, k_d, v_d, rec_d, pt_d, off, w.n_ex, pt8_d, off8, w.n8, o_d, lse_d,
-                                  ws, nbytes, stream)
+        slot, _ = st.stage([(img_h, 0, off["nbytes"])])
+        st.acquire(slot, stream)
+        rec, k, v, q, pt, pt8 = views[slot]
+        tpk.decode_hybrid_batched(shape2, 1, q, k, v, rec, pt, off["req_page_off"], w.n_ex, pt8,
+                                  off["req_page_off8"], w.n8, o_d, lse_d, ws, nbytes, stream)
+        st.release(slot, stream)
         o_h.copy_(o_d, non_blocking=True)
         lse_h.copy_(lse_d, non_blocking=True)
 
-    with torch.cuda.stream(stream):
-        tpk.workspace_init(ws, nbytes, stream)
-        for _ in range(max(1, args.warmup)):
-            step()
-        stream.synchronize()
-        barrier(dist)
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
-        steps = max(3, args.steps // 2)
-        ev[0].record(stream)
-        for _ in range(steps):
-            step()
-        ev[1].record(stream)
-        stream.synchronize()
-        barrier(dist)
+    try:
+        with torch.cuda.stream(stream):
+            tpk.workspace_init(ws, nbytes, stream)
+            for _ in range(max(1, args.warmup)):
+                step()
+            stream.synchronize()
+            barrier(dist)
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+            steps = max(3, args.steps // 2)
+            ev[0].record(stream)
+            ev[0].synchronize()             # the first staging copy starts after the start event
+            for _ in range(steps):
+                step()
+            ev[1].record(stream)
+            stream.synchronize()
+            barrier(dist)
+    finally:
+        st.close()
     ms = ev[0].elapsed_time(ev[1]) / steps
     ms = max_over_ranks(dist, ms)
     world = dist.get_world_size() if dist is not None else 1
     return {"value": round(world * w.history_bytes() / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
-            "us_per_step": round(ms * 1e3, 1), "h2d_bytes_per_step": int(h2d_bytes),
-            "d2h_bytes_per_step": int(d2h_bytes), "steps": steps}
+            "us_per_step": round(ms * 1e3, 1), "h2d_bytes_per_step": int(off["nbytes"]),
+            "d2h_bytes_per_step": int(d2h_bytes), "steps": steps,
+            "path": "tpk_stager_stage/acquire/release + tpk_decode_hybrid_batched from pinned host memory"}
+
+
+def slot_views(s, off, w):
+    """Typed device views of one staged history image (a uint8 tensor)."""
+    H, G = w.H, w.G
+    n8, ne = off["n_int8_pages"], off["n_exact_pages"]
+    return (s[off["rec"]:off["rec"] + n8 * H * 35072],
+            s[off["k"]:off["k"] + ne * H * 64 * 256 * 2],
+            s[off["v"]:off["v"] + ne * H * 64 * 256 * 2],
+            s[off["q"]:off["q"] + w.B * H * G * 256 * 2],
+            s[off["pt"]:off["pt"] + max(ne, 1) * 4],
+            s[off["pt8"]:off["pt8"] + max(n8, 1) * 4])
+
+
+def host_mem_available():
+    try:
+        for line in open("/proc/meminfo"):
+            if line.startswith("MemAvailable:"):
+                return int(line.split()[1]) * 1024
+    except OSError:
+        pass
+    return 0
+
+
+def run_host_resident(args, w, rec_dev, shape, stream, dev, dist):
+    """Many layers of the same-sized history in pinned host memory (one image per
+    layer; the content of every layer is this workload's), two device slots: per
+    step every layer is staged while the previous layer decodes.  Bound by the
+    host->device link; the link peak is a plain 1 GiB pinned copy in the same run."""
+    import torch
+
+    import tiered_paged_kv_gb300 as tpk
+
+    H, G = w.H, w.G
+    img, off = w.packed_image(rec_dev.cpu().numpy())
+    layers = args.layers
+    avail = host_mem_available()
+    if avail and layers * off["nbytes"] * 2 > avail:  # keep well inside the host's memory
+        layers = max(2, int(avail // (2 * off["nbytes"])))
+    host = []
+    for _ in range(layers):
+        h = torch.empty(off["nbytes"], dtype=torch.uint8).pin_memory()
+        h.copy_(torch.from_numpy(img))
+        host.append(h)
+    slots = [torch.empty(off["nbytes"], dtype=torch.uint8, device=dev) for _ in range(2)]
+    shape2 = tpk.Shape(H, impl=shape.impl, kv_slots=off["n_exact_pages"], rec_slots=off["n_int8_pages"])
+    nbytes = tpk.hybrid_workspace_bytes(shape2, 1)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    outs = [(torch.empty(1, H * G, 256, dtype=torch.float32, device=dev),
+             torch.empty(1, H * G, dtype=torch.float32, device=dev)) for _ in range(layers)]
+    views = [slot_views(s, off, w) for s in slots]
+    st = tpk.Stager(slots, off["nbytes"])
+
+    def one_step():
+        pending = st.stage([(host[0], 0, off["nbytes"])])
+        for l in range(layers):
+            nxt = st.stage([(host[l + 1], 0, off["nbytes"])]) if l + 1 < layers else None
+            slot, _ = pending
+            st.acquire(slot, stream)
+            rec, k, v, q, pt, pt8 = views[slot]
+            tpk.decode_hybrid_batched(shape2, 1, q, k, v, rec, pt, off["req_page_off"], w.n_ex, pt8,
+                                      off["req_page_off8"], w.n8, outs[l][0], outs[l][1], ws, nbytes, stream)
+            st.release(slot, stream)
+            pending = nxt
+
+    try:
+        with torch.cuda.stream(stream):
+            one_step()
+            stream.synchronize()
+            times = []
+            for _ in range(args.host_steps):
+                ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+                ev[0].record(stream)
+                ev[0].synchronize()
+                one_step()
+                ev[1].record(stream)
+                stream.synchronize()
+                times.append(ev[0].elapsed_time(ev[1]))
+            # link peak: one plain pinned host->device copy of 1 GiB
+            big_h = torch.empty(1 << 30, dtype=torch.uint8).pin_memory()
+            big_d = torch.empty(1 << 30, dtype=torch.uint8, device=dev)
+            best = 0.0
+            for _ in range(3):
+                e = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+                e[0].record(stream)
+                big_d.copy_(big_h, non_blocking=True)
+                e[1].record(stream)
+                stream.synchronize()
+                best = max(best, (1 << 30) / (e[0].elapsed_time(e[1]) * 1e-3) / 1e9)
+            del big_h, big_d
+    finally:
+        st.close()
+    ms = statistics.median(times)
+    ms = max_over_ranks(dist, ms)
+    link = layers * off["nbytes"] / (ms * 1e-3) / 1e9
+    return {"layers": layers, "ms_per_step": round(ms, 3), "steps": len(times),
+            "h2d_bytes_per_step": int(layers * off["nbytes"]),
+            "link_GBps": round(link, 1), "link_peak_GBps": round(best, 1), "link_frac": round(link / best, 4),
+            "history_GBps": round(layers * w.history_bytes() / (ms * 1e-3) / 1e9, 1),
+            "slots": 2, "slot_bytes": int(off["nbytes"]),
+            "workload": f"{layers} layers x the 128K hybrid history (one pinned host image per layer)"}
 
 
 # ------------------------------------------------------------- reference arm
@@ -438,6 +538,8 @@ def main():
     ap.add_argument("--kernel", default="default", choices=["default", "simt", "tensor"])
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--soak", type=float, default=1.0, help="seconds of back-to-back steps before timing")
+    ap.add_argument("--layers", type=int, default=16, help="layers of the host-resident measurement (0: skip)")
+    ap.add_argument("--host-steps", type=int, default=5, help="timed steps of the host-resident measurement")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "tpk":
         args.warmup = 3

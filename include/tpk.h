@@ -225,6 +225,46 @@ tpk_status tpk_decode_hybrid_batched_static(const tpk_shape* shape, int n_req, c
                                             tpk_stream_t stream);
 
 /*
+ * Host-resident history staging ("ActiveKV", section on the host-authoritative KV
+ * tier: pinned host memory holds every layer's history, the GPU a per-layer
+ * staging working set of bounded size, filled by fenced asynchronous copies with
+ * an explicit lifecycle, so a buffer is never reused while a copy or a kernel
+ * still touches it).
+ *
+ * A stager owns one copy stream and two events per slot, created by
+ * tpk_stager_create (not on the hot path); the slots are caller-owned device
+ * buffers (16-byte aligned, slot_bytes each, on the device current at creation,
+ * which must be current for every later call).  One host thread drives a stager.
+ * Each slot cycles free -> staged -> acquired -> free:
+ *   tpk_stager_stage    copies n_regions pinned host ranges (host_src[i], bytes[i])
+ *                       to offsets slot_offset[i] of the next slot in round-robin
+ *                       order, on the copy stream, after that slot's last release;
+ *                       returns the slot index and its device address.  The host
+ *                       ranges are read asynchronously: keep them valid until the
+ *                       slot is acquired and the consumer has synchronised, or call
+ *                       tpk_stager_sync.  Pageable sources are rejected.
+ *   tpk_stager_acquire  makes `stream` wait for the slot's copies (call it right
+ *                       before the work that reads the slot, so the copies of the
+ *                       next layer overlap the current layer's decode).
+ *   tpk_stager_release  records, on `stream`, that the work queued so far has
+ *                       finished with the slot; the next staging into the slot
+ *                       waits for it.
+ * A call out of this order (staging into a slot that was not released, acquiring
+ * a slot that is not staged, releasing one that is not acquired) returns
+ * TPK_ERR_INVALID and changes nothing.  Not for use inside a stream capture.
+ * tpk_stager_sync waits for every copy issued so far; tpk_stager_destroy waits for
+ * them, then frees the stream and events (the slots stay the caller's).
+ */
+typedef struct tpk_stager tpk_stager;
+tpk_status tpk_stager_create(int n_slots, void* const* slots, size_t slot_bytes, tpk_stager** out);
+tpk_status tpk_stager_destroy(tpk_stager* stager);
+tpk_status tpk_stager_stage(tpk_stager* stager, int n_regions, const void* const* host_src,
+                            const size_t* slot_offset, const size_t* bytes, int* slot, void** slot_dev);
+tpk_status tpk_stager_acquire(tpk_stager* stager, int slot, tpk_stream_t stream);
+tpk_status tpk_stager_release(tpk_stager* stager, int slot, tpk_stream_t stream);
+tpk_status tpk_stager_sync(tpk_stager* stager);
+
+/*
  * Device status word: bit 0 = a page-table entry outside the pool was skipped.
  * Synchronises `stream`, stores the word in *flags and, if reset != 0, clears it.
  */

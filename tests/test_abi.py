@@ -101,3 +101,17 @@ def test_package_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(build, "LIB", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="not built"):
         tpk.lib()
+
+
+def test_stager_arguments_are_validated_before_any_device_call(L):
+    out = ctypes.c_void_p(1)
+    slots = (ctypes.c_void_p * 2)(16, 32)
+    assert L.tpk_stager_create(0, slots, 1024, ctypes.byref(out)) == 1 and out.value is None
+    assert L.tpk_stager_create(2, None, 1024, ctypes.byref(out)) == 1
+    assert L.tpk_stager_create(2, slots, 0, ctypes.byref(out)) == 1
+    assert L.tpk_stager_create(2, slots, 1024, None) == 1
+    assert L.tpk_stager_stage(None, 0, None, None, None, None, None) == 1
+    assert L.tpk_stager_acquire(None, 0, None) == 1
+    assert L.tpk_stager_release(None, 0, None) == 1
+    assert L.tpk_stager_sync(None) == 1
+    assert L.tpk_stager_destroy(None) == 0

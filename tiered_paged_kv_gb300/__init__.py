@@ -20,7 +20,7 @@ __all__ = [
     "Shape", "TpkError", "lib", "RECORD_BYTES", "IMPL_DEFAULT", "IMPL_SIMT", "IMPL_TENSOR",
     "kv_quantize_pages", "kv_quantize_pages_given_scales", "decode_attn_exact", "decode_attn_int8",
     "merge_lse", "hybrid_workspace_bytes", "workspace_init", "decode_hybrid_batched", "get_device_status",
-    "static_scratch_bytes", "decode_hybrid_batched_static",
+    "static_scratch_bytes", "decode_hybrid_batched_static", "Stager",
 ]
 
 RECORD_BYTES = 35072
@@ -73,6 +73,17 @@ def lib():
         L.tpk_static_scratch_bytes.argtypes = []
         L.tpk_static_scratch_bytes.restype = sz
         L.tpk_decode_hybrid_batched_static.argtypes = [sp, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+        pp = ctypes.POINTER(ctypes.c_void_p)
+        L.tpk_stager_create.argtypes = [i32, pp, sz, pp]
+        L.tpk_stager_destroy.argtypes = [vp]
+        L.tpk_stager_stage.argtypes = [vp, i32, pp, ctypes.POINTER(sz), ctypes.POINTER(sz),
+                                       ctypes.POINTER(i32), pp]
+        L.tpk_stager_acquire.argtypes = [vp, i32, vp]
+        L.tpk_stager_release.argtypes = [vp, i32, vp]
+        L.tpk_stager_sync.argtypes = [vp]
+        for name in ("tpk_stager_create", "tpk_stager_destroy", "tpk_stager_stage", "tpk_stager_acquire",
+                     "tpk_stager_release", "tpk_stager_sync"):
+            getattr(L, name).restype = i32
         for name in ("tpk_kv_quantize_pages", "tpk_kv_quantize_pages_given_scales", "tpk_decode_attn_exact",
                      "tpk_decode_attn_int8", "tpk_merge_lse", "tpk_workspace_init", "tpk_decode_hybrid_batched",
                      "tpk_get_device_status", "tpk_decode_hybrid_batched_static"):
@@ -182,3 +193,48 @@ def get_device_status(reset=True, stream=None):
     flags = ctypes.c_int(0)
     st = lib().tpk_get_device_status(ctypes.byref(flags), 1 if reset else 0, _stream(stream))
     return st, flags.value
+
+
+class Stager:
+    """Host-resident history staging through n caller-owned device slots (see
+    tpk_stager_* in include/tpk.h).  `slots` are device buffers (tensors or raw
+    pointers) of `slot_bytes` each; the stager keeps references to them."""
+
+    def __init__(self, slots, slot_bytes):
+        self._keep = list(slots)
+        arr = (ctypes.c_void_p * len(slots))(*[_ptr(x) for x in slots])
+        h = ctypes.c_void_p()
+        _check(lib().tpk_stager_create(len(slots), arr, int(slot_bytes), ctypes.byref(h)))
+        self._h = h
+
+    def stage(self, regions):
+        """regions: [(host_src, slot_offset, nbytes)], host_src a pinned tensor or a
+        raw pointer.  Returns (slot index, slot device address)."""
+        n = len(regions)
+        src = (ctypes.c_void_p * max(n, 1))(*[_ptr(r[0]) for r in regions])
+        off = (ctypes.c_size_t * max(n, 1))(*[int(r[1]) for r in regions])
+        nb = (ctypes.c_size_t * max(n, 1))(*[int(r[2]) for r in regions])
+        slot = ctypes.c_int(-1)
+        dev = ctypes.c_void_p()
+        _check(lib().tpk_stager_stage(self._h, n, src, off, nb, ctypes.byref(slot), ctypes.byref(dev)))
+        return slot.value, dev.value
+
+    def acquire(self, slot, stream=None):
+        _check(lib().tpk_stager_acquire(self._h, int(slot), _stream(stream)))
+
+    def release(self, slot, stream=None):
+        _check(lib().tpk_stager_release(self._h, int(slot), _stream(stream)))
+
+    def sync(self):
+        _check(lib().tpk_stager_sync(self._h))
+
+    def close(self):
+        if getattr(self, "_h", None) is not None and self._h.value:
+            h, self._h = self._h, None
+            _check(lib().tpk_stager_destroy(h))
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()

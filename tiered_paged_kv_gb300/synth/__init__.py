@@ -165,6 +165,37 @@ class Workload:
         s = [np.asarray(self.pages[b][:self.n8[b]]) for b in range(self.B)]
         return np.concatenate(s).astype(np.int32) if s else np.zeros(0, np.int32)
 
+    def packed_image(self, rec_pool):
+        """One step's history packed for host-resident staging: the 8-bit records
+        (from rec_pool, [n_slots][H] records) and exact-tier BF16 pages of every
+        request in page order, then q and identity page tables, each part at a
+        256-byte-aligned offset of one byte image.  Returns (image uint8, off) where
+        off maps 'rec', 'k', 'v', 'q', 'pt', 'pt8' to byte offsets, and holds the
+        CSR arrays 'req_page_off', 'req_page_off8' and the page counts."""
+        H = self.H
+        rb = RECORD_BYTES * H
+        rec_v = np.asarray(rec_pool, np.uint8).reshape(self.n_slots, rb)
+        s8 = self.int8_slots()
+        ex, off_e = self.exact_page_table()
+        _, off_8 = self.int8_page_table()
+        parts = [("rec", rec_v[s8].reshape(-1)),
+                 ("k", self.k_pool[ex].reshape(-1).view(np.uint8)),
+                 ("v", self.v_pool[ex].reshape(-1).view(np.uint8)),
+                 ("q", self.q.reshape(-1).view(np.uint8)),
+                 ("pt", np.arange(len(ex), dtype=np.int32).view(np.uint8)),
+                 ("pt8", np.arange(len(s8), dtype=np.int32).view(np.uint8))]
+        off = {}
+        pos = 0
+        for name, a in parts:
+            off[name] = pos
+            pos = (pos + a.size + 255) & ~255
+        img = np.zeros(max(pos, 256), np.uint8)
+        for name, a in parts:
+            img[off[name]:off[name] + a.size] = a
+        off.update(req_page_off=off_e, req_page_off8=off_8, n_exact_pages=len(ex), n_int8_pages=len(s8),
+                   nbytes=int(pos))
+        return img, off
+
     def history_bytes(self):
         """Algorithmic history bytes of one hybrid step: 548 B per 8-bit token-head
         (codes and all scales), 1024 B per BF16 token-head (K and V)."""
