@@ -16,12 +16,13 @@
 //      x_c = ms_c / G needs one multiplication; shat_c = x_c^(1/4);
 //   4. the float32 neighbours of shat_c are found exactly (c^4 against x_c with
 //      an FMA-exact product), and one thread walks the channels choosing the
-//      neighbour that keeps the running log-error of the product nearest zero;
+//      neighbour that keeps the running log-error of the product nearest zero,
+//      while the other seven warps write the value codes (they need only u_c);
 //   5. threads (token, quarter row) divide keys by s_c, take the per-token
 //      absolute maximum r_t = max|y| / 127 and form the codes with IEEE float32
-//      divisions and half-to-even rint; thread c also codes value channel c
-//      (stored channel-major, one 64-byte row per channel).  Fields are written
-//      at their swizzled positions (kc_byte, vc_byte, ks_index).
+//      divisions and half-to-even rint.  Value codes are stored channel-major
+//      (one 64-byte row per channel).  Fields are written at their swizzled
+//      positions (kc_byte, vc_byte, ks_index).
 #include "common.cuh"
 
 namespace tpk {
@@ -33,10 +34,13 @@ struct QSmem {
   double red_m[8];
   int red_e[8];
   double invG;
-  float s[kHeadDim];
-  float u[kHeadDim];
-  float slo[kHeadDim], shi[kHeadDim], dlo[kHeadDim], dhi[kHeadDim];
-  int exact[kHeadDim];
+  alignas(16) float s[kHeadDim];
+  alignas(16) float u[kHeadDim];
+  alignas(16) float slo[kHeadDim];
+  alignas(16) float shi[kHeadDim];
+  alignas(16) float dlo[kHeadDim];
+  alignas(16) float dhi[kHeadDim];
+  alignas(16) int exact[kHeadDim];
   int bad;
 };
 
@@ -56,7 +60,9 @@ __device__ __forceinline__ uint32_t code_byte(float x, float scale) {
   return (uint32_t)((int)z + 128);
 }
 
-__global__ void __launch_bounds__(256) quantize_kernel(const __grid_constant__ QuantParams p) {
+constexpr int kQuantThreads = 256;  // one thread per channel in the per-channel phases
+
+__global__ void __launch_bounds__(kQuantThreads) quantize_kernel(const __grid_constant__ QuantParams p) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   QSmem& S = *reinterpret_cast<QSmem*>(smem_raw);
   const int tid = threadIdx.x;
@@ -90,18 +96,17 @@ __global__ void __launch_bounds__(256) quantize_kernel(const __grid_constant__ Q
   {
     float vmax = 0.f;
     for (int t = 0; t < kPageTokens; ++t) vmax = fmaxf(vmax, fabsf(bf16_lo(S.v[t][c])));
-    const float u = given ? p.g_vchan[gidx * kHeadDim + c] : __fdiv_rn(vmax, 127.f);
-    S.u[c] = u;
-    // value codes of channel c: one contiguous 64-byte row (channel-major layout)
-#pragma unroll
-    for (int t0 = 0; t0 < kPageTokens; t0 += 16) {
-      uint32_t wv[4] = {0u, 0u, 0u, 0u};
-#pragma unroll
-      for (int e = 0; e < 16; ++e)
-        wv[e >> 2] |= code_byte(bf16_lo(S.v[t0 + e][c]), u) << (8 * (e & 3));
-      *reinterpret_cast<uint4*>(rec + kOffVc + vc_byte(c, t0)) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
-    }
+    S.u[c] = given ? p.g_vchan[gidx * kHeadDim + c] : __fdiv_rn(vmax, 127.f);
   }
+  // value codes of channel ch, tokens t0 .. t0 + 15: 16 bytes of the channel's
+  // 64-byte row (channel-major layout)
+  auto value_codes = [&](int ch, int t0) {
+    const float u = S.u[ch];
+    uint32_t wv[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+    for (int e = 0; e < 16; ++e) wv[e >> 2] |= code_byte(bf16_lo(S.v[t0 + e][ch]), u) << (8 * (e & 3));
+    *reinterpret_cast<uint4*>(rec + kOffVc + vc_byte(ch, t0)) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+  };
   double mant = 1.0;
   int expo = 0;
   double ms = 0.0;
@@ -195,22 +200,40 @@ __global__ void __launch_bounds__(256) quantize_kernel(const __grid_constant__ Q
   __syncthreads();
   if (given) {
     S.s[c] = p.g_kchan[gidx * kHeadDim + c];
-  } else if (tid == 0) {
-    float E = 0.f;
-    for (int ch = 0; ch < kHeadDim; ++ch) {
-      if (S.exact[ch]) {
-        S.s[ch] = S.slo[ch];
-        continue;
-      }
-      float a = E + S.dlo[ch], b = E + S.dhi[ch];
-      if (fabsf(a) <= fabsf(b)) {
-        S.s[ch] = S.slo[ch];
-        E = a;
-      } else {
-        S.s[ch] = S.shi[ch];
-        E = b;
+    for (int t0 = 0; t0 < kPageTokens; t0 += 16) value_codes(c, t0);
+  } else if (tid < 32) {
+    // The compensated walk is sequential in the channels; one lane runs it with
+    // each group of 8 channels' candidates loaded into registers first, while the
+    // other seven warps write the value codes, which do not depend on s.
+    if (tid == 0) {
+      float E = 0.f;
+      for (int ch0 = 0; ch0 < kHeadDim; ch0 += 8) {
+        float lo[8], hi[8], dl[8], dh[8], sv[8];
+        int ex[8];
+        *reinterpret_cast<float4*>(lo) = *reinterpret_cast<const float4*>(&S.slo[ch0]);
+        *reinterpret_cast<float4*>(lo + 4) = *reinterpret_cast<const float4*>(&S.slo[ch0 + 4]);
+        *reinterpret_cast<float4*>(hi) = *reinterpret_cast<const float4*>(&S.shi[ch0]);
+        *reinterpret_cast<float4*>(hi + 4) = *reinterpret_cast<const float4*>(&S.shi[ch0 + 4]);
+        *reinterpret_cast<float4*>(dl) = *reinterpret_cast<const float4*>(&S.dlo[ch0]);
+        *reinterpret_cast<float4*>(dl + 4) = *reinterpret_cast<const float4*>(&S.dlo[ch0 + 4]);
+        *reinterpret_cast<float4*>(dh) = *reinterpret_cast<const float4*>(&S.dhi[ch0]);
+        *reinterpret_cast<float4*>(dh + 4) = *reinterpret_cast<const float4*>(&S.dhi[ch0 + 4]);
+        *reinterpret_cast<int4*>(ex) = *reinterpret_cast<const int4*>(&S.exact[ch0]);
+        *reinterpret_cast<int4*>(ex + 4) = *reinterpret_cast<const int4*>(&S.exact[ch0 + 4]);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float a = E + dl[e], b = E + dh[e];
+          const bool take_lo = ex[e] || fabsf(a) <= fabsf(b);
+          sv[e] = take_lo ? lo[e] : hi[e];
+          E = ex[e] ? E : (take_lo ? a : b);
+        }
+        *reinterpret_cast<float4*>(&S.s[ch0]) = *reinterpret_cast<const float4*>(sv);
+        *reinterpret_cast<float4*>(&S.s[ch0 + 4]) = *reinterpret_cast<const float4*>(sv + 4);
       }
     }
+  } else {
+    // (channel, 16-token quarter) items spread evenly over the seven warps
+    for (int it = tid - 32; it < kHeadDim * 4; it += kQuantThreads - 32) value_codes(it >> 2, (it & 3) * 16);
   }
   __syncthreads();
   // ---- 5. codes: thread (token t, quarter q) handles 64 channels, chunks rotated
@@ -258,7 +281,7 @@ cudaError_t launch_quantize(const QuantParams& p, int n_pages, cudaStream_t stre
     configured = true;
   }
   if (n_pages == 0) return cudaSuccess;
-  quantize_kernel<<<n_pages * p.H, 256, smem, stream>>>(p);
+  quantize_kernel<<<n_pages * p.H, kQuantThreads, smem, stream>>>(p);
   return cudaGetLastError();
 }
 
