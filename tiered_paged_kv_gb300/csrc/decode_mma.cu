@@ -2,11 +2,13 @@
 // FP32 accumulation).
 //
 // One thread block = one unit (a range of pages of one tier for one (request,
-// KV head)).  A producer warp streams the unit's items into a ring of 6
-// shared-memory slots.  8 consumer warps work in 4 pairs: item j goes to pair
-// j % 4, and the two warps of the pair split the item's tokens in halves.  Each
-// warp keeps its own online-softmax state and FP32 output for the 8 query rows
-// of the GQA group; the epilogue merges the 8 warps.
+// KV head)).  The unit's items stream into a ring of 6 shared-memory slots: the
+// first six are issued at the start, and every later one by the warp that lets
+// go of its slot's previous item last.  8 warps work in 4 pairs: item j goes to
+// pair j % 4, and the two warps of the pair split the item's channels in halves
+// (partial scores are summed through shared memory, both warps run the same
+// online softmax, each accumulates the output of its 128 channels).  The
+// epilogue merges the 4 pairs' states.
 //
 // Thread (g, t) = (lane / 4, lane % 4) of a consumer warp:
 //   - in QK (S = Q K^T, M = 16 query-row slots, N = 8 tokens per tile) it owns
@@ -47,7 +49,7 @@
 namespace tpk {
 
 constexpr int kCons = 8;                       // consumer warps (4 pairs)
-constexpr int kMmaThreads = (kCons + 1) * 32;  // + one producer warp
+constexpr int kMmaThreads = kCons * 32;
 constexpr int kMmaSlots = 6;
 constexpr unsigned kAll = 0xffffffffu;
 
@@ -55,6 +57,9 @@ struct MmaSmem {
   alignas(128) uint8_t slot[kMmaSlots][kSlotBytes];
   uint64_t full[kMmaSlots];
   uint64_t empty[kMmaSlots];
+  uint64_t pairbar[kCons / 2];
+  int rel[kMmaSlots];    // releases of the slot's current item (the second one refills it)
+  int fills[kMmaSlots];  // copies issued into the slot
   int valid[kMmaSlots];
   int pt[kPtCache];
   alignas(16) uint32_t q[kGroup][kHeadDim / 2];  // the unit's query rows, bf16 pairs
@@ -167,8 +172,8 @@ __device__ __forceinline__ void mma_issue(const DecodeParams& p, const UnitInfo&
 // Online-softmax update for this thread's base-2 scores x[] of query row g (-inf
 // where masked).  Rescales O (rows 2t, 2t + 1) when a row maximum moved, turns
 // x[] into weights and returns the factor alpha the row sum must be scaled by.
-template <int N>
-__device__ __forceinline__ float softmax_rescale(float (&x)[N], float& m_run, float (&O)[16][4]) {
+template <int N, int M>
+__device__ __forceinline__ float softmax_rescale(float (&x)[N], float& m_run, float (&O)[M][4]) {
   const int lane = threadIdx.x & 31, t = lane & 3;
   float mx = kNegInf;
 #pragma unroll
@@ -181,7 +186,7 @@ __device__ __forceinline__ float softmax_rescale(float (&x)[N], float& m_run, fl
     const float a0 = __shfl_sync(kAll, alpha, 8 * t);      // row 2t is held by lanes 4 * (2t) ..
     const float a1 = __shfl_sync(kAll, alpha, 8 * t + 4);  // row 2t + 1
 #pragma unroll
-    for (int m = 0; m < 16; ++m) {
+    for (int m = 0; m < M; ++m) {
       O[m][0] *= a0;
       O[m][1] *= a1;
       O[m][2] *= a0;
@@ -194,36 +199,78 @@ __device__ __forceinline__ float softmax_rescale(float (&x)[N], float& m_run, fl
   return alpha;
 }
 
-// ------------------------------------------------------- 8-bit half page
-// Warp half h (0 or 1) of a record: tokens 32h .. 32h + 31.  Within the half,
-// thread t owns tokens 8t .. 8t + 7: QK tile j column 2t + e is token
-// 8t + 2j + e, and PV k-step i covers tokens 8t + 4i + {0..3} of every thread t.
-__device__ __forceinline__ void process_int8_half(const uint8_t* rec, int h, const MmaSmem& S, float qk_scale,
-                                                  float& m_run, float& l_run, float (&O)[16][4]) {
+// The two warps of a pair add up N partial scores per thread through shared
+// memory: each writes its own values into `mine` (bytes of the slot that only it
+// reads, and has finished reading), the pair meets at its mbarrier (a bounded
+// wait: false if the partner did not arrive), and each adds the partner's values
+// for the same lane (a + b = b + a, so both warps get the same sums).  Float4 k of
+// lane l sits at row (32k + l) / 8, byte 16 (l % 8) of rows RowStride bytes apart.
+struct PairSync {
+  uint64_t* bar;    // the pair's mbarrier (count 2: one arrival per warp)
+  uint32_t parity;  // phase of this item
+  int* status;
+};
+template <int N, int RowStride>
+__device__ __forceinline__ bool pair_exchange(float (&v)[N], uint8_t* mine, const uint8_t* theirs, const PairSync& ps) {
+  const int lane = threadIdx.x & 31;
+  __syncwarp();
+#pragma unroll
+  for (int k = 0; k < N / 4; ++k)
+    *reinterpret_cast<float4*>(mine + ((32 * k + lane) >> 3) * RowStride + (lane & 7) * 16) =
+        make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+  __syncwarp();
+  if (lane == 0) mbar_arrive(ps.bar);
+  if (!mbar_wait(ps.bar, ps.parity, ps.status)) return false;
+#pragma unroll
+  for (int k = 0; k < N / 4; ++k) {
+    const float4 o = *reinterpret_cast<const float4*>(theirs + ((32 * k + lane) >> 3) * RowStride + (lane & 7) * 16);
+    v[4 * k] += o.x;
+    v[4 * k + 1] += o.y;
+    v[4 * k + 2] += o.z;
+    v[4 * k + 3] += o.w;
+  }
+  return true;
+}
+
+// Generic-proxy writes into a slot (the score exchange, zeroed rows) must be
+// ordered before the next bulk copy refills the slot.
+__device__ __forceinline__ void fence_slot_writes() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// ------------------------------------------------------- 8-bit record
+// Warp half h of a pair owns channels 128h .. 128h + 127 of a whole record (64
+// tokens).  QK: tile j (0..7) column 2t + e is token 16t + 2j + e, so thread t
+// receives the scores of tokens 16t .. 16t + 15; the warp's partial scores over
+// its channels are summed with the partner's through shared memory, and both
+// warps then hold the full scores and run the same softmax.  PV k-step i (0..3)
+// covers tokens 16t + 4i + {0..3} of every thread t; the warp accumulates its 128
+// channels.
+__device__ __forceinline__ bool process_int8_record(uint8_t* rec, int h, const PairSync& psync, const MmaSmem& S,
+                                                    float qk_scale, float& m_run, float& l_run, float (&O)[8][4]) {
   const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
   const float* ks = reinterpret_cast<const float*>(rec + kOffKsChan);
-  const float* kr = reinterpret_cast<const float*>(rec + kOffKsTok) + 32 * h;
-  const float* vs = reinterpret_cast<const float*>(rec + kOffVsChan);
-  const uint8_t* kc = rec + kOffKc + 32 * h * kHeadDim;
+  const float* kr = reinterpret_cast<const float*>(rec + kOffKsTok);
+  const float* vs = reinterpret_cast<const float*>(rec + kOffVsChan) + 128 * h;
+  const uint8_t* kc = rec + kOffKc;
   const uint8_t* vc = rec + kOffVc;
   const float* qrow = S.qs[g];
 
-  // ---- QK: 4 tiles of 8 tokens, 16 k-steps of 16 channels.  k-step 4J + i uses
-  // channels 64J + 16t + 4i + {0, 1} (k = 2t, 2t+1) and + {2, 3} (k = 2t+8, 2t+9).
-  float acc[4][4];
+  // ---- QK over this warp's channels: 8 tiles of 8 tokens, 8 k-steps of 16
+  // channels.  k-step 4J + i uses channels 128h + 64J + 16t + 4i + {0, 1} (k = 2t,
+  // 2t+1) and + {2, 3} (k = 2t+8, 2t+9).
+  float acc[8][4];
 #pragma unroll
-  for (int j = 0; j < 4; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
-  float qsum = 0.f;  // sum of this thread's 64 folded-query values of row g
+  for (int j = 0; j < 8; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+  float qsum = 0.f;  // sum of this thread's 32 folded-query values of row g
 #pragma unroll
-  for (int J = 0; J < 4; ++J) {
-    uint4 kw[4];
+  for (int J = 0; J < 2; ++J) {
+    const int cb = 128 * h + 64 * J + 16 * t;
+    uint4 kw[8];
 #pragma unroll
-    for (int j = 0; j < 4; ++j)  // token 8 (g >> 1) + 2j + (g & 1) of the half (odd tokens: 64-byte halves swapped)
-      kw[j] = *reinterpret_cast<const uint4*>(kc + (8 * (g >> 1) + 2 * j + (g & 1)) * kHeadDim +
-                                              ((64 * J + 16 * t) ^ ((g & 1) << 6)));
+    for (int j = 0; j < 8; ++j)  // token 16 (g >> 1) + 2j + (g & 1) (odd tokens: 64-byte halves swapped)
+      kw[j] = *reinterpret_cast<const uint4*>(kc + (16 * (g >> 1) + 2 * j + (g & 1)) * kHeadDim + (cb ^ ((g & 1) << 6)));
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const int ch = 64 * J + 16 * t + 4 * i;
+      const int ch = cb + 4 * i;
       const float4 s4 = *reinterpret_cast<const float4*>(ks + ks_index(ch));
       const float4 q4 = *reinterpret_cast<const float4*>(qrow + ks_index(ch));
       const float x0 = q4.x * s4.x, x1 = q4.y * s4.y, x2 = q4.z * s4.z, x3 = q4.w * s4.w;
@@ -232,7 +279,7 @@ __device__ __forceinline__ void process_int8_half(const uint8_t* rec, int h, con
       const uint32_t l01 = pack_f16(x0 - f16_lo(h01), x1 - f16_hi(h01));
       const uint32_t l23 = pack_f16(x2 - f16_lo(h23), x3 - f16_hi(h23));
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
+      for (int j = 0; j < 8; ++j) {
         const uint32_t w = i == 0 ? kw[j].x : i == 1 ? kw[j].y : i == 2 ? kw[j].z : kw[j].w;
         uint32_t b0, b1;
         codes_to_f16(w, b0, b1);
@@ -240,51 +287,64 @@ __device__ __forceinline__ void process_int8_half(const uint8_t* rec, int h, con
       }
     }
   }
-  // The products ran on 1152 + code: remove 1152 * sum_c q'_c (row g, all 256
-  // channels) from the high plane's dot before the low plane's is added.
+  // The products ran on 1152 + code: remove 1152 * sum_c q'_c over this warp's
+  // channels (row g) from the high plane's dot before the low plane's is added.
   qsum += __shfl_xor_sync(kAll, qsum, 1);
   qsum += __shfl_xor_sync(kAll, qsum, 2);
-  // scores (base 2): high + low planes, times r_t of each token
-  float x[8];
-  {
-    const float4 r0 = *reinterpret_cast<const float4*>(kr + 8 * t);
-    const float4 r1 = *reinterpret_cast<const float4*>(kr + 8 * t + 4);
-    const float rr[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+  float x[16];  // x[2j + e]: token 16t + 2j + e
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      x[2 * j] = (fmaf(-kCodeOffset, qsum, acc[j][0]) + acc[j][2]) * qk_scale * rr[2 * j];
-      x[2 * j + 1] = (fmaf(-kCodeOffset, qsum, acc[j][1]) + acc[j][3]) * qk_scale * rr[2 * j + 1];
-    }
+  for (int j = 0; j < 8; ++j) {
+    x[2 * j] = fmaf(-kCodeOffset, qsum, acc[j][0]) + acc[j][2];
+    x[2 * j + 1] = fmaf(-kCodeOffset, qsum, acc[j][1]) + acc[j][3];
   }
-  const float alpha = softmax_rescale<8>(x, m_run, O);
-  // P^T as one f16 plane: pw[k] = tokens 8t + 2k, 8t + 2k + 1 of row g.  The
+  // partial scores of the two channel halves -> full scores in both warps (the
+  // exchange area: rows 0..15 of this warp's half of the key codes)
+  if (!pair_exchange<16, kHeadDim>(x, rec + kOffKc + 128 * h, rec + kOffKc + 128 * (h ^ 1), psync)) return false;
+  {
+    // r_t of tokens 16t .. 16t + 15, then base-2 scores
+    float rr[16];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float4 r4 = *reinterpret_cast<const float4*>(kr + 16 * t + 4 * k);
+      rr[4 * k] = r4.x;
+      rr[4 * k + 1] = r4.y;
+      rr[4 * k + 2] = r4.z;
+      rr[4 * k + 3] = r4.w;
+    }
+#pragma unroll
+    for (int k = 0; k < 16; ++k) x[k] = x[k] * qk_scale * rr[k];
+  }
+  const float alpha = softmax_rescale<16, 8>(x, m_run, O);
+  // P^T as one f16 plane: pw[k] = tokens 16t + 2k, 16t + 2k + 1 of row g.  The
   // rounded weights are the ones summed into l, so numerator and denominator
   // use the same probabilities.
-  uint32_t pw[4];
+  uint32_t pw[8];
   float lp = 0.f;
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
+  for (int k = 0; k < 8; ++k) {
     pw[k] = pack_f16(x[2 * k], x[2 * k + 1]);
     lp += f16_lo(pw[k]) + f16_hi(pw[k]);
   }
   l_run = l_run * alpha + lp;
-  // sum of the half's 32 weights of each row; the PV accumulator of rows 2t and
+  // sum of the record's 64 weights of each row; the PV accumulator of rows 2t and
   // 2t + 1 starts at -1152 times it, cancelling the code offset
   float ps = lp + __shfl_xor_sync(kAll, lp, 1);
   ps += __shfl_xor_sync(kAll, ps, 2);
   const float c0 = -kCodeOffset * __shfl_sync(kAll, ps, 8 * t);
   const float c1 = -kCodeOffset * __shfl_sync(kAll, ps, 8 * t + 4);
-  // ---- PV: 16 channel tiles; each page result times u_c into the accumulator
+  // ---- PV: this warp's 8 channel tiles, 4 k-steps of 16 tokens; each page's
+  // result times u_c into the accumulator
 #pragma unroll
-  for (int m = 0; m < 16; ++m) {
-    const uint2 va = *reinterpret_cast<const uint2*>(vc + vc_byte(16 * m + g, 32 * h + 8 * t));
-    const uint2 vb = *reinterpret_cast<const uint2*>(vc + vc_byte(16 * m + g + 8, 32 * h + 8 * t));
+  for (int m = 0; m < 8; ++m) {
+    const int ch = 128 * h + 16 * m + g;
+    const uint4 va = *reinterpret_cast<const uint4*>(vc + vc_byte(ch, 16 * t));
+    const uint4 vb = *reinterpret_cast<const uint4*>(vc + vc_byte(ch + 8, 16 * t));
     float c[4] = {c0, c1, c0, c1};
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < 4; ++i) {
       uint32_t a0, a2, a1, a3;
-      codes_to_f16(i == 0 ? va.x : va.y, a0, a2);
-      codes_to_f16(i == 0 ? vb.x : vb.y, a1, a3);
+      codes_to_f16(i == 0 ? va.x : i == 1 ? va.y : i == 2 ? va.z : va.w, a0, a2);
+      codes_to_f16(i == 0 ? vb.x : i == 1 ? vb.y : i == 2 ? vb.z : vb.w, a1, a3);
       mma_f16(c, a0, a1, a2, a3, pw[2 * i], pw[2 * i + 1]);
     }
     const float ua = vs[16 * m + g], ub = vs[16 * m + g + 8];
@@ -293,62 +353,83 @@ __device__ __forceinline__ void process_int8_half(const uint8_t* rec, int h, con
     O[m][2] = fmaf(ub, c[2], O[m][2]);
     O[m][3] = fmaf(ub, c[3], O[m][3]);
   }
+  return true;
 }
 
-// ------------------------------------------------------ BF16 quarter page
-// Warp half h of a BF16 half-page item: tokens 16h .. 16h + 15 of the item.
-__device__ __forceinline__ void process_bf16_quarter(uint8_t* slot, int h, int tok0, int tb, int te,
-                                                     const MmaSmem& S, float qscale, float& m_run, float& l_run,
-                                                     float (&O)[16][4]) {
+// ------------------------------------------------------ BF16 half page
+// Warp half h of a pair owns channels 128h .. 128h + 127 of a BF16 half-page item
+// (32 tokens, K at tiles 0-3 and V at tiles 4-7 of the slot).  QK tile j (0..3)
+// column 2t + e is token 8j + 2t + e of the item; the partial scores over the
+// warp's channels are exchanged as for the 8-bit tier.  PV k-step i (0..1)
+// covers tokens 16i .. 16i + 15.
+__device__ __forceinline__ bool process_bf16_half(uint8_t* slot, int h, const PairSync& psync, int tok0, int tb,
+                                                  int te, const MmaSmem& S, float qscale, float& m_run, float& l_run,
+                                                  float (&O)[8][4]) {
   const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
   uint8_t* K = bf16_tiles(slot);
   uint8_t* V = K + 16384;
-  const int base = tok0 + 16 * h;
-  if (base < tb || base + 16 > te) {  // zero value rows of tokens outside the range
-    for (int k = 0; k < 16; ++k) {
-      const int tok = base + k, r = 16 * h + k;
+  if (tok0 < tb || tok0 + 32 > te) {  // zero this warp's value channels of tokens outside the range
+    for (int r0 = 0; r0 < 32; r0 += 2) {
+      const int r = r0 + (lane >> 4), tok = tok0 + r;
       if (tok < tb || tok >= te)
-        *reinterpret_cast<uint4*>(V + (lane >> 3) * 4096 + r * 128 + (lane & 7) * 16) = make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(V + (2 * h + ((lane >> 3) & 1)) * 4096 + r * 128 + (lane & 7) * 16) =
+            make_uint4(0, 0, 0, 0);
     }
     __syncwarp();
   }
   const uint32_t* qrow = S.q[g];
-  float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll 4
-  for (int kk = 0; kk < 8; ++kk) {
+  float acc[4][4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+#pragma unroll
+  for (int kq = 0; kq < 4; ++kq) {
+    const int kk = 4 * h + kq;  // 32 channels 32kk .. 32kk + 31
     const uint32_t qa0 = qrow[16 * kk + t], qa1 = qrow[16 * kk + 4 + t];
     const uint32_t qa2 = qrow[16 * kk + 8 + t], qa3 = qrow[16 * kk + 12 + t];
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
+    for (int j = 0; j < 4; ++j) {
       uint32_t m4[4];
-      ldsm_x4(m4, K + swz(16 * h + 8 * j + (lane & 7), 4 * kk + (lane >> 3)));
+      ldsm_x4(m4, K + swz(8 * j + (lane & 7), 4 * kk + (lane >> 3)));
       mma_bf16(acc[j], qa0, 0u, qa1, 0u, m4[0], m4[1]);
       mma_bf16(acc[j], qa2, 0u, qa3, 0u, m4[2], m4[3]);
     }
   }
-  float x[4];
+  float x[8];  // x[2j + e]: token 8j + 2t + e of the item
 #pragma unroll
-  for (int j = 0; j < 2; ++j)
+  for (int j = 0; j < 4; ++j) {
+    x[2 * j] = acc[j][0];
+    x[2 * j + 1] = acc[j][1];
+  }
+  // exchange area: the first 1 KB of this warp's key tiles (2h, 2h + 1)
+  if (!pair_exchange<8, 128>(x, K + 2 * h * 4096, K + 2 * (h ^ 1) * 4096, psync)) return false;
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
-      const int tok = base + 8 * j + 2 * t + e;
-      x[2 * j + e] = (tok >= tb && tok < te) ? acc[j][e] * qscale : kNegInf;
+      const int tok = tok0 + 8 * j + 2 * t + e;
+      x[2 * j + e] = (tok >= tb && tok < te) ? x[2 * j + e] * qscale : kNegInf;
     }
   {
-    const float alpha = softmax_rescale<4>(x, m_run, O);
-    l_run = l_run * alpha + ((x[0] + x[1]) + (x[2] + x[3]));
+    const float alpha = softmax_rescale<8, 8>(x, m_run, O);
+    l_run = l_run * alpha + (((x[0] + x[1]) + (x[2] + x[3])) + ((x[4] + x[5]) + (x[6] + x[7])));
   }
-  const uint32_t ph0 = pack_bf16(x[0], x[1]), ph1 = pack_bf16(x[2], x[3]);
-  const uint32_t pl0 = pack_bf16(x[0] - bf16_lo(ph0), x[1] - bf16_hi(ph0));
-  const uint32_t pl1 = pack_bf16(x[2] - bf16_lo(ph1), x[3] - bf16_hi(ph1));
-  const int i = lane >> 3;
+  // P^T for k-step i: tokens 16i + 2t + {0, 1} (tile 2i) and 16i + 8 + 2t + {0, 1}
+  // (tile 2i + 1), as bf16 high and low planes
+  const int mi = lane >> 3;
 #pragma unroll
-  for (int m = 0; m < 16; ++m) {
-    uint32_t a[4];
-    ldsm_x4_t(a, V + swz(16 * h + (i >> 1) * 8 + (lane & 7), 2 * m + (i & 1)));
-    mma_bf16(O[m], a[0], a[1], a[2], a[3], ph0, ph1);
-    mma_bf16(O[m], a[0], a[1], a[2], a[3], pl0, pl1);
+  for (int i = 0; i < 2; ++i) {
+    const uint32_t ph0 = pack_bf16(x[4 * i], x[4 * i + 1]), ph1 = pack_bf16(x[4 * i + 2], x[4 * i + 3]);
+    const uint32_t pl0 = pack_bf16(x[4 * i] - bf16_lo(ph0), x[4 * i + 1] - bf16_hi(ph0));
+    const uint32_t pl1 = pack_bf16(x[4 * i + 2] - bf16_lo(ph1), x[4 * i + 3] - bf16_hi(ph1));
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      uint32_t a[4];
+      ldsm_x4_t(a, V + swz(16 * i + (mi >> 1) * 8 + (lane & 7), 2 * (8 * h + m) + (mi & 1)));
+      mma_bf16(O[m], a[0], a[1], a[2], a[3], ph0, ph1);
+      mma_bf16(O[m], a[0], a[1], a[2], a[3], pl0, pl1);
+    }
   }
+  return true;
 }
 
 // ------------------------------------------------------------------ kernel
@@ -367,6 +448,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1) decode_mma_kernel(const __grid
       mbar_init(&S.full[s], 1);
       mbar_init(&S.empty[s], 2);
     }
+    for (int q = 0; q < kCons / 2; ++q) mbar_init(&S.pairbar[q], 2);
+    for (int s = 0; s < kMmaSlots; ++s) S.rel[s] = S.fills[s] = 0;
     S.abort = 0;
     fence_mbar_init();
   }
@@ -376,6 +459,13 @@ __global__ void __launch_bounds__(kMmaThreads, 1) decode_mma_kernel(const __grid
     for (int i = tid; i < kGroup * kHeadDim / 2; i += blockDim.x) (&S.q[0][0])[i] = __ldg(q32 + i);
   }
   __syncthreads();
+  // the first items go out at once; every later one is issued by the warp that
+  // releases its slot's previous item last
+  if (tid == 0)
+    for (int j = 0; j < min(it.n, kMmaSlots); ++j) {
+      mma_issue(p, ui, it, S, j, j);
+      S.fills[j] = 1;
+    }
   // Float copy of q times 2^-(e+1), e the exponent of the row's max |q|: with
   // s_c <= 2^14 every q'_c = q_c s_c of this row then stays below 2^13, inside
   // f16 range, whatever the page.
@@ -401,28 +491,14 @@ __global__ void __launch_bounds__(kMmaThreads, 1) decode_mma_kernel(const __grid
   }
   __syncthreads();
 
-  int issued = 0;
-  float O[16][4];
+  float O[8][4];  // this warp's 128 channels of the pair's output
 #pragma unroll
-  for (int m = 0; m < 16; ++m) O[m][0] = O[m][1] = O[m][2] = O[m][3] = 0.f;
+  for (int m = 0; m < 8; ++m) O[m][0] = O[m][1] = O[m][2] = O[m][3] = 0.f;
   float m_run = kNegInf, l_run = 0.f;
 
-  if (warp == kCons) {
-    // ---------------------------------------------------------- producer
-    if (lane == 0) {
-      for (int j = 0; j < it.n; ++j) {
-        const int s = j % kMmaSlots;
-        if (j >= kMmaSlots && !mbar_wait(&S.empty[s], ((j / kMmaSlots) - 1) & 1, p.status)) {
-          S.abort = 1;
-          break;
-        }
-        mma_issue(p, ui, it, S, j, s);
-        issued = j + 1;
-      }
-    }
-  } else {
-    // ---------------------------------------------------------- consumers
+  {
     const int pair = warp >> 1, half = warp & 1;
+    uint32_t pair_phase = 0;  // items this pair has exchanged scores for (both warps skip the same items)
     for (int j = pair; j < it.n; j += kCons / 2) {
       const int s = j % kMmaSlots;
       // Slot s last held item j - 6, which another pair may still own.  A parity
@@ -438,39 +514,60 @@ __global__ void __launch_bounds__(kMmaThreads, 1) decode_mma_kernel(const __grid
         break;
       }
       if (S.valid[s]) {
-        if (ui.tier == 1)
-          process_int8_half(S.slot[s], half, S, qk_scale, m_run, l_run, O);
-        else
-          process_bf16_quarter(S.slot[s], half, (it.first + j) * 32, ui.tok_begin, ui.tok_end, S, p.qscale, m_run,
-                               l_run, O);
+        const PairSync psync{&S.pairbar[pair], pair_phase & 1, p.status};
+        ++pair_phase;
+        const bool ok = ui.tier == 1
+                            ? process_int8_record(S.slot[s], half, psync, S, qk_scale, m_run, l_run, O)
+                            : process_bf16_half(S.slot[s], half, psync, (it.first + j) * 32, ui.tok_begin,
+                                                ui.tok_end, S, p.qscale, m_run, l_run, O);
+        if (!ok) {
+          S.abort = 1;
+          break;
+        }
+        fence_slot_writes();
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&S.empty[s]);
+      if (lane == 0) {
+        mbar_arrive(&S.empty[s]);
+        // the second warp of the pair to let go of the slot refills it
+        if (j + kMmaSlots < it.n) {
+          __threadfence_block();
+          if (atomicAdd(&S.rel[s], 1) == 1) {
+            S.rel[s] = 0;
+            __threadfence_block();
+            mma_issue(p, ui, it, S, j + kMmaSlots, s);
+            S.fills[s] += 1;
+          }
+        }
+      }
     }
   }
   __syncthreads();
   if (S.abort) {
-    // A wait gave up: let the copies this block issued land (bounded), then leave
-    // without a result; the status word reports the timeout.
-    if (warp == kCons && lane == 0)
-      for (int j = max(0, issued - kMmaSlots); j < issued; ++j)
-        mbar_wait(&S.full[j % kMmaSlots], (j / kMmaSlots) & 1, p.status);
+    // A wait gave up: let every copy issued into the slots land (bounded: the
+    // latest fill of each slot), then leave without a result; the status word
+    // reports the timeout.
+    if (tid == 0)
+      for (int s = 0; s < kMmaSlots; ++s)
+        if (S.fills[s] > 0) mbar_wait(&S.full[s], (S.fills[s] - 1) & 1, p.status);
     __syncthreads();
     return;
   }
-  // ---- per-warp states into shared memory (the stages are idle now)
-  float* ep_o = reinterpret_cast<float*>(S.slot[0]);  // [8 warps][8 rows][256], spans slots 0-1
+  // ---- per-pair states into shared memory (the stages are idle now); the two
+  // warps of a pair hold the same softmax state and one channel half each
+  float* ep_o = reinterpret_cast<float*>(S.slot[0]);  // [4 pairs][8 rows][256], in slot 0
   if (warp < kCons) {
+    const int pair = warp >> 1, half = warp & 1;
     float L = l_run;
     L += __shfl_xor_sync(kAll, L, 1);
     L += __shfl_xor_sync(kAll, L, 2);
-    if (t == 0) {
-      S.ep_m[warp][g] = m_run;
-      S.ep_l[warp][g] = L;
+    if (t == 0 && half == 0) {
+      S.ep_m[pair][g] = m_run;
+      S.ep_l[pair][g] = L;
     }
-    float* base = ep_o + warp * kGroup * kHeadDim;
+    float* base = ep_o + pair * kGroup * kHeadDim + 128 * half;
 #pragma unroll
-    for (int m = 0; m < 16; ++m) {
+    for (int m = 0; m < 8; ++m) {
       base[(2 * t) * kHeadDim + 16 * m + g] = O[m][0];
       base[(2 * t + 1) * kHeadDim + 16 * m + g] = O[m][1];
       base[(2 * t) * kHeadDim + 16 * m + g + 8] = O[m][2];
@@ -478,7 +575,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) decode_mma_kernel(const __grid
     }
   }
   __syncthreads();
-  write_and_fold<kCons>(p, ui, S, ep_o);
+  write_and_fold<kCons / 2>(p, ui, S, ep_o);
 }
 
 template <int R>
