@@ -14,6 +14,9 @@ e2e    = the same metric through the library's host-resident path: the step's
          pinned host memory; each step stages it into a device slot through the
          stager (tpk_stager_*), runs the decode call on the slot and reads o and
          lse back.
+tiers_128k = each tier alone over a 131,072-token history (all BF16: 536.9 MB; all
+         8-bit: 287.3 MB), same call and timing, for the exact and the 8-bit
+         kernel paths separately.
 host_resident = 16 layers of such history images in pinned host memory through
          two device slots, each layer staged while the previous one decodes;
          link GB/s against a plain pinned copy measured in the same run.
@@ -192,6 +195,79 @@ def head_slice(w, heads, rec_host):
 
 
 # ------------------------------------------------------------------ GPU arm
+def graph_times(step, steps, warmup, stream, flush, flush_r):
+    """Device times (ms) of `steps` CUDA-graph replays of step(), L2 flushed
+    before each (256 MB written, then 256 MB read)."""
+    import torch
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            step()
+        stream.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream, capture_error_mode="thread_local"):
+            step()
+        stream.synchronize()
+        for _ in range(warmup):
+            graph.replay()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for i, (a, b) in enumerate(ev):
+            flush.fill_(float(i))
+            flush_r.max()
+            a.record(stream)
+            graph.replay()
+            b.record(stream)
+        stream.synchronize()
+    return [a.elapsed_time(b) for a, b in ev]
+
+
+def run_tier(which, impl, args, stream, dev, flush, flush_r, peak):
+    """One tier alone over a 131,072-token history of the main workload's shape
+    (4 KV heads x 8 q rows, head_dim 256, 4 outlier key channels at 20x std):
+    'exact' = all BF16, 'int8' = all 8-bit (2048 pages, converted on the GPU
+    first), through the same multi-request call."""
+    import torch
+
+    import tiered_paged_kv_gb300 as tpk
+    from tiered_paged_kv_gb300 import synth
+
+    w = synth.make_workload([131072], None if which == "exact" else 0, H=4, seed=12,
+                            key_sigma="outliers")
+    H, G = w.H, w.G
+    shape = tpk.Shape(H, impl=impl, kv_slots=w.n_slots, rec_slots=w.n_slots)
+    with torch.cuda.stream(stream):
+        kp = torch.from_numpy(w.k_pool.view(np.int16)).to(dev)
+        vp = torch.from_numpy(w.v_pool.view(np.int16)).to(dev)
+        q = torch.from_numpy(w.q.view(np.int16)).to(dev)
+        rec = torch.zeros(w.n_slots * H * tpk.RECORD_BYTES if which == "int8" else 16, dtype=torch.uint8,
+                          device=dev)
+        if which == "int8":
+            slots = torch.from_numpy(w.int8_slots()).to(dev)
+            tpk.kv_quantize_pages(shape, kp, vp, slots, slots, len(slots), rec, stream)
+        pt, off = w.exact_page_table()
+        pt8, off8 = w.int8_page_table()
+        pt_d = torch.from_numpy(np.concatenate([pt, np.zeros(1, np.int32)])).to(dev)
+        pt8_d = torch.from_numpy(np.concatenate([pt8, np.zeros(1, np.int32)])).to(dev)
+        o = torch.empty(1, H * G, 256, dtype=torch.float32, device=dev)
+        lse = torch.empty(1, H * G, dtype=torch.float32, device=dev)
+        nbytes = tpk.hybrid_workspace_bytes(shape, 1)
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+
+    def step():
+        tpk.decode_hybrid_batched(shape, 1, q, kp, vp, rec, pt_d, off, w.n_ex, pt8_d, off8, w.n8, o, lse, ws,
+                                  nbytes, stream)
+
+    times = graph_times(step, args.tier_steps, 3, stream, flush, flush_r)
+    st, flags = tpk.get_device_status(reset=True, stream=stream)
+    if st != 0:
+        raise RuntimeError(f"device status {st} flags {flags} ({which} tier)")
+    ms = statistics.median(times)
+    gbs = w.history_bytes() / (ms * 1e-3) / 1e9
+    return {"history_bytes": w.history_bytes(), "us_per_step_median": round(ms * 1e3, 2),
+            "GBps": round(gbs, 1), "hbm_frac": round(gbs / peak, 4), "steps": len(times),
+            "workload": f"131072 tokens {'all BF16' if which == 'exact' else 'all 8-bit (2048 pages)'}, "
+                        "4 KV heads x 8 q rows, head_dim 256, outlier keys, seed 12"}
+
+
 def run_gpu(args, dist, rank, world):
     import torch
 
@@ -222,15 +298,17 @@ def run_gpu(args, dist, rank, world):
         nbytes = tpk.hybrid_workspace_bytes(shape, 1)
         ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
         tpk.workspace_init(ws, nbytes, stream)
-        # fresh page conversion of every 8-bit page (timed separately)
-        q_ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
-        q_ev[0].record(stream)
-        tpk.kv_quantize_pages(shape, kp, vp, slots, slots, len(slots), rec, stream)
-        q_ev[1].record(stream)
+        # fresh page conversion of every 8-bit page (timed separately: the median of
+        # five conversions of all 7,936 page-heads, each rewriting the same records)
+        q_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(6)]
+        for a, b in q_ev:
+            a.record(stream)
+            tpk.kv_quantize_pages(shape, kp, vp, slots, slots, len(slots), rec, stream)
+            b.record(stream)
         flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
         flush_r = torch.zeros(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     stream.synchronize()
-    quant_ms = q_ev[0].elapsed_time(q_ev[1])
+    quant_ms = statistics.median([a.elapsed_time(b) for a, b in q_ev[1:]])
     st, flags = tpk.get_device_status(reset=True, stream=stream)
     if st != 0:
         raise RuntimeError(f"device status {st} flags {flags}")
@@ -283,6 +361,12 @@ def run_gpu(args, dist, rank, world):
     if st != 0:
         raise RuntimeError(f"device status {st} flags {flags} after timing")
 
+    # ---- each tier alone at 128K (the exact and the 8-bit kernel paths)
+    peak, peak_kind = hbm_peak()
+    tiers = None
+    if args.tier_steps > 0:
+        tiers = {k: run_tier(k, impl, args, stream, dev, flush, flush_r, peak) for k in ("exact", "int8")}
+
     # ---- end to end from pinned host memory (packed history, identity page tables)
     e2e = run_e2e(args, w, rec, shape, stream, dev, dist)
     host_res = run_host_resident(args, w, rec, shape, stream, dev, dist) if args.layers > 0 else None
@@ -296,7 +380,6 @@ def run_gpu(args, dist, rank, world):
         cpu = {"value": round(nb / dt / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
                "sample": f"the full 128K hybrid step (all 4 KV heads), once, {dt:.1f} s; "
                          f"threads over (request, KV head)"}
-    peak, peak_kind = hbm_peak()
     achieved = hist_bytes / (ms_mean * 1e-3) / 1e9
     value = world * hist_bytes / (ms_max * 1e-3) / 1e9
     traffic = measured_traffic(args.kernel)
@@ -322,6 +405,7 @@ def run_gpu(args, dist, rank, world):
                      else "fallback 6.8 TB/s"},
         "e2e": e2e,
         "host_resident": host_res,
+        "tiers_128k": tiers,
         "gpu_launches": args.steps * launches_per_step,
         "clocks": clk.summary(),
         "cpu_baseline": cpu,
@@ -540,6 +624,7 @@ def main():
     ap.add_argument("--soak", type=float, default=1.0, help="seconds of back-to-back steps before timing")
     ap.add_argument("--layers", type=int, default=16, help="layers of the host-resident measurement (0: skip)")
     ap.add_argument("--host-steps", type=int, default=5, help="timed steps of the host-resident measurement")
+    ap.add_argument("--tier-steps", type=int, default=20, help="timed steps of each single-tier 128K line (0: skip)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "tpk":
         args.warmup = 3
