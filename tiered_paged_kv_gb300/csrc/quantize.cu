@@ -9,18 +9,19 @@
 // One thread block converts one page-head (64 tokens x 256 channels of K and V):
 //   1. the page-head is bulk-copied into shared memory;
 //   2. thread c owns channel c: the key channel's mean square is accumulated
-//      exactly (bfloat16 squares summed as 64-bit fixed point), the value
-//      channel's absolute maximum gives u_c = max|v| / 127;
+//      with compensated float32 additions of exact squares (relative error below
+//      2^-42), the value channel's absolute maximum gives u_c = max|v| / 127;
 //   3. the geometric mean of the mean squares is formed as a product of
 //      mantissas (double) and a sum of exponents, so the normalised fourth power
 //      x_c = ms_c / G needs one multiplication; shat_c = x_c^(1/4);
-//   4. the float32 neighbours of shat_c are found exactly (c^4 against x_c with
-//      an FMA-exact product), and one thread walks the channels choosing the
+//   4. the float32 neighbours of shat_c are found exactly (c^4 against x_c in
+//      integer arithmetic), and one thread walks the channels choosing the
 //      neighbour that keeps the running log-error of the product nearest zero,
 //      while the other seven warps write the value codes (they need only u_c);
 //   5. threads (token, quarter row) divide keys by s_c, take the per-token
-//      absolute maximum r_t = max|y| / 127 and form the codes with IEEE float32
-//      divisions and half-to-even rint.  Value codes are stored channel-major
+//      absolute maximum r_t = max|y| / 127 and form the codes as rint of the
+//      correctly rounded quotients (by reciprocal multiplication, with IEEE
+//      divisions wherever that could differ).  Value codes are stored channel-major
 //      (one 64-byte row per channel).  Fields are written at their swizzled
 //      positions (kc_byte, vc_byte, ks_index).
 #include "common.cuh"
@@ -35,6 +36,7 @@ struct QSmem {
   int red_e[8];
   double invG;
   alignas(16) float s[kHeadDim];
+  alignas(16) float inv_s[kHeadDim];
   alignas(16) float u[kHeadDim];
   alignas(16) float slo[kHeadDim];
   alignas(16) float shi[kHeadDim];
@@ -44,25 +46,67 @@ struct QSmem {
   int bad;
 };
 
-// c^4 - x, with c^2 exact in double and c^4 = hi + lo exact by FMA.
-__device__ __forceinline__ double pow4_minus(float c, double x) {
-  double c2 = (double)c * (double)c;
-  double hi = c2 * c2;
-  double lo = fma(c2, c2, -hi);
-  return (hi - x) + lo;
+// c^4 - x for a normal float c and a normal double x: the sign exactly, and the
+// relative difference (c^4 - x) / x as a float estimate.  With c = mc 2^ec (mc
+// 24 bits) and x = mx 2^ex (mx 53 bits), c^4 - x = 2^(4ec) (mc^4 - mx 2^s) for
+// s = ex - 4ec; mc^4 < 2^96 is formed exactly in two 64-bit words, so the
+// comparison needs no double-precision arithmetic (scarce on this GPU).
+struct Pow4Diff {
+  int sign;
+  float rel;
+};
+__device__ __forceinline__ Pow4Diff pow4_diff(float c, double x) {
+  const uint32_t cb = __float_as_uint(c);
+  const uint64_t mc = (cb & 0x7fffffu) | 0x800000u;
+  const int ec = (int)((cb >> 23) & 0xff) - 150;
+  const uint64_t xb = (uint64_t)__double_as_longlong(x);
+  const uint64_t mx = (xb & 0xfffffffffffffull) | 0x10000000000000ull;
+  const int ex = (int)((xb >> 52) & 0x7ff) - 1075;
+  const int s = ex - 4 * ec;
+  if (s <= 39) return {1, 1.f};    // mx 2^s < 2^92 <= mc^4
+  if (s >= 44) return {-1, -1.f};  // mx 2^s >= 2^96 > mc^4
+  const uint64_t m2 = mc * mc;     // < 2^48
+  const uint64_t p_lo = m2 * m2, p_hi = __umul64hi(m2, m2);
+  const uint64_t q_lo = mx << s, q_hi = mx >> (64 - s);
+  const uint64_t d_lo = p_lo - q_lo;
+  const int64_t d_hi = (int64_t)(p_hi - q_hi - (p_lo < q_lo ? 1u : 0u));
+  if (d_hi == 0 && d_lo == 0) return {0, 0.f};
+  // |D| of D = d_hi 2^64 + d_lo (two's complement), then rel = D / (mx 2^s)
+  uint64_t m_lo = d_lo, m_hi = (uint64_t)d_hi;
+  if (d_hi < 0) {
+    m_lo = ~d_lo + 1u;
+    m_hi = ~(uint64_t)d_hi + (m_lo == 0 ? 1u : 0u);
+  }
+  const float mag = (float)m_hi * 0x1p64f + (float)m_lo;
+  const float rel = mag * (1.f / (float)mx) * __int_as_float((127 - s) << 23);
+  return {d_hi < 0 ? -1 : 1, d_hi < 0 ? -rel : rel};
 }
 
-// The stored byte of a code: clamp(rint(x / scale), -127, 127) + 128 (offset binary).
-__device__ __forceinline__ uint32_t code_byte(float x, float scale) {
-  if (!(scale > 0.f)) return 128u;
-  float z = rintf(__fdiv_rn(x, scale));
-  z = fminf(fmaxf(z, -127.f), 127.f);
+// The stored byte of a code: clamp(rint(q), -127, 127) + 128 (offset binary) for
+// the quotient q = x / scale, correctly rounded.
+__device__ __forceinline__ uint32_t quotient_byte(float q) {
+  const float z = fminf(fmaxf(rintf(q), -127.f), 127.f);
   return (uint32_t)((int)z + 128);
 }
+__device__ __forceinline__ uint32_t code_byte(float x, float scale) {
+  if (!(scale > 0.f)) return 128u;
+  return quotient_byte(__fdiv_rn(x, scale));
+}
+
+// Codes by multiplication.  With inv = 1/scale correctly rounded, z = x * inv (a
+// value) or x * inv_s * inv_r (a key) is within 6 * 2^-24 * |z| of the correctly
+// rounded quotient (of the two correctly rounded divisions), i.e. within 2^-14.4
+// for |z| <= 128, where all codes live.  rint(z) is then the code unless z lies
+// within kCodeSlack (2^-12, a 4x margin) of a half-integer; a group of codes with
+// such an element, or with a scale outside [2^-100, 2^100], is redone with the
+// divisions.
+constexpr float kCodeSlack = 0x1p-12f;
+__device__ __forceinline__ bool near_half(float z) { return 0.5f - fabsf(z - rintf(z)) <= kCodeSlack; }
+__device__ __forceinline__ bool fast_scale(float scale) { return scale >= 0x1p-100f && scale <= 0x1p100f; }
 
 constexpr int kQuantThreads = 256;  // one thread per channel in the per-channel phases
 
-__global__ void __launch_bounds__(kQuantThreads) quantize_kernel(const __grid_constant__ QuantParams p) {
+__global__ void __launch_bounds__(kQuantThreads, 2) quantize_kernel(const __grid_constant__ QuantParams p) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   QSmem& S = *reinterpret_cast<QSmem*>(smem_raw);
   const int tid = threadIdx.x;
@@ -102,34 +146,47 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_kernel(const __grid_co
   // 64-byte row (channel-major layout)
   auto value_codes = [&](int ch, int t0) {
     const float u = S.u[ch];
+    const float inv = fast_scale(u) ? __frcp_rn(u) : 0.f;
+    bool redo = !fast_scale(u);
     uint32_t wv[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
-    for (int e = 0; e < 16; ++e) wv[e >> 2] |= code_byte(bf16_lo(S.v[t0 + e][ch]), u) << (8 * (e & 3));
+    for (int e = 0; e < 16; ++e) {
+      const float z = bf16_lo(S.v[t0 + e][ch]) * inv;
+      redo |= near_half(z);
+      wv[e >> 2] |= quotient_byte(z) << (8 * (e & 3));
+    }
+    if (redo) {
+      wv[0] = wv[1] = wv[2] = wv[3] = 0u;
+      for (int e = 0; e < 16; ++e) wv[e >> 2] |= code_byte(bf16_lo(S.v[t0 + e][ch]), u) << (8 * (e & 3));
+    }
     *reinterpret_cast<uint4*>(rec + kOffVc + vc_byte(ch, t0)) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
   };
   double mant = 1.0;
   int expo = 0;
   double ms = 0.0;
   if (!given) {
-    int emax = 1;
-    for (int t = 0; t < kPageTokens; ++t) {
-      int e = (S.k[t][c] >> 7) & 0xff;
-      emax = max(emax, e);
+    // Sum of squares: the channel is scaled by a power of two 2^-e (e the exponent
+    // of its largest |k|), so every square of a bfloat16 is exact in float32 and
+    // below 4; the squares are added with TwoSum into a float pair (relative error
+    // below 2^-42), then the mean is formed in double with the scale put back.
+    float kmax = 0.f;
+    for (int t = 0; t < kPageTokens; ++t) kmax = fmaxf(kmax, fabsf(bf16_lo(S.k[t][c])));
+    if (kmax > 0.f) {
+      int e = 0;
+      frexpf(kmax, &e);
+      const float sc = ldexpf(1.f, -e);  // kmax * sc in [0.5, 1)
+      float hi = 0.f, lo = 0.f;
+      for (int t = 0; t < kPageTokens; ++t) {
+        const float y = bf16_lo(S.k[t][c]) * sc;
+        const float sq = y * y;
+        const float s = hi + sq, bb = s - hi;
+        lo += (hi - (s - bb)) + (sq - bb);
+        hi = s;
+      }
+      ms = ldexp((double)hi + (double)lo, 2 * e - 6);  // mean over 64 tokens
+    } else {
+      ms = 0x1p-252;  // a zero channel: a = 2^-63 before the logarithm
     }
-    // element = m * 2^(e - 134) (m with the hidden bit; subnormals use e = 1);
-    // square = m^2 * 2^(2e - 268); fixed point unit 2^(2 emax - 308)
-    unsigned long long acc = 0;
-    for (int t = 0; t < kPageTokens; ++t) {
-      uint32_t bits = S.k[t][c] & 0x7fffu;
-      int e = bits >> 7;
-      uint32_t m = bits & 0x7fu;
-      if (e) m |= 0x80u; else e = 1;
-      unsigned long long m2 = (unsigned long long)(m * m);
-      int sh = 2 * (emax - e);
-      if (sh <= 40) acc += m2 << (40 - sh);
-      else if (sh < 56) acc += m2 >> (sh - 40);
-    }
-    ms = acc ? ldexp((double)acc, 2 * emax - 308 - 6) : 0x1p-252;  // mean over 64 tokens
     mant = frexp(ms, &expo);
   }
   // ---- 3. geometric mean of ms over channels: product of mantissas, sum of exponents
@@ -174,21 +231,21 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_kernel(const __grid_co
     } else {
       float cc = sqrtf(sqrtf((float)x));
       for (int it = 0; it < 4; ++it) {
-        if (pow4_minus(cc, x) > 0.0) cc = nextafterf(cc, 0.f);
-        else if (pow4_minus(nextafterf(cc, 0x1p127f), x) <= 0.0) cc = nextafterf(cc, 0x1p127f);
+        if (pow4_diff(cc, x).sign > 0) cc = nextafterf(cc, 0.f);
+        else if (pow4_diff(nextafterf(cc, 0x1p127f), x).sign <= 0) cc = nextafterf(cc, 0x1p127f);
         else break;
       }
-      double df = pow4_minus(cc, x);
-      if (df == 0.0) {
+      const Pow4Diff dlo_ = pow4_diff(cc, x);
+      if (dlo_.sign == 0) {
         lo = hi = cc;
         ex = 1;
       } else {
         lo = cc;
         hi = nextafterf(cc, 0x1p127f);
-        double rx = 1.0 / x;
-        double a = df * rx, b = pow4_minus(hi, x) * rx;  // relative error of the fourth power
-        dl = (float)(0.25 * a - 0.125 * a * a);           // ln(lo / shat)
-        dh = (float)(0.25 * b - 0.125 * b * b);           // ln(hi / shat)
+        // ln(c / shat) = ln(1 + a) / 4 for the relative error a of the fourth power
+        const float a = dlo_.rel, b = pow4_diff(hi, x).rel;
+        dl = fmaf(-0.125f * a, a, 0.25f * a);
+        dh = fmaf(-0.125f * b, b, 0.25f * b);
       }
     }
     S.slo[c] = lo;
@@ -236,34 +293,89 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_kernel(const __grid_co
     for (int it = tid - 32; it < kHeadDim * 4; it += kQuantThreads - 32) value_codes(it >> 2, (it & 3) * 16);
   }
   __syncthreads();
+  S.inv_s[c] = __frcp_rn(S.s[c]);
+  __syncthreads();
   // ---- 5. codes: thread (token t, quarter q) handles 64 channels, chunks rotated
-  //         by lane so that shared-memory reads do not conflict
+  //         by lane so that shared-memory reads do not conflict.  y_tc = k_tc / s_c
+  //         is estimated as k * (1/s_c); the exact max |y| of the row comes from
+  //         correctly rounded divisions of the elements whose estimate is within
+  //         2^-20 of the estimated maximum (the argmax is among them).
   {
     const int t = tid >> 2, q = tid & 3, lane = tid & 31;
-    float y[8][8];
-    float ymax = 0.f;
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
+    // the estimates y = k * (1/s_c) of chunk k (8 channels); recomputed in each
+    // pass, which costs less than holding 64 of them in registers
+    auto estimates = [&](int k, float (&yv)[8]) {
       const int ch0 = q * 64 + ((k + lane) & 7) * 8;
-      uint4 w = *reinterpret_cast<const uint4*>(&S.k[t][ch0]);
-      float f[8] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y),
-                    bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w)};
+      const uint4 w = *reinterpret_cast<const uint4*>(&S.k[t][ch0]);
+      const float4 i0 = *reinterpret_cast<const float4*>(&S.inv_s[ch0]);
+      const float4 i1 = *reinterpret_cast<const float4*>(&S.inv_s[ch0 + 4]);
+      yv[0] = bf16_lo(w.x) * i0.x;
+      yv[1] = bf16_hi(w.x) * i0.y;
+      yv[2] = bf16_lo(w.y) * i0.z;
+      yv[3] = bf16_hi(w.y) * i0.w;
+      yv[4] = bf16_lo(w.z) * i1.x;
+      yv[5] = bf16_hi(w.z) * i1.y;
+      yv[6] = bf16_lo(w.w) * i1.z;
+      yv[7] = bf16_hi(w.w) * i1.w;
+    };
+    float amax = 0.f;
+    bool s_fast = true;
+#pragma unroll 2
+    for (int k = 0; k < 8; ++k) {
+      float yv[8];
+      estimates(k, yv);
+      const int ch0 = q * 64 + ((k + lane) & 7) * 8;
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        y[k][e] = __fdiv_rn(f[e], S.s[ch0 + e]);
-        ymax = fmaxf(ymax, fabsf(y[k][e]));
+        amax = fmaxf(amax, fabsf(yv[e]));
+        s_fast &= fast_scale(S.s[ch0 + e]);
       }
+    }
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    // candidates for the exact maximum: a bit mask, then divisions for its bits only
+    const float thr = amax * (1.f - 0x1p-20f);
+    uint64_t cand = 0;
+#pragma unroll 2
+    for (int k = 0; k < 8; ++k) {
+      float yv[8];
+      estimates(k, yv);
+      uint32_t m = 0;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) m |= (uint32_t)(!s_fast || fabsf(yv[e]) >= thr) << e;
+      cand |= (uint64_t)m << (8 * k);
+    }
+    float ymax = 0.f;
+    while (cand) {
+      const int i = __ffsll((long long)cand) - 1;
+      cand &= cand - 1;
+      const int ch = q * 64 + (((i >> 3) + lane) & 7) * 8 + (i & 7);
+      ymax = fmaxf(ymax, fabsf(__fdiv_rn(bf16_lo(S.k[t][ch]), S.s[ch])));
     }
     ymax = fmaxf(ymax, __shfl_xor_sync(0xffffffffu, ymax, 1));
     ymax = fmaxf(ymax, __shfl_xor_sync(0xffffffffu, ymax, 2));
     const float r = given ? p.g_ktok[gidx * kPageTokens + t] : __fdiv_rn(ymax, 127.f);
+    const bool fast = s_fast && fast_scale(r);
+    const float inv_r = fast ? __frcp_rn(r) : 0.f;
     uint8_t* kc = rec + kOffKc;
-#pragma unroll
+#pragma unroll 2
     for (int k = 0; k < 8; ++k) {
+      float yv[8];
+      estimates(k, yv);
       const int ch0 = q * 64 + ((k + lane) & 7) * 8;
       uint32_t wk[2] = {0u, 0u};
+      bool redo = !fast;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) wk[e >> 2] |= code_byte(y[k][e], r) << (8 * (e & 3));
+      for (int e = 0; e < 8; ++e) {
+        const float z = yv[e] * inv_r;
+        redo |= near_half(z);
+        wk[e >> 2] |= quotient_byte(z) << (8 * (e & 3));
+      }
+      if (redo) {
+        wk[0] = wk[1] = 0u;
+        for (int e = 0; e < 8; ++e)
+          wk[e >> 2] |= code_byte(__fdiv_rn(bf16_lo(S.k[t][ch0 + e]), S.s[ch0 + e]), r) << (8 * (e & 3));
+      }
       *reinterpret_cast<uint2*>(kc + kc_byte(t, ch0)) = make_uint2(wk[0], wk[1]);
     }
     if (q == 0) reinterpret_cast<float*>(rec + kOffKsTok)[t] = r;
