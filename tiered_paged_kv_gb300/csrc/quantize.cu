@@ -8,22 +8,22 @@
 //
 // One thread block converts one page-head (64 tokens x 256 channels of K and V):
 //   1. the page-head is bulk-copied into shared memory;
-//   2. thread c owns channel c: the key channel's mean square is accumulated
-//      with compensated float32 additions of exact squares (relative error below
-//      2^-42), the value channel's absolute maximum gives u_c = max|v| / 127;
-//   3. the geometric mean of the mean squares is formed as a product of
-//      mantissas (double) and a sum of exponents, so the normalised fourth power
-//      x_c = ms_c / G needs one multiplication; shat_c = x_c^(1/4);
-//   4. the float32 neighbours of shat_c are found exactly (c^4 against x_c in
-//      integer arithmetic), and one thread walks the channels choosing the
+//   2. thread c owns channel c: u_c = max|v| / 127, and the key mean square with
+//      compensated float32 additions of exact squares (relative error below
+//      2^-42);
+//   3. the geometric mean of the mean squares as a product of mantissas (double)
+//      and a sum of exponents, so the normalised fourth power x_c = ms_c / G
+//      needs one multiplication; shat_c = x_c^(1/4);
+//   4. the float32 neighbours of shat_c, found exactly (c^4 against x_c in
+//      integer arithmetic); then one lane walks the channels choosing the
 //      neighbour that keeps the running log-error of the product nearest zero,
-//      while the other seven warps write the value codes (they need only u_c);
-//   5. threads (token, quarter row) divide keys by s_c, take the per-token
-//      absolute maximum r_t = max|y| / 127 and form the codes as rint of the
-//      correctly rounded quotients (by reciprocal multiplication, with IEEE
-//      divisions wherever that could differ).  Value codes are stored channel-major
-//      (one 64-byte row per channel).  Fields are written at their swizzled
-//      positions (kc_byte, vc_byte, ks_index).
+//      while warps 1-7 write the value codes (channel-major, one 64-byte row per
+//      channel), which need only u_c;
+//   5. threads (token, quarter row) take y = k / s_c, the per-token absolute
+//      maximum r_t = max|y| / 127 and the key codes, as rint of the correctly
+//      rounded quotients (by reciprocal multiplication, with IEEE divisions
+//      wherever that could differ).
+// Fields are written at their swizzled positions (kc_byte, vc_byte, ks_index).
 #include "common.cuh"
 
 namespace tpk {
@@ -42,7 +42,6 @@ struct QSmem {
   alignas(16) float shi[kHeadDim];
   alignas(16) float dlo[kHeadDim];
   alignas(16) float dhi[kHeadDim];
-  alignas(16) int exact[kHeadDim];
   int bad;
 };
 
@@ -97,14 +96,16 @@ __device__ __forceinline__ uint32_t code_byte(float x, float scale) {
 // value) or x * inv_s * inv_r (a key) is within 6 * 2^-24 * |z| of the correctly
 // rounded quotient (of the two correctly rounded divisions), i.e. within 2^-14.4
 // for |z| <= 128, where all codes live.  rint(z) is then the code unless z lies
-// within kCodeSlack (2^-12, a 4x margin) of a half-integer; a group of codes with
-// such an element, or with a scale outside [2^-100, 2^100], is redone with the
-// divisions.
+// within kCodeSlack (2^-12, a 4x margin) of a half-integer -- which happens
+// often (an element equal to half its row's or channel's maximum gives exactly
+// 63.5) -- so those bytes are rewritten from the divisions after the group is
+// stored, as are all bytes of a scale outside [2^-100, 2^100].
 constexpr float kCodeSlack = 0x1p-12f;
 __device__ __forceinline__ bool near_half(float z) { return 0.5f - fabsf(z - rintf(z)) <= kCodeSlack; }
 __device__ __forceinline__ bool fast_scale(float scale) { return scale >= 0x1p-100f && scale <= 0x1p100f; }
 
 constexpr int kQuantThreads = 256;  // one thread per channel in the per-channel phases
+
 
 __global__ void __launch_bounds__(kQuantThreads, 2) quantize_kernel(const __grid_constant__ QuantParams p) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -136,39 +137,50 @@ __global__ void __launch_bounds__(kQuantThreads, 2) quantize_kernel(const __grid
   const int64_t gidx = (int64_t)i * p.H + h;  // index into given-scale arrays
   const int c = tid;
 
-  // ---- 2. per-channel statistics
-  {
-    float vmax = 0.f;
-    for (int t = 0; t < kPageTokens; ++t) vmax = fmaxf(vmax, fabsf(bf16_lo(S.v[t][c])));
-    S.u[c] = given ? p.g_vchan[gidx * kHeadDim + c] : __fdiv_rn(vmax, 127.f);
-  }
   // value codes of channel ch, tokens t0 .. t0 + 15: 16 bytes of the channel's
   // 64-byte row (channel-major layout)
+  // (t0 is a multiple of 16, so the 16 bytes are contiguous: vc_byte(ch, t0 + e) =
+  // vc_byte(ch, t0) + e)
   auto value_codes = [&](int ch, int t0) {
     const float u = S.u[ch];
-    const float inv = fast_scale(u) ? __frcp_rn(u) : 0.f;
-    bool redo = !fast_scale(u);
+    const bool fast = fast_scale(u);
+    const float inv = fast ? __frcp_rn(u) : 0.f;
+    uint32_t redo = fast ? 0u : 0xffffu;
     uint32_t wv[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
     for (int e = 0; e < 16; ++e) {
       const float z = bf16_lo(S.v[t0 + e][ch]) * inv;
-      redo |= near_half(z);
+      redo |= (uint32_t)near_half(z) << e;
       wv[e >> 2] |= quotient_byte(z) << (8 * (e & 3));
     }
-    if (redo) {
-      wv[0] = wv[1] = wv[2] = wv[3] = 0u;
-      for (int e = 0; e < 16; ++e) wv[e >> 2] |= code_byte(bf16_lo(S.v[t0 + e][ch]), u) << (8 * (e & 3));
+    uint8_t* dst = rec + kOffVc + vc_byte(ch, t0);
+    *reinterpret_cast<uint4*>(dst) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+    while (redo) {
+      const int e = __ffs(redo) - 1;
+      redo &= redo - 1;
+      dst[e] = (uint8_t)code_byte(bf16_lo(S.v[t0 + e][ch]), u);
     }
-    *reinterpret_cast<uint4*>(rec + kOffVc + vc_byte(ch, t0)) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
   };
-  double mant = 1.0;
-  int expo = 0;
-  double ms = 0.0;
-  if (!given) {
-    // Sum of squares: the channel is scaled by a power of two 2^-e (e the exponent
-    // of its largest |k|), so every square of a bfloat16 is exact in float32 and
-    // below 4; the squares are added with TwoSum into a float pair (relative error
-    // below 2^-42), then the mean is formed in double with the scale put back.
+  // (channel, 16-token quarter) items, channel fastest, so that a warp's lanes read
+  // neighbouring channels of the same tokens
+  constexpr int kValueItems = kHeadDim * kPageTokens / 16;
+
+  if (given) {
+    S.u[c] = p.g_vchan[gidx * kHeadDim + c];
+    S.s[c] = p.g_kchan[gidx * kHeadDim + c];
+    __syncthreads();
+    for (int it = tid; it < kValueItems; it += kQuantThreads) value_codes(it & 255, (it >> 8) * 16);
+  } else {
+    // 2. thread c: u_c = max|v| / 127, and the key mean square.  The key channel
+    //    is scaled by a power of two 2^-e (e the exponent of its largest |k|), so
+    //    every square of a bfloat16 is exact in float32 and below 4; the squares
+    //    are added with TwoSum into a float pair (relative error below 2^-42),
+    //    then the mean is formed in double with the scale put back.  A zero
+    //    channel takes a = 2^-63 before the logarithm.
+    float vmax = 0.f;
+    for (int t = 0; t < kPageTokens; ++t) vmax = fmaxf(vmax, fabsf(bf16_lo(S.v[t][c])));
+    S.u[c] = __fdiv_rn(vmax, 127.f);
+    double ms;
     float kmax = 0.f;
     for (int t = 0; t < kPageTokens; ++t) kmax = fmaxf(kmax, fabsf(bf16_lo(S.k[t][c])));
     if (kmax > 0.f) {
@@ -179,22 +191,21 @@ __global__ void __launch_bounds__(kQuantThreads, 2) quantize_kernel(const __grid
       for (int t = 0; t < kPageTokens; ++t) {
         const float y = bf16_lo(S.k[t][c]) * sc;
         const float sq = y * y;
-        const float s = hi + sq, bb = s - hi;
-        lo += (hi - (s - bb)) + (sq - bb);
-        hi = s;
+        const float sum = hi + sq, bb = sum - hi;
+        lo += (hi - (sum - bb)) + (sq - bb);
+        hi = sum;
       }
       ms = ldexp((double)hi + (double)lo, 2 * e - 6);  // mean over 64 tokens
     } else {
-      ms = 0x1p-252;  // a zero channel: a = 2^-63 before the logarithm
+      ms = 0x1p-252;
     }
-    mant = frexp(ms, &expo);
-  }
-  // ---- 3. geometric mean of ms over channels: product of mantissas, sum of exponents
-  if (!given) {
+    // 3. geometric mean of ms over channels: product of mantissas, sum of exponents
+    int expo = 0;
+    double mant = frexp(ms, &expo);
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) {
-      double mo = __shfl_xor_sync(0xffffffffu, mant, off);
-      int eo = __shfl_xor_sync(0xffffffffu, expo, off);
+      const double mo = __shfl_xor_sync(0xffffffffu, mant, off);
+      const int eo = __shfl_xor_sync(0xffffffffu, expo, off);
       int t;
       mant = frexp(mant * mo, &t);
       expo += eo + t;
@@ -203,94 +214,97 @@ __global__ void __launch_bounds__(kQuantThreads, 2) quantize_kernel(const __grid
       S.red_m[tid >> 5] = mant;
       S.red_e[tid >> 5] = expo;
     }
-  }
-  __syncthreads();
-  if (!given && tid == 0) {
-    double m = S.red_m[0];
-    int e = S.red_e[0];
-    for (int w = 1; w < 8; ++w) {
-      int t;
-      m = frexp(m * S.red_m[w], &t);
-      e += S.red_e[w] + t;
-    }
-    double lnG = (log(m) + (double)e * 0.69314718055994530942) / kHeadDim;
-    S.invG = exp(-lnG);
-  }
-  __syncthreads();
-  // ---- 4. float32 neighbours of shat_c = (ms_c / G)^(1/4), clamped to 2^+-14
-  if (!given) {
-    double x = ms * S.invG;
-    float lo, hi, dl = 0.f, dh = 0.f;
-    int ex = 0;
-    if (x >= 0x1p56) {
-      lo = hi = 0x1p14f;
-      ex = 1;
-    } else if (x <= 0x1p-56) {
-      lo = hi = 0x1p-14f;
-      ex = 1;
-    } else {
-      float cc = sqrtf(sqrtf((float)x));
-      for (int it = 0; it < 4; ++it) {
-        if (pow4_diff(cc, x).sign > 0) cc = nextafterf(cc, 0.f);
-        else if (pow4_diff(nextafterf(cc, 0x1p127f), x).sign <= 0) cc = nextafterf(cc, 0x1p127f);
-        else break;
-      }
-      const Pow4Diff dlo_ = pow4_diff(cc, x);
-      if (dlo_.sign == 0) {
-        lo = hi = cc;
-        ex = 1;
-      } else {
-        lo = cc;
-        hi = nextafterf(cc, 0x1p127f);
-        // ln(c / shat) = ln(1 + a) / 4 for the relative error a of the fourth power
-        const float a = dlo_.rel, b = pow4_diff(hi, x).rel;
-        dl = fmaf(-0.125f * a, a, 0.25f * a);
-        dh = fmaf(-0.125f * b, b, 0.25f * b);
-      }
-    }
-    S.slo[c] = lo;
-    S.shi[c] = hi;
-    S.dlo[c] = dl;
-    S.dhi[c] = dh;
-    S.exact[c] = ex;
-  }
-  __syncthreads();
-  if (given) {
-    S.s[c] = p.g_kchan[gidx * kHeadDim + c];
-    for (int t0 = 0; t0 < kPageTokens; t0 += 16) value_codes(c, t0);
-  } else if (tid < 32) {
-    // The compensated walk is sequential in the channels; one lane runs it with
-    // each group of 8 channels' candidates loaded into registers first, while the
-    // other seven warps write the value codes, which do not depend on s.
+    __syncthreads();
     if (tid == 0) {
+      double m = S.red_m[0];
+      int e = S.red_e[0];
+      for (int w = 1; w < kQuantThreads / 32; ++w) {
+        int t;
+        m = frexp(m * S.red_m[w], &t);
+        e += S.red_e[w] + t;
+      }
+      const double lnG = (log(m) + (double)e * 0.69314718055994530942) / kHeadDim;
+      S.invG = exp(-lnG);
+    }
+    __syncthreads();
+    // 4. float32 neighbours of shat_c = (ms_c / G)^(1/4), clamped to 2^+-14.  A
+    //    channel whose scale is fixed (clamped, or shat_c a float) gets lo = hi and
+    //    zero log errors, so the walk keeps its running error unchanged there.
+    {
+      const double x = ms * S.invG;
+      float lo, hi, dl = 0.f, dh = 0.f;
+      if (x >= 0x1p56) {
+        lo = hi = 0x1p14f;
+      } else if (x <= 0x1p-56) {
+        lo = hi = 0x1p-14f;
+      } else {
+        float cc = sqrtf(sqrtf((float)x));
+        for (int it = 0; it < 4; ++it) {
+          if (pow4_diff(cc, x).sign > 0) cc = nextafterf(cc, 0.f);
+          else if (pow4_diff(nextafterf(cc, 0x1p127f), x).sign <= 0) cc = nextafterf(cc, 0x1p127f);
+          else break;
+        }
+        const Pow4Diff d = pow4_diff(cc, x);
+        lo = hi = cc;
+        if (d.sign != 0) {
+          hi = nextafterf(cc, 0x1p127f);
+          // ln(c / shat) = ln(1 + a) / 4 for the relative error a of the fourth power
+          const float a = d.rel, b = pow4_diff(hi, x).rel;
+          dl = fmaf(-0.125f * a, a, 0.25f * a);
+          dh = fmaf(-0.125f * b, b, 0.25f * b);
+        }
+      }
+      S.slo[c] = lo;
+      S.shi[c] = hi;
+      S.dlo[c] = dl;
+      S.dhi[c] = dh;
+    }
+    __syncthreads();
+    if (tid == 0) {
+      // 5. the compensated walk, sequential in the channels: one lane, each group
+      //    of 8 channels' candidates loaded one group ahead
       float E = 0.f;
+      float4 c_lo[2], c_hi[2], c_dl[2], c_dh[2];
+      auto load = [&](int ch0, float4 (&lo)[2], float4 (&hi)[2], float4 (&dl)[2], float4 (&dh)[2]) {
+        lo[0] = *reinterpret_cast<const float4*>(&S.slo[ch0]);
+        lo[1] = *reinterpret_cast<const float4*>(&S.slo[ch0 + 4]);
+        hi[0] = *reinterpret_cast<const float4*>(&S.shi[ch0]);
+        hi[1] = *reinterpret_cast<const float4*>(&S.shi[ch0 + 4]);
+        dl[0] = *reinterpret_cast<const float4*>(&S.dlo[ch0]);
+        dl[1] = *reinterpret_cast<const float4*>(&S.dlo[ch0 + 4]);
+        dh[0] = *reinterpret_cast<const float4*>(&S.dhi[ch0]);
+        dh[1] = *reinterpret_cast<const float4*>(&S.dhi[ch0 + 4]);
+      };
+      load(0, c_lo, c_hi, c_dl, c_dh);
       for (int ch0 = 0; ch0 < kHeadDim; ch0 += 8) {
-        float lo[8], hi[8], dl[8], dh[8], sv[8];
-        int ex[8];
-        *reinterpret_cast<float4*>(lo) = *reinterpret_cast<const float4*>(&S.slo[ch0]);
-        *reinterpret_cast<float4*>(lo + 4) = *reinterpret_cast<const float4*>(&S.slo[ch0 + 4]);
-        *reinterpret_cast<float4*>(hi) = *reinterpret_cast<const float4*>(&S.shi[ch0]);
-        *reinterpret_cast<float4*>(hi + 4) = *reinterpret_cast<const float4*>(&S.shi[ch0 + 4]);
-        *reinterpret_cast<float4*>(dl) = *reinterpret_cast<const float4*>(&S.dlo[ch0]);
-        *reinterpret_cast<float4*>(dl + 4) = *reinterpret_cast<const float4*>(&S.dlo[ch0 + 4]);
-        *reinterpret_cast<float4*>(dh) = *reinterpret_cast<const float4*>(&S.dhi[ch0]);
-        *reinterpret_cast<float4*>(dh + 4) = *reinterpret_cast<const float4*>(&S.dhi[ch0 + 4]);
-        *reinterpret_cast<int4*>(ex) = *reinterpret_cast<const int4*>(&S.exact[ch0]);
-        *reinterpret_cast<int4*>(ex + 4) = *reinterpret_cast<const int4*>(&S.exact[ch0 + 4]);
+        float4 n_lo[2], n_hi[2], n_dl[2], n_dh[2];
+        load(ch0 + 8 < kHeadDim ? ch0 + 8 : ch0, n_lo, n_hi, n_dl, n_dh);
+        const float lo[8] = {c_lo[0].x, c_lo[0].y, c_lo[0].z, c_lo[0].w, c_lo[1].x, c_lo[1].y, c_lo[1].z, c_lo[1].w};
+        const float hi[8] = {c_hi[0].x, c_hi[0].y, c_hi[0].z, c_hi[0].w, c_hi[1].x, c_hi[1].y, c_hi[1].z, c_hi[1].w};
+        const float dl[8] = {c_dl[0].x, c_dl[0].y, c_dl[0].z, c_dl[0].w, c_dl[1].x, c_dl[1].y, c_dl[1].z, c_dl[1].w};
+        const float dh[8] = {c_dh[0].x, c_dh[0].y, c_dh[0].z, c_dh[0].w, c_dh[1].x, c_dh[1].y, c_dh[1].z, c_dh[1].w};
+        float sv[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const float a = E + dl[e], b = E + dh[e];
-          const bool take_lo = ex[e] || fabsf(a) <= fabsf(b);
+          const bool take_lo = fabsf(a) <= fabsf(b);
           sv[e] = take_lo ? lo[e] : hi[e];
-          E = ex[e] ? E : (take_lo ? a : b);
+          E = take_lo ? a : b;
         }
-        *reinterpret_cast<float4*>(&S.s[ch0]) = *reinterpret_cast<const float4*>(sv);
-        *reinterpret_cast<float4*>(&S.s[ch0 + 4]) = *reinterpret_cast<const float4*>(sv + 4);
+        *reinterpret_cast<float4*>(&S.s[ch0]) = make_float4(sv[0], sv[1], sv[2], sv[3]);
+        *reinterpret_cast<float4*>(&S.s[ch0 + 4]) = make_float4(sv[4], sv[5], sv[6], sv[7]);
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          c_lo[k] = n_lo[k];
+          c_hi[k] = n_hi[k];
+          c_dl[k] = n_dl[k];
+          c_dh[k] = n_dh[k];
+        }
       }
+    } else if (tid >= 32) {
+      // meanwhile warps 1-7 write the value codes, which do not depend on s
+      for (int it = tid - 32; it < kValueItems; it += kQuantThreads - 32) value_codes(it & 255, (it >> 8) * 16);
     }
-  } else {
-    // (channel, 16-token quarter) items spread evenly over the seven warps
-    for (int it = tid - 32; it < kHeadDim * 4; it += kQuantThreads - 32) value_codes(it >> 2, (it & 3) * 16);
   }
   __syncthreads();
   S.inv_s[c] = __frcp_rn(S.s[c]);
@@ -364,19 +378,21 @@ __global__ void __launch_bounds__(kQuantThreads, 2) quantize_kernel(const __grid
       estimates(k, yv);
       const int ch0 = q * 64 + ((k + lane) & 7) * 8;
       uint32_t wk[2] = {0u, 0u};
-      bool redo = !fast;
+      uint32_t redo = fast ? 0u : 0xffu;
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         const float z = yv[e] * inv_r;
-        redo |= near_half(z);
+        redo |= (uint32_t)near_half(z) << e;
         wk[e >> 2] |= quotient_byte(z) << (8 * (e & 3));
       }
-      if (redo) {
-        wk[0] = wk[1] = 0u;
-        for (int e = 0; e < 8; ++e)
-          wk[e >> 2] |= code_byte(__fdiv_rn(bf16_lo(S.k[t][ch0 + e]), S.s[ch0 + e]), r) << (8 * (e & 3));
+      // (ch0 is a multiple of 8: kc_byte(t, ch0 + e) = kc_byte(t, ch0) + e)
+      uint8_t* dst = kc + kc_byte(t, ch0);
+      *reinterpret_cast<uint2*>(dst) = make_uint2(wk[0], wk[1]);
+      while (redo) {
+        const int e = __ffs(redo) - 1;
+        redo &= redo - 1;
+        dst[e] = (uint8_t)code_byte(__fdiv_rn(bf16_lo(S.k[t][ch0 + e]), S.s[ch0 + e]), r);
       }
-      *reinterpret_cast<uint2*>(kc + kc_byte(t, ch0)) = make_uint2(wk[0], wk[1]);
     }
     if (q == 0) reinterpret_cast<float*>(rec + kOffKsTok)[t] = r;
   }
