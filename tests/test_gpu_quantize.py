@@ -101,3 +101,53 @@ def test_bad_slot_is_skipped_and_reported():
     st, flags = tpk.get_device_status(reset=True)
     assert st == 4 and flags & 1
     assert int(d.rec.sum().item()) == 0
+
+
+def tie_pages(seed, n_pages):
+    """Pages whose quotients land on and next to half-integers: K is a
+    half-integer times s_c * r_t, V a half-integer times u_c, with the given scales
+    powers of two (exact quotients: ties to even) or not (ties broken by the
+    roundings of the two divisions), plus elements one bfloat16 ulp off."""
+    rng = np.random.default_rng(seed)
+    ks = np.where(rng.random((n_pages, 256)) < 0.5, 2.0 ** rng.integers(-3, 4, (n_pages, 256)),
+                  rng.uniform(0.3, 3.0, (n_pages, 256))).astype(np.float32)
+    kt = np.where(rng.random((n_pages, 64)) < 0.5, 2.0 ** rng.integers(-3, 4, (n_pages, 64)),
+                  rng.uniform(0.3, 3.0, (n_pages, 64))).astype(np.float32)
+    vs = np.where(rng.random((n_pages, 256)) < 0.5, 2.0 ** rng.integers(-3, 4, (n_pages, 256)),
+                  rng.uniform(0.3, 3.0, (n_pages, 256))).astype(np.float32)
+    half = (rng.integers(-127, 127, (n_pages, 64, 256)) + 0.5).astype(np.float32)
+    kf = half * ks[:, None, :] * kt[:, :, None]
+    vf = (rng.integers(-127, 127, (n_pages, 64, 256)) + 0.5).astype(np.float32) * vs[:, None, :]
+    kb = synth.f32_to_bf16(kf)
+    vb = synth.f32_to_bf16(vf)
+    nudge = rng.random(kb.shape) < 0.1                   # one bfloat16 ulp away from the value
+    kb = np.where(nudge, kb + np.where(rng.random(kb.shape) < 0.5, 1, -1).astype(np.int32), kb).astype(np.uint16)
+    vb = np.where(nudge, vb + np.where(rng.random(vb.shape) < 0.5, 1, -1).astype(np.int32), vb).astype(np.uint16)
+    return kb, vb, ks, kt, vs
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_codes_at_half_integer_quotients(seed):
+    """Codes whose quotients are exact half-integers (the reciprocal-multiplication
+    estimate cannot decide them) or next to one: bit-exact with the oracle given
+    the scales, and self-consistent with the GPU's own scales."""
+    n = 24
+    kb, vb, ks, kt, vs = tie_pages(seed, n)
+    w = synth.make_workload([64 * n], 0, H=1, seed=40 + seed)
+    slots = w.int8_slots()
+    for i, slot in enumerate(slots):
+        w.k_pool[slot, 0] = kb[i]
+        w.v_pool[slot, 0] = vb[i]
+    d = DevWorkload(w)
+    s = dev_i32(slots)
+    tpk.kv_quantize_pages_given_scales(d.shape, d.k, d.v, s, s, n, dev_f32(ks), dev_f32(kt), dev_f32(vs), d.rec)
+    got = d.rec.cpu().numpy().reshape(w.n_slots, oracle.REC_BYTES)
+    for i, slot in enumerate(slots):
+        ref = oracle.codes_given(w.k_pool[slot, 0], w.v_pool[slot, 0], ks[i], kt[i], vs[i])
+        assert np.array_equal(got[slot], ref), f"page {i}"
+    # own scales: the codes follow from the scales the GPU wrote, exactly
+    got = d.quantize_gpu().reshape(w.n_slots, oracle.REC_BYTES)
+    for slot in slots:
+        _, _, s_, r_, u_ = oracle.record_fields(got[slot])
+        again = oracle.codes_given(w.k_pool[slot, 0], w.v_pool[slot, 0], s_, r_, u_)
+        assert np.array_equal(again, got[slot])
