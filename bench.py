@@ -497,7 +497,7 @@ def host_mem_available():
     return 0
 
 
-def run_host_resident(args, w, rec_dev, shape, stream, dev, dist):
+def run_host_resident(args, w, rec_dev, shape, stream, dev, dist, layers=None, steps=None, label=None):
     """Many layers of the same-sized history in pinned host memory (one image per
     layer; the content of every layer is this workload's), two device slots: per
     step every layer is staged while the previous layer decodes.  Bound by the
@@ -508,7 +508,8 @@ def run_host_resident(args, w, rec_dev, shape, stream, dev, dist):
 
     H, G = w.H, w.G
     img, off = w.packed_image(rec_dev.cpu().numpy())
-    layers = args.layers
+    layers = args.layers if layers is None else layers
+    steps = args.host_steps if steps is None else steps
     avail = host_mem_available()
     if avail and layers * off["nbytes"] * 2 > avail:  # keep well inside the host's memory
         layers = max(2, int(avail // (2 * off["nbytes"])))
@@ -543,7 +544,7 @@ def run_host_resident(args, w, rec_dev, shape, stream, dev, dist):
             one_step()
             stream.synchronize()
             times = []
-            for _ in range(args.host_steps):
+            for _ in range(steps):
                 ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
                 ev[0].record(stream)
                 ev[0].synchronize()
@@ -573,7 +574,74 @@ def run_host_resident(args, w, rec_dev, shape, stream, dev, dist):
             "link_GBps": round(link, 1), "link_peak_GBps": round(best, 1), "link_frac": round(link / best, 4),
             "history_GBps": round(layers * w.history_bytes() / (ms * 1e-3) / 1e9, 1),
             "slots": 2, "slot_bytes": int(off["nbytes"]),
-            "workload": f"{layers} layers x the 128K hybrid history (one pinned host image per layer)"}
+            "workload": label or f"{layers} layers x the 128K hybrid history (one pinned host image per layer)"}
+
+
+def run_gate_sweep(args):
+    """Exact vs hybrid over history lengths (the pages' economic gate: bytes saved
+    per token against GPU time added): for each length, an all-BF16 history and a
+    hybrid one (4096 recent BF16 tokens, older pages 8-bit) of one request, 4 KV
+    heads x 8 q rows, outlier keys; device-resident decode time (graph replays, L2
+    flushed) and host-resident step time per layer (layers staged through two slots)."""
+    import torch
+
+    import tiered_paged_kv_gb300 as tpk
+    from tiered_paged_kv_gb300 import build as tbuild
+    from tiered_paged_kv_gb300 import synth
+
+    torch.cuda.set_device(0)
+    tbuild.build()
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.Stream(dev)
+    with torch.cuda.stream(stream):
+        flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+        flush_r = torch.zeros(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    peak, _ = hbm_peak()
+    rows = []
+    for n in [int(x) for x in args.gate_lengths.split(",")]:
+        row = {"tokens": n}
+        for tier in ("exact", "hybrid"):
+            w = synth.make_workload([n], None if tier == "exact" else 4096, H=4, seed=20, key_sigma="outliers")
+            H, G = w.H, w.G
+            shape = tpk.Shape(H, kv_slots=w.n_slots, rec_slots=w.n_slots)
+            with torch.cuda.stream(stream):
+                kp = torch.from_numpy(w.k_pool.view(np.int16)).to(dev)
+                vp = torch.from_numpy(w.v_pool.view(np.int16)).to(dev)
+                q = torch.from_numpy(w.q.view(np.int16)).to(dev)
+                rec = torch.zeros(max(16, w.n_slots * H * tpk.RECORD_BYTES * int(tier == "hybrid")),
+                                  dtype=torch.uint8, device=dev)
+                if tier == "hybrid":
+                    slots = torch.from_numpy(w.int8_slots()).to(dev)
+                    tpk.kv_quantize_pages(shape, kp, vp, slots, slots, len(slots), rec, stream)
+                pt, off = w.exact_page_table()
+                pt8, off8 = w.int8_page_table()
+                pt_d = torch.from_numpy(np.concatenate([pt, np.zeros(1, np.int32)])).to(dev)
+                pt8_d = torch.from_numpy(np.concatenate([pt8, np.zeros(1, np.int32)])).to(dev)
+                o = torch.empty(1, H * G, 256, dtype=torch.float32, device=dev)
+                lse = torch.empty(1, H * G, dtype=torch.float32, device=dev)
+                nbytes = tpk.hybrid_workspace_bytes(shape, 1)
+                ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+
+            def step():
+                tpk.decode_hybrid_batched(shape, 1, q, kp, vp, rec, pt_d, off, w.n_ex, pt8_d, off8, w.n8, o, lse,
+                                          ws, nbytes, stream)
+
+            dev_ms = statistics.median(graph_times(step, 20, 3, stream, flush, flush_r))
+            hr = run_host_resident(args, w, rec, shape, stream, dev, None, layers=args.gate_layers, steps=3,
+                                   label=f"{args.gate_layers} layers x {n} tokens {tier}")
+            row[tier] = {"history_bytes": w.history_bytes(), "device_us": round(dev_ms * 1e3, 2),
+                         "device_GBps": round(w.history_bytes() / (dev_ms * 1e-3) / 1e9, 1),
+                         "host_ms_per_layer": round(hr["ms_per_step"] / hr["layers"], 4),
+                         "link_GBps": hr["link_GBps"], "link_peak_GBps": hr["link_peak_GBps"]}
+            del kp, vp, q, rec, ws
+        e, h = row["exact"], row["hybrid"]
+        row["bytes_saved_per_layer_step"] = e["history_bytes"] - h["history_bytes"]
+        row["device_us_added"] = round(h["device_us"] - e["device_us"], 2)
+        row["host_ms_added_per_layer"] = round(h["host_ms_per_layer"] - e["host_ms_per_layer"], 4)
+        row["host_speedup"] = round(e["host_ms_per_layer"] / h["host_ms_per_layer"], 3)
+        rows.append(row)
+        print(json.dumps(row), flush=True, file=sys.stderr)
+    print(json.dumps({"mode": "gate_sweep", "hbm_peak_GBps": peak, "rows": rows}), flush=True)
 
 
 # ------------------------------------------------------------- reference arm
@@ -625,6 +693,10 @@ def main():
     ap.add_argument("--layers", type=int, default=16, help="layers of the host-resident measurement (0: skip)")
     ap.add_argument("--host-steps", type=int, default=5, help="timed steps of the host-resident measurement")
     ap.add_argument("--tier-steps", type=int, default=20, help="timed steps of each single-tier 128K line (0: skip)")
+    ap.add_argument("--gate-sweep", action="store_true",
+                    help="instead of the bench line: exact vs hybrid over history lengths (device and host-resident)")
+    ap.add_argument("--gate-lengths", default="8192,16384,32768,65536,131072")
+    ap.add_argument("--gate-layers", type=int, default=4)
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "tpk":
         args.warmup = 3
@@ -632,6 +704,8 @@ def main():
     try:
         if args.impl == "reference":
             run_reference(args, dist, rank, world)
+        elif args.gate_sweep:
+            run_gate_sweep(args)
         else:
             run_gpu(args, dist, rank, world)
     finally:

@@ -174,11 +174,12 @@ class Workload:
         CSR arrays 'req_page_off', 'req_page_off8' and the page counts."""
         H = self.H
         rb = RECORD_BYTES * H
-        rec_v = np.asarray(rec_pool, np.uint8).reshape(self.n_slots, rb)
         s8 = self.int8_slots()
+        recs = (np.asarray(rec_pool, np.uint8).reshape(self.n_slots, rb)[s8].reshape(-1) if len(s8)
+                else np.zeros(0, np.uint8))
         ex, off_e = self.exact_page_table()
         _, off_8 = self.int8_page_table()
-        parts = [("rec", rec_v[s8].reshape(-1)),
+        parts = [("rec", recs),
                  ("k", self.k_pool[ex].reshape(-1).view(np.uint8)),
                  ("v", self.v_pool[ex].reshape(-1).view(np.uint8)),
                  ("q", self.q.reshape(-1).view(np.uint8)),
