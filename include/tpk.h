@@ -265,6 +265,55 @@ tpk_status tpk_stager_release(tpk_stager* stager, int slot, tpk_stream_t stream)
 tpk_status tpk_stager_sync(tpk_stager* stager);
 
 /*
+ * Incremental conversion and publication during decode ("ActiveKV": history
+ * converted in the background and published to the decoder; "model
+ * quantization": only whole pages older than the recent tokens become 8-bit).
+ *
+ * A tier manager follows the paged histories of n_req requests of one layer
+ * (page p of request b in BF16 slot slots[p]; its record goes to the same slot of
+ * rec_pool).  Each tpk_tiers_step:
+ *   1. publishes the pages whose conversion has finished (its event completed):
+ *      they leave the exact tier and join the 8-bit tier;
+ *   2. starts, on conv_stream, the conversion of every whole page that is now
+ *      older than the recent_tokens newest tokens (after the work queued so far
+ *      on decode_stream, which wrote those pages);
+ *   3. fills `plan` with the step's tiers for tpk_decode_hybrid_batched: device
+ *      page tables uploaded on decode_stream (use them on decode_stream), and host
+ *      CSR offsets and counts valid until the next tpk_tiers_step.
+ * A page is served exact until its conversion has finished, so a decode never
+ * reads a record being written; the swap happens between steps.
+ * tpk_tiers_update records request b's history after it grew: n_tokens and the
+ * BF16 slots of its ceil(n_tokens / 64) pages (host array); a page converted or
+ * being converted must keep its slot, and histories do not shrink.
+ * Memory: dev_scratch (caller-owned, 256-byte aligned, tpk_tiers_device_bytes)
+ * holds the page tables and conversion lists; two pinned host staging buffers
+ * are allocated at creation and freed by tpk_tiers_destroy, which first waits
+ * for the conversions in flight (tpk_tiers_sync waits without destroying).
+ * One host thread drives a manager.
+ */
+typedef struct tpk_tiers tpk_tiers;
+typedef struct {
+  const int32_t* page_table;      /* dev: exact-tier slots, CSR by req_page_off */
+  const int32_t* req_page_off;    /* host [n_req + 1] */
+  const int32_t* n_exact_tokens;  /* host [n_req] */
+  const int32_t* page_table8;     /* dev: 8-bit-tier slots, CSR by req_page_off8 */
+  const int32_t* req_page_off8;   /* host [n_req + 1] */
+  const int32_t* n_int8_pages;    /* host [n_req] */
+  int pages_published;            /* pages that joined the 8-bit tier at this step */
+  int pages_started;              /* conversions started at this step */
+  int pages_converting;           /* conversions in flight after this step */
+} tpk_tiers_plan;
+size_t tpk_tiers_device_bytes(int n_req, int max_pages);
+tpk_status tpk_tiers_create(const tpk_shape* shape, int n_req, int max_pages, int recent_tokens, const void* k_pool,
+                            const void* v_pool, void* rec_pool, void* dev_scratch, size_t dev_scratch_bytes,
+                            tpk_tiers** out);
+tpk_status tpk_tiers_update(tpk_tiers* tiers, int b, int n_tokens, const int32_t* page_slots);
+tpk_status tpk_tiers_step(tpk_tiers* tiers, tpk_stream_t conv_stream, tpk_stream_t decode_stream,
+                          tpk_tiers_plan* plan);
+tpk_status tpk_tiers_sync(tpk_tiers* tiers);
+tpk_status tpk_tiers_destroy(tpk_tiers* tiers);
+
+/*
  * Device status word: bit 0 = a page-table entry outside the pool was skipped.
  * Synchronises `stream`, stores the word in *flags and, if reset != 0, clears it.
  */

@@ -115,3 +115,22 @@ def test_stager_arguments_are_validated_before_any_device_call(L):
     assert L.tpk_stager_release(None, 0, None) == 1
     assert L.tpk_stager_sync(None) == 1
     assert L.tpk_stager_destroy(None) == 0
+
+
+def test_tier_manager_arguments_are_validated_before_any_device_call(L):
+    out = ctypes.c_void_p(1)
+    s = tpk.Shape(2)
+    assert L.tpk_tiers_device_bytes(0, 4) == 0 and L.tpk_tiers_device_bytes(2, 0) == 0
+    need = L.tpk_tiers_device_bytes(2, 4)
+    assert need > 0
+    assert L.tpk_tiers_create(ctypes.byref(s), 2, 4, 0, 16, 16, 16, 256, need, None) == 1
+    assert L.tpk_tiers_create(None, 2, 4, 0, 16, 16, 16, 256, need, ctypes.byref(out)) == 1 and out.value is None
+    assert L.tpk_tiers_create(ctypes.byref(s), 0, 4, 0, 16, 16, 16, 256, need, ctypes.byref(out)) == 1
+    assert L.tpk_tiers_create(ctypes.byref(s), 2, 4, -1, 16, 16, 16, 256, need, ctypes.byref(out)) == 1
+    assert L.tpk_tiers_create(ctypes.byref(s), 2, 4, 0, None, 16, 16, 256, need, ctypes.byref(out)) == 1
+    assert L.tpk_tiers_create(ctypes.byref(s), 2, 4, 0, 16, 16, 16, 256, need - 1, ctypes.byref(out)) == 5
+    assert L.tpk_tiers_create(ctypes.byref(s), 2, 4, 0, 16, 16, 16, 260, need, ctypes.byref(out)) == 1
+    assert L.tpk_tiers_update(None, 0, 10, None) == 1
+    assert L.tpk_tiers_step(None, None, None, None) == 1
+    assert L.tpk_tiers_sync(None) == 1
+    assert L.tpk_tiers_destroy(None) == 0

@@ -20,7 +20,7 @@ __all__ = [
     "Shape", "TpkError", "lib", "RECORD_BYTES", "IMPL_DEFAULT", "IMPL_SIMT", "IMPL_TENSOR",
     "kv_quantize_pages", "kv_quantize_pages_given_scales", "decode_attn_exact", "decode_attn_int8",
     "merge_lse", "hybrid_workspace_bytes", "workspace_init", "decode_hybrid_batched", "get_device_status",
-    "static_scratch_bytes", "decode_hybrid_batched_static", "Stager",
+    "static_scratch_bytes", "decode_hybrid_batched_static", "Stager", "Tiers", "TiersPlan",
 ]
 
 RECORD_BYTES = 35072
@@ -37,6 +37,14 @@ class Shape(ctypes.Structure):
     def __init__(self, kv_heads, group=8, head_dim=256, page_tokens=64, sm_scale=0.0, impl=IMPL_DEFAULT,
                  kv_slots=0, rec_slots=0):
         super().__init__(kv_heads, group, head_dim, page_tokens, sm_scale, impl, kv_slots, rec_slots)
+
+
+class TiersPlan(ctypes.Structure):
+    _fields_ = [("page_table", ctypes.c_void_p), ("req_page_off", ctypes.POINTER(ctypes.c_int32)),
+                ("n_exact_tokens", ctypes.POINTER(ctypes.c_int32)), ("page_table8", ctypes.c_void_p),
+                ("req_page_off8", ctypes.POINTER(ctypes.c_int32)), ("n_int8_pages", ctypes.POINTER(ctypes.c_int32)),
+                ("pages_published", ctypes.c_int), ("pages_started", ctypes.c_int),
+                ("pages_converting", ctypes.c_int)]
 
 
 class TpkError(RuntimeError):
@@ -83,6 +91,16 @@ def lib():
         L.tpk_stager_sync.argtypes = [vp]
         for name in ("tpk_stager_create", "tpk_stager_destroy", "tpk_stager_stage", "tpk_stager_acquire",
                      "tpk_stager_release", "tpk_stager_sync"):
+            getattr(L, name).restype = i32
+        L.tpk_tiers_device_bytes.argtypes = [i32, i32]
+        L.tpk_tiers_device_bytes.restype = sz
+        L.tpk_tiers_create.argtypes = [sp, i32, i32, i32, vp, vp, vp, vp, sz, pp]
+        L.tpk_tiers_update.argtypes = [vp, i32, i32, vp]
+        L.tpk_tiers_step.argtypes = [vp, vp, vp, ctypes.POINTER(TiersPlan)]
+        L.tpk_tiers_sync.argtypes = [vp]
+        L.tpk_tiers_destroy.argtypes = [vp]
+        for name in ("tpk_tiers_create", "tpk_tiers_update", "tpk_tiers_step", "tpk_tiers_sync",
+                     "tpk_tiers_destroy"):
             getattr(L, name).restype = i32
         for name in ("tpk_kv_quantize_pages", "tpk_kv_quantize_pages_given_scales", "tpk_decode_attn_exact",
                      "tpk_decode_attn_int8", "tpk_merge_lse", "tpk_workspace_init", "tpk_decode_hybrid_batched",
@@ -232,6 +250,57 @@ class Stager:
         if getattr(self, "_h", None) is not None and self._h.value:
             h, self._h = self._h, None
             _check(lib().tpk_stager_destroy(h))
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+
+class Tiers:
+    """Incremental conversion and publication during decode (see tpk_tiers_* in
+    include/tpk.h).  `scratch` is a device buffer of at least
+    Tiers.device_bytes(n_req, max_pages) bytes; the pools must outlive the object."""
+
+    @staticmethod
+    def device_bytes(n_req, max_pages):
+        return int(lib().tpk_tiers_device_bytes(int(n_req), int(max_pages)))
+
+    def __init__(self, shape, n_req, max_pages, recent_tokens, k_pool, v_pool, rec_pool, scratch, scratch_bytes):
+        self._keep = (shape, k_pool, v_pool, rec_pool, scratch)
+        self.n_req = int(n_req)
+        h = ctypes.c_void_p()
+        _check(lib().tpk_tiers_create(ctypes.byref(shape), self.n_req, int(max_pages), int(recent_tokens),
+                                      _ptr(k_pool), _ptr(v_pool), _ptr(rec_pool), _ptr(scratch), int(scratch_bytes),
+                                      ctypes.byref(h)))
+        self._h = h
+
+    def update(self, b, n_tokens, page_slots):
+        arr, p = _host_i32(page_slots)
+        _check(lib().tpk_tiers_update(self._h, int(b), int(n_tokens), p))
+
+    def step(self, conv_stream=None, decode_stream=None):
+        """Returns a dict: device page tables (raw pointers) and host numpy copies of
+        the CSR offsets and counts, plus the publication counters."""
+        plan = TiersPlan()
+        _check(lib().tpk_tiers_step(self._h, _stream(conv_stream), _stream(decode_stream), ctypes.byref(plan)))
+        n = self.n_req
+        return {"page_table": plan.page_table, "page_table8": plan.page_table8,
+                "req_page_off": np.ctypeslib.as_array(plan.req_page_off, (n + 1,)).copy(),
+                "n_exact_tokens": np.ctypeslib.as_array(plan.n_exact_tokens, (n,)).copy(),
+                "req_page_off8": np.ctypeslib.as_array(plan.req_page_off8, (n + 1,)).copy(),
+                "n_int8_pages": np.ctypeslib.as_array(plan.n_int8_pages, (n,)).copy(),
+                "published": plan.pages_published, "started": plan.pages_started,
+                "converting": plan.pages_converting}
+
+    def sync(self):
+        _check(lib().tpk_tiers_sync(self._h))
+
+    def close(self):
+        if getattr(self, "_h", None) is not None and self._h.value:
+            h, self._h = self._h, None
+            _check(lib().tpk_tiers_destroy(h))
 
     def __enter__(self):
         return self
