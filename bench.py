@@ -17,6 +17,8 @@ e2e    = the same metric through the library's host-resident path: the step's
 tiers_128k = each tier alone over a 131,072-token history (all BF16: 536.9 MB; all
          8-bit: 287.3 MB), same call and timing, for the exact and the 8-bit
          kernel paths separately.
+batched_16 = the 16-request batched hybrid decode (8K-64K tokens each, 1.35 GB),
+         one multi-request call per step, same timing.
 host_resident = 16 layers of such history images in pinned host memory through
          two device slots, each layer staged while the previous one decodes;
          link GB/s against a plain pinned copy measured in the same run.
@@ -220,6 +222,51 @@ def graph_times(step, steps, warmup, stream, flush, flush_r):
     return [a.elapsed_time(b) for a, b in ev]
 
 
+def run_batched(impl, args, stream, dev, flush, flush_r, peak):
+    """The 16-request batched hybrid decode (lengths uniform in [8K, 64K], 2048
+    recent BF16 tokens each, 4 KV heads x 8 q rows, outlier keys, seed 3): one
+    multi-request call per step, each request with its own page tables."""
+    import torch
+
+    import tiered_paged_kv_gb300 as tpk
+    from tiered_paged_kv_gb300 import synth
+
+    w = synth.batched_hybrid(seed=3)
+    H, G, B = w.H, w.G, w.B
+    shape = tpk.Shape(H, impl=impl, kv_slots=w.n_slots, rec_slots=w.n_slots)
+    with torch.cuda.stream(stream):
+        kp = torch.from_numpy(w.k_pool.view(np.int16)).to(dev)
+        vp = torch.from_numpy(w.v_pool.view(np.int16)).to(dev)
+        q = torch.from_numpy(w.q.view(np.int16)).to(dev)
+        rec = torch.zeros(w.n_slots * H * tpk.RECORD_BYTES, dtype=torch.uint8, device=dev)
+        slots = torch.from_numpy(w.int8_slots()).to(dev)
+        tpk.kv_quantize_pages(shape, kp, vp, slots, slots, len(slots), rec, stream)
+        pt, off = w.exact_page_table()
+        pt8, off8 = w.int8_page_table()
+        pt_d = torch.from_numpy(pt).to(dev)
+        pt8_d = torch.from_numpy(pt8).to(dev)
+        o = torch.empty(B, H * G, 256, dtype=torch.float32, device=dev)
+        lse = torch.empty(B, H * G, dtype=torch.float32, device=dev)
+        nbytes = tpk.hybrid_workspace_bytes(shape, B)
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+
+    def step():
+        tpk.decode_hybrid_batched(shape, B, q, kp, vp, rec, pt_d, off, w.n_ex, pt8_d, off8, w.n8, o, lse, ws,
+                                  nbytes, stream)
+
+    times = graph_times(step, args.tier_steps, 3, stream, flush, flush_r)
+    st, flags = tpk.get_device_status(reset=True, stream=stream)
+    if st != 0:
+        raise RuntimeError(f"device status {st} flags {flags} (batched)")
+    ms = statistics.median(times)
+    gbs = w.history_bytes() / (ms * 1e-3) / 1e9
+    return {"history_bytes": w.history_bytes(), "requests": B, "tokens": int(w.n_tokens.sum()),
+            "us_per_step_median": round(ms * 1e3, 2), "GBps": round(gbs, 1), "hbm_frac": round(gbs / peak, 4),
+            "steps": len(times),
+            "workload": "16 requests, lengths uniform in [8192, 65536] (seed 3), 2048 BF16 recent each, "
+                        "4 KV heads x 8 q rows, head_dim 256, outlier keys"}
+
+
 def run_tier(which, impl, args, stream, dev, flush, flush_r, peak):
     """One tier alone over a 131,072-token history of the main workload's shape
     (4 KV heads x 8 q rows, head_dim 256, 4 outlier key channels at 20x std):
@@ -363,9 +410,10 @@ def run_gpu(args, dist, rank, world):
 
     # ---- each tier alone at 128K (the exact and the 8-bit kernel paths)
     peak, peak_kind = hbm_peak()
-    tiers = None
+    tiers = batched = None
     if args.tier_steps > 0:
         tiers = {k: run_tier(k, impl, args, stream, dev, flush, flush_r, peak) for k in ("exact", "int8")}
+        batched = run_batched(impl, args, stream, dev, flush, flush_r, peak)
 
     # ---- end to end from pinned host memory (packed history, identity page tables)
     e2e = run_e2e(args, w, rec, shape, stream, dev, dist)
@@ -406,6 +454,7 @@ def run_gpu(args, dist, rank, world):
         "e2e": e2e,
         "host_resident": host_res,
         "tiers_128k": tiers,
+        "batched_16": batched,
         "gpu_launches": args.steps * launches_per_step,
         "clocks": clk.summary(),
         "cpu_baseline": cpu,
