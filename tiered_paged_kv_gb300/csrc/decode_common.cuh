@@ -99,12 +99,13 @@ __device__ __forceinline__ void issue_item(const DecodeParams& p, const UnitInfo
 }
 
 // -------------------------------------------------------------- epilogue
-// On entry every one of the NW consumer warps w has stored its online-softmax state for the 8
+// On entry each of the NW online-softmax states w (a warp's in the CUDA-core
+// kernel, a warp pair's in the tensor-core kernel) is in shared memory for the 8
 // query rows: ep_m[w][r] (base-2 running max, integer valued, or -inf),
-// ep_l[w][r] (sum of weights) and its unnormalised accumulator in
+// ep_l[w][r] (sum of weights) and the unnormalised accumulator in
 // ep_o[w][r][256] (shared memory aliasing the idle stages).
 //
-// Threads 0..127 combine the NW warps into the unit's partial (o, lse) and
+// Threads 0..127 combine the NW states into the unit's partial (o, lse) and
 // write it: to the caller's partial arrays (primitive calls), straight to the
 // output when the head has a single unit, or to the workspace, where the fold
 // kernel merges the head's partials.  Every thread of the block must

@@ -10,7 +10,7 @@
 // online softmax, each accumulates the output of its 128 channels).  The
 // epilogue merges the 4 pairs' states.
 //
-// Thread (g, t) = (lane / 4, lane % 4) of a consumer warp:
+// Thread (g, t) = (lane / 4, lane % 4) of a warp:
 //   - in QK (S = Q K^T, M = 16 query-row slots, N = 8 tokens per tile) it owns
 //     query row g and receives the scores of 2 tokens per tile;
 //   - in PV the output is computed transposed, O^T = V^T P^T (M = 16 channels,
@@ -48,7 +48,7 @@
 
 namespace tpk {
 
-constexpr int kCons = 8;                       // consumer warps (4 pairs)
+constexpr int kCons = 8;  // warps (4 pairs), all of them consumers
 constexpr int kMmaThreads = kCons * 32;
 constexpr int kMmaSlots = 6;
 constexpr unsigned kAll = 0xffffffffu;
@@ -129,7 +129,7 @@ __device__ __forceinline__ void codes_to_f16(uint32_t w, uint32_t& lo, uint32_t&
   hi = __byte_perm(w, 0x64646464u, 0x5342);
 }
 
-// ----------------------------------------------------------------- producer
+// ----------------------------------------------------------------- copies in
 // BF16 half-pages arrive by TMA as 128-byte-swizzled tiles: K at tiles 0-3 and V
 // at tiles 4-7 of the slot (1024-byte aligned), tile c = channels 64c .. 64c+63
 // of the 32 tokens, row r at byte 128 r, 16-byte chunk k stored at chunk k ^ (r % 8).
