@@ -103,14 +103,15 @@ __device__ __forceinline__ void issue_item(const DecodeParams& p, const UnitInfo
 // kernel, a warp pair's in the tensor-core kernel) is in shared memory for the 8
 // query rows: ep_m[w][r] (base-2 running max, integer valued, or -inf),
 // ep_l[w][r] (sum of weights) and the unnormalised accumulator in
-// ep_o[w][r][256] (shared memory aliasing the idle stages).
+// ep_o[w][r][RowStride] (shared memory aliasing the idle stages; channels 0..255
+// of a row, rows RowStride floats apart).
 //
 // Threads 0..127 combine the NW states into the unit's partial (o, lse) and
 // write it: to the caller's partial arrays (primitive calls), straight to the
 // output when the head has a single unit, or to the workspace, where the fold
 // kernel merges the head's partials.  Every thread of the block must
 // call this (it contains block barriers); threads >= 128 only take part in them.
-template <int NW, typename Smem>
+template <int NW, typename Smem, int RowStride = kHeadDim>
 __device__ __forceinline__ void write_and_fold(const DecodeParams& p, const UnitInfo& ui, Smem& S,
                                                const float* ep_o) {
   const int tid = threadIdx.x;
@@ -153,7 +154,7 @@ __device__ __forceinline__ void write_and_fold(const DecodeParams& p, const Unit
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
       for (int w = 0; w < NW; ++w) {
-        float4 v = *reinterpret_cast<const float4*>(ep_o + (w * G + r) * kHeadDim + c0 + c);
+        float4 v = *reinterpret_cast<const float4*>(ep_o + (w * G + r) * RowStride + c0 + c);
         acc.x += fw[w] * v.x;
         acc.y += fw[w] * v.y;
         acc.z += fw[w] * v.z;

@@ -555,7 +555,10 @@ __global__ void __launch_bounds__(kMmaThreads, 1) decode_mma_kernel(const __grid
   }
   // ---- per-pair states into shared memory (the stages are idle now); the two
   // warps of a pair hold the same softmax state and one channel half each
-  float* ep_o = reinterpret_cast<float*>(S.slot[0]);  // [4 pairs][8 rows][256], in slot 0
+  // [4 pairs][8 rows][kEpStride]: rows padded by 4 floats so that the scattered
+  // accumulator stores (rows 2t, 2t + 1 of lane (g, t)) hit distinct banks
+  constexpr int kEpStride = kHeadDim + 4;
+  float* ep_o = reinterpret_cast<float*>(S.slot[0]);
   if (warp < kCons) {
     const int pair = warp >> 1, half = warp & 1;
     float L = l_run;
@@ -565,17 +568,17 @@ __global__ void __launch_bounds__(kMmaThreads, 1) decode_mma_kernel(const __grid
       S.ep_m[pair][g] = m_run;
       S.ep_l[pair][g] = L;
     }
-    float* base = ep_o + pair * kGroup * kHeadDim + 128 * half;
+    float* base = ep_o + pair * kGroup * kEpStride + 128 * half;
 #pragma unroll
     for (int m = 0; m < 8; ++m) {
-      base[(2 * t) * kHeadDim + 16 * m + g] = O[m][0];
-      base[(2 * t + 1) * kHeadDim + 16 * m + g] = O[m][1];
-      base[(2 * t) * kHeadDim + 16 * m + g + 8] = O[m][2];
-      base[(2 * t + 1) * kHeadDim + 16 * m + g + 8] = O[m][3];
+      base[(2 * t) * kEpStride + 16 * m + g] = O[m][0];
+      base[(2 * t + 1) * kEpStride + 16 * m + g] = O[m][1];
+      base[(2 * t) * kEpStride + 16 * m + g + 8] = O[m][2];
+      base[(2 * t + 1) * kEpStride + 16 * m + g + 8] = O[m][3];
     }
   }
   __syncthreads();
-  write_and_fold<kCons / 2>(p, ui, S, ep_o);
+  write_and_fold<kCons / 2, MmaSmem, kEpStride>(p, ui, S, ep_o);
 }
 
 template <int R>
