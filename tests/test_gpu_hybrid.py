@@ -115,3 +115,34 @@ def test_back_to_back_launches_share_a_workspace(impl):
     assert st == 0, flags
     for o, lse in outs[1:]:
         assert t.equal(o, outs[0][0]) and t.equal(lse, outs[0][1])
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+def test_maximum_request_count(impl):
+    """256 requests in one launch (the largest plan; with 4 KV heads their 2032
+    (request, head, tier) segments nearly fill the 2048 partial slots), ragged
+    lengths including empty and single-token histories; 257 requests are refused."""
+    rng = np.random.default_rng(60)
+    lengths = rng.integers(200, 1500, 256)
+    lengths[:4] = [0, 1, 64, 65]
+    w = synth.make_workload(list(lengths), 100, H=4, seed=60)
+    check_hybrid(w, impl, what="256 requests")
+    d = DevWorkload(w, impl)
+    t = __import__("torch")
+    o = t.empty(257, w.H * w.G, 256, dtype=t.float32, device="cuda")
+    lse = t.empty(257, w.H * w.G, dtype=t.float32, device="cuda")
+    nbytes = tpk.hybrid_workspace_bytes(d.shape, 256)
+    ws = t.empty(nbytes, dtype=t.uint8, device="cuda")
+    off = np.concatenate([d.off, d.off[-1:]])
+    off8 = np.concatenate([d.off8, d.off8[-1:]])
+    with pytest.raises(tpk.TpkError):
+        tpk.decode_hybrid_batched(d.shape, 257, d.q, d.k, d.v, d.rec, d.pt, off, list(w.n_ex) + [0], d.pt8, off8,
+                                  list(w.n8) + [0], o, lse, ws, nbytes)
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+def test_million_token_history(impl):
+    """One request over 1,048,576 tokens (16,320 8-bit pages + 4,096 BF16 tokens),
+    one KV head."""
+    w = synth.make_workload([1 << 20], 4096, H=1, seed=61, key_sigma="outliers")
+    check_hybrid(w, impl, gpu_records=True, what="1M tokens")

@@ -378,15 +378,30 @@ tpk_status tpk_decode_hybrid_batched(const tpk_shape* shape, int n_req, const vo
   }
   int used = 0;
   std::vector<std::pair<double, int>> rem;
+  std::vector<double> ideal(2 * n_req, 0.0);
   for (int x = 0; x < 2 * n_req; ++x) {
     if (cap[x] == 0) {
       cnt[x] = 0;
       continue;
     }
-    const double ideal = W > 0 ? U * wgt[x] / W : 0.0;
-    cnt[x] = std::min(cap[x], std::max(1, (int)std::floor(ideal)));
+    ideal[x] = W > 0 ? U * wgt[x] / W : 0.0;
+    cnt[x] = std::min(cap[x], std::max(1, (int)std::floor(ideal[x])));
     used += cnt[x];
-    if (cnt[x] < cap[x]) rem.push_back({ideal - std::floor(ideal), x});
+    if (cnt[x] < cap[x]) rem.push_back({ideal[x] - std::floor(ideal[x]), x});
+  }
+  // the one-unit minimum of small segments can overshoot the budget: take units
+  // back from the most over-allocated segments (U >= min_units, so this ends)
+  while (used > U) {
+    int best = -1;
+    double over = -1e300;
+    for (int x = 0; x < 2 * n_req; ++x)
+      if (cnt[x] > 1 && cnt[x] - ideal[x] > over) {
+        over = cnt[x] - ideal[x];
+        best = x;
+      }
+    if (best < 0) break;
+    cnt[best] -= 1;
+    used -= 1;
   }
   std::sort(rem.begin(), rem.end(), [](const std::pair<double, int>& a, const std::pair<double, int>& c) {
     return a.first > c.first || (a.first == c.first && a.second < c.second);
