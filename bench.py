@@ -693,6 +693,92 @@ def run_gate_sweep(args):
     print(json.dumps({"mode": "gate_sweep", "hbm_peak_GBps": peak, "rows": rows}), flush=True)
 
 
+def run_tiers_loop(args):
+    """Decode loop with incremental conversion and publication: 16 requests of
+    32,768 tokens grow by one token per step for `--tiers-steps` steps (recent
+    window 2048 tokens, 4 KV heads x 8 q rows, outlier keys); per step the tier
+    manager publishes finished conversions, starts new ones on a side stream and
+    uploads the page tables, then the multi-request decode runs.  Compared with the
+    same loop on fixed tables (no conversion, no upload); wall time per step with
+    the host driving both streams, pages converted in the background reported."""
+    import torch
+
+    import tiered_paged_kv_gb300 as tpk
+    from tiered_paged_kv_gb300 import build as tbuild
+    from tiered_paged_kv_gb300 import synth
+
+    torch.cuda.set_device(0)
+    tbuild.build()
+    dev = torch.device("cuda", 0)
+    B, n0, steps, recent = 16, 32768, args.tiers_steps, 2048
+    final = n0 + steps
+    w = synth.make_workload([final] * B, None, H=4, seed=30, key_sigma="outliers")
+    H, G = w.H, w.G
+    max_pages = max(len(p) for p in w.pages)
+    shape = tpk.Shape(H, kv_slots=w.n_slots, rec_slots=w.n_slots)
+    dec, conv = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    with torch.cuda.stream(dec):
+        kp = torch.from_numpy(w.k_pool.view(np.int16)).to(dev)
+        vp = torch.from_numpy(w.v_pool.view(np.int16)).to(dev)
+        q = torch.from_numpy(w.q.view(np.int16)).to(dev)
+        rec = torch.zeros(w.n_slots * H * tpk.RECORD_BYTES, dtype=torch.uint8, device=dev)
+        o = torch.empty(B, H * G, 256, dtype=torch.float32, device=dev)
+        lse = torch.empty(B, H * G, dtype=torch.float32, device=dev)
+        ws_bytes = tpk.hybrid_workspace_bytes(shape, B)
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+        sc_bytes = tpk.Tiers.device_bytes(B, max_pages)
+        scratch = torch.empty(sc_bytes, dtype=torch.uint8, device=dev)
+    torch.cuda.synchronize()
+    result = {}
+    with tpk.Tiers(shape, B, max_pages, recent, kp, vp, rec, scratch, sc_bytes) as tiers:
+        # warm state: the starting histories fully converted and published
+        for b in range(B):
+            tiers.update(b, n0, w.pages[b][: (n0 + 63) // 64])
+        tiers.step(conv, dec)
+        tiers.sync()
+        plan = tiers.step(conv, dec)
+        tiers.sync()
+        dec.synchronize()
+        # the reference loop's fixed tables: the starting split (every eligible page 8-bit)
+        n8_0 = (n0 - recent) // 64
+        pt_h = np.concatenate([np.asarray(w.pages[b][n8_0:(n0 + 63) // 64]) for b in range(B)]).astype(np.int32)
+        pt8_h = np.concatenate([np.asarray(w.pages[b][:n8_0]) for b in range(B)]).astype(np.int32)
+        pt_fixed = torch.from_numpy(pt_h).to(dev)
+        pt8_fixed = torch.from_numpy(pt8_h).to(dev)
+        fixed = {"req_page_off": np.arange(B + 1, dtype=np.int32) * ((n0 + 63) // 64 - n8_0),
+                 "req_page_off8": np.arange(B + 1, dtype=np.int32) * n8_0,
+                 "n_exact_tokens": np.full(B, n0 - 64 * n8_0, np.int32), "n_int8_pages": np.full(B, n8_0, np.int32)}
+        assert list(plan["n_int8_pages"]) == [n8_0] * B
+        for mode in ("fixed tables", "tier manager"):
+            n = n0
+            published = started = 0
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            for step in range(steps):
+                n += 1
+                if mode == "tier manager":
+                    for b in range(B):
+                        tiers.update(b, n, w.pages[b][: (n + 63) // 64])
+                    pl = tiers.step(conv, dec)
+                    published += pl["published"]
+                    started += pl["started"]
+                    tpk.decode_hybrid_batched(shape, B, q, kp, vp, rec, pl["page_table"], pl["req_page_off"],
+                                              pl["n_exact_tokens"], pl["page_table8"], pl["req_page_off8"],
+                                              pl["n_int8_pages"], o, lse, ws, ws_bytes, dec)
+                else:
+                    tpk.decode_hybrid_batched(shape, B, q, kp, vp, rec, pt_fixed, fixed["req_page_off"],
+                                              fixed["n_exact_tokens"], pt8_fixed, fixed["req_page_off8"],
+                                              fixed["n_int8_pages"], o, lse, ws, ws_bytes, dec)
+            torch.cuda.synchronize()
+            dt = (time.perf_counter() - t0) / steps
+            result[mode] = {"us_per_step": round(dt * 1e6, 1), "pages_started": started,
+                            "pages_published": published}
+    out = {"mode": "tiers_loop", "requests": B, "start_tokens": n0, "steps": steps, "recent_tokens": recent,
+           **result}
+    out["overhead_us_per_step"] = round(result["tier manager"]["us_per_step"] - result["fixed tables"]["us_per_step"], 1)
+    print(json.dumps(out), flush=True)
+
+
 # ------------------------------------------------------------- reference arm
 def run_reference(args, dist, rank, world):
     """The CPU oracle as the reference arm: each step is a bounded sample of the
@@ -746,6 +832,9 @@ def main():
                     help="instead of the bench line: exact vs hybrid over history lengths (device and host-resident)")
     ap.add_argument("--gate-lengths", default="8192,16384,32768,65536,131072")
     ap.add_argument("--gate-layers", type=int, default=4)
+    ap.add_argument("--tiers-loop", action="store_true",
+                    help="instead of the bench line: a decode loop with incremental conversion and publication")
+    ap.add_argument("--tiers-steps", type=int, default=256)
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "tpk":
         args.warmup = 3
@@ -755,6 +844,8 @@ def main():
             run_reference(args, dist, rank, world)
         elif args.gate_sweep:
             run_gate_sweep(args)
+        elif args.tiers_loop:
+            run_tiers_loop(args)
         else:
             run_gpu(args, dist, rank, world)
     finally:

@@ -16,6 +16,7 @@
 // pools).  All device and pinned host buffers are allocated once, at creation.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -83,6 +84,9 @@ struct tpk_tiers {
   int gen = 0;
   // the plan handed back to the caller (host arrays live here)
   std::vector<int32_t> off, off8, n_ex, n8;
+  // the tables last uploaded (and into which generation), to skip unchanged uploads
+  std::vector<int32_t> last_pt, last_pt8;
+  int last_gen = -1;
   long long published_total = 0, started_total = 0;
 };
 
@@ -203,11 +207,13 @@ tpk_status tpk_tiers_step(tpk_tiers* t, tpk_stream_t conv_stream, tpk_stream_t d
   // 2. pick the staging generation (its previous uploads must have been read)
   const int g = t->gen;
   t->gen ^= 1;
-  if (t->stage_used[g]) {
-    cudaError_t e = cudaEventSynchronize(t->stage_done[g]);
+  {
+    cudaError_t e = cudaSuccess;
+    if (t->stage_used[g]) e = cudaEventSynchronize(t->stage_done[g]);
     if (e == cudaSuccess && t->stage_conv_used[g]) e = cudaEventSynchronize(t->stage_conv_done[g]);
     if (e != cudaSuccess) return tcuda(e, "staging reuse");
   }
+  t->stage_used[g] = false;
   t->stage_conv_used[g] = false;
   int32_t* hs = t->h_stage[g];
   const size_t table_words = (size_t)t->n_req * t->max_pages;
@@ -260,6 +266,8 @@ tpk_status tpk_tiers_step(tpk_tiers* t, tpk_stream_t conv_stream, tpk_stream_t d
     }
   }
   // 4. the step's page tables: 8-bit pages [0, published), exact pages after them
+  //    (uploaded only when they differ from the last upload; otherwise the
+  //    generation holding that upload is handed out again)
   int e_off = 0, p_off = 0;
   for (int b = 0; b < t->n_req; ++b) {
     const Request& r = t->req[b];
@@ -273,24 +281,36 @@ tpk_status tpk_tiers_step(tpk_tiers* t, tpk_stream_t conv_stream, tpk_stream_t d
   }
   t->off[t->n_req] = e_off;
   t->off8[t->n_req] = p_off;
-  if (e_off > 0) {
-    cudaError_t e = cudaMemcpyAsync(t->d_pt[g], h_pt, e_off * sizeof(int32_t), cudaMemcpyHostToDevice, ds);
-    if (e != cudaSuccess) return tcuda(e, "page table upload");
+  const bool same = t->last_gen >= 0 && (int)t->last_pt.size() == e_off && (int)t->last_pt8.size() == p_off &&
+                    std::equal(t->last_pt.begin(), t->last_pt.end(), h_pt) &&
+                    std::equal(t->last_pt8.begin(), t->last_pt8.end(), h_pt8);
+  int tg = g;  // generation whose device tables this step uses
+  if (same) {
+    tg = t->last_gen;
+    t->gen = g;  // this step's staging generation stays free for the next one
+  } else {
+    if (e_off > 0) {
+      cudaError_t e = cudaMemcpyAsync(t->d_pt[g], h_pt, e_off * sizeof(int32_t), cudaMemcpyHostToDevice, ds);
+      if (e != cudaSuccess) return tcuda(e, "page table upload");
+    }
+    if (p_off > 0) {
+      cudaError_t e = cudaMemcpyAsync(t->d_pt8[g], h_pt8, p_off * sizeof(int32_t), cudaMemcpyHostToDevice, ds);
+      if (e != cudaSuccess) return tcuda(e, "page table upload");
+    }
+    // this staging generation is reused two uploads later, once these copies are done
+    cudaError_t e = cudaEventRecord(t->stage_done[g], ds);
+    if (e != cudaSuccess) return tcuda(e, "staging event");
+    t->stage_used[g] = true;
+    t->last_pt.assign(h_pt, h_pt + e_off);
+    t->last_pt8.assign(h_pt8, h_pt8 + p_off);
+    t->last_gen = g;
   }
-  if (p_off > 0) {
-    cudaError_t e = cudaMemcpyAsync(t->d_pt8[g], h_pt8, p_off * sizeof(int32_t), cudaMemcpyHostToDevice, ds);
-    if (e != cudaSuccess) return tcuda(e, "page table upload");
-  }
-  // this staging generation is reused two steps later, once these copies are done
-  cudaError_t e = cudaEventRecord(t->stage_done[g], ds);
-  if (e != cudaSuccess) return tcuda(e, "staging event");
-  t->stage_used[g] = true;
   t->published_total += published;
   t->started_total += started;
-  plan->page_table = t->d_pt[g];
+  plan->page_table = t->d_pt[tg];
   plan->req_page_off = t->off.data();
   plan->n_exact_tokens = t->n_ex.data();
-  plan->page_table8 = t->d_pt8[g];
+  plan->page_table8 = t->d_pt8[tg];
   plan->req_page_off8 = t->off8.data();
   plan->n_int8_pages = t->n8.data();
   plan->pages_published = published;
