@@ -15,7 +15,8 @@
 //      and a sum of exponents, so the normalised fourth power x_c = ms_c / G
 //      needs one multiplication; shat_c = x_c^(1/4);
 //   4. the float32 neighbours of shat_c, found exactly (c^4 against x_c in
-//      integer arithmetic); then one lane walks the channels choosing the
+//      integer arithmetic); then warp 0 walks the channels (lane j holds 8
+//      channels, the running log-error passes from lane to lane) choosing the
 //      neighbour that keeps the running log-error of the product nearest zero,
 //      while warps 1-7 write the value codes (channel-major, one 64-byte row per
 //      channel), which need only u_c;
@@ -260,47 +261,39 @@ __global__ void __launch_bounds__(kQuantThreads, 2) quantize_kernel(const __grid
       S.dhi[c] = dh;
     }
     __syncthreads();
-    if (tid == 0) {
-      // 5. the compensated walk, sequential in the channels: one lane, each group
-      //    of 8 channels' candidates loaded one group ahead
+    if (tid < 32) {
+      // 5. the compensated walk, sequential in the channels: lane j holds the
+      //    candidates of channels 8j .. 8j + 7 in registers, and the running error
+      //    E passes from lane to lane (every lane runs the same steps; lane j's
+      //    result is kept)
+      const int lane = tid;
+      const float4 lo0 = *reinterpret_cast<const float4*>(&S.slo[8 * lane]);
+      const float4 lo1 = *reinterpret_cast<const float4*>(&S.slo[8 * lane + 4]);
+      const float4 hi0 = *reinterpret_cast<const float4*>(&S.shi[8 * lane]);
+      const float4 hi1 = *reinterpret_cast<const float4*>(&S.shi[8 * lane + 4]);
+      const float4 dl0 = *reinterpret_cast<const float4*>(&S.dlo[8 * lane]);
+      const float4 dl1 = *reinterpret_cast<const float4*>(&S.dlo[8 * lane + 4]);
+      const float4 dh0 = *reinterpret_cast<const float4*>(&S.dhi[8 * lane]);
+      const float4 dh1 = *reinterpret_cast<const float4*>(&S.dhi[8 * lane + 4]);
+      const float lo[8] = {lo0.x, lo0.y, lo0.z, lo0.w, lo1.x, lo1.y, lo1.z, lo1.w};
+      const float hi[8] = {hi0.x, hi0.y, hi0.z, hi0.w, hi1.x, hi1.y, hi1.z, hi1.w};
+      const float dl[8] = {dl0.x, dl0.y, dl0.z, dl0.w, dl1.x, dl1.y, dl1.z, dl1.w};
+      const float dh[8] = {dh0.x, dh0.y, dh0.z, dh0.w, dh1.x, dh1.y, dh1.z, dh1.w};
+      float sv[8];
       float E = 0.f;
-      float4 c_lo[2], c_hi[2], c_dl[2], c_dh[2];
-      auto load = [&](int ch0, float4 (&lo)[2], float4 (&hi)[2], float4 (&dl)[2], float4 (&dh)[2]) {
-        lo[0] = *reinterpret_cast<const float4*>(&S.slo[ch0]);
-        lo[1] = *reinterpret_cast<const float4*>(&S.slo[ch0 + 4]);
-        hi[0] = *reinterpret_cast<const float4*>(&S.shi[ch0]);
-        hi[1] = *reinterpret_cast<const float4*>(&S.shi[ch0 + 4]);
-        dl[0] = *reinterpret_cast<const float4*>(&S.dlo[ch0]);
-        dl[1] = *reinterpret_cast<const float4*>(&S.dlo[ch0 + 4]);
-        dh[0] = *reinterpret_cast<const float4*>(&S.dhi[ch0]);
-        dh[1] = *reinterpret_cast<const float4*>(&S.dhi[ch0 + 4]);
-      };
-      load(0, c_lo, c_hi, c_dl, c_dh);
-      for (int ch0 = 0; ch0 < kHeadDim; ch0 += 8) {
-        float4 n_lo[2], n_hi[2], n_dl[2], n_dh[2];
-        load(ch0 + 8 < kHeadDim ? ch0 + 8 : ch0, n_lo, n_hi, n_dl, n_dh);
-        const float lo[8] = {c_lo[0].x, c_lo[0].y, c_lo[0].z, c_lo[0].w, c_lo[1].x, c_lo[1].y, c_lo[1].z, c_lo[1].w};
-        const float hi[8] = {c_hi[0].x, c_hi[0].y, c_hi[0].z, c_hi[0].w, c_hi[1].x, c_hi[1].y, c_hi[1].z, c_hi[1].w};
-        const float dl[8] = {c_dl[0].x, c_dl[0].y, c_dl[0].z, c_dl[0].w, c_dl[1].x, c_dl[1].y, c_dl[1].z, c_dl[1].w};
-        const float dh[8] = {c_dh[0].x, c_dh[0].y, c_dh[0].z, c_dh[0].w, c_dh[1].x, c_dh[1].y, c_dh[1].z, c_dh[1].w};
-        float sv[8];
+      for (int j = 0; j < 32; ++j) {
+        float Ej = E;
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          const float a = E + dl[e], b = E + dh[e];
+          const float a = Ej + dl[e], b = Ej + dh[e];
           const bool take_lo = fabsf(a) <= fabsf(b);
-          sv[e] = take_lo ? lo[e] : hi[e];
-          E = take_lo ? a : b;
+          if (lane == j) sv[e] = take_lo ? lo[e] : hi[e];
+          Ej = take_lo ? a : b;
         }
-        *reinterpret_cast<float4*>(&S.s[ch0]) = make_float4(sv[0], sv[1], sv[2], sv[3]);
-        *reinterpret_cast<float4*>(&S.s[ch0 + 4]) = make_float4(sv[4], sv[5], sv[6], sv[7]);
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {
-          c_lo[k] = n_lo[k];
-          c_hi[k] = n_hi[k];
-          c_dl[k] = n_dl[k];
-          c_dh[k] = n_dh[k];
-        }
+        E = __shfl_sync(0xffffffffu, Ej, j);
       }
+      *reinterpret_cast<float4*>(&S.s[8 * lane]) = make_float4(sv[0], sv[1], sv[2], sv[3]);
+      *reinterpret_cast<float4*>(&S.s[8 * lane + 4]) = make_float4(sv[4], sv[5], sv[6], sv[7]);
     } else if (tid >= 32) {
       // meanwhile warps 1-7 write the value codes, which do not depend on s
       for (int it = tid - 32; it < kValueItems; it += kQuantThreads - 32) value_codes(it & 255, (it >> 8) * 16);
