@@ -140,11 +140,15 @@ __device__ __forceinline__ uint32_t swz(int r, int chunk) {  // byte offset of (
   return (chunk >> 3) * 4096 + r * 128 + (((chunk & 7) ^ (r & 7)) << 4);
 }
 
+// (pt_staged: the page table is in shared memory; the first items are issued
+// before it is, straight from the global table)
 __device__ __forceinline__ void mma_issue(const DecodeParams& p, const UnitInfo& ui, const Items& it, MmaSmem& S,
-                                          int j, int s) {
+                                          int j, int s, bool pt_staged = true) {
   int page = item_page(ui, it, j);
   int idx = page - it.pg_first;
-  int64_t slot = idx < kPtCache ? S.pt[idx] : __ldg((ui.tier == 0 ? p.page_table : p.page_table8) + ui.pt_off + page);
+  int64_t slot = pt_staged && idx < kPtCache
+                     ? S.pt[idx]
+                     : __ldg((ui.tier == 0 ? p.page_table : p.page_table8) + ui.pt_off + page);
   int64_t lim = ui.tier == 0 ? p.kv_slots : p.rec_slots;
   const bool ok = slot >= 0 && (lim == 0 || slot < lim);
   S.valid[s] = ok;
@@ -452,6 +456,12 @@ __global__ void __launch_bounds__(kMmaThreads, 1) decode_mma_kernel(const __grid
     for (int s = 0; s < kMmaSlots; ++s) S.rel[s] = S.fills[s] = 0;
     S.abort = 0;
     fence_mbar_init();
+    // the first items go out at once (every later one is issued by the warp that
+    // releases its slot's previous item last)
+    for (int j = 0; j < min(it.n, kMmaSlots); ++j) {
+      mma_issue(p, ui, it, S, j, j, false);
+      S.fills[j] = 1;
+    }
   }
   load_page_table(p, ui, it, S);
   {
@@ -459,13 +469,6 @@ __global__ void __launch_bounds__(kMmaThreads, 1) decode_mma_kernel(const __grid
     for (int i = tid; i < kGroup * kHeadDim / 2; i += blockDim.x) (&S.q[0][0])[i] = __ldg(q32 + i);
   }
   __syncthreads();
-  // the first items go out at once; every later one is issued by the warp that
-  // releases its slot's previous item last
-  if (tid == 0)
-    for (int j = 0; j < min(it.n, kMmaSlots); ++j) {
-      mma_issue(p, ui, it, S, j, j);
-      S.fills[j] = 1;
-    }
   // Float copy of q times 2^-(e+1), e the exponent of the row's max |q|: with
   // s_c <= 2^14 every q'_c = q_c s_c of this row then stays below 2^13, inside
   // f16 range, whatever the page.
