@@ -12,7 +12,7 @@ import pytest
 import oracle
 import tiered_paged_kv_gb300 as tpk
 from tiered_paged_kv_gb300 import synth
-from tpk_testutil import assert_close, dev_u16, torch
+from tpk_testutil import REC_POISON, assert_close, dev_u16, torch
 
 pytestmark = pytest.mark.gpu
 
@@ -36,7 +36,7 @@ def test_histories_grow_and_pages_are_published(impl):
     k = dev_u16(w.k_pool)
     v = dev_u16(w.v_pool)
     q = dev_u16(w.q)
-    rec = t.zeros(w.n_slots * H * tpk.RECORD_BYTES, dtype=t.uint8, device="cuda")
+    rec = t.full((w.n_slots * H * tpk.RECORD_BYTES,), REC_POISON, dtype=t.uint8, device="cuda")
     nbytes = tpk.Tiers.device_bytes(B, max_pages)
     scratch = t.empty(nbytes, dtype=t.uint8, device="cuda")
     ws_bytes = tpk.hybrid_workspace_bytes(shape, B)

@@ -13,6 +13,10 @@ from tiered_paged_kv_gb300 import synth
 O_TOL = 1e-3
 LSE_TOL = 1e-3
 
+# Record slots no page uses are filled with this byte: every scale reads as a NaN
+# (0xffffffff), so a stray read of an unused record shows up in the output.
+REC_POISON = 0xFF
+
 
 def torch():
     import torch as t
@@ -52,7 +56,7 @@ class DevWorkload:
         self.k = dev_u16(w.k_pool)
         self.v = dev_u16(w.v_pool)
         self.q = dev_u16(w.q)
-        self.rec = t.zeros(w.n_slots * w.H * tpk.RECORD_BYTES, dtype=t.uint8, device="cuda")
+        self.rec = t.full((w.n_slots * w.H * tpk.RECORD_BYTES,), REC_POISON, dtype=t.uint8, device="cuda")
         pt, self.off = w.exact_page_table()
         pt8, self.off8 = w.int8_page_table()
         self.pt = dev_i32(pt)
@@ -82,7 +86,7 @@ class DevWorkload:
 
 
 def oracle_records(w):
-    rec = np.zeros(w.n_slots * w.H * oracle.REC_BYTES, np.uint8)
+    rec = np.full(w.n_slots * w.H * oracle.REC_BYTES, REC_POISON, np.uint8)
     s = w.int8_slots()
     oracle.quantize_pages(w.H, w.k_pool, w.v_pool, s, s, rec)
     return rec
