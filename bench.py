@@ -425,9 +425,13 @@ def run_gpu(args, dist, rank, world):
         rec_host = rec.cpu().numpy()
         n_thr = os.cpu_count() or 1
         dt, nb, cores = oracle_time(w, rec_host, n_thr)
+        dt1, nb1, _ = oracle_time(w, rec_host, 1, sample_heads=1)
         cpu = {"value": round(nb / dt / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
                "sample": f"the full 128K hybrid step (all 4 KV heads), once, {dt:.1f} s; "
-                         f"threads over (request, KV head)"}
+                         f"threads over (request, KV head)",
+               "value_1_thread": round(nb1 / dt1 / 1e9, 4),
+               "sample_1_thread": f"one KV head of the same step on one thread, once, {dt1:.1f} s",
+               "host_cores_available": os.cpu_count()}
     achieved = hist_bytes / (ms_mean * 1e-3) / 1e9
     value = world * hist_bytes / (ms_max * 1e-3) / 1e9
     traffic = measured_traffic(args.kernel)
