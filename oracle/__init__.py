@@ -55,7 +55,11 @@ def lib():
         L.orc_partial_int8.restype = None
         L.orc_merge.argtypes = [i32, i32, i32, vp, vp, vp, vp]
         L.orc_merge.restype = None
-        L.orc_hybrid_batched.argtypes = [i32, i32, i32] + [vp] * 12 + [i32]
+        L.orc_partial_int8_iq.argtypes = [i32, i32, vp, vp, vp, i32, i32, vp, vp]
+        L.orc_partial_int8_iq.restype = None
+        L.orc_query_codes.argtypes = [vp, vp, vp]
+        L.orc_query_codes.restype = ctypes.c_float
+        L.orc_hybrid_batched.argtypes = [i32, i32, i32] + [vp] * 12 + [i32, i32]
         L.orc_hybrid_batched.restype = None
         _lib = L
     return _lib
@@ -176,6 +180,26 @@ def partial_int8(H, G, q, rec_pool, page_table8, page_begin, page_end):
     return o, lse
 
 
+def query_codes(q_row, s):
+    """Integer query of one row for one page ("SYCL", "Attention that reads 8-bit
+    history": the integer query cache).  q_row: 256 bf16 bit patterns, s: the
+    page's key channel scales in channel order -> (alpha float32, int8 codes)."""
+    qi = np.empty(D_HEAD, np.int8)
+    alpha = lib().orc_query_codes(_p(_c(q_row, np.uint16)), _p(_c(s, np.float32)), _p(qi))
+    return np.float32(alpha), qi
+
+
+def partial_int8_iq(H, G, q, rec_pool, page_table8, page_begin, page_end):
+    """8-bit partial with the integer query (codes per page and row, integer dots)."""
+    q = _c(q, np.uint16)
+    pt = _c(page_table8, np.int32) if len(page_table8) else np.zeros(1, np.int32)
+    o = np.empty((H * G, D_HEAD))
+    lse = np.empty(H * G)
+    lib().orc_partial_int8_iq(H, G, _p(q), _p(_c(rec_pool, np.uint8)), _p(pt), int(page_begin), int(page_end),
+                              _p(o), _p(lse))
+    return o, lse
+
+
 def merge(o_parts, lse_parts):
     """o_parts [k][rows][d], lse_parts [k][rows] -> (o [rows][d], lse [rows])."""
     o_parts = _c(o_parts, np.float64)
@@ -188,7 +212,7 @@ def merge(o_parts, lse_parts):
 
 
 def hybrid_batched(H, G, q, k_pool, v_pool, rec_pool, page_table, req_page_off, n_exact_tokens,
-                   page_table8, req_page_off8, n_int8_pages, n_threads=1):
+                   page_table8, req_page_off8, n_int8_pages, n_threads=1, int_query=False):
     q = _c(q, np.uint16)
     B = q.shape[0]
     o = np.empty((B, H * G, D_HEAD))
@@ -198,16 +222,17 @@ def hybrid_batched(H, G, q, k_pool, v_pool, rec_pool, page_table, req_page_off, 
     lib().orc_hybrid_batched(B, H, G, _p(q), _p(_c(k_pool, np.uint16)), _p(_c(v_pool, np.uint16)),
                              _p(_c(rec_pool, np.uint8)), _p(pt), _p(_c(req_page_off, np.int32)),
                              _p(_c(n_exact_tokens, np.int32)), _p(pt8), _p(_c(req_page_off8, np.int32)),
-                             _p(_c(n_int8_pages, np.int32)), _p(o), _p(lse), int(n_threads))
+                             _p(_c(n_int8_pages, np.int32)), _p(o), _p(lse), int(bool(int_query)),
+                             int(n_threads))
     return o, lse
 
 
-def hybrid_workload(w, rec_pool, n_threads=1):
+def hybrid_workload(w, rec_pool, n_threads=1, int_query=False):
     """Oracle hybrid step over a synth.Workload whose 8-bit pages are in rec_pool."""
     pt, off = w.exact_page_table()
     pt8, off8 = w.int8_page_table()
     return hybrid_batched(w.H, w.G, w.q, w.k_pool, w.v_pool, rec_pool, pt, off, w.n_ex.astype(np.int32),
-                          pt8, off8, w.n8.astype(np.int32), n_threads)
+                          pt8, off8, w.n8.astype(np.int32), n_threads, int_query)
 
 
 def full_precision_workload(w, n_threads=1):

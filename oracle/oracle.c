@@ -20,6 +20,9 @@
  *           log-sum-exp) folded into one accumulator; -inf is a valid empty partial.
  *   [TIERS] "ActiveKV", section "The idea": recent context exact, older history
  *           8-bit, joined with exact attention arithmetic.
+ *   [IQ]    "SYCL", section "Attention that reads 8-bit history": the kernel keeps
+ *           an integer query cache of 8 rows x 256 channels (2 KB) and a
+ *           two-by-two experiment decided which products run on integers.
  *
  * Readings where the pages are silent (each is listed in the design notes):
  *   - scales are stored as float32; key channel scales are rounded to float32 by
@@ -31,7 +34,13 @@
  *   - codes: two correctly rounded float32 divisions (k / s_c, then / r_t),
  *     rint (half to even), clamp to +-127; a zero scale gives zero codes;
  *   - softmax scale 1/sqrt(d), log-sum-exp in natural-log units; an empty range
- *     gives o = 0, lse = -inf.
+ *     gives o = 0, lse = -inf;
+ *   - integer query (the variant with integer QK products): the query folded with
+ *     the page's key channel scales, q'_c = q_c s_c, is coded per page and query
+ *     row with the absmax rule of the key codes: m = max_c |q'_c|, alpha = m / 127,
+ *     qi_c = rint(q'_c * (127 / m)) clamped to +-127, every step in float32 (one
+ *     division for 127 / m, one for m / 127, then products); m = 0 gives alpha = 0
+ *     and zero codes.  The scores are alpha * r_t * sum_c qi_c kc_tc.
  *
  * Record layout of one 8-bit page-head (35,072 bytes):
  *   u8    kc[64][256]      keys, token-major       offset 0
@@ -208,36 +217,43 @@ void orc_quantize_pages(int H, const uint16_t* k_pool, const uint16_t* v_pool, c
 /* ================================================================ attention */
 
 /*
+ * Softmax of one query row over n precomputed scores s_t, in double:
+ *   m = max_t s_t;  l = sum_t exp(s_t - m);  o = sum_t exp(s_t - m) v_t / l;
+ *   lse = m + ln l.   n = 0 gives o = 0 and lse = -inf (the empty partial).
+ */
+static void attend_scores(int n, int d, const double* s, const double* V, double* orow, double* lse) {
+  for (int c = 0; c < d; ++c) orow[c] = 0.0;
+  if (n == 0) {
+    *lse = -INFINITY;
+    return;
+  }
+  double m = -INFINITY;
+  for (int t = 0; t < n; ++t)
+    if (s[t] > m) m = s[t];
+  double l = 0.0;
+  for (int t = 0; t < n; ++t) {
+    double w = exp(s[t] - m);
+    l += w;
+    for (int c = 0; c < d; ++c) orow[c] += w * V[(int64_t)t * d + c];
+  }
+  for (int c = 0; c < d; ++c) orow[c] /= l;
+  *lse = m + log(l);
+}
+
+/*
  * Softmax attention of `rows` query rows over n tokens, in double:
- *   s_t = scale * q . k_t;  m = max_t s_t;  l = sum_t exp(s_t - m)
- *   o = sum_t exp(s_t - m) v_t / l;  lse = m + ln l.
- * n = 0 gives o = 0 and lse = -inf (the empty partial).
+ *   s_t = scale * q . k_t, then attend_scores.
  */
 void orc_attend(int n, int d, int rows, const double* q, const double* K, const double* V, double scale,
                 double* o, double* lse) {
   double* s = (double*)malloc(sizeof(double) * (n > 0 ? n : 1));
   for (int r = 0; r < rows; ++r) {
-    double* orow = o + (int64_t)r * d;
-    for (int c = 0; c < d; ++c) orow[c] = 0.0;
-    if (n == 0) {
-      lse[r] = -INFINITY;
-      continue;
-    }
-    double m = -INFINITY;
     for (int t = 0; t < n; ++t) {
       double acc = 0.0;
       for (int c = 0; c < d; ++c) acc += q[(int64_t)r * d + c] * K[(int64_t)t * d + c];
       s[t] = scale * acc;
-      if (s[t] > m) m = s[t];
     }
-    double l = 0.0;
-    for (int t = 0; t < n; ++t) {
-      double w = exp(s[t] - m);
-      l += w;
-      for (int c = 0; c < d; ++c) orow[c] += w * V[(int64_t)t * d + c];
-    }
-    for (int c = 0; c < d; ++c) orow[c] /= l;
-    lse[r] = m + log(l);
+    attend_scores(n, d, s, V, o + (int64_t)r * d, lse + r);
   }
   free(s);
 }
@@ -303,6 +319,75 @@ static void partial_int8_head(int H, int G, int h, const uint16_t* q, const uint
   free(qd);
 }
 
+/*
+ * Integer query of one query row for one page [IQ]: q'_c = q_c * s_c in float32
+ * (s in channel order), m = max_c |q'_c|; alpha = m / 127 and inv = 127 / m, each
+ * one float32 division; qi_c = rint(q'_c * inv) (float32 product, half to even),
+ * clamped to +-127.  m = 0 gives alpha = 0 and zero codes.  Returns alpha.
+ */
+float orc_query_codes(const uint16_t* q_row, const float* s, int8_t* qi) {
+  float qp[D_HEAD];
+  float m = 0.0f;
+  for (int c = 0; c < D_HEAD; ++c) {
+    qp[c] = bf16_float(q_row[c]) * s[c];
+    float a = fabsf(qp[c]);
+    if (a > m) m = a;
+  }
+  if (m == 0.0f) {
+    for (int c = 0; c < D_HEAD; ++c) qi[c] = 0;
+    return 0.0f;
+  }
+  const float inv = 127.0f / m;
+  for (int c = 0; c < D_HEAD; ++c) {
+    float y = rintf(qp[c] * inv);
+    if (y > 127.0f) y = 127.0f;
+    if (y < -127.0f) y = -127.0f;
+    qi[c] = (int8_t)y;
+  }
+  return m / 127.0f;
+}
+
+/* 8-bit-tier partial with the integer query [IQ, FMT, ATT]: per page and row the
+ * query is coded by orc_query_codes with the page's s_c, and
+ *   score_t = scale * alpha * r_t * sum_c qi_c kc_tc   (the sum is exact);
+ * values are dequantised (v = vc * u_c) and attended in double. */
+static void partial_int8_iq_head(int H, int G, int h, const uint16_t* q, const uint8_t* rec_pool,
+                                 const int32_t* page_table8, int page_begin, int page_end, double* o,
+                                 double* lse) {
+  const int d = D_HEAD;
+  const double scale = 1.0 / sqrt((double)d);
+  int np = page_end > page_begin ? page_end - page_begin : 0;
+  int n = np * T_PAGE;
+  double* V = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1) * d);
+  double* sc = (double*)malloc(sizeof(double) * (size_t)G * (n > 0 ? n : 1));
+  for (int p = 0; p < np; ++p) {
+    const uint8_t* rec = rec_pool + ((int64_t)page_table8[page_begin + p] * H + h) * REC_BYTES;
+    const uint8_t* kc = rec + OFF_KC;
+    const uint8_t* vc = rec + OFF_VC;
+    float s[D_HEAD], r[T_PAGE], u[D_HEAD], s_stored[D_HEAD];
+    memcpy(s_stored, rec + OFF_KS_CHAN, sizeof s_stored);
+    for (int c = 0; c < D_HEAD; ++c) s[c] = s_stored[ks_pos(c)];
+    memcpy(r, rec + OFF_KS_TOK, sizeof r);
+    memcpy(u, rec + OFF_VS_CHAN, sizeof u);
+    for (int t = 0; t < T_PAGE; ++t)
+      for (int c = 0; c < d; ++c)
+        V[((int64_t)p * T_PAGE + t) * d + c] = (double)((int)vc[vc_pos(c, t)] - 128) * (double)u[c];
+    for (int g = 0; g < G; ++g) {
+      int8_t qi[D_HEAD];
+      const float alpha = orc_query_codes(q + ((int64_t)h * G + g) * d, s, qi);
+      for (int t = 0; t < T_PAGE; ++t) {
+        int64_t dot = 0;
+        for (int c = 0; c < d; ++c) dot += (int64_t)qi[c] * ((int)kc[kc_pos(t, c)] - 128);
+        sc[(int64_t)g * n + p * T_PAGE + t] = scale * (double)alpha * (double)r[t] * (double)dot;
+      }
+    }
+  }
+  for (int g = 0; g < G; ++g)
+    attend_scores(n, d, sc + (int64_t)g * n, V, o + ((int64_t)h * G + g) * d, lse + h * G + g);
+  free(V);
+  free(sc);
+}
+
 void orc_partial_exact(int H, int G, const uint16_t* q, const uint16_t* k_pool, const uint16_t* v_pool,
                        const int32_t* page_table, int tok_begin, int tok_end, double* o, double* lse) {
   for (int h = 0; h < H; ++h)
@@ -313,6 +398,12 @@ void orc_partial_int8(int H, int G, const uint16_t* q, const uint8_t* rec_pool, 
                       int page_begin, int page_end, double* o, double* lse) {
   for (int h = 0; h < H; ++h)
     partial_int8_head(H, G, h, q, rec_pool, page_table8, page_begin, page_end, o, lse);
+}
+
+void orc_partial_int8_iq(int H, int G, const uint16_t* q, const uint8_t* rec_pool, const int32_t* page_table8,
+                         int page_begin, int page_end, double* o, double* lse) {
+  for (int h = 0; h < H; ++h)
+    partial_int8_iq_head(H, G, h, q, rec_pool, page_table8, page_begin, page_end, o, lse);
 }
 
 /*
@@ -362,7 +453,8 @@ typedef struct {
   const int32_t *page_table, *req_page_off, *n_exact_tokens;
   const int32_t *page_table8, *req_page_off8, *n_int8_pages;
   double *o, *lse;
-  int next; /* next (request, head) item, under the lock */
+  int int_query; /* 1: the 8-bit partials use the integer query [IQ] */
+  int next;      /* next (request, head) item, under the lock */
   pthread_mutex_t lock;
 } hybrid_job;
 
@@ -375,8 +467,10 @@ static void hybrid_item(hybrid_job* J, int item) {
   const uint16_t* qb = J->q + (int64_t)b * rows * d;
   partial_exact_head(J->H, J->G, h, qb, J->k_pool, J->v_pool, J->page_table + J->req_page_off[b], 0,
                      J->n_exact_tokens[b], parts_o, parts_lse);
-  partial_int8_head(J->H, J->G, h, qb, J->rec_pool, J->page_table8 + J->req_page_off8[b], 0,
-                    J->n_int8_pages[b], parts_o + (int64_t)rows * d, parts_lse + rows);
+  (J->int_query ? partial_int8_iq_head : partial_int8_head)(J->H, J->G, h, qb, J->rec_pool,
+                                                             J->page_table8 + J->req_page_off8[b], 0,
+                                                             J->n_int8_pages[b], parts_o + (int64_t)rows * d,
+                                                             parts_lse + rows);
   /* gather this head's G rows of both partials and fold them [TIERS, MERGE] */
   double po[2 * 8 * D_HEAD], pl[2 * 8], oo[8 * D_HEAD], ll[8];
   double *po_h = po, *pl_h = pl, *oo_h = oo, *ll_h = ll;
@@ -423,13 +517,14 @@ static void* hybrid_worker(void* arg) {
  * exact partial over the request's BF16 tokens [0, n_exact_tokens[b]) (CSR page
  * table page_table / req_page_off) and the 8-bit partial over its pages
  * [0, n_int8_pages[b]) (CSR page_table8 / req_page_off8), folded by orc_merge.
- * o is [B][H*G][256], lse is [B][H*G].  Work is spread over n_threads threads by
- * (request, KV head); the result does not depend on the thread count.
+ * o is [B][H*G][256], lse is [B][H*G].  int_query = 1 takes the 8-bit partials
+ * with the integer query.  Work is spread over n_threads threads by (request, KV
+ * head); the result does not depend on the thread count.
  */
 void orc_hybrid_batched(int B, int H, int G, const uint16_t* q, const uint16_t* k_pool, const uint16_t* v_pool,
                         const uint8_t* rec_pool, const int32_t* page_table, const int32_t* req_page_off,
                         const int32_t* n_exact_tokens, const int32_t* page_table8, const int32_t* req_page_off8,
-                        const int32_t* n_int8_pages, double* o, double* lse, int n_threads) {
+                        const int32_t* n_int8_pages, double* o, double* lse, int int_query, int n_threads) {
   hybrid_job J;
   J.B = B;
   J.H = H;
@@ -446,6 +541,7 @@ void orc_hybrid_batched(int B, int H, int G, const uint16_t* q, const uint16_t* 
   J.n_int8_pages = n_int8_pages;
   J.o = o;
   J.lse = lse;
+  J.int_query = int_query;
   J.next = 0;
   pthread_mutex_init(&J.lock, 0);
   if (n_threads < 1) n_threads = 1;
