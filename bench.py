@@ -222,7 +222,7 @@ def graph_times(step, steps, warmup, stream, flush, flush_r):
     return [a.elapsed_time(b) for a, b in ev]
 
 
-def run_batched(impl, args, stream, dev, flush, flush_r, peak):
+def run_batched(impl, args, stream, dev, flush, flush_r, peak, int_query=0):
     """The 16-request batched hybrid decode (lengths uniform in [8K, 64K], 2048
     recent BF16 tokens each, 4 KV heads x 8 q rows, outlier keys, seed 3): one
     multi-request call per step, each request with its own page tables."""
@@ -233,7 +233,7 @@ def run_batched(impl, args, stream, dev, flush, flush_r, peak):
 
     w = synth.batched_hybrid(seed=3)
     H, G, B = w.H, w.G, w.B
-    shape = tpk.Shape(H, impl=impl, kv_slots=w.n_slots, rec_slots=w.n_slots)
+    shape = tpk.Shape(H, impl=impl, kv_slots=w.n_slots, rec_slots=w.n_slots, int_query=int_query)
     with torch.cuda.stream(stream):
         kp = torch.from_numpy(w.k_pool.view(np.int16)).to(dev)
         vp = torch.from_numpy(w.v_pool.view(np.int16)).to(dev)
@@ -267,7 +267,7 @@ def run_batched(impl, args, stream, dev, flush, flush_r, peak):
                         "4 KV heads x 8 q rows, head_dim 256, outlier keys"}
 
 
-def run_tier(which, impl, args, stream, dev, flush, flush_r, peak):
+def run_tier(which, impl, args, stream, dev, flush, flush_r, peak, int_query=0):
     """One tier alone over a 131,072-token history of the main workload's shape
     (4 KV heads x 8 q rows, head_dim 256, 4 outlier key channels at 20x std):
     'exact' = all BF16, 'int8' = all 8-bit (2048 pages, converted on the GPU
@@ -280,7 +280,7 @@ def run_tier(which, impl, args, stream, dev, flush, flush_r, peak):
     w = synth.make_workload([131072], None if which == "exact" else 0, H=4, seed=12,
                             key_sigma="outliers")
     H, G = w.H, w.G
-    shape = tpk.Shape(H, impl=impl, kv_slots=w.n_slots, rec_slots=w.n_slots)
+    shape = tpk.Shape(H, impl=impl, kv_slots=w.n_slots, rec_slots=w.n_slots, int_query=int_query)
     with torch.cuda.stream(stream):
         kp = torch.from_numpy(w.k_pool.view(np.int16)).to(dev)
         vp = torch.from_numpy(w.v_pool.view(np.int16)).to(dev)
@@ -329,7 +329,9 @@ def run_gpu(args, dist, rank, world):
     H, G = w.H, w.G
     dev = torch.device("cuda", local)
     stream = torch.cuda.Stream(dev)
-    shape = tpk.Shape(H, impl=impl, kv_slots=w.n_slots, rec_slots=w.n_slots)
+    if args.int_query and impl == tpk.IMPL_SIMT:
+        raise SystemExit("--int-query runs on the tensor-core kernel only")
+    shape = tpk.Shape(H, impl=impl, kv_slots=w.n_slots, rec_slots=w.n_slots, int_query=int(args.int_query))
     with torch.cuda.stream(stream):
         kp = torch.from_numpy(w.k_pool.view(np.int16)).to(dev)
         vp = torch.from_numpy(w.v_pool.view(np.int16)).to(dev)
@@ -410,10 +412,13 @@ def run_gpu(args, dist, rank, world):
 
     # ---- each tier alone at 128K (the exact and the 8-bit kernel paths)
     peak, peak_kind = hbm_peak()
-    tiers = batched = None
+    tiers = batched = int_query = None
     if args.tier_steps > 0:
         tiers = {k: run_tier(k, impl, args, stream, dev, flush, flush_r, peak) for k in ("exact", "int8")}
         batched = run_batched(impl, args, stream, dev, flush, flush_r, peak)
+        if impl != tpk.IMPL_SIMT and not args.int_query:
+            int_query = run_int_query(w, shape, step, args, stream, dev, flush, flush_r, peak, impl,
+                                      (q, kp, vp, rec, pt_d, off, pt8_d, off8, o, lse, ws, nbytes))
 
     # ---- end to end from pinned host memory (packed history, identity page tables)
     e2e = run_e2e(args, w, rec, shape, stream, dev, dist)
@@ -434,7 +439,7 @@ def run_gpu(args, dist, rank, world):
                "host_cores_available": os.cpu_count()}
     achieved = hist_bytes / (ms_mean * 1e-3) / 1e9
     value = world * hist_bytes / (ms_max * 1e-3) / 1e9
-    traffic = measured_traffic(args.kernel)
+    traffic = measured_traffic(args.kernel + ("_int_query" if args.int_query else ""))
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_max, 5), "us_per_step": round(ms_max * 1e3, 2),
@@ -444,6 +449,7 @@ def run_gpu(args, dist, rank, world):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
         "config": {"workload": WORKLOAD, "history_bytes_per_step": hist_bytes, "kernel": args.kernel,
+                   "query": "8-bit integer query on the 8-bit tier" if args.int_query else "float",
                    "l2": "flushed between timed steps (256 MB written, then 256 MB read so dirty lines are written back outside the timed step); inputs 295 MB also exceed L2",
                    "clocks_sampled": "nvidia-smi every 100 ms over a soak of back-to-back steps and the timed steps",
                    "launch": "device time of CUDA-graph replays of the step (decode + fold kernels); e2e calls the C ABI directly",
@@ -459,12 +465,42 @@ def run_gpu(args, dist, rank, world):
         "host_resident": host_res,
         "tiers_128k": tiers,
         "batched_16": batched,
+        "int_query_variant": int_query,
         "gpu_launches": args.steps * launches_per_step,
         "clocks": clk.summary(),
         "cpu_baseline": cpu,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def run_int_query(w, shape, step_float, args, stream, dev, flush, flush_r, peak, impl, bufs):
+    """The integer-query variant of the 8-bit tier (its QK on the integer tensor
+    path) beside the float query, same protocol (graph replays, L2 flushed): the
+    128K hybrid step, the 8-bit tier alone and the 16-request batch."""
+    import tiered_paged_kv_gb300 as tpk
+
+    q, kp, vp, rec, pt_d, off, pt8_d, off8, o, lse, ws, nbytes = bufs
+    shape_iq = tpk.Shape(shape.kv_heads, impl=shape.impl, kv_slots=shape.kv_slots, rec_slots=shape.rec_slots,
+                         int_query=1)
+
+    def step_iq():
+        tpk.decode_hybrid_batched(shape_iq, 1, q, kp, vp, rec, pt_d, off, w.n_ex, pt8_d, off8, w.n8, o, lse, ws,
+                                  nbytes, stream)
+
+    out = {}
+    for name, fn in (("float_query", step_float), ("int_query", step_iq)):
+        times = graph_times(fn, args.tier_steps, 3, stream, flush, flush_r)
+        st, flags = tpk.get_device_status(reset=True, stream=stream)
+        if st != 0:
+            raise RuntimeError(f"device status {st} flags {flags} ({name})")
+        ms = statistics.median(times)
+        gbs = w.history_bytes() / (ms * 1e-3) / 1e9
+        out[f"hybrid_128k_{name}"] = {"us_per_step_median": round(ms * 1e3, 2), "GBps": round(gbs, 1),
+                                      "hbm_frac": round(gbs / peak, 4), "steps": len(times)}
+    out["int8_128k_int_query"] = run_tier("int8", impl, args, stream, dev, flush, flush_r, peak, int_query=1)
+    out["batched_16_int_query"] = run_batched(impl, args, stream, dev, flush, flush_r, peak, int_query=1)
+    return out
 
 
 def run_e2e(args, w, rec_dev, shape, stream, dev, dist):
@@ -484,7 +520,8 @@ def run_e2e(args, w, rec_dev, shape, stream, dev, dist):
     lse_d = torch.empty(1, H * G, dtype=torch.float32, device=dev)
     o_h = torch.empty(1, H * G, 256, dtype=torch.float32).pin_memory()
     lse_h = torch.empty(1, H * G, dtype=torch.float32).pin_memory()
-    shape2 = tpk.Shape(H, impl=shape.impl, kv_slots=off["n_exact_pages"], rec_slots=off["n_int8_pages"])
+    shape2 = tpk.Shape(H, impl=shape.impl, kv_slots=off["n_exact_pages"], rec_slots=off["n_int8_pages"],
+                       int_query=shape.int_query)
     nbytes = tpk.hybrid_workspace_bytes(shape2, 1)
     ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
     views = [slot_views(s, off, w) for s in slots]
@@ -572,7 +609,8 @@ def run_host_resident(args, w, rec_dev, shape, stream, dev, dist, layers=None, s
         h.copy_(torch.from_numpy(img))
         host.append(h)
     slots = [torch.empty(off["nbytes"], dtype=torch.uint8, device=dev) for _ in range(2)]
-    shape2 = tpk.Shape(H, impl=shape.impl, kv_slots=off["n_exact_pages"], rec_slots=off["n_int8_pages"])
+    shape2 = tpk.Shape(H, impl=shape.impl, kv_slots=off["n_exact_pages"], rec_slots=off["n_int8_pages"],
+                       int_query=shape.int_query)
     nbytes = tpk.hybrid_workspace_bytes(shape2, 1)
     ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
     outs = [(torch.empty(1, H * G, 256, dtype=torch.float32, device=dev),
@@ -827,6 +865,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="tpk", choices=["tpk", "reference"])
     ap.add_argument("--kernel", default="default", choices=["default", "simt", "tensor"])
+    ap.add_argument("--int-query", action="store_true",
+                    help="time the integer-query variant of the 8-bit tier as the main step")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--soak", type=float, default=1.0, help="seconds of back-to-back steps before timing")
     ap.add_argument("--layers", type=int, default=16, help="layers of the host-resident measurement (0: skip)")

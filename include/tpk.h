@@ -86,6 +86,15 @@ typedef struct {
                         allowed only with TPK_IMPL_SIMT: the tensor-core kernel reads the BF16
                         pools through TMA tensor maps that need the pool size */
   int64_t rec_slots; /* slots in the 8-bit pool (bounds for page_table8 entries); 0 = unchecked */
+  int int_query;     /* 0 (default): the 8-bit tier's QK uses the query in floating point.
+                        1: the integer-query variant ("SYCL", "Attention that reads 8-bit
+                        history": the integer query cache): per record and query row the
+                        folded query q'_c = q_c s_c is coded as qi_c = rint(q'_c * (127 / m)),
+                        m = max_c |q'_c| over the 256 channels, float32 steps with correctly
+                        rounded divisions, half to even; the score is
+                        (m / 127) * r_t * sum_c qi_c kc_tc, the sum exact.  This changes the
+                        result (the query is coded to 8 bits); the exact tier is unaffected.
+                        Tensor-core kernel only (TPK_IMPL_SIMT gives TPK_ERR_UNSUPPORTED). */
 } tpk_shape;
 
 const char* tpk_version(void);

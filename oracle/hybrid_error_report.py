@@ -4,6 +4,10 @@ reference are all oracle functions).  Prints one line per workload.
 
     python oracle/hybrid_error_report.py [--full]
 
+Each workload is reported twice: with the query in floating point, and with the
+integer-query variant ("SYCL", "Attention that reads 8-bit history": the query
+folded with each page's channel scales coded to 8 bits per page and row).
+
 The pages' quality bound is 0.005 on the worst merged error ("model
 quantization": a fixed loss bound against the format's own higher-precision
 reference); this reports max |o_hybrid - o_fp| over all rows and channels, the
@@ -26,12 +30,14 @@ def report(name, w, threads):
     rec = np.zeros(w.n_slots * w.H * oracle.REC_BYTES, np.uint8)
     s = w.int8_slots()
     oracle.quantize_pages(w.H, w.k_pool, w.v_pool, s, s, rec)
-    oh, _ = oracle.hybrid_workload(w, rec, n_threads=threads)
     of, _ = oracle.full_precision_workload(w, n_threads=threads)
-    err = np.abs(oh - of)
-    print(f"{name:34s} max_abs {err.max():.5f}  max_abs/max|o| {err.max() / np.abs(of).max():.5f}  "
-          f"rms_rel {np.sqrt((err ** 2).mean() / (of ** 2).mean()):.5f}  max|o| {np.abs(of).max():.4f}  "
-          f"bound 0.005 {'met' if err.max() <= 0.005 else 'exceeded'}  ({time.time() - t0:.1f} s)", flush=True)
+    for query in ("float", "integer"):
+        oh, _ = oracle.hybrid_workload(w, rec, n_threads=threads, int_query=query == "integer")
+        err = np.abs(oh - of)
+        print(f"{name:34s} {query:7s} query  max_abs {err.max():.5f}  max_abs/max|o| "
+              f"{err.max() / np.abs(of).max():.5f}  rms_rel {np.sqrt((err ** 2).mean() / (of ** 2).mean()):.5f}  "
+              f"max|o| {np.abs(of).max():.4f}  bound 0.005 {'met' if err.max() <= 0.005 else 'exceeded'}  "
+              f"({time.time() - t0:.1f} s)", flush=True)
 
 
 def main():

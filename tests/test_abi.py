@@ -46,7 +46,7 @@ def err(L):
 
 def test_unsupported_shapes_are_rejected(L):
     for kw, code in [({"group": 4}, 2), ({"head_dim": 128}, 2), ({"page_tokens": 32}, 2), ({"sm_scale": 0.1}, 2),
-                     ({"impl": 7}, 1)]:
+                     ({"impl": 7}, 1), ({"int_query": 2}, 1), ({"int_query": 1, "impl": tpk.IMPL_SIMT}, 2)]:
         s = tpk.Shape(4, **kw)
         st = L.tpk_decode_attn_exact(ctypes.byref(s), 16, 16, 16, 16, 0, 64, 1, 16, 16, None)
         assert st == code, (kw, st, err(L))

@@ -32,11 +32,12 @@ STATUS_NAMES = {0: "TPK_OK", 1: "TPK_ERR_INVALID", 2: "TPK_ERR_UNSUPPORTED", 3: 
 class Shape(ctypes.Structure):
     _fields_ = [("kv_heads", ctypes.c_int), ("group", ctypes.c_int), ("head_dim", ctypes.c_int),
                 ("page_tokens", ctypes.c_int), ("sm_scale", ctypes.c_float), ("impl", ctypes.c_int),
-                ("kv_slots", ctypes.c_int64), ("rec_slots", ctypes.c_int64)]
+                ("kv_slots", ctypes.c_int64), ("rec_slots", ctypes.c_int64), ("int_query", ctypes.c_int)]
 
     def __init__(self, kv_heads, group=8, head_dim=256, page_tokens=64, sm_scale=0.0, impl=IMPL_DEFAULT,
-                 kv_slots=0, rec_slots=0):
-        super().__init__(kv_heads, group, head_dim, page_tokens, sm_scale, impl, kv_slots, rec_slots)
+                 kv_slots=0, rec_slots=0, int_query=0):
+        super().__init__(kv_heads, group, head_dim, page_tokens, sm_scale, impl, kv_slots, rec_slots,
+                         int(int_query))
 
 
 class TiersPlan(ctypes.Structure):

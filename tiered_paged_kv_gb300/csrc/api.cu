@@ -65,6 +65,9 @@ tpk_status check_shape(const tpk_shape* s) {
     return fail(TPK_ERR_UNSUPPORTED, "sm_scale %g (only 1/sqrt(256) supported)", (double)s->sm_scale);
   if (s->impl < TPK_IMPL_DEFAULT || s->impl > TPK_IMPL_TENSOR) return fail(TPK_ERR_INVALID, "impl %d", s->impl);
   if (s->kv_slots < 0 || s->rec_slots < 0) return fail(TPK_ERR_INVALID, "negative pool size");
+  if (s->int_query != 0 && s->int_query != 1) return fail(TPK_ERR_INVALID, "int_query %d (0 or 1)", s->int_query);
+  if (s->int_query && s->impl == TPK_IMPL_SIMT)
+    return fail(TPK_ERR_UNSUPPORTED, "the integer query runs on the tensor-core kernel only");
   return TPK_OK;
 }
 
@@ -100,6 +103,7 @@ void fill_common(DecodeParams& p, const tpk_shape* s, const void* q) {
   p.kv_slots = s->kv_slots;
   p.rec_slots = s->rec_slots;
   p.qscale = 0.0625f * kLog2e;
+  p.int_query = s->int_query;
   p.H = s->kv_heads;
 }
 

@@ -81,6 +81,7 @@ struct DecodeParams {
   float* out_lse;
   int* status;              // device status word
   float qscale;             // sm_scale * log2(e)
+  int int_query;            // 1: the 8-bit tier's QK runs on the integer query
   int H;
   int mode;
   int n_req;

@@ -31,8 +31,10 @@
 // permute per two codes; the 1152 offset is removed once per page and row: from
 // the scores as 1152 * sum_c q'_c, and from the PV accumulator, which starts at
 // -1152 * sum_t p_t.
-// The integer tensor path (s8 x s8) is not used: on this GPU it runs at about a
-// quarter of the f16 rate.
+// The integer tensor path runs at about a quarter of the f16 rate on this GPU, so
+// the default keeps the query in floating point; the integer-query variant (the
+// pages' "integer query cache") runs QK on it with the operands swapped so that
+// no row of the tile is idle (qk_int_query below).
 //
 // Exact tier: BF16 half-pages (32 tokens) arrive by TMA tensor copies in the
 // 128-byte-swizzled layout, so ldmatrix reads are conflict-free; q is exact in
@@ -53,6 +55,10 @@ constexpr int kMmaThreads = kCons * 32;
 constexpr int kMmaSlots = 6;
 constexpr unsigned kAll = 0xffffffffu;
 
+// float query rows padded by 64 bytes, so that rows g and g + 1 sit in opposite
+// bank halves for the contiguous row reads of the integer-query absmax
+constexpr int kQsStride = kHeadDim + 16;
+
 struct MmaSmem {
   alignas(128) uint8_t slot[kMmaSlots][kSlotBytes];
   uint64_t full[kMmaSlots];
@@ -63,7 +69,7 @@ struct MmaSmem {
   int valid[kMmaSlots];
   int pt[kPtCache];
   alignas(16) uint32_t q[kGroup][kHeadDim / 2];  // the unit's query rows, bf16 pairs
-  alignas(16) float qs[kGroup][kHeadDim];        // the same rows as float, times a power of two
+  alignas(16) float qs[kGroup][kQsStride];       // the same rows as float, times a power of two
   float ep_m[kCons][kGroup];
   float ep_l[kCons][kGroup];
   int is_last;
@@ -87,6 +93,16 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1
       "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
       "{%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// D (s32) += A (unsigned bytes, 16 x 32, row-major) * B (signed bytes, 32 x 8)
+__device__ __forceinline__ void mma_u8s8(int (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k32.row.col.s32.u8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+r"(d[0]), "+r"(d[1]), "+r"(d[2]), "+r"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
@@ -242,25 +258,22 @@ __device__ __forceinline__ void fence_slot_writes() { asm volatile("fence.proxy.
 
 // ------------------------------------------------------- 8-bit record
 // Warp half h of a pair owns channels 128h .. 128h + 127 of a whole record (64
-// tokens).  QK: tile j (0..7) column 2t + e is token 16t + 2j + e, so thread t
-// receives the scores of tokens 16t .. 16t + 15; the warp's partial scores over
-// its channels are summed with the partner's through shared memory, and both
-// warps then hold the full scores and run the same softmax.  PV k-step i (0..3)
+// tokens).  QK leaves in x[k] the full (both halves) dot product of query row g
+// with the codes of token 16t + k, before the per-token factor; the warp's partial
+// scores over its channels are summed with the partner's through shared memory, so
+// both warps hold the full scores and run the same softmax.  PV k-step i (0..3)
 // covers tokens 16t + 4i + {0..3} of every thread t; the warp accumulates its 128
 // channels.
-__device__ __forceinline__ bool process_int8_record(uint8_t* rec, int h, const PairSync& psync, const MmaSmem& S,
-                                                    float qk_scale, float& m_run, float& l_run, float (&O)[8][4]) {
+
+// Float query: tile j (0..7) column 2t + e is token 16t + 2j + e; k-step 4J + i
+// uses channels 128h + 64J + 16t + 4i + {0, 1} (k = 2t, 2t+1) and + {2, 3} (k =
+// 2t+8, 2t+9).
+__device__ __forceinline__ bool qk_float_query(uint8_t* rec, int h, const PairSync& psync, const MmaSmem& S,
+                                               float (&x)[16]) {
   const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
   const float* ks = reinterpret_cast<const float*>(rec + kOffKsChan);
-  const float* kr = reinterpret_cast<const float*>(rec + kOffKsTok);
-  const float* vs = reinterpret_cast<const float*>(rec + kOffVsChan) + 128 * h;
   const uint8_t* kc = rec + kOffKc;
-  const uint8_t* vc = rec + kOffVc;
   const float* qrow = S.qs[g];
-
-  // ---- QK over this warp's channels: 8 tiles of 8 tokens, 8 k-steps of 16
-  // channels.  k-step 4J + i uses channels 128h + 64J + 16t + 4i + {0, 1} (k = 2t,
-  // 2t+1) and + {2, 3} (k = 2t+8, 2t+9).
   float acc[8][4];
 #pragma unroll
   for (int j = 0; j < 8; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
@@ -295,7 +308,6 @@ __device__ __forceinline__ bool process_int8_record(uint8_t* rec, int h, const P
   // channels (row g) from the high plane's dot before the low plane's is added.
   qsum += __shfl_xor_sync(kAll, qsum, 1);
   qsum += __shfl_xor_sync(kAll, qsum, 2);
-  float x[16];  // x[2j + e]: token 16t + 2j + e
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
     x[2 * j] = fmaf(-kCodeOffset, qsum, acc[j][0]) + acc[j][2];
@@ -303,7 +315,127 @@ __device__ __forceinline__ bool process_int8_record(uint8_t* rec, int h, const P
   }
   // partial scores of the two channel halves -> full scores in both warps (the
   // exchange area: rows 0..15 of this warp's half of the key codes)
-  if (!pair_exchange<16, kHeadDim>(x, rec + kOffKc + 128 * h, rec + kOffKc + 128 * (h ^ 1), psync)) return false;
+  return pair_exchange<16, kHeadDim>(x, rec + kOffKc + 128 * h, rec + kOffKc + 128 * (h ^ 1), psync);
+}
+
+// Integer query ("SYCL", "Attention that reads 8-bit history": the integer query
+// cache; the two-by-two experiment on which products run on integers).  Row g of
+// q' = q s_c is coded per record with the absmax rule of the key codes: alpha =
+// max_c |q'_c| / 127 over all 256 channels, codes rint(q'_c * (127 / max)), the
+// divisions correctly rounded.  QK then runs on the integer tensor path with the
+// operands swapped, so every row of the tile carries work: A = 16 tokens of stored
+// key bytes (code + 128, unsigned), B = the 8 rows' query codes (signed), D = 16
+// tokens x 8 rows in exact s32.  m-tile mt, row r is token 16mt + r; k-step (J, i2)
+// uses channels 128h + 64J + 16t + 8i2 + {0..3} (k = 4t..4t+3) and + {4..7} (k =
+// 16+4t..), the same 16 channels per thread as the float query.  The offset 128 is
+// removed as 128 * sum_c qi_c; the partial dots of the two halves are added (exactly)
+// through shared memory, transposed on the way to the score layout of the softmax.
+__device__ __forceinline__ bool qk_int_query(uint8_t* rec, int h, const PairSync& psync, const MmaSmem& S,
+                                             float (&x)[16]) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+  const float* ks = reinterpret_cast<const float*>(rec + kOffKsChan);
+  const uint8_t* kc = rec + kOffKc;
+  const float* qrow = S.qs[g];
+  // q' of this thread's own channels, and the absmax over the whole row (the
+  // partner half read contiguously: channels 128 (h ^ 1) + 16i + 4t)
+  float y[2][4][4];
+  float mx = 0.f;
+#pragma unroll
+  for (int J = 0; J < 2; ++J)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int ch = 128 * h + 64 * J + 16 * t + 4 * i;
+      const float4 s4 = *reinterpret_cast<const float4*>(ks + ks_index(ch));
+      const float4 q4 = *reinterpret_cast<const float4*>(qrow + ks_index(ch));
+      y[J][i][0] = q4.x * s4.x;
+      y[J][i][1] = q4.y * s4.y;
+      y[J][i][2] = q4.z * s4.z;
+      y[J][i][3] = q4.w * s4.w;
+      mx = fmaxf(mx, fmaxf(fmaxf(fabsf(y[J][i][0]), fabsf(y[J][i][1])), fmaxf(fabsf(y[J][i][2]), fabsf(y[J][i][3]))));
+    }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int ch = 128 * (h ^ 1) + 16 * i + 4 * t;
+    const float4 s4 = *reinterpret_cast<const float4*>(ks + ks_index(ch));
+    const float4 q4 = *reinterpret_cast<const float4*>(qrow + ks_index(ch));
+    mx = fmaxf(mx, fmaxf(fmaxf(fabsf(q4.x * s4.x), fabsf(q4.y * s4.y)), fmaxf(fabsf(q4.z * s4.z), fabsf(q4.w * s4.w))));
+  }
+  mx = fmaxf(mx, __shfl_xor_sync(kAll, mx, 1));
+  mx = fmaxf(mx, __shfl_xor_sync(kAll, mx, 2));
+  const float inv = mx > 0.f ? __fdiv_rn(127.f, mx) : 0.f;
+  const float alpha = __fdiv_rn(mx, 127.f);
+  // codes, four to a word (channel order = byte order); |y * inv| <= 127 (1 + 2^-24)
+  // rounds to at most 127, so no clamp is needed
+  uint32_t qw[2][4];
+  int qsum = 0;
+#pragma unroll
+  for (int J = 0; J < 2; ++J)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int c0 = __float2int_rn(y[J][i][0] * inv), c1 = __float2int_rn(y[J][i][1] * inv);
+      const int c2 = __float2int_rn(y[J][i][2] * inv), c3 = __float2int_rn(y[J][i][3] * inv);
+      qsum += (c0 + c1) + (c2 + c3);
+      qw[J][i] = __byte_perm(__byte_perm(c0, c1, 0x0040), __byte_perm(c2, c3, 0x0040), 0x5410);
+    }
+  int acc[4][4];
+#pragma unroll
+  for (int mt = 0; mt < 4; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0;
+#pragma unroll
+  for (int J = 0; J < 2; ++J) {
+    const int cb = (128 * h + 64 * J + 16 * t) ^ ((g & 1) << 6);  // tokens g, g + 8 share g's parity
+#pragma unroll
+    for (int mt = 0; mt < 4; ++mt) {
+      const uint4 ka = *reinterpret_cast<const uint4*>(kc + (16 * mt + g) * kHeadDim + cb);
+      const uint4 kb = *reinterpret_cast<const uint4*>(kc + (16 * mt + g + 8) * kHeadDim + cb);
+      mma_u8s8(acc[mt], ka.x, kb.x, ka.y, kb.y, qw[J][0], qw[J][1]);
+      mma_u8s8(acc[mt], ka.z, kb.z, ka.w, kb.w, qw[J][2], qw[J][3]);
+    }
+  }
+  // sum_c qi_c of rows 2t and 2t + 1 over this warp's channels (the code offset)
+  qsum += __shfl_xor_sync(kAll, qsum, 1);
+  qsum += __shfl_xor_sync(kAll, qsum, 2);
+  const int cq0 = 128 * __shfl_sync(kAll, qsum, 8 * t), cq1 = 128 * __shfl_sync(kAll, qsum, 8 * t + 4);
+  // Exchange area: bytes 128h .. 128h + 127 of key-code rows 0..15 (codes only
+  // this warp reads, and has read).  Dot (token tau, row rho) sits in row tau / 4,
+  // word rho + 8 ((tau + tau / 16) mod 4): conflict-free both for the stores
+  // (tau = 16mt + g (+ 8), rho = 2t, 2t + 1) and for the transposed loads (tau =
+  // 16t + k, rho = g).
+  uint8_t* mine = rec + kOffKc + 128 * h;
+  const uint8_t* theirs = rec + kOffKc + 128 * (h ^ 1);
+  __syncwarp();
+#pragma unroll
+  for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int tau = 16 * mt + 8 * e + g;
+      *reinterpret_cast<int2*>(mine + (tau >> 2) * kHeadDim + 4 * (2 * t + 8 * ((tau + mt) & 3))) =
+          make_int2(acc[mt][2 * e] - cq0, acc[mt][2 * e + 1] - cq1);
+    }
+  __syncwarp();
+  if (lane == 0) mbar_arrive(psync.bar);
+  if (!mbar_wait(psync.bar, psync.parity, psync.status)) return false;
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    const int off = ((16 * t + k) >> 2) * kHeadDim + 4 * (g + 8 * ((k + t) & 3));
+    const int d = *reinterpret_cast<const int*>(mine + off) + *reinterpret_cast<const int*>(theirs + off);
+    x[k] = (float)d * alpha;  // |d| <= 256 * 127 * 127 < 2^24: exact
+  }
+  return true;
+}
+
+template <bool IntQuery>
+__device__ __forceinline__ bool process_int8_record(uint8_t* rec, int h, const PairSync& psync, const MmaSmem& S,
+                                                    float qk_scale, float& m_run, float& l_run, float (&O)[8][4]) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+  const float* kr = reinterpret_cast<const float*>(rec + kOffKsTok);
+  const float* vs = reinterpret_cast<const float*>(rec + kOffVsChan) + 128 * h;
+  const uint8_t* vc = rec + kOffVc;
+  float x[16];  // x[k]: token 16t + k
+  if (IntQuery) {
+    if (!qk_int_query(rec, h, psync, S, x)) return false;
+  } else {
+    if (!qk_float_query(rec, h, psync, S, x)) return false;
+  }
   {
     // r_t of tokens 16t .. 16t + 15, then base-2 scores
     float rr[16];
@@ -437,7 +569,7 @@ __device__ __forceinline__ bool process_bf16_half(uint8_t* slot, int h, const Pa
 }
 
 // ------------------------------------------------------------------ kernel
-template <int R>
+template <int R, bool IntQuery>
 __global__ void __launch_bounds__(kMmaThreads, 1) decode_mma_kernel(const __grid_constant__ DecodeParams p,
                                                                   const __grid_constant__ Plan<R> plan) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -520,7 +652,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) decode_mma_kernel(const __grid
         const PairSync psync{&S.pairbar[pair], pair_phase & 1, p.status};
         ++pair_phase;
         const bool ok = ui.tier == 1
-                            ? process_int8_record(S.slot[s], half, psync, S, qk_scale, m_run, l_run, O)
+                            ? process_int8_record<IntQuery>(S.slot[s], half, psync, S, qk_scale, m_run, l_run, O)
                             : process_bf16_half(S.slot[s], half, psync, (it.first + j) * 32, ui.tok_begin,
                                                 ui.tok_end, S, p.qscale, m_run, l_run, O);
         if (!ok) {
@@ -584,32 +716,37 @@ __global__ void __launch_bounds__(kMmaThreads, 1) decode_mma_kernel(const __grid
   write_and_fold<kCons / 2, MmaSmem, kEpStride>(p, ui, S, ep_o);
 }
 
-template <int R>
+template <int R, bool IntQuery>
 static cudaError_t launch_mma(const DecodeParams& p, const ReqPlan* req, cudaStream_t stream) {
   static bool configured = false;
   const int smem = (int)sizeof(MmaSmem);
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<R>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e =
+        cudaFuncSetAttribute(decode_mma_kernel<R, IntQuery>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     configured = true;
   }
   Plan<R> plan = {};
   for (int b = 0; b < p.n_req; ++b) plan.req[b] = req[b];
-  decode_mma_kernel<R><<<p.n_units, kMmaThreads, smem, stream>>>(p, plan);
+  decode_mma_kernel<R, IntQuery><<<p.n_units, kMmaThreads, smem, stream>>>(p, plan);
   return cudaGetLastError();
 }
 
 cudaError_t launch_decode_mma(const DecodeParams& p, const ReqPlan* req, cudaStream_t stream) {
   if (p.n_units == 0) return cudaSuccess;
-  return p.n_req <= kShortPlan ? launch_mma<kShortPlan>(p, req, stream)
-                               : launch_mma<kMaxReqPerLaunch>(p, req, stream);
+  if (p.int_query)
+    return p.n_req <= kShortPlan ? launch_mma<kShortPlan, true>(p, req, stream)
+                                 : launch_mma<kMaxReqPerLaunch, true>(p, req, stream);
+  return p.n_req <= kShortPlan ? launch_mma<kShortPlan, false>(p, req, stream)
+                               : launch_mma<kMaxReqPerLaunch, false>(p, req, stream);
 }
 
 int decode_mma_blocks_per_sm() {
   int n = 0;
   const int smem = (int)sizeof(MmaSmem);
-  cudaFuncSetAttribute(decode_mma_kernel<kMaxReqPerLaunch>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_mma_kernel<kMaxReqPerLaunch>, kMmaThreads, smem) !=
+  cudaFuncSetAttribute(decode_mma_kernel<kMaxReqPerLaunch, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_mma_kernel<kMaxReqPerLaunch, false>, kMmaThreads,
+                                                    smem) !=
       cudaSuccess)
     return 1;
   return n > 0 ? n : 1;
