@@ -330,6 +330,8 @@ __device__ __forceinline__ bool qk_float_query(uint8_t* rec, int h, const PairSy
 // 16+4t..), the same 16 channels per thread as the float query.  The offset 128 is
 // removed as 128 * sum_c qi_c; the partial dots of the two halves are added (exactly)
 // through shared memory, transposed on the way to the score layout of the softmax.
+constexpr float kRoundMagic = 12582912.f;  // 1.5 * 2^23
+constexpr int kRoundMagicBits = 0x4B400000;  // its float32 encoding
 __device__ __forceinline__ bool qk_int_query(uint8_t* rec, int h, const PairSync& psync, const MmaSmem& S,
                                              float (&x)[16]) {
   const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
@@ -364,18 +366,22 @@ __device__ __forceinline__ bool qk_int_query(uint8_t* rec, int h, const PairSync
   mx = fmaxf(mx, __shfl_xor_sync(kAll, mx, 2));
   const float inv = mx > 0.f ? __fdiv_rn(127.f, mx) : 0.f;
   const float alpha = __fdiv_rn(mx, 127.f);
-  // codes, four to a word (channel order = byte order); |y * inv| <= 127 (1 + 2^-24)
-  // rounds to at most 127, so no clamp is needed
+  // codes, four to a word (channel order = byte order).  |y * inv| <= 127 (1 + 2^-24)
+  // rounds to at most 127, so no clamp is needed.  Rounding to an integer by adding
+  // 1.5 * 2^23 (the sum lands in [2^23, 2^24), where the float32 spacing is 1, so the
+  // addition rounds half to even exactly like rint) leaves the code in the low bits
+  // of the sum's encoding: its low byte is the code's two's-complement byte.
   uint32_t qw[2][4];
   int qsum = 0;
 #pragma unroll
   for (int J = 0; J < 2; ++J)
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const int c0 = __float2int_rn(y[J][i][0] * inv), c1 = __float2int_rn(y[J][i][1] * inv);
-      const int c2 = __float2int_rn(y[J][i][2] * inv), c3 = __float2int_rn(y[J][i][3] * inv);
-      qsum += (c0 + c1) + (c2 + c3);
-      qw[J][i] = __byte_perm(__byte_perm(c0, c1, 0x0040), __byte_perm(c2, c3, 0x0040), 0x5410);
+      uint32_t c[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) c[e] = __float_as_uint(__fadd_rn(__fmul_rn(y[J][i][e], inv), kRoundMagic));
+      qw[J][i] = __byte_perm(__byte_perm(c[0], c[1], 0x0040), __byte_perm(c[2], c[3], 0x0040), 0x5410);
+      qsum = __dp4a((int)qw[J][i], 0x01010101, qsum);
     }
   int acc[4][4];
 #pragma unroll
@@ -418,7 +424,9 @@ __device__ __forceinline__ bool qk_int_query(uint8_t* rec, int h, const PairSync
   for (int k = 0; k < 16; ++k) {
     const int off = ((16 * t + k) >> 2) * kHeadDim + 4 * (g + 8 * ((k + t) & 3));
     const int d = *reinterpret_cast<const int*>(mine + off) + *reinterpret_cast<const int*>(theirs + off);
-    x[k] = (float)d * alpha;  // |d| <= 256 * 127 * 127 < 2^24: exact
+    // |d| <= 256 * 127 * 127 < 2^22: the encoding of 1.5 * 2^23 + d, minus 1.5 * 2^23,
+    // is d as a float, exactly
+    x[k] = __fmul_rn(__fsub_rn(__int_as_float(d + kRoundMagicBits), kRoundMagic), alpha);
   }
   return true;
 }
