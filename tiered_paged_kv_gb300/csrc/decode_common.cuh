@@ -109,8 +109,8 @@ __device__ __forceinline__ void issue_item(const DecodeParams& p, const UnitInfo
 // Threads 0..127 combine the NW states into the unit's partial (o, lse) and
 // write it: to the caller's partial arrays (primitive calls), straight to the
 // output when the head has a single unit, or to the workspace, where the fold
-// kernel merges the head's partials.  Every thread of the block must
-// call this (it contains block barriers); threads >= 128 only take part in them.
+// kernel merges the head's partials.  Threads 0..127 do the work (row (tid / 16)
+// mod 8, 16 channels each); the others return at once.
 template <int NW, typename Smem, int RowStride = kHeadDim>
 __device__ __forceinline__ void write_and_fold(const DecodeParams& p, const UnitInfo& ui, Smem& S,
                                                const float* ep_o) {
