@@ -60,6 +60,16 @@ def lib():
         L.orc_query_codes.argtypes = [vp, vp, vp]
         L.orc_query_codes.restype = ctypes.c_float
         L.orc_hybrid_batched.argtypes = [i32, i32, i32] + [vp] * 12 + [i32, i32]
+        L.orc_pack13_plane.argtypes = [vp, vp]
+        L.orc_pack13_plane.restype = i32
+        L.orc_unpack13_plane.argtypes = [vp, i32, vp]
+        L.orc_unpack13_plane.restype = i32
+        L.orc_pack13_page_head.argtypes = [vp, vp, vp]
+        L.orc_pack13_page_head.restype = i32
+        L.orc_unpack13_page_head.argtypes = [vp, vp, vp]
+        L.orc_unpack13_page_head.restype = i32
+        L.orc_pack13_pages.argtypes = [i32, vp, vp, vp, vp, i32, vp]
+        L.orc_pack13_pages.restype = None
         L.orc_hybrid_batched.restype = None
         _lib = L
     return _lib
@@ -141,6 +151,52 @@ def pack_record(kc, vc, s, r, u):
     rec[OFF_KS_TOK:OFF_VS_CHAN] = np.asarray(r, np.float32).view(np.uint8)
     rec[OFF_VS_CHAN:REC_BYTES] = np.asarray(u, np.float32).view(np.uint8)
     return rec
+
+
+# ------------------------------------------------------------------ lossless tier
+PLANE_ENC_BYTES = 26656
+PLANE_RAW_BYTES = 32768
+PACK13_RECORD_BYTES = 16 + 2 * PLANE_RAW_BYTES
+
+
+def pack13_plane(v):
+    """One 64 x 256 plane of BF16 bit patterns -> its 13-bit (or raw) encoding
+    ("model quantization", "A lossless tier first")."""
+    out = np.zeros(PLANE_RAW_BYTES, np.uint8)
+    n = lib().orc_pack13_plane(_p(_c(v, np.uint16)), _p(out))
+    return out[:n].copy()
+
+
+def unpack13_plane(enc):
+    enc = _c(enc, np.uint8)
+    v = np.empty(T_PAGE * D_HEAD, np.uint16)
+    if lib().orc_unpack13_plane(_p(enc), len(enc), _p(v)) != 0:
+        raise ValueError("not a 13-bit or raw plane")
+    return v.reshape(T_PAGE, D_HEAD)
+
+
+def pack13_page_head(k_page, v_page):
+    rec = np.zeros(PACK13_RECORD_BYTES, np.uint8)
+    n = lib().orc_pack13_page_head(_p(_c(k_page, np.uint16)), _p(_c(v_page, np.uint16)), _p(rec))
+    return rec[:n].copy()
+
+
+def unpack13_page_head(rec):
+    rec = _c(rec, np.uint8)
+    k = np.empty((T_PAGE, D_HEAD), np.uint16)
+    v = np.empty((T_PAGE, D_HEAD), np.uint16)
+    if lib().orc_unpack13_page_head(_p(rec), _p(k), _p(v)) != 0:
+        raise ValueError("malformed record")
+    return k, v
+
+
+def pack13_pages(H, k_pool, v_pool, src_slots, dst_slots, pack_pool):
+    """In place into pack_pool (uint8, [n_slots*H*65552]): fixed-stride records."""
+    src = _c(src_slots, np.int32)
+    dst = _c(dst_slots, np.int32)
+    assert pack_pool.flags.c_contiguous and pack_pool.dtype == np.uint8
+    lib().orc_pack13_pages(H, _p(_c(k_pool, np.uint16)), _p(_c(v_pool, np.uint16)), _p(src), _p(dst), len(src),
+                           _p(pack_pool))
 
 
 # ------------------------------------------------------------------ attention

@@ -20,6 +20,9 @@
  *           log-sum-exp) folded into one accumulator; -inf is a valid empty partial.
  *   [TIERS] "ActiveKV", section "The idea": recent context exact, older history
  *           8-bit, joined with exact attention arithmetic.
+ *   [LOSSLESS] "model quantization", section "A lossless tier first": 13 bits per
+ *           value (an 18.7 % saving) with a raw fallback when a plane needs more
+ *           than a 32-entry table.
  *   [IQ]    "SYCL", section "Attention that reads 8-bit history": the kernel keeps
  *           an integer query cache of 8 rows x 256 channels (2 KB) and a
  *           two-by-two experiment decided which products run on integers.
@@ -35,6 +38,9 @@
  *     rint (half to even), clamp to +-127; a zero scale gives zero codes;
  *   - softmax scale 1/sqrt(d), log-sum-exp in natural-log units; an empty range
  *     gives o = 0, lse = -inf;
+ *   - lossless tier: a plane is one page-head's keys (or values); the 32-entry
+ *     table holds the plane's distinct BF16 exponent fields, so a value is its
+ *     sign and mantissa (8 bits) plus a 5-bit table index;
  *   - integer query (the variant with integer QK products): the query folded with
  *     the page's key channel scales, q'_c = q_c s_c, is coded per page and query
  *     row with the absmax rule of the key codes: m = max_c |q'_c|, alpha = m / 127,
@@ -211,6 +217,120 @@ void orc_quantize_pages(int H, const uint16_t* k_pool, const uint16_t* v_pool, c
       int64_t src = ((int64_t)src_slots[p] * H + h) * ph;
       orc_quantize_page_head(k_pool + src, v_pool + src,
                              rec_pool + ((int64_t)dst_slots[p] * H + h) * REC_BYTES);
+    }
+}
+
+/* ============================================================ lossless tier */
+
+/*
+ * Lossless 13-bit plane [LOSSLESS].  A plane is one page-head's keys (or values):
+ * 64 x 256 BF16 values in token-major order.  Each BF16 value is a sign bit, an
+ * 8-bit exponent field and a 7-bit mantissa.  When the plane holds at most 32
+ * distinct exponent fields, each value is stored as its sign and mantissa (one
+ * byte) plus the 5-bit position of its exponent in the plane's table of distinct
+ * exponents (sorted ascending): 8 + 5 = 13 bits per value.  Otherwise the plane is
+ * stored raw (16 bits per value).  Encoded plane, 26,656 bytes:
+ *   u8 table[32]      distinct exponent fields, ascending; unused entries 0   offset 0
+ *   u8 sm[16384]      (sign << 7) | mantissa of value i                     offset 32
+ *   u8 lo4[8192]      index bits 0-3: value 2j in the low nibble of byte j,
+ *                     value 2j + 1 in the high nibble                        offset 16416
+ *   u8 hi1[2048]      index bit 4 of value 8j + b in bit b of byte j          offset 24608
+ * Raw plane, 32,768 bytes: the BF16 values, little-endian.
+ * Page-head record: u32 k_bytes, u32 v_bytes, u32 0, u32 0 (16 bytes), then the
+ * key plane, then the value plane (k_bytes and v_bytes are 26656 or 32768).
+ */
+#define PLANE_VALUES (T_PAGE * D_HEAD)
+#define PLANE_ENC_BYTES 26656
+#define PLANE_RAW_BYTES 32768
+#define P13_HEADER 16
+#define P13_RECORD_BYTES (P13_HEADER + 2 * PLANE_RAW_BYTES)
+
+/* Encode one plane into out; returns the bytes written. */
+int orc_pack13_plane(const uint16_t* v, uint8_t* out) {
+  int present[256] = {0};
+  for (int i = 0; i < PLANE_VALUES; ++i) present[(v[i] >> 7) & 0xFF] = 1;
+  uint8_t table[32];
+  int n = 0;
+  for (int e = 0; e < 256; ++e)
+    if (present[e]) {
+      if (n == 32) { /* a 33rd exponent: raw fallback */
+        for (int i = 0; i < PLANE_VALUES; ++i) {
+          out[2 * i] = (uint8_t)(v[i] & 0xFF);
+          out[2 * i + 1] = (uint8_t)(v[i] >> 8);
+        }
+        return PLANE_RAW_BYTES;
+      }
+      table[n++] = (uint8_t)e;
+    }
+  memset(out, 0, PLANE_ENC_BYTES);
+  for (int k = 0; k < n; ++k) out[k] = table[k];
+  uint8_t* sm = out + 32;
+  uint8_t* lo4 = out + 32 + 16384;
+  uint8_t* hi1 = out + 32 + 16384 + 8192;
+  for (int i = 0; i < PLANE_VALUES; ++i) {
+    int e = (v[i] >> 7) & 0xFF;
+    int idx = 0;
+    while (table[idx] != e) ++idx; /* e is in the table */
+    sm[i] = (uint8_t)(((v[i] >> 8) & 0x80) | (v[i] & 0x7F));
+    lo4[i / 2] |= (uint8_t)((idx & 15) << (4 * (i % 2)));
+    hi1[i / 8] |= (uint8_t)((idx >> 4) << (i % 8));
+  }
+  return PLANE_ENC_BYTES;
+}
+
+/* Decode a plane of nbytes (26656 or 32768) bytes; returns 0, or -1 for any other size. */
+int orc_unpack13_plane(const uint8_t* in, int nbytes, uint16_t* v) {
+  if (nbytes == PLANE_RAW_BYTES) {
+    for (int i = 0; i < PLANE_VALUES; ++i) v[i] = (uint16_t)(in[2 * i] | (in[2 * i + 1] << 8));
+    return 0;
+  }
+  if (nbytes != PLANE_ENC_BYTES) return -1;
+  const uint8_t* sm = in + 32;
+  const uint8_t* lo4 = in + 32 + 16384;
+  const uint8_t* hi1 = in + 32 + 16384 + 8192;
+  for (int i = 0; i < PLANE_VALUES; ++i) {
+    int idx = ((lo4[i / 2] >> (4 * (i % 2))) & 15) | (((hi1[i / 8] >> (i % 8)) & 1) << 4);
+    int e = in[idx];
+    v[i] = (uint16_t)(((sm[i] & 0x80) << 8) | (e << 7) | (sm[i] & 0x7F));
+  }
+  return 0;
+}
+
+static void put_u32(uint8_t* p, uint32_t x) {
+  for (int b = 0; b < 4; ++b) p[b] = (uint8_t)(x >> (8 * b));
+}
+static uint32_t get_u32(const uint8_t* p) {
+  return (uint32_t)p[0] | ((uint32_t)p[1] << 8) | ((uint32_t)p[2] << 16) | ((uint32_t)p[3] << 24);
+}
+
+/* One page-head record (at most 65,552 bytes); returns its size. */
+int orc_pack13_page_head(const uint16_t* k, const uint16_t* v, uint8_t* rec) {
+  memset(rec, 0, P13_HEADER);
+  int kb = orc_pack13_plane(k, rec + P13_HEADER);
+  int vb = orc_pack13_plane(v, rec + P13_HEADER + kb);
+  put_u32(rec, (uint32_t)kb);
+  put_u32(rec + 4, (uint32_t)vb);
+  return P13_HEADER + kb + vb;
+}
+
+/* Inverse of orc_pack13_page_head; returns 0, or -1 for a malformed header. */
+int orc_unpack13_page_head(const uint8_t* rec, uint16_t* k, uint16_t* v) {
+  int kb = (int)get_u32(rec), vb = (int)get_u32(rec + 4);
+  if (orc_unpack13_plane(rec + P13_HEADER, kb, k) != 0) return -1;
+  return orc_unpack13_plane(rec + P13_HEADER + kb, vb, v);
+}
+
+/* Pack n_pages pages of a [slot][H][64][256] BF16 pool into 65,552-byte slots of
+ * pack_pool: page-head (src_slots[i], h) -> slot dst_slots[i] * H + h. */
+void orc_pack13_pages(int H, const uint16_t* k_pool, const uint16_t* v_pool, const int32_t* src_slots,
+                      const int32_t* dst_slots, int n_pages, uint8_t* pack_pool) {
+  const int64_t ph = (int64_t)PLANE_VALUES;
+  for (int p = 0; p < n_pages; ++p)
+    for (int h = 0; h < H; ++h) {
+      int64_t src = ((int64_t)src_slots[p] * H + h) * ph;
+      uint8_t* rec = pack_pool + ((int64_t)dst_slots[p] * H + h) * P13_RECORD_BYTES;
+      memset(rec, 0, P13_RECORD_BYTES);
+      orc_pack13_page_head(k_pool + src, v_pool + src, rec);
     }
 }
 
