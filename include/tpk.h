@@ -54,7 +54,8 @@ typedef enum {
   TPK_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed */
   TPK_ERR_BOUNDS = 4,      /* a kernel met a page-table entry outside the pool */
   TPK_ERR_NOMEM = 5,       /* a caller-provided buffer is smaller than required */
-  TPK_ERR_TIMEOUT = 6      /* reserved: a bounded device-side wait gave up */
+  TPK_ERR_TIMEOUT = 6,     /* a bounded device-side wait gave up */
+  TPK_ERR_FORMAT = 7       /* a kernel met a malformed 13-bit record */
 } tpk_status;
 
 /* Which dot-product engine the decode kernels use. */
@@ -132,6 +133,52 @@ tpk_status tpk_kv_quantize_pages_given_scales(const tpk_shape* shape, const void
                                               const int32_t* src_slots, const int32_t* dst_slots, int n_pages,
                                               const float* ks_chan, const float* ks_tok, const float* vs_chan,
                                               void* rec_pool, tpk_stream_t stream);
+
+/*
+ * Lossless 13-bit page format ("model quantization", section "A lossless tier
+ * first": 13 bits per value, an 18.7 % saving, with a raw fallback when a plane
+ * needs more than a 32-entry table).  A plane is one page-head's keys (or values):
+ * 64 x 256 BF16 values, token-major.  A plane with at most 32 distinct exponent
+ * fields is stored encoded (TPK_PACK13_PLANE_ENC bytes):
+ *   u8 table[32]    the distinct exponent fields, ascending; unused entries 0  offset 0
+ *   u8 sm[16384]    value i: (sign << 7) | 7-bit mantissa                     offset 32
+ *   u8 lo4[8192]    table index bits 0-3: value 2j low nibble of byte j,
+ *                   value 2j + 1 high nibble                                    offset 16416
+ *   u8 hi1[2048]    table index bit 4 of value 8j + b in bit b of byte j        offset 24608
+ * (8 + 5 bits per value), otherwise raw: the BF16 values (TPK_PACK13_PLANE_RAW
+ * bytes).  A page-head record is a 16-byte header (u32 key-plane bytes, u32
+ * value-plane bytes, two zero words) followed by the key plane and the value
+ * plane; its size is 16 + both plane sizes, at most TPK_PACK13_RECORD_BYTES.
+ */
+#define TPK_PACK13_PLANE_ENC 26656
+#define TPK_PACK13_PLANE_RAW 32768
+#define TPK_PACK13_RECORD_BYTES 65552
+
+/*
+ * Pack n_pages BF16 pages into 13-bit records: page-head (src_slots[i], h) of
+ * k_pool / v_pool -> record at pack_pool + (dst_slots[i] * H + h) *
+ * TPK_PACK13_RECORD_BYTES (fixed-stride slots; the bytes of a slot past its
+ * record's size are left unchanged).  src_slots, dst_slots: dev int32[n_pages];
+ * pack_slots bounds dst_slots (0 = unchecked), shape->kv_slots bounds src_slots.
+ * Pools 16-byte aligned.  An out-of-range slot skips that page-head and sets bit 0
+ * of the device status word.  Lossless: tpk_kv_unpack13_pages restores every bit.
+ */
+tpk_status tpk_kv_pack13_pages(const tpk_shape* shape, const void* k_pool, const void* v_pool,
+                               const int32_t* src_slots, const int32_t* dst_slots, int n_pages, void* pack_pool,
+                               int64_t pack_slots, tpk_stream_t stream);
+
+/*
+ * Unpack n_pages pages of 13-bit records into BF16 pools: the record of page i,
+ * KV head h starts rec_offsets[i * H + h] bytes into src (dev int64; 16-byte
+ * aligned; fixed-stride slots or a compacted image alike) and is written to page
+ * (dst_slots[i], h) of k_pool / v_pool.  src_bytes bounds the records (0 =
+ * unchecked); shape->kv_slots bounds dst_slots.  A record whose header or extent
+ * is invalid is skipped and sets bit 2 of the device status word (TPK_ERR_FORMAT
+ * from tpk_get_device_status); an out-of-range slot sets bit 0.
+ */
+tpk_status tpk_kv_unpack13_pages(const tpk_shape* shape, const void* src, int64_t src_bytes,
+                                 const int64_t* rec_offsets, const int32_t* dst_slots, int n_pages, void* k_pool,
+                                 void* v_pool, tpk_stream_t stream);
 
 /*
  * Exact-tier partial attention ("SYCL", section "A merge that joins the tiers":
@@ -323,8 +370,11 @@ tpk_status tpk_tiers_sync(tpk_tiers* tiers);
 tpk_status tpk_tiers_destroy(tpk_tiers* tiers);
 
 /*
- * Device status word: bit 0 = a page-table entry outside the pool was skipped.
- * Synchronises `stream`, stores the word in *flags and, if reset != 0, clears it.
+ * Device status word: bit 0 = a page-table entry outside the pool was skipped,
+ * bit 1 = a bounded device-side wait gave up, bit 2 = a malformed 13-bit record was
+ * skipped.  Synchronises `stream`, stores the word in *flags and, if reset != 0,
+ * clears it; returns TPK_ERR_TIMEOUT, TPK_ERR_BOUNDS or TPK_ERR_FORMAT (in that
+ * order of precedence) when a bit is set.
  */
 tpk_status tpk_get_device_status(int* flags, int reset, tpk_stream_t stream);
 

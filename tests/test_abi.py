@@ -71,6 +71,21 @@ def test_bad_ranges_and_pointers_are_rejected(L):
     assert L.tpk_kv_quantize_pages_given_scales(ctypes.byref(s), 16, 16, 16, 16, 1, None, 16, 16, 16, None) == 1
 
 
+def test_pack13_arguments_are_validated_before_any_device_call(L):
+    s = tpk.Shape(4)
+    assert L.tpk_kv_pack13_pages(ctypes.byref(s), 16, 16, 16, 16, -1, 16, 0, None) == 1
+    assert L.tpk_kv_pack13_pages(ctypes.byref(s), 16, 16, 16, 16, 0, 16, 0, None) == 0   # nothing to do
+    assert L.tpk_kv_pack13_pages(ctypes.byref(s), 16, 16, 16, 16, 1, 16, -2, None) == 1
+    assert L.tpk_kv_pack13_pages(ctypes.byref(s), 16, None, 16, 16, 1, 16, 0, None) == 1
+    assert L.tpk_kv_pack13_pages(ctypes.byref(s), 16, 16, 16, 16, 1, 24, 0, None) == 1
+    assert "aligned" in err(L)
+    assert L.tpk_kv_unpack13_pages(ctypes.byref(s), 16, -1, 16, 16, 1, 16, 16, None) == 1
+    assert L.tpk_kv_unpack13_pages(ctypes.byref(s), 16, 0, None, 16, 1, 16, 16, None) == 1
+    assert L.tpk_kv_unpack13_pages(ctypes.byref(s), 8, 0, 16, 16, 1, 16, 16, None) == 1
+    assert L.tpk_kv_unpack13_pages(ctypes.byref(s), 16, 0, 16, 16, -3, 16, 16, None) == 1
+    assert L.tpk_kv_unpack13_pages(ctypes.byref(tpk.Shape(4, group=4)), 16, 0, 16, 16, 1, 16, 16, None) == 2
+
+
 def test_hybrid_host_metadata_is_validated(L):
     s = tpk.Shape(2)
     need = L.tpk_hybrid_workspace_bytes(ctypes.byref(s), 2)

@@ -21,12 +21,14 @@ __all__ = [
     "kv_quantize_pages", "kv_quantize_pages_given_scales", "decode_attn_exact", "decode_attn_int8",
     "merge_lse", "hybrid_workspace_bytes", "workspace_init", "decode_hybrid_batched", "get_device_status",
     "static_scratch_bytes", "decode_hybrid_batched_static", "Stager", "Tiers", "TiersPlan",
+    "PACK13_RECORD_BYTES", "PACK13_PLANE_ENC", "PACK13_PLANE_RAW", "kv_pack13_pages", "kv_unpack13_pages",
 ]
 
 RECORD_BYTES = 35072
+PACK13_RECORD_BYTES, PACK13_PLANE_ENC, PACK13_PLANE_RAW = 65552, 26656, 32768
 IMPL_DEFAULT, IMPL_SIMT, IMPL_TENSOR = 0, 1, 2
 STATUS_NAMES = {0: "TPK_OK", 1: "TPK_ERR_INVALID", 2: "TPK_ERR_UNSUPPORTED", 3: "TPK_ERR_CUDA",
-                4: "TPK_ERR_BOUNDS", 5: "TPK_ERR_NOMEM", 6: "TPK_ERR_TIMEOUT"}
+                4: "TPK_ERR_BOUNDS", 5: "TPK_ERR_NOMEM", 6: "TPK_ERR_TIMEOUT", 7: "TPK_ERR_FORMAT"}
 
 
 class Shape(ctypes.Structure):
@@ -71,6 +73,9 @@ def lib():
         L.tpk_last_error_string.restype = ctypes.c_char_p
         L.tpk_kv_quantize_pages.argtypes = [sp, vp, vp, vp, vp, i32, vp, vp]
         L.tpk_kv_quantize_pages_given_scales.argtypes = [sp, vp, vp, vp, vp, i32, vp, vp, vp, vp, vp]
+        i64 = ctypes.c_int64
+        L.tpk_kv_pack13_pages.argtypes = [sp, vp, vp, vp, vp, i32, vp, i64, vp]
+        L.tpk_kv_unpack13_pages.argtypes = [sp, vp, i64, vp, vp, i32, vp, vp, vp]
         L.tpk_decode_attn_exact.argtypes = [sp, vp, vp, vp, vp, i32, i32, i32, vp, vp, vp]
         L.tpk_decode_attn_int8.argtypes = [sp, vp, vp, vp, i32, i32, i32, vp, vp, vp]
         L.tpk_merge_lse.argtypes = [i32, i32, i32, vp, vp, vp, vp, vp]
@@ -103,7 +108,8 @@ def lib():
         for name in ("tpk_tiers_create", "tpk_tiers_update", "tpk_tiers_step", "tpk_tiers_sync",
                      "tpk_tiers_destroy"):
             getattr(L, name).restype = i32
-        for name in ("tpk_kv_quantize_pages", "tpk_kv_quantize_pages_given_scales", "tpk_decode_attn_exact",
+        for name in ("tpk_kv_quantize_pages", "tpk_kv_quantize_pages_given_scales", "tpk_kv_pack13_pages",
+                     "tpk_kv_unpack13_pages", "tpk_decode_attn_exact",
                      "tpk_decode_attn_int8", "tpk_merge_lse", "tpk_workspace_init", "tpk_decode_hybrid_batched",
                      "tpk_get_device_status", "tpk_decode_hybrid_batched_static"):
             getattr(L, name).restype = i32
@@ -149,6 +155,17 @@ def kv_quantize_pages_given_scales(shape, k_pool, v_pool, src_slots, dst_slots, 
     _check(lib().tpk_kv_quantize_pages_given_scales(ctypes.byref(shape), _ptr(k_pool), _ptr(v_pool),
                                                     _ptr(src_slots), _ptr(dst_slots), int(n_pages), _ptr(ks_chan),
                                                     _ptr(ks_tok), _ptr(vs_chan), _ptr(rec_pool), _stream(stream)))
+
+
+def kv_pack13_pages(shape, k_pool, v_pool, src_slots, dst_slots, n_pages, pack_pool, pack_slots=0, stream=None):
+    _check(lib().tpk_kv_pack13_pages(ctypes.byref(shape), _ptr(k_pool), _ptr(v_pool), _ptr(src_slots),
+                                     _ptr(dst_slots), int(n_pages), _ptr(pack_pool), int(pack_slots),
+                                     _stream(stream)))
+
+
+def kv_unpack13_pages(shape, src, src_bytes, rec_offsets, dst_slots, n_pages, k_pool, v_pool, stream=None):
+    _check(lib().tpk_kv_unpack13_pages(ctypes.byref(shape), _ptr(src), int(src_bytes), _ptr(rec_offsets),
+                                       _ptr(dst_slots), int(n_pages), _ptr(k_pool), _ptr(v_pool), _stream(stream)))
 
 
 def decode_attn_exact(shape, q, k_pool, v_pool, page_table, tok_begin, tok_end, num_splits, o_part, lse_part,

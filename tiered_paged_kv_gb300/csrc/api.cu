@@ -471,6 +471,65 @@ tpk_status tpk_get_device_status(int* flags, int reset, tpk_stream_t stream) {
   }
   if (*flags & kStatusTimeout) return fail(TPK_ERR_TIMEOUT, "a device-side wait gave up (status %d)", *flags);
   if (*flags & kStatusBadSlot) return fail(TPK_ERR_BOUNDS, "a page-table entry outside the pool was skipped");
+  if (*flags & kStatusBadRecord) return fail(TPK_ERR_FORMAT, "a malformed 13-bit record was skipped");
+  return TPK_OK;
+}
+
+tpk_status tpk_kv_pack13_pages(const tpk_shape* shape, const void* k_pool, const void* v_pool,
+                               const int32_t* src_slots, const int32_t* dst_slots, int n_pages, void* pack_pool,
+                               int64_t pack_slots, tpk_stream_t stream) {
+  tpk_status st = check_shape(shape);
+  if (st != TPK_OK) return st;
+  if (n_pages < 0) return fail(TPK_ERR_INVALID, "n_pages %d < 0", n_pages);
+  if (pack_slots < 0) return fail(TPK_ERR_INVALID, "pack_slots %lld < 0", (long long)pack_slots);
+  if (n_pages == 0) return TPK_OK;
+  if (!k_pool || !v_pool || !src_slots || !dst_slots || !pack_pool) return fail(TPK_ERR_INVALID, "null pointer argument");
+  if (!aligned16(k_pool) || !aligned16(v_pool) || !aligned16(pack_pool))
+    return fail(TPK_ERR_INVALID, "pools must be 16-byte aligned");
+  if ((int64_t)n_pages * shape->kv_heads > 0x7fffffffLL) return fail(TPK_ERR_INVALID, "too many pages");
+  int* status = status_ptr();
+  if (!status) return fail(TPK_ERR_CUDA, "cannot resolve the device status word");
+  Pack13Params p;
+  p.k_pool = static_cast<const uint16_t*>(k_pool);
+  p.v_pool = static_cast<const uint16_t*>(v_pool);
+  p.src = src_slots;
+  p.dst = dst_slots;
+  p.out = static_cast<uint8_t*>(pack_pool);
+  p.kv_slots = shape->kv_slots;
+  p.out_slots = pack_slots;
+  p.status = status;
+  p.H = shape->kv_heads;
+  cudaError_t e = launch_pack13(p, n_pages, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "pack13 launch");
+  return TPK_OK;
+}
+
+tpk_status tpk_kv_unpack13_pages(const tpk_shape* shape, const void* src, int64_t src_bytes,
+                                 const int64_t* rec_offsets, const int32_t* dst_slots, int n_pages, void* k_pool,
+                                 void* v_pool, tpk_stream_t stream) {
+  tpk_status st = check_shape(shape);
+  if (st != TPK_OK) return st;
+  if (n_pages < 0) return fail(TPK_ERR_INVALID, "n_pages %d < 0", n_pages);
+  if (src_bytes < 0) return fail(TPK_ERR_INVALID, "src_bytes %lld < 0", (long long)src_bytes);
+  if (n_pages == 0) return TPK_OK;
+  if (!src || !rec_offsets || !dst_slots || !k_pool || !v_pool) return fail(TPK_ERR_INVALID, "null pointer argument");
+  if (!aligned16(src) || !aligned16(k_pool) || !aligned16(v_pool))
+    return fail(TPK_ERR_INVALID, "src and pools must be 16-byte aligned");
+  if ((int64_t)n_pages * shape->kv_heads > 0x7fffffffLL) return fail(TPK_ERR_INVALID, "too many pages");
+  int* status = status_ptr();
+  if (!status) return fail(TPK_ERR_CUDA, "cannot resolve the device status word");
+  Unpack13Params p;
+  p.src = static_cast<const uint8_t*>(src);
+  p.offsets = rec_offsets;
+  p.src_bytes = src_bytes;
+  p.dst = dst_slots;
+  p.k_pool = static_cast<uint16_t*>(k_pool);
+  p.v_pool = static_cast<uint16_t*>(v_pool);
+  p.kv_slots = shape->kv_slots;
+  p.status = status;
+  p.H = shape->kv_heads;
+  cudaError_t e = launch_unpack13(p, n_pages, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "unpack13 launch");
   return TPK_OK;
 }
 

@@ -137,6 +137,36 @@ __device__ __forceinline__ UnitInfo decode_unit(const DecodeParams& p, const Req
 
 // Page conversion launch parameters (given-scale arrays are null for a full
 // conversion).
+// 13-bit lossless records (pack13.cu)
+constexpr int kStatusBadRecord = 4;
+
+struct Pack13Params {
+  const uint16_t* k_pool;
+  const uint16_t* v_pool;
+  const int32_t* src;
+  const int32_t* dst;
+  uint8_t* out;
+  int64_t kv_slots;   // 0 = unchecked
+  int64_t out_slots;  // 0 = unchecked
+  int* status;
+  int H;
+};
+
+struct Unpack13Params {
+  const uint8_t* src;
+  const int64_t* offsets;  // per page-head, bytes
+  int64_t src_bytes;       // 0 = unchecked
+  const int32_t* dst;
+  uint16_t* k_pool;
+  uint16_t* v_pool;
+  int64_t kv_slots;  // 0 = unchecked
+  int* status;
+  int H;
+};
+
+cudaError_t launch_pack13(const Pack13Params& p, int n_pages, cudaStream_t stream);
+cudaError_t launch_unpack13(const Unpack13Params& p, int n_pages, cudaStream_t stream);
+
 struct QuantParams {
   const uint16_t* k_pool;
   const uint16_t* v_pool;

@@ -27,6 +27,7 @@ BF16_NAN = 0x7FC0
 PAGE_TOKENS = 64
 HEAD_DIM = 256
 RECORD_BYTES = 35072
+PACK13_RECORD_BYTES = 65552  # fixed-stride slot of a 13-bit page-head record
 
 # tensor ids of the generator streams
 TID_Q, TID_K, TID_V, TID_SIGK, TID_SIGV, TID_OUTLIER, TID_SLOTS, TID_LENS, TID_SPLIT = range(1, 10)
@@ -165,13 +166,19 @@ class Workload:
         s = [np.asarray(self.pages[b][:self.n8[b]]) for b in range(self.B)]
         return np.concatenate(s).astype(np.int32) if s else np.zeros(0, np.int32)
 
-    def packed_image(self, rec_pool):
+    def packed_image(self, rec_pool, pack13_pool=None):
         """One step's history packed for host-resident staging: the 8-bit records
         (from rec_pool, [n_slots][H] records) and exact-tier BF16 pages of every
         request in page order, then q and identity page tables, each part at a
         256-byte-aligned offset of one byte image.  Returns (image uint8, off) where
         off maps 'rec', 'k', 'v', 'q', 'pt', 'pt8' to byte offsets, and holds the
-        CSR arrays 'req_page_off', 'req_page_off8' and the page counts."""
+        CSR arrays 'req_page_off', 'req_page_off8' and the page counts.
+
+        With pack13_pool (fixed-stride 13-bit records of the exact-tier pages,
+        [n_slots][H][65552] bytes) the exact tier travels as those records instead,
+        each cut to its size (header words 0 and 1) and 16-byte aligned: part 'p13'
+        holds them in (page, head) order and part 'p13off' their int64 offsets
+        relative to 'p13'; 'k' and 'v' are then empty."""
         H = self.H
         rb = RECORD_BYTES * H
         s8 = self.int8_slots()
@@ -179,9 +186,25 @@ class Workload:
                 else np.zeros(0, np.uint8))
         ex, off_e = self.exact_page_table()
         _, off_8 = self.int8_page_table()
-        parts = [("rec", recs),
-                 ("k", self.k_pool[ex].reshape(-1).view(np.uint8)),
-                 ("v", self.v_pool[ex].reshape(-1).view(np.uint8)),
+        empty = np.zeros(0, np.uint8)
+        p13 = p13off = empty
+        if pack13_pool is not None:
+            pool = np.asarray(pack13_pool, np.uint8).reshape(self.n_slots, H, PACK13_RECORD_BYTES)
+            chunks, offs, pos = [], [], 0
+            for slot in ex:
+                for h in range(H):
+                    r = pool[slot, h]
+                    size = 16 + int(r[0:4].view(np.uint32)[0]) + int(r[4:8].view(np.uint32)[0])
+                    offs.append(pos)
+                    chunks.append(r[:size])
+                    pos += (size + 15) & ~15
+                    if size & 15:
+                        chunks.append(np.zeros(16 - (size & 15), np.uint8))
+            p13 = np.concatenate(chunks) if chunks else empty
+            p13off = np.asarray(offs, np.int64).view(np.uint8)
+        exact_k = self.k_pool[ex].reshape(-1).view(np.uint8) if pack13_pool is None else empty
+        exact_v = self.v_pool[ex].reshape(-1).view(np.uint8) if pack13_pool is None else empty
+        parts = [("rec", recs), ("k", exact_k), ("v", exact_v), ("p13", p13), ("p13off", p13off),
                  ("q", self.q.reshape(-1).view(np.uint8)),
                  ("pt", np.arange(len(ex), dtype=np.int32).view(np.uint8)),
                  ("pt8", np.arange(len(s8), dtype=np.int32).view(np.uint8))]
@@ -194,7 +217,7 @@ class Workload:
         for name, a in parts:
             img[off[name]:off[name] + a.size] = a
         off.update(req_page_off=off_e, req_page_off8=off_8, n_exact_pages=len(ex), n_int8_pages=len(s8),
-                   nbytes=int(pos))
+                   nbytes=int(pos), p13_bytes=int(p13.size))
         return img, off
 
     def history_bytes(self):
