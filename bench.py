@@ -587,17 +587,23 @@ def host_mem_available():
     return 0
 
 
-def run_host_resident(args, w, rec_dev, shape, stream, dev, dist, layers=None, steps=None, label=None):
+def run_host_resident(args, w, rec_dev, shape, stream, dev, dist, layers=None, steps=None, label=None,
+                      pack13_dev=None):
     """Many layers of the same-sized history in pinned host memory (one image per
     layer; the content of every layer is this workload's), two device slots: per
     step every layer is staged while the previous layer decodes.  Bound by the
-    host->device link; the link peak is a plain 1 GiB pinned copy in the same run."""
+    host->device link; the link peak is a plain 1 GiB pinned copy in the same run.
+    With pack13_dev (the exact pages' 13-bit records) the exact tier travels as
+    compacted 13-bit records and is unpacked into a BF16 scratch pool before each
+    layer's decode."""
     import torch
 
     import tiered_paged_kv_gb300 as tpk
 
     H, G = w.H, w.G
-    img, off = w.packed_image(rec_dev.cpu().numpy())
+    img, off = w.packed_image(rec_dev.cpu().numpy(),
+                              None if pack13_dev is None else pack13_dev.cpu().numpy())
+    lossless = pack13_dev is not None
     layers = args.layers if layers is None else layers
     steps = args.host_steps if steps is None else steps
     avail = host_mem_available()
@@ -616,6 +622,12 @@ def run_host_resident(args, w, rec_dev, shape, stream, dev, dist, layers=None, s
     outs = [(torch.empty(1, H * G, 256, dtype=torch.float32, device=dev),
              torch.empty(1, H * G, dtype=torch.float32, device=dev)) for _ in range(layers)]
     views = [slot_views(s, off, w) for s in slots]
+    ne = off["n_exact_pages"]
+    if lossless:  # BF16 scratch pool the staged records are unpacked into, reused layer after layer
+        k13 = torch.empty(max(ne, 1) * H * 64 * 256, dtype=torch.int16, device=dev)
+        v13 = torch.empty_like(k13)
+        p13 = [(sl[off["p13"]:off["p13"] + off["p13_bytes"]], sl[off["p13off"]:off["p13off"] + 8 * ne * H])
+               for sl in slots]
     st = tpk.Stager(slots, off["nbytes"])
 
     def one_step():
@@ -625,6 +637,10 @@ def run_host_resident(args, w, rec_dev, shape, stream, dev, dist, layers=None, s
             slot, _ = pending
             st.acquire(slot, stream)
             rec, k, v, q, pt, pt8 = views[slot]
+            if lossless:
+                tpk.kv_unpack13_pages(shape2, p13[slot][0], off["p13_bytes"], p13[slot][1], pt, ne, k13, v13,
+                                      stream)
+                k, v = k13, v13
             tpk.decode_hybrid_batched(shape2, 1, q, k, v, rec, pt, off["req_page_off"], w.n_ex, pt8,
                                       off["req_page_off8"], w.n8, outs[l][0], outs[l][1], ws, nbytes, stream)
             st.release(slot, stream)
@@ -657,6 +673,9 @@ def run_host_resident(args, w, rec_dev, shape, stream, dev, dist, layers=None, s
             del big_h, big_d
     finally:
         st.close()
+    status, flags = tpk.get_device_status(reset=True, stream=stream)
+    if status != 0:
+        raise RuntimeError(f"device status {status} flags {flags} (host-resident)")
     ms = statistics.median(times)
     ms = max_over_ranks(dist, ms)
     link = layers * off["nbytes"] / (ms * 1e-3) / 1e9
@@ -733,6 +752,116 @@ def run_gate_sweep(args):
         rows.append(row)
         print(json.dumps(row), flush=True, file=sys.stderr)
     print(json.dumps({"mode": "gate_sweep", "hbm_peak_GBps": peak, "rows": rows}), flush=True)
+
+
+def run_lossless(args):
+    """The lossless 13-bit exact tier as a third candidate format for the gate: per
+    history length, one request of all-BF16 history (4 KV heads x 8 q rows,
+    outlier keys, seed 20).  Page packing and unpacking rates (median of 5, L2
+    flushed), the device step unpack + decode against decode alone, and the
+    host-resident step per layer with the exact tier staged as BF16 or as
+    compacted 13-bit records (unpacked on the device before the decode)."""
+    import torch
+
+    import tiered_paged_kv_gb300 as tpk
+    from tiered_paged_kv_gb300 import build as tbuild
+    from tiered_paged_kv_gb300 import synth
+
+    torch.cuda.set_device(0)
+    tbuild.build()
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.Stream(dev)
+    R = tpk.PACK13_RECORD_BYTES
+    with torch.cuda.stream(stream):
+        flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+        flush_r = torch.zeros(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    peak, _ = hbm_peak()
+
+    def timed(fn, reps=5):
+        ev = []
+        with torch.cuda.stream(stream):
+            fn()
+            for i in range(reps):
+                flush.fill_(float(i))
+                flush_r.max()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                fn()
+                b.record(stream)
+                ev.append((a, b))
+            stream.synchronize()
+        return statistics.median([a.elapsed_time(b) for a, b in ev])
+
+    rows = []
+    for n in [int(x) for x in args.gate_lengths.split(",")]:
+        w = synth.make_workload([n], None, H=4, seed=20, key_sigma="outliers")
+        H, G = w.H, w.G
+        shape = tpk.Shape(H, kv_slots=w.n_slots, rec_slots=w.n_slots)
+        ex, off_e = w.exact_page_table()
+        ne = len(ex)
+        with torch.cuda.stream(stream):
+            kp = torch.from_numpy(w.k_pool.view(np.int16)).to(dev)
+            vp = torch.from_numpy(w.v_pool.view(np.int16)).to(dev)
+            q = torch.from_numpy(w.q.view(np.int16)).to(dev)
+            rec = torch.zeros(16, dtype=torch.uint8, device=dev)
+            pool = torch.zeros(w.n_slots * H * R, dtype=torch.uint8, device=dev)
+            k2 = torch.zeros_like(kp)
+            v2 = torch.zeros_like(vp)
+            ex_d = torch.from_numpy(ex.astype(np.int32)).to(dev)
+            offs = (np.repeat(ex.astype(np.int64), H) * H + np.tile(np.arange(H), ne)) * R
+            offs_d = torch.from_numpy(offs).to(dev)
+            pt_d = torch.from_numpy(np.concatenate([ex.astype(np.int32), np.zeros(1, np.int32)])).to(dev)
+            pt8_d = torch.zeros(1, dtype=torch.int32, device=dev)
+            off8 = np.zeros(2, np.int32)
+            o = torch.empty(1, H * G, 256, dtype=torch.float32, device=dev)
+            lse = torch.empty(1, H * G, dtype=torch.float32, device=dev)
+            nbytes = tpk.hybrid_workspace_bytes(shape, 1)
+            ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+
+        def pack():
+            tpk.kv_pack13_pages(shape, kp, vp, ex_d, ex_d, ne, pool, w.n_slots, stream)
+
+        def unpack():
+            tpk.kv_unpack13_pages(shape, pool, pool.numel(), offs_d, ex_d, ne, k2, v2, stream)
+
+        def decode(k, v):
+            tpk.decode_hybrid_batched(shape, 1, q, k, v, rec, pt_d, off_e, w.n_ex, pt8_d, off8, w.n8, o, lse, ws,
+                                      nbytes, stream)
+
+        pack_ms = timed(pack)
+        host = pool.cpu().numpy().reshape(w.n_slots, H, R)
+        sizes = [16 + int(host[s, h, 0:4].view(np.uint32)[0]) + int(host[s, h, 4:8].view(np.uint32)[0])
+                 for s in ex for h in range(H)]
+        compact = int(sum((z + 15) & ~15 for z in sizes))
+        bf16 = ne * H * 65536
+        unpack_ms = timed(unpack)
+        dec_ms = statistics.median(graph_times(lambda: decode(kp, vp), 20, 3, stream, flush, flush_r))
+        both_ms = statistics.median(graph_times(lambda: (unpack(), decode(k2, v2)), 20, 3, stream, flush,
+                                                flush_r))
+        st, flags = tpk.get_device_status(reset=True, stream=stream)
+        if st != 0:
+            raise RuntimeError(f"device status {st} flags {flags} (lossless {n})")
+        hr_bf16 = run_host_resident(args, w, rec, shape, stream, dev, None, layers=args.gate_layers, steps=3,
+                                    label=f"{args.gate_layers} layers x {n} tokens BF16")
+        hr_13 = run_host_resident(args, w, rec, shape, stream, dev, None, layers=args.gate_layers, steps=3,
+                                  label=f"{args.gate_layers} layers x {n} tokens 13-bit", pack13_dev=pool)
+        row = {"tokens": n, "bf16_bytes": bf16, "pack13_bytes": compact, "saving": round(1 - compact / bf16, 4),
+               "planes_raw": int(sum((z - 16 - 2 * 26656) // (32768 - 26656) for z in sizes)),
+               "pack_us": round(pack_ms * 1e3, 1),
+               "pack_GBps": round((bf16 + compact) / (pack_ms * 1e-3) / 1e9, 1),
+               "unpack_us": round(unpack_ms * 1e3, 1),
+               "unpack_GBps": round((bf16 + compact) / (unpack_ms * 1e-3) / 1e9, 1),
+               "hbm_peak_GBps": peak,
+               "device_decode_us": round(dec_ms * 1e3, 2), "device_unpack_decode_us": round(both_ms * 1e3, 2),
+               "host_ms_per_layer_bf16": round(hr_bf16["ms_per_step"] / hr_bf16["layers"], 4),
+               "host_ms_per_layer_13bit": round(hr_13["ms_per_step"] / hr_13["layers"], 4),
+               "link_GBps_bf16": hr_bf16["link_GBps"], "link_GBps_13bit": hr_13["link_GBps"],
+               "link_peak_GBps": hr_13["link_peak_GBps"]}
+        row["host_speedup"] = round(row["host_ms_per_layer_bf16"] / row["host_ms_per_layer_13bit"], 3)
+        rows.append(row)
+        print(json.dumps(row), flush=True, file=sys.stderr)
+        del kp, vp, q, pool, k2, v2, ws
+    print(json.dumps({"mode": "lossless_gate", "rows": rows}), flush=True)
 
 
 def run_tiers_loop(args):
@@ -875,6 +1004,9 @@ def main():
     ap.add_argument("--gate-sweep", action="store_true",
                     help="instead of the bench line: exact vs hybrid over history lengths (device and host-resident)")
     ap.add_argument("--gate-lengths", default="8192,16384,32768,65536,131072")
+    ap.add_argument("--lossless", action="store_true",
+                    help="lossless 13-bit exact tier against BF16 over --gate-lengths (pack, unpack, device and "
+                         "host-resident steps)")
     ap.add_argument("--gate-layers", type=int, default=4)
     ap.add_argument("--tiers-loop", action="store_true",
                     help="instead of the bench line: a decode loop with incremental conversion and publication")
@@ -888,6 +1020,8 @@ def main():
             run_reference(args, dist, rank, world)
         elif args.gate_sweep:
             run_gate_sweep(args)
+        elif args.lossless:
+            run_lossless(args)
         elif args.tiers_loop:
             run_tiers_loop(args)
         else:
