@@ -621,53 +621,29 @@ __device__ __forceinline__ void fused_fold(const DecodeParams& p, const ReqPlan&
     const int row0 = hid * G;  // first output row of this head
     const int e0 = ui.unit_in_head * G * kHeadDim / n, e1 = (ui.unit_in_head + 1) * G * kHeadDim / n;
     const int r0 = e0 / kHeadDim, r1 = (e1 - 1) / kHeadDim;
-    float* w = scratch;                            // [G][kFusedFoldMax] merge weights
+    float* w = scratch;                       // [G][kFusedFoldMax]
     float* row_lse = scratch + G * kFusedFoldMax;  // [G]
     const float ninf = -__builtin_huge_valf();
-    // each thread's first element: every partial's value is requested now, before
-    // the weights exist (one L2 round trip for both)
-    const int e_first = e0 + tid;
-    float v[kFusedFoldMax];
-    {
-      const int r = min(e_first, e1 - 1) / kHeadDim, c = min(e_first, e1 - 1) % kHeadDim;
-      const float* src = p.part_o + ((int64_t)first * G + r) * kHeadDim + c;
-#pragma unroll
-      for (int i = 0; i < kFusedFoldMax; ++i)
-        v[i] = (i < n && e_first < e1) ? __ldcg(src + (int64_t)i * G * kHeadDim) : 0.f;
-    }
-    // warp r - r0 computes row r's weights: lane l holds partials l and l + 32, max
-    // and sum by shuffles
-    const int warp = tid >> 5, lane = tid & 31;
-    if (warp <= r1 - r0) {
-      const int r = r0 + warp;
-      const float la = lane < n ? __ldcg(p.part_lse + (first + lane) * G + r) : ninf;
-      const float lb = lane + 32 < n ? __ldcg(p.part_lse + (first + lane + 32) * G + r) : ninf;
-      float M = fmaxf(la, lb);
-#pragma unroll
-      for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-      const float wa = (la == ninf) ? 0.f : expf(la - M), wb = (lb == ninf) ? 0.f : expf(lb - M);
-      float L = wa + wb;
-#pragma unroll
-      for (int off = 16; off >= 1; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
-      const bool empty = (M == ninf);
-      if (lane < n) w[r * kFusedFoldMax + lane] = empty ? 0.f : wa / L;
-      if (lane + 32 < n) w[r * kFusedFoldMax + lane + 32] = empty ? 0.f : wb / L;
-      if (lane == 0) row_lse[r] = empty ? ninf : M + logf(L);
+    if (tid <= r1 - r0) {
+      const int r = r0 + tid;
+      float M = ninf;
+      for (int i = 0; i < n; ++i) M = fmaxf(M, __ldcg(p.part_lse + (first + i) * G + r));
+      float L = 0.f;
+      for (int i = 0; i < n; ++i) {
+        const float li = __ldcg(p.part_lse + (first + i) * G + r);
+        const float wi = (li == ninf) ? 0.f : expf(li - M);
+        w[r * kFusedFoldMax + i] = wi;
+        L += wi;
+      }
+      for (int i = 0; i < n; ++i) w[r * kFusedFoldMax + i] = M == ninf ? 0.f : w[r * kFusedFoldMax + i] / L;
+      row_lse[r] = M == ninf ? ninf : M + logf(L);
     }
     __syncthreads();
-    // sum in unit order; heads of fewer than 8 units leave more than one element
-    // per thread
-    for (int e = e_first; e < e1; e += blockDim.x) {
+    for (int e = e0 + tid; e < e1; e += blockDim.x) {
       const int r = e / kHeadDim, c = e % kHeadDim;
-      if (e != e_first) {
-        const float* src = p.part_o + ((int64_t)first * G + r) * kHeadDim + c;
-#pragma unroll
-        for (int i = 0; i < kFusedFoldMax; ++i) v[i] = i < n ? __ldcg(src + (int64_t)i * G * kHeadDim) : 0.f;
-      }
+      const float* src = p.part_o + ((int64_t)first * G + r) * kHeadDim + c;
       float acc = 0.f;
-#pragma unroll
-      for (int i = 0; i < kFusedFoldMax; ++i)
-        if (i < n) acc += w[r * kFusedFoldMax + i] * v[i];
+      for (int i = 0; i < n; ++i) acc += w[r * kFusedFoldMax + i] * __ldcg(src + (int64_t)i * G * kHeadDim);
       p.out_o[(int64_t)(row0 + r) * kHeadDim + c] = acc;
       if (c == 0) p.out_lse[row0 + r] = row_lse[r];
     }
