@@ -248,7 +248,7 @@ def run_batched(impl, args, stream, dev, flush, flush_r, peak, int_query=0):
         o = torch.empty(B, H * G, 256, dtype=torch.float32, device=dev)
         lse = torch.empty(B, H * G, dtype=torch.float32, device=dev)
         nbytes = tpk.hybrid_workspace_bytes(shape, B)
-        ws = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
 
     def step():
         tpk.decode_hybrid_batched(shape, B, q, kp, vp, rec, pt_d, off, w.n_ex, pt8_d, off8, w.n8, o, lse, ws,
@@ -297,7 +297,7 @@ def run_tier(which, impl, args, stream, dev, flush, flush_r, peak, int_query=0):
         o = torch.empty(1, H * G, 256, dtype=torch.float32, device=dev)
         lse = torch.empty(1, H * G, dtype=torch.float32, device=dev)
         nbytes = tpk.hybrid_workspace_bytes(shape, 1)
-        ws = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
 
     def step():
         tpk.decode_hybrid_batched(shape, 1, q, kp, vp, rec, pt_d, off, w.n_ex, pt8_d, off8, w.n8, o, lse, ws,
@@ -345,7 +345,7 @@ def run_gpu(args, dist, rank, world):
         o = torch.empty(1, H * G, 256, dtype=torch.float32, device=dev)
         lse = torch.empty(1, H * G, dtype=torch.float32, device=dev)
         nbytes = tpk.hybrid_workspace_bytes(shape, 1)
-        ws = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
         tpk.workspace_init(ws, nbytes, stream)
         # fresh page conversion of every 8-bit page (timed separately: the median of
         # five conversions of all 7,936 page-heads, each rewriting the same records)
@@ -523,7 +523,7 @@ def run_e2e(args, w, rec_dev, shape, stream, dev, dist):
     shape2 = tpk.Shape(H, impl=shape.impl, kv_slots=off["n_exact_pages"], rec_slots=off["n_int8_pages"],
                        int_query=shape.int_query)
     nbytes = tpk.hybrid_workspace_bytes(shape2, 1)
-    ws = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
     views = [slot_views(s, off, w) for s in slots]
     d2h_bytes = o_h.numel() * 4 + lse_h.numel() * 4
     st = tpk.Stager(slots, off["nbytes"])
@@ -618,7 +618,7 @@ def run_host_resident(args, w, rec_dev, shape, stream, dev, dist, layers=None, s
     shape2 = tpk.Shape(H, impl=shape.impl, kv_slots=off["n_exact_pages"], rec_slots=off["n_int8_pages"],
                        int_query=shape.int_query)
     nbytes = tpk.hybrid_workspace_bytes(shape2, 1)
-    ws = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
     outs = [(torch.empty(1, H * G, 256, dtype=torch.float32, device=dev),
              torch.empty(1, H * G, dtype=torch.float32, device=dev)) for _ in range(layers)]
     views = [slot_views(s, off, w) for s in slots]
@@ -730,7 +730,7 @@ def run_gate_sweep(args):
                 o = torch.empty(1, H * G, 256, dtype=torch.float32, device=dev)
                 lse = torch.empty(1, H * G, dtype=torch.float32, device=dev)
                 nbytes = tpk.hybrid_workspace_bytes(shape, 1)
-                ws = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
+                ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
 
             def step():
                 tpk.decode_hybrid_batched(shape, 1, q, kp, vp, rec, pt_d, off, w.n_ex, pt8_d, off8, w.n8, o, lse,
@@ -816,7 +816,7 @@ def run_lossless(args):
             o = torch.empty(1, H * G, 256, dtype=torch.float32, device=dev)
             lse = torch.empty(1, H * G, dtype=torch.float32, device=dev)
             nbytes = tpk.hybrid_workspace_bytes(shape, 1)
-            ws = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
+            ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
 
         def pack():
             tpk.kv_pack13_pages(shape, kp, vp, ex_d, ex_d, ne, pool, w.n_slots, stream)
@@ -896,7 +896,7 @@ def run_tiers_loop(args):
         o = torch.empty(B, H * G, 256, dtype=torch.float32, device=dev)
         lse = torch.empty(B, H * G, dtype=torch.float32, device=dev)
         ws_bytes = tpk.hybrid_workspace_bytes(shape, B)
-        ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
         sc_bytes = tpk.Tiers.device_bytes(B, max_pages)
         scratch = torch.empty(sc_bytes, dtype=torch.uint8, device=dev)
     torch.cuda.synchronize()

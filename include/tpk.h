@@ -221,11 +221,8 @@ tpk_status tpk_merge_lse(int n_parts, int rows, int head_dim, const float* o_par
 
 /*
  * Workspace bytes tpk_decode_hybrid_batched needs (partial results of the split
- * units and 16 KB of fold counters, about 16 MiB; independent of the lengths).
- * Before its first use a workspace must be zero-filled (tpk_workspace_init does
- * it); every call leaves the counters zero again, so one initialisation serves
- * any number of calls.  After a call whose status was TPK_ERR_TIMEOUT, zero-fill
- * it again.
+ * units, about 16 MiB; independent of the lengths).  The contents need no
+ * initialisation.  tpk_workspace_init zero-fills a buffer (a convenience only).
  */
 size_t tpk_hybrid_workspace_bytes(const tpk_shape* shape, int n_req);
 tpk_status tpk_workspace_init(void* ws, size_t ws_bytes, tpk_stream_t stream);
@@ -236,12 +233,9 @@ tpk_status tpk_workspace_init(void* ws, size_t ws_bytes, tpk_stream_t stream);
  * merge accumulator).  For each request b and KV head h: the exact partial over
  * its BF16 tokens [0, n_exact_tokens[b]) and the 8-bit partial over its pages
  * [0, n_int8_pages[b]), split across thread blocks of one decode launch, then
- * folded, in a fixed order, into o[b] (dev float32 [n_req][H*G][256]) and lse[b]
- * (dev float32 [n_req][H*G]), which are overwritten.  When the split plan fits in
- * one wave of resident blocks of the tensor-core kernel (and no head has more than
- * 64 units), the decode launch is cooperative and its blocks fold each head
- * themselves once the head's units are done (a bounded wait on a workspace
- * counter); otherwise a second small launch folds.
+ * folded, in a fixed order, by a second small launch into o[b] (dev float32
+ * [n_req][H*G][256]) and lse[b] (dev float32 [n_req][H*G]), which are
+ * overwritten.
  *   q           dev bf16 [n_req][H*G][256]
  *   page_table  dev int32, flat; request b's exact-tier slots start at
  *               req_page_off[b] (host int32 [n_req + 1])
@@ -269,19 +263,16 @@ tpk_status tpk_decode_hybrid_batched(const tpk_shape* shape, int n_req, const vo
  * runtime whose memory budget is fixed once serving starts.
  * Same arguments and results as tpk_decode_hybrid_batched, minus ws/ws_bytes.
  * Scratch: a file-scope device array of tpk_static_scratch_bytes() bytes
- * (16,859,136: the partials of the largest split plan, 2048 units, and the fold
- * counters; zero at load), held by every
+ * (16,842,752: the partials of the largest split plan, 2048 units), held by every
  * GPU that loads the library until the process exits.  A call whose plan needs
  * more fails with TPK_ERR_NOMEM.
  * The first call on a device resolves the array's device address (once per
  * device, with that device current); make that first call before any stream
- * capture.  Every call shares the one array and leaves its fold counters zero,
- * but calls that overlap on the GPU (for example on two streams) race on it:
- * serialise them.  After a call whose status was TPK_ERR_TIMEOUT the counters may
- * be left set: tpk_static_scratch_reset zero-fills the array (on `stream`).
+ * capture.  Every call shares the one array and no state carries over between
+ * calls that needs clearing, but calls that overlap on the GPU (for example on two
+ * streams) race on it: serialise them.
  */
 size_t tpk_static_scratch_bytes(void);
-tpk_status tpk_static_scratch_reset(tpk_stream_t stream);
 tpk_status tpk_decode_hybrid_batched_static(const tpk_shape* shape, int n_req, const void* q, const void* k_pool,
                                             const void* v_pool, const void* rec_pool, const int32_t* page_table,
                                             const int32_t* req_page_off, const int32_t* n_exact_tokens,

@@ -101,7 +101,7 @@ def test_back_to_back_launches_share_a_workspace(impl):
     d = DevWorkload(w, impl)
     d.quantize_gpu()
     nbytes = tpk.hybrid_workspace_bytes(d.shape, w.B)
-    ws = t.zeros(nbytes, dtype=t.uint8, device="cuda")
+    ws = t.empty(nbytes, dtype=t.uint8, device="cuda")
     tpk.workspace_init(ws, nbytes)
     outs = []
     for _ in range(20):
@@ -132,7 +132,7 @@ def test_maximum_request_count(impl):
     o = t.empty(257, w.H * w.G, 256, dtype=t.float32, device="cuda")
     lse = t.empty(257, w.H * w.G, dtype=t.float32, device="cuda")
     nbytes = tpk.hybrid_workspace_bytes(d.shape, 256)
-    ws = t.zeros(nbytes, dtype=t.uint8, device="cuda")
+    ws = t.empty(nbytes, dtype=t.uint8, device="cuda")
     off = np.concatenate([d.off, d.off[-1:]])
     off8 = np.concatenate([d.off8, d.off8[-1:]])
     with pytest.raises(tpk.TpkError):

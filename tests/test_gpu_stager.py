@@ -57,7 +57,7 @@ def test_layers_through_two_slots(impl):
     with tpk.Stager(slots, slot_bytes) as st:
         shape0 = tpk.Shape(2, impl=impl)
         nbytes = tpk.hybrid_workspace_bytes(shape0, 2)
-        ws = t.zeros(nbytes, dtype=t.uint8, device="cuda")
+        ws = t.empty(nbytes, dtype=t.uint8, device="cuda")
         pending = st.stage([(layers[0][2], 0, layers[0][3]["nbytes"])])
         for l in range(L):
             w, _, img, off = layers[l]

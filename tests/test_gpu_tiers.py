@@ -40,7 +40,7 @@ def test_histories_grow_and_pages_are_published(impl):
     nbytes = tpk.Tiers.device_bytes(B, max_pages)
     scratch = t.empty(nbytes, dtype=t.uint8, device="cuda")
     ws_bytes = tpk.hybrid_workspace_bytes(shape, B)
-    ws = t.zeros(ws_bytes, dtype=t.uint8, device="cuda")
+    ws = t.empty(ws_bytes, dtype=t.uint8, device="cuda")
     conv, dec = t.cuda.Stream(), t.cuda.Stream()
     n = [min(f, 700 + 300 * b) for b, f in enumerate(final)]   # starting lengths
     published_total = 0

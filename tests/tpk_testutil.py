@@ -77,7 +77,7 @@ class DevWorkload:
         o = t.empty(w.B, w.H * w.G, 256, dtype=t.float32, device="cuda")
         lse = t.empty(w.B, w.H * w.G, dtype=t.float32, device="cuda")
         nbytes = tpk.hybrid_workspace_bytes(self.shape, w.B)
-        ws = t.zeros(nbytes, dtype=t.uint8, device="cuda")
+        ws = t.empty(nbytes, dtype=t.uint8, device="cuda")
         tpk.workspace_init(ws, nbytes)
         tpk.decode_hybrid_batched(self.shape, w.B, self.q, self.k, self.v, self.rec, self.pt, self.off, w.n_ex,
                                   self.pt8, self.off8, w.n8, o, lse, ws, nbytes)

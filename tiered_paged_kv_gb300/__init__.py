@@ -20,7 +20,7 @@ __all__ = [
     "Shape", "TpkError", "lib", "RECORD_BYTES", "IMPL_DEFAULT", "IMPL_SIMT", "IMPL_TENSOR",
     "kv_quantize_pages", "kv_quantize_pages_given_scales", "decode_attn_exact", "decode_attn_int8",
     "merge_lse", "hybrid_workspace_bytes", "workspace_init", "decode_hybrid_batched", "get_device_status",
-    "static_scratch_bytes", "static_scratch_reset", "decode_hybrid_batched_static", "Stager", "Tiers", "TiersPlan",
+    "static_scratch_bytes", "decode_hybrid_batched_static", "Stager", "Tiers", "TiersPlan",
     "PACK13_RECORD_BYTES", "PACK13_PLANE_ENC", "PACK13_PLANE_RAW", "kv_pack13_pages", "kv_unpack13_pages",
 ]
 
@@ -84,8 +84,6 @@ def lib():
         L.tpk_workspace_init.argtypes = [vp, sz, vp]
         L.tpk_decode_hybrid_batched.argtypes = [sp, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         L.tpk_get_device_status.argtypes = [ctypes.POINTER(ctypes.c_int), i32, vp]
-        L.tpk_static_scratch_reset.argtypes = [vp]
-        L.tpk_static_scratch_reset.restype = i32
         L.tpk_static_scratch_bytes.argtypes = []
         L.tpk_static_scratch_bytes.restype = sz
         L.tpk_decode_hybrid_batched_static.argtypes = [sp, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
@@ -211,10 +209,6 @@ def decode_hybrid_batched(shape, n_req, q, k_pool, v_pool, rec_pool, page_table,
 
 def static_scratch_bytes():
     return int(lib().tpk_static_scratch_bytes())
-
-
-def static_scratch_reset(stream=None):
-    _check(lib().tpk_static_scratch_reset(_stream(stream)))
 
 
 def decode_hybrid_batched_static(shape, n_req, q, k_pool, v_pool, rec_pool, page_table, req_page_off,

@@ -33,6 +33,7 @@ void set_error(const char* msg);
 
 namespace {
 
+constexpr int kMaxUnits = 2048;       // partial slots in the hybrid workspace (256 requests x 4 heads x 2 tiers)
 constexpr int kMaxSplits = 4096;      // primitive calls
 constexpr int kMaxHeads = 1024;
 
@@ -305,15 +306,9 @@ tpk_status tpk_merge_lse(int n_parts, int rows, int head_dim, const float* o_par
 
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-// Workspace: partial lse [kMaxUnits][G], partial o [kMaxUnits][G][256], then the
-// fused fold's counters [2][kMaxUnits] (zero between calls).
-static size_t ws_counters_offset() {
-  return align256((size_t)kMaxUnits * kGroup * 4) + align256((size_t)kMaxUnits * kGroup * kHeadDim * 4);
-}
-
 size_t tpk_hybrid_workspace_bytes(const tpk_shape* shape, int n_req) {
   if (!shape || n_req < 1 || shape->kv_heads < 1) return 0;
-  return ws_counters_offset() + align256((size_t)2 * kMaxUnits * 4);
+  return align256((size_t)kMaxUnits * kGroup * 4) + (size_t)kMaxUnits * kGroup * kHeadDim * 4;
 }
 
 tpk_status tpk_workspace_init(void* ws, size_t ws_bytes, tpk_stream_t stream) {
@@ -445,25 +440,17 @@ tpk_status tpk_decode_hybrid_batched(const tpk_shape* shape, int n_req, const vo
   p.out_lse = lse;
   p.mode = kModeFold;
   p.n_req = n_req;
-  p.fold_cnt = reinterpret_cast<int*>(static_cast<uint8_t*>(ws) + ws_counters_offset());
   p.status = status_ptr();
   if (!p.status) return fail(TPK_ERR_CUDA, "cannot resolve the device status word");
   if (any_e) {
     st = make_pool_maps(p, shape, k_pool, v_pool);
     if (st != TPK_OK) return st;
   }
-  bool any_split = false;
-  int max_per_head = 0;
-  for (int b = 0; b < n_req; ++b) {
-    any_split |= req[b].splits_e + req[b].splits_8 > 1;
-    max_per_head = std::max(max_per_head, req[b].splits_e + req[b].splits_8);
-  }
-  // One wave of resident blocks on the tensor-core kernel: the decode blocks fold
-  // their heads themselves (cooperative launch), saving the fold launch.
-  p.fused_fold = any_split && !use_simt(shape) && units <= per_wave && max_per_head <= kFusedFoldMaxUnits;
   st = launch_decode(shape, p, req.data(), reinterpret_cast<cudaStream_t>(stream));
   if (st != TPK_OK) return st;
-  if (any_split && !p.fused_fold) {
+  bool any_split = false;
+  for (int b = 0; b < n_req; ++b) any_split |= req[b].splits_e + req[b].splits_8 > 1;
+  if (any_split) {
     cudaError_t e = launch_fold(p, req.data(), reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "fold launch");
   }

@@ -53,8 +53,6 @@ struct ReqPlan {
 };
 
 constexpr int kMaxReqPerLaunch = 256;
-constexpr int kMaxUnits = 2048;  // partial slots in the hybrid workspace (256 requests x 4 heads x 2 tiers)
-constexpr int kFusedFoldMaxUnits = 64;  // units per head the decode kernel folds itself
 // Launches of at most kShortPlan requests pass a short plan: the kernels take
 // the plan as a parameter, and a smaller parameter block is set up faster at
 // every launch.
@@ -84,10 +82,6 @@ struct DecodeParams {
   int* status;              // device status word
   float qscale;             // sm_scale * log2(e)
   int int_query;            // 1: the 8-bit tier's QK runs on the integer query
-  int fused_fold;           // 1: the decode blocks fold each head's partials themselves (one
-                            // co-resident wave, cooperative launch) instead of a fold launch
-  int* fold_cnt;            // workspace: per (request, head) arrivals [kMaxUnits], then
-                            // finished folds [kMaxUnits]; zero between calls
   int H;
   int mode;
   int n_req;
@@ -227,12 +221,6 @@ __device__ __forceinline__ uint64_t global_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
-}
-
-__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
-  int v;
-  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
 }
 
 // Bounded wait on an mbarrier phase: gives up after about two seconds of wall

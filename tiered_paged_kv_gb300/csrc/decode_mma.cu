@@ -76,9 +76,6 @@ struct MmaSmem {
   int abort;
 };
 static_assert(sizeof(MmaSmem) <= 227 * 1024, "shared memory per block");
-// the epilogue rows (4 pairs x 8 rows x 260 floats) and the fused fold's scratch
-// (8 x 64 weights, 8 log-sum-exps, one flag) reuse the slots
-static_assert((4 * 8 * 260 + 8 * 64 + 8 + 1) * 4 <= sizeof(MmaSmem::slot), "epilogue scratch");
 
 // ----------------------------------------------------------------- PTX
 __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
@@ -579,82 +576,6 @@ __device__ __forceinline__ bool process_bf16_half(uint8_t* slot, int h, const Pa
   return true;
 }
 
-// ------------------------------------------------------------- fused fold
-// Every unit of a (request, KV head) with more than one unit wrote its partial to
-// the workspace; the head's n blocks (all resident: cooperative launch) meet on a
-// per-head arrival counter, then block k folds output elements [k * 2048 / n,
-// (k + 1) * 2048 / n) of the head's 8 rows x 256 channels ("SYCL", "A merge that
-// joins the tiers": the partials' log-sum-exp merge, -inf an empty partial), in
-// unit order like the fold kernel.  The last block to finish clears both counters,
-// so the workspace is ready for the next call.  `scratch` holds 8 x 64 weights and
-// 8 row log-sum-exps.
-constexpr int kFusedFoldMax = kFusedFoldMaxUnits;  // heads with more units use the fold launch
-__device__ __forceinline__ void fused_fold(const DecodeParams& p, const ReqPlan& rp, const UnitInfo& ui, float* scratch,
-                                        bool skip) {
-  const int tid = threadIdx.x;
-  const int G = kGroup, n = ui.per_head;
-  const int hid = ui.b * p.H + ui.h;
-  int* arrived = p.fold_cnt + hid;
-  int* folded = p.fold_cnt + kMaxUnits + hid;
-  int& go = *reinterpret_cast<int*>(scratch + G * kFusedFoldMax + G);
-  // publish this block's partial, then wait (bounded) for the head's other units
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) {
-    atomicAdd(arrived, 1);
-    bool ok = ld_acquire_gpu(arrived) >= n;
-    const uint64_t t0 = global_ns();
-    while (!ok) {
-      __nanosleep(200);
-      ok = ld_acquire_gpu(arrived) >= n;
-      if (!ok && global_ns() - t0 > kWaitLimitNs) {
-        atomicOr(p.status, kStatusTimeout);
-        break;
-      }
-    }
-    go = ok && !skip;
-  }
-  __syncthreads();
-  __threadfence();
-  if (go) {
-    const int first = rp.unit_base + ui.h * n;
-    const int row0 = hid * G;  // first output row of this head
-    const int e0 = ui.unit_in_head * G * kHeadDim / n, e1 = (ui.unit_in_head + 1) * G * kHeadDim / n;
-    const int r0 = e0 / kHeadDim, r1 = (e1 - 1) / kHeadDim;
-    float* w = scratch;                       // [G][kFusedFoldMax]
-    float* row_lse = scratch + G * kFusedFoldMax;  // [G]
-    const float ninf = -__builtin_huge_valf();
-    if (tid <= r1 - r0) {
-      const int r = r0 + tid;
-      float M = ninf;
-      for (int i = 0; i < n; ++i) M = fmaxf(M, __ldcg(p.part_lse + (first + i) * G + r));
-      float L = 0.f;
-      for (int i = 0; i < n; ++i) {
-        const float li = __ldcg(p.part_lse + (first + i) * G + r);
-        const float wi = (li == ninf) ? 0.f : expf(li - M);
-        w[r * kFusedFoldMax + i] = wi;
-        L += wi;
-      }
-      for (int i = 0; i < n; ++i) w[r * kFusedFoldMax + i] = M == ninf ? 0.f : w[r * kFusedFoldMax + i] / L;
-      row_lse[r] = M == ninf ? ninf : M + logf(L);
-    }
-    __syncthreads();
-    for (int e = e0 + tid; e < e1; e += blockDim.x) {
-      const int r = e / kHeadDim, c = e % kHeadDim;
-      const float* src = p.part_o + ((int64_t)first * G + r) * kHeadDim + c;
-      float acc = 0.f;
-      for (int i = 0; i < n; ++i) acc += w[r * kFusedFoldMax + i] * __ldcg(src + (int64_t)i * G * kHeadDim);
-      p.out_o[(int64_t)(row0 + r) * kHeadDim + c] = acc;
-      if (c == 0) p.out_lse[row0 + r] = row_lse[r];
-    }
-  }
-  __syncthreads();
-  if (tid == 0 && atomicAdd(folded, 1) == n - 1) {  // every unit of the head is past its wait
-    *arrived = 0;
-    *folded = 0;
-  }
-}
-
 // ------------------------------------------------------------------ kernel
 template <int R, bool IntQuery>
 __global__ void __launch_bounds__(kMmaThreads, 1) decode_mma_kernel(const __grid_constant__ DecodeParams p,
@@ -768,14 +689,11 @@ __global__ void __launch_bounds__(kMmaThreads, 1) decode_mma_kernel(const __grid
   if (S.abort) {
     // A wait gave up: let every copy issued into the slots land (bounded: the
     // latest fill of each slot), then leave without a result; the status word
-    // reports the timeout.  With the fused fold the block still arrives (and the
-    // head's fold is skipped), so no other block waits for it.
+    // reports the timeout.
     if (tid == 0)
       for (int s = 0; s < kMmaSlots; ++s)
         if (S.fills[s] > 0) mbar_wait(&S.full[s], (S.fills[s] - 1) & 1, p.status);
     __syncthreads();
-    if (p.fused_fold && ui.per_head > 1)
-      fused_fold(p, plan.req[ui.b], ui, reinterpret_cast<float*>(S.slot[0]), true);
     return;
   }
   // ---- per-pair states into shared memory (the stages are idle now); the two
@@ -804,10 +722,6 @@ __global__ void __launch_bounds__(kMmaThreads, 1) decode_mma_kernel(const __grid
   }
   __syncthreads();
   write_and_fold<kCons / 2, MmaSmem, kEpStride>(p, ui, S, ep_o);
-  if (p.fused_fold && ui.per_head > 1) {
-    // the fold's scratch lies past the epilogue rows (4 pairs x 8 rows x kEpStride floats)
-    fused_fold(p, plan.req[ui.b], ui, ep_o + kCons / 2 * kGroup * kEpStride, false);
-  }
 }
 
 template <int R, bool IntQuery>
@@ -822,23 +736,8 @@ static cudaError_t launch_mma(const DecodeParams& p, const ReqPlan* req, cudaStr
   }
   Plan<R> plan = {};
   for (int b = 0; b < p.n_req; ++b) plan.req[b] = req[b];
-  if (!p.fused_fold) {
-    decode_mma_kernel<R, IntQuery><<<p.n_units, kMmaThreads, smem, stream>>>(p, plan);
-    return cudaGetLastError();
-  }
-  // the fused fold waits on other blocks of the grid: a cooperative launch makes
-  // the whole grid resident at once (the host only fuses one-wave plans)
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.n_units);
-  cfg.blockDim = dim3(kMmaThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_mma_kernel<R, IntQuery>, p, plan);
+  decode_mma_kernel<R, IntQuery><<<p.n_units, kMmaThreads, smem, stream>>>(p, plan);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_decode_mma(const DecodeParams& p, const ReqPlan* req, cudaStream_t stream) {

@@ -21,9 +21,8 @@ void set_error(const char* msg);  // api.cu: sets the message tpk_last_error_str
 namespace {
 
 // Fixed scratch: room for the largest split plan the multi-request call makes
-// (2048 units x 8 rows x (256 + 1) floats) and the fused fold's 2 x 2048 counters;
-// zero at load, and every call leaves the counters zero.
-constexpr size_t kStaticScratchBytes = 16859136;
+// (2048 units x 8 rows x (256 + 1) floats).
+constexpr size_t kStaticScratchBytes = 16842752;
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
 
 constexpr int kMaxDevices = 64;
@@ -58,18 +57,6 @@ void* scratch_on_current_device(tpk_status* st) {
 }  // namespace
 
 extern "C" size_t tpk_static_scratch_bytes(void) { return kStaticScratchBytes; }
-
-extern "C" tpk_status tpk_static_scratch_reset(tpk_stream_t stream) {
-  tpk_status st;
-  void* scratch = scratch_on_current_device(&st);
-  if (!scratch) return st;
-  cudaError_t e = cudaMemsetAsync(scratch, 0, kStaticScratchBytes, reinterpret_cast<cudaStream_t>(stream));
-  if (e != cudaSuccess) {
-    tpk::set_error(cudaGetErrorString(e));
-    return TPK_ERR_CUDA;
-  }
-  return TPK_OK;
-}
 
 extern "C" tpk_status tpk_decode_hybrid_batched_static(const tpk_shape* shape, int n_req, const void* q,
                                                        const void* k_pool, const void* v_pool, const void* rec_pool,
