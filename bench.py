@@ -184,6 +184,33 @@ def oracle_time(w, rec_host, n_threads, sample_heads=None):
     return dt, w.history_bytes(), min(n_threads, w.B * w.H)
 
 
+def oracle_quant_time(w, n_threads):
+    """Time the oracle's page conversion (as it stands) on host cores: every 8-bit
+    page of the workload on one thread, then the same pages split over n_threads
+    threads (the C oracle releases the GIL).  Returns GB/s of BF16 read + records
+    written, as the GPU conversion figure counts them."""
+    import oracle
+    from concurrent.futures import ThreadPoolExecutor
+    s8 = w.int8_slots()
+    per_ph = 65536 + oracle.REC_BYTES
+    rec = np.empty(w.n_slots * w.H * oracle.REC_BYTES, np.uint8)
+    rec.fill(0)                                              # fault the pages in before timing
+    oracle.quantize_pages(w.H, w.k_pool, w.v_pool, s8[:1], s8[:1], rec)   # load the library
+    t0 = time.perf_counter()
+    oracle.quantize_pages(w.H, w.k_pool, w.v_pool, s8, s8, rec)
+    dt1 = time.perf_counter() - t0
+    n = max(1, min(n_threads, len(s8)))
+    parts = np.array_split(s8, n)
+    t0 = time.perf_counter()
+    with ThreadPoolExecutor(n) as ex:
+        list(ex.map(lambda sl: oracle.quantize_pages(w.H, w.k_pool, w.v_pool, sl, sl, rec), parts))
+    dt = time.perf_counter() - t0
+    nb = len(s8) * w.H * per_ph
+    return {"value": round(nb / dt / 1e9, 4), "unit": "GB/s", "cores": n, "value_1_thread": round(nb / dt1 / 1e9, 4),
+            "sample": f"all {len(s8)} 8-bit pages x {w.H} heads of the workload ({dt1:.1f} s on one thread, "
+                      f"{dt:.2f} s on {n})", "kind": "oracle"}
+
+
 def head_slice(w, heads, rec_host):
     """The same history restricted to the first `heads` KV heads (a sample)."""
     from tiered_paged_kv_gb300 import synth
@@ -436,7 +463,8 @@ def run_gpu(args, dist, rank, world):
                          f"threads over (request, KV head)",
                "value_1_thread": round(nb1 / dt1 / 1e9, 4),
                "sample_1_thread": f"one KV head of the same step on one thread, once, {dt1:.1f} s",
-               "host_cores_available": os.cpu_count()}
+               "host_cores_available": os.cpu_count(),
+               "page_conversion": oracle_quant_time(w, n_thr)}
     achieved = hist_bytes / (ms_mean * 1e-3) / 1e9
     value = world * hist_bytes / (ms_max * 1e-3) / 1e9
     traffic = measured_traffic(args.kernel + ("_int_query" if args.int_query else ""))
