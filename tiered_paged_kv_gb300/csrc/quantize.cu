@@ -301,7 +301,9 @@ __global__ void __launch_bounds__(kQuantThreads, 2) quantize_kernel(const __grid
   }
   __syncthreads();
   S.inv_s[c] = __frcp_rn(S.s[c]);
-  __syncthreads();
+  // one flag for the block: every key channel scale is in the range where the
+  // reciprocal estimates hold
+  const bool s_fast = __syncthreads_and(fast_scale(S.s[c]));
   // ---- 5. codes: thread (token t, quarter q) handles 64 channels, chunks rotated
   //         by lane so that shared-memory reads do not conflict.  y_tc = k_tc / s_c
   //         is estimated as k * (1/s_c); the exact max |y| of the row comes from
@@ -326,17 +328,12 @@ __global__ void __launch_bounds__(kQuantThreads, 2) quantize_kernel(const __grid
       yv[7] = bf16_hi(w.w) * i1.w;
     };
     float amax = 0.f;
-    bool s_fast = true;
 #pragma unroll 2
     for (int k = 0; k < 8; ++k) {
       float yv[8];
       estimates(k, yv);
-      const int ch0 = q * 64 + ((k + lane) & 7) * 8;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        amax = fmaxf(amax, fabsf(yv[e]));
-        s_fast &= fast_scale(S.s[ch0 + e]);
-      }
+      for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(yv[e]));
     }
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
