@@ -103,6 +103,25 @@ __device__ __forceinline__ uint32_t code_byte(float x, float scale) {
 // stored, as are all bytes of a scale outside [2^-100, 2^100].
 constexpr float kCodeSlack = 0x1p-12f;
 __device__ __forceinline__ bool near_half(float z) { return 0.5f - fabsf(z - rintf(z)) <= kCodeSlack; }
+
+// Four codes from estimates known to lie within 127 (1 + 2^-20) in magnitude (codes
+// of pages converted here: the scales come from the maxima, so no clamp is
+// needed): adding 1.5 * 2^23 puts z in [2^23, 2^24), where float32 spacing is 1, so
+// the addition rounds half to even exactly like rint, and the low byte of the sum's
+// encoding is rint(z) mod 256; XOR 0x80 makes it the stored byte rint(z) + 128.
+// Sets bit e of `near` when estimate e is within kCodeSlack of a half-integer.
+constexpr float kRoundMagic = 12582912.f;  // 1.5 * 2^23
+__device__ __forceinline__ uint32_t code_word4(const float (&z)[4], uint32_t& near, int shift) {
+  uint32_t t[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float te = __fadd_rn(z[e], kRoundMagic);
+    const float r = __fsub_rn(te, kRoundMagic);
+    near |= (uint32_t)(0.5f - fabsf(z[e] - r) <= kCodeSlack) << (shift + e);
+    t[e] = __float_as_uint(te);
+  }
+  return __byte_perm(__byte_perm(t[0], t[1], 0x0040), __byte_perm(t[2], t[3], 0x0040), 0x5410) ^ 0x80808080u;
+}
 __device__ __forceinline__ bool fast_scale(float scale) { return scale >= 0x1p-100f && scale <= 0x1p100f; }
 
 constexpr int kQuantThreads = 256;  // one thread per channel in the per-channel phases
@@ -148,11 +167,21 @@ __global__ void __launch_bounds__(kQuantThreads, 2) quantize_kernel(const __grid
     const float inv = fast ? __frcp_rn(u) : 0.f;
     uint32_t redo = fast ? 0u : 0xffffu;
     uint32_t wv[4] = {0u, 0u, 0u, 0u};
+    if (given) {  // scales from the caller: any magnitude, so clamp
 #pragma unroll
-    for (int e = 0; e < 16; ++e) {
-      const float z = bf16_lo(S.v[t0 + e][ch]) * inv;
-      redo |= (uint32_t)near_half(z) << e;
-      wv[e >> 2] |= quotient_byte(z) << (8 * (e & 3));
+      for (int e = 0; e < 16; ++e) {
+        const float z = bf16_lo(S.v[t0 + e][ch]) * inv;
+        redo |= (uint32_t)near_half(z) << e;
+        wv[e >> 2] |= quotient_byte(z) << (8 * (e & 3));
+      }
+    } else {
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        float z[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) z[e] = bf16_lo(S.v[t0 + 4 * g + e][ch]) * inv;
+        wv[g] = code_word4(z, redo, 4 * g);
+      }
     }
     uint8_t* dst = rec + kOffVc + vc_byte(ch, t0);
     *reinterpret_cast<uint4*>(dst) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
@@ -369,11 +398,20 @@ __global__ void __launch_bounds__(kQuantThreads, 2) quantize_kernel(const __grid
       const int ch0 = q * 64 + ((k + lane) & 7) * 8;
       uint32_t wk[2] = {0u, 0u};
       uint32_t redo = fast ? 0u : 0xffu;
+      if (given) {  // r from the caller: any magnitude, so clamp
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const float z = yv[e] * inv_r;
-        redo |= (uint32_t)near_half(z) << e;
-        wk[e >> 2] |= quotient_byte(z) << (8 * (e & 3));
+        for (int e = 0; e < 8; ++e) {
+          const float z = yv[e] * inv_r;
+          redo |= (uint32_t)near_half(z) << e;
+          wk[e >> 2] |= quotient_byte(z) << (8 * (e & 3));
+        }
+      } else {
+#pragma unroll
+        for (int g = 0; g < 2; ++g) {
+          const float z[4] = {yv[4 * g] * inv_r, yv[4 * g + 1] * inv_r, yv[4 * g + 2] * inv_r,
+                              yv[4 * g + 3] * inv_r};
+          wk[g] = code_word4(z, redo, 4 * g);
+        }
       }
       // (ch0 is a multiple of 8: kc_byte(t, ch0 + e) = kc_byte(t, ch0) + e)
       uint8_t* dst = kc + kc_byte(t, ch0);
