@@ -52,6 +52,8 @@ def test_unsupported_shapes_are_rejected(L):
         assert st == code, (kw, st, err(L))
     s = tpk.Shape(0)
     assert L.tpk_decode_attn_int8(ctypes.byref(s), 16, 16, 16, 0, 1, 1, 16, 16, None) == 1
+    s = tpk.Shape(1025)   # more KV heads than the library takes
+    assert L.tpk_decode_attn_int8(ctypes.byref(s), 16, 16, 16, 0, 1, 1, 16, 16, None) == 1
     assert L.tpk_decode_attn_exact(None, 16, 16, 16, 16, 0, 64, 1, 16, 16, None) == 1
 
 

@@ -146,3 +146,19 @@ def test_million_token_history(impl):
     one KV head."""
     w = synth.make_workload([1 << 20], 4096, H=1, seed=61, key_sigma="outliers")
     check_hybrid(w, impl, gpu_records=True, what="1M tokens")
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+def test_many_kv_heads(impl):
+    """64 KV heads (512 query rows) over a ragged hybrid batch, records converted on
+    the GPU: head indexing in the decode, fold and conversion kernels at large H."""
+    w = synth.make_workload([700, 64 * 3 + 5], 100, H=64, seed=62, key_sigma="outliers")
+    check_hybrid(w, impl, gpu_records=True, what="64 heads")
+
+
+def test_maximum_kv_heads():
+    """1024 KV heads, the largest shape the library takes: one short exact history
+    (1024 units, one per head) and one 8-bit page per head."""
+    w = synth.make_workload([64 + 40], 40, H=1024, seed=63)
+    assert w.n8[0] == 1
+    check_hybrid(w, tpk.IMPL_TENSOR, gpu_records=True, what="1024 heads")

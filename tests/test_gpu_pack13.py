@@ -174,3 +174,28 @@ def test_full_exact_history_round_trip():
     frac = sizes.sum() / (len(ex) * w.H * 65536)
     print(f"13-bit image of the 128K history: {sizes.sum() / 1e6:.1f} MB = {frac:.4f} of BF16")
     assert frac < 0.82
+
+
+def test_many_heads_round_trip():
+    t = torch()
+    w = synth.make_workload([64 * 3 + 7], None, H=64, seed=84, key_sigma="loguniform")
+    d = DevWorkload(w, tpk.IMPL_TENSOR)
+    pool = gpu_pack(w, d)
+    ex, _ = w.exact_page_table()
+    ref = np.zeros(w.n_slots * w.H * R, np.uint8)
+    oracle.pack13_pages(w.H, w.k_pool, w.v_pool, ex, ex, ref)
+    host = pool.cpu().numpy().reshape(w.n_slots, w.H, R)
+    ref = ref.reshape(w.n_slots, w.H, R)
+    for slot in ex:
+        for h in range(w.H):
+            n = record_size(ref[slot, h])
+            assert np.array_equal(host[slot, h, :n], ref[slot, h, :n])
+    k2, v2 = t.zeros_like(d.k), t.zeros_like(d.v)
+    offs = (np.repeat(ex.astype(np.int64), w.H) * w.H + np.tile(np.arange(w.H), len(ex))) * R
+    tpk.kv_unpack13_pages(d.shape, pool, pool.numel(), dev_u8(offs.view(np.uint8)), dev_i32(ex), len(ex), k2, v2)
+    t.cuda.synchronize()
+    st, flags = tpk.get_device_status(reset=True)
+    assert st == 0, flags
+    k2h = k2.cpu().numpy().view(np.uint16).reshape(w.k_pool.shape)
+    v2h = v2.cpu().numpy().view(np.uint16).reshape(w.v_pool.shape)
+    assert np.array_equal(k2h[ex], w.k_pool[ex]) and np.array_equal(v2h[ex], w.v_pool[ex])
