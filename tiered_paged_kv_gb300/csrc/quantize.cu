@@ -7,7 +7,8 @@
 // symmetric in -127..127; values carry one scale per channel per page.
 //
 // One thread block converts one page-head (64 tokens x 256 channels of K and V):
-//   1. the page-head is bulk-copied into shared memory;
+//   1. the keys are bulk-copied into shared memory (the values, read twice, come
+//      from global memory, so four blocks fit on an SM);
 //   2. thread c owns channel c: u_c = max|v| / 127, and the key mean square with
 //      compensated float32 additions of exact squares (relative error below
 //      2^-42);
@@ -31,7 +32,6 @@ namespace tpk {
 
 struct QSmem {
   alignas(128) uint16_t k[kPageTokens][kHeadDim];
-  alignas(128) uint16_t v[kPageTokens][kHeadDim];
   uint64_t bar;
   double red_m[8];
   int red_e[8];
@@ -143,9 +143,8 @@ __global__ void __launch_bounds__(kQuantThreads, 2) quantize_kernel(const __grid
     fence_mbar_init();
     if (ok) {
       int64_t off = (src * p.H + h) * (int64_t)(kPageTokens * kHeadDim);
-      mbar_arrive_expect_tx(&S.bar, 2 * kBf16PageHeadBytes);
+      mbar_arrive_expect_tx(&S.bar, kBf16PageHeadBytes);
       bulk_g2s(&S.k[0][0], p.k_pool + off, kBf16PageHeadBytes, &S.bar);
-      bulk_g2s(&S.v[0][0], p.v_pool + off, kBf16PageHeadBytes, &S.bar);
     }
   }
   __syncthreads();
@@ -154,6 +153,11 @@ __global__ void __launch_bounds__(kQuantThreads, 2) quantize_kernel(const __grid
   if (__syncthreads_or(!landed)) return;
 
   uint8_t* rec = p.rec_pool + ((int64_t)p.dst[i] * p.H + h) * kRecordBytes;
+  // values are read from global memory (twice: the maximum, then the codes; a
+  // warp reads 32 neighbouring channels of one token, and the second pass hits
+  // L2), so only the keys occupy shared memory
+  const uint16_t(*gv)[kHeadDim] = reinterpret_cast<const uint16_t(*)[kHeadDim]>(
+      p.v_pool + ((int64_t)p.src[i] * p.H + h) * (int64_t)(kPageTokens * kHeadDim));
   const int64_t gidx = (int64_t)i * p.H + h;  // index into given-scale arrays
   const int c = tid;
 
@@ -170,7 +174,7 @@ __global__ void __launch_bounds__(kQuantThreads, 2) quantize_kernel(const __grid
     if (given) {  // scales from the caller: any magnitude, so clamp
 #pragma unroll
       for (int e = 0; e < 16; ++e) {
-        const float z = bf16_lo(S.v[t0 + e][ch]) * inv;
+        const float z = bf16_lo(__ldg(&gv[t0 + e][ch])) * inv;
         redo |= (uint32_t)near_half(z) << e;
         wv[e >> 2] |= quotient_byte(z) << (8 * (e & 3));
       }
@@ -179,7 +183,7 @@ __global__ void __launch_bounds__(kQuantThreads, 2) quantize_kernel(const __grid
       for (int g = 0; g < 4; ++g) {
         float z[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) z[e] = bf16_lo(S.v[t0 + 4 * g + e][ch]) * inv;
+        for (int e = 0; e < 4; ++e) z[e] = bf16_lo(__ldg(&gv[t0 + 4 * g + e][ch])) * inv;
         wv[g] = code_word4(z, redo, 4 * g);
       }
     }
@@ -188,7 +192,7 @@ __global__ void __launch_bounds__(kQuantThreads, 2) quantize_kernel(const __grid
     while (redo) {
       const int e = __ffs(redo) - 1;
       redo &= redo - 1;
-      dst[e] = (uint8_t)code_byte(bf16_lo(S.v[t0 + e][ch]), u);
+      dst[e] = (uint8_t)code_byte(bf16_lo(__ldg(&gv[t0 + e][ch])), u);
     }
   };
   // (channel, 16-token quarter) items, channel fastest, so that a warp's lanes read
@@ -208,7 +212,8 @@ __global__ void __launch_bounds__(kQuantThreads, 2) quantize_kernel(const __grid
     //    then the mean is formed in double with the scale put back.  A zero
     //    channel takes a = 2^-63 before the logarithm.
     float vmax = 0.f;
-    for (int t = 0; t < kPageTokens; ++t) vmax = fmaxf(vmax, fabsf(bf16_lo(S.v[t][c])));
+    #pragma unroll 16
+    for (int t = 0; t < kPageTokens; ++t) vmax = fmaxf(vmax, fabsf(bf16_lo(__ldg(&gv[t][c]))));
     S.u[c] = __fdiv_rn(vmax, 127.f);
     double ms;
     float kmax = 0.f;
