@@ -256,6 +256,20 @@ tpk_status tpk_decode_hybrid_batched(const tpk_shape* shape, int n_req, const vo
                                      tpk_stream_t stream);
 
 /*
+ * The split plan tpk_decode_hybrid_batched makes, for inspection and sizing (host
+ * only, no device work when resident_blocks > 0): for request b the thread blocks
+ * (units) per KV head of the exact tier, splits_exact[b], and of the 8-bit tier,
+ * splits_int8[b] (host int32 [n_req] each), and *n_units = H * the sum of both.
+ * resident_blocks is the number of decode blocks the device holds at once (SMs x
+ * blocks per SM), which sets the unit budget; 0 takes it from the current device
+ * and shape->impl.  A segment gets at least one unit and at most one per page, an
+ * empty request one empty exact unit; units carry about equal bytes.
+ */
+tpk_status tpk_hybrid_plan(const tpk_shape* shape, int n_req, const int32_t* n_exact_tokens,
+                           const int32_t* n_int8_pages, int resident_blocks, int32_t* splits_exact,
+                           int32_t* splits_int8, int32_t* n_units);
+
+/*
  * Multi-request hybrid decode that allocates nothing and takes no workspace.
  * There is no counterpart in the pages this library follows: it exists for
  * callers that cannot hand the library device memory -- a plugin whose host

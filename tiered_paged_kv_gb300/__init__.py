@@ -19,7 +19,8 @@ from . import build as _build_mod
 __all__ = [
     "Shape", "TpkError", "lib", "RECORD_BYTES", "IMPL_DEFAULT", "IMPL_SIMT", "IMPL_TENSOR",
     "kv_quantize_pages", "kv_quantize_pages_given_scales", "decode_attn_exact", "decode_attn_int8",
-    "merge_lse", "hybrid_workspace_bytes", "workspace_init", "decode_hybrid_batched", "get_device_status",
+    "merge_lse", "hybrid_workspace_bytes", "workspace_init", "decode_hybrid_batched", "hybrid_plan",
+    "get_device_status",
     "static_scratch_bytes", "decode_hybrid_batched_static", "Stager", "Tiers", "TiersPlan",
     "PACK13_RECORD_BYTES", "PACK13_PLANE_ENC", "PACK13_PLANE_RAW", "kv_pack13_pages", "kv_unpack13_pages",
 ]
@@ -84,6 +85,9 @@ def lib():
         L.tpk_workspace_init.argtypes = [vp, sz, vp]
         L.tpk_decode_hybrid_batched.argtypes = [sp, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         L.tpk_get_device_status.argtypes = [ctypes.POINTER(ctypes.c_int), i32, vp]
+        ip = ctypes.POINTER(ctypes.c_int32)
+        L.tpk_hybrid_plan.argtypes = [sp, i32, ip, ip, i32, ip, ip, ip]
+        L.tpk_hybrid_plan.restype = i32
         L.tpk_static_scratch_bytes.argtypes = []
         L.tpk_static_scratch_bytes.restype = sz
         L.tpk_decode_hybrid_batched_static.argtypes = [sp, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
@@ -222,6 +226,20 @@ def decode_hybrid_batched_static(shape, n_req, q, k_pool, v_pool, rec_pool, page
     _check(lib().tpk_decode_hybrid_batched_static(ctypes.byref(shape), int(n_req), _ptr(q), _ptr(k_pool),
                                                   _ptr(v_pool), _ptr(rec_pool), _ptr(page_table), pa, pb,
                                                   _ptr(page_table8), pc, pd, _ptr(o), _ptr(lse), _stream(stream)))
+
+
+def hybrid_plan(shape, n_exact_tokens, n_int8_pages, resident_blocks=0):
+    """The split plan of decode_hybrid_batched: (splits_exact, splits_int8, n_units)."""
+    ne = np.ascontiguousarray(n_exact_tokens, np.int32)
+    n8 = np.ascontiguousarray(n_int8_pages, np.int32)
+    se = np.zeros(len(ne), np.int32)
+    s8 = np.zeros(len(ne), np.int32)
+    units = ctypes.c_int32(0)
+    ip = ctypes.POINTER(ctypes.c_int32)
+    _check(lib().tpk_hybrid_plan(ctypes.byref(shape), len(ne), ne.ctypes.data_as(ip), n8.ctypes.data_as(ip),
+                                 int(resident_blocks), se.ctypes.data_as(ip), s8.ctypes.data_as(ip),
+                                 ctypes.byref(units)))
+    return se, s8, units.value
 
 
 def get_device_status(reset=True, stream=None):

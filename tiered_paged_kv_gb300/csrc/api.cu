@@ -164,6 +164,72 @@ int blocks_per_sm(const tpk_shape* s) {
   return mma;
 }
 
+// Split plan of the multi-request call: cnt[2b] / cnt[2b + 1] = units per KV head
+// of request b's exact / 8-bit tier.  Every request's heads share one split of
+// each tier.  The U = waves * per_wave / H unit budget per head (waves: the fewest
+// whole waves of resident blocks giving every segment about 4 units) is shared
+// among the (request, tier) segments in proportion to their bytes (largest
+// remainder, at least one unit per non-empty segment, at most one per page), so
+// units carry about equal bytes and whole waves of resident blocks are filled.
+tpk_status plan_splits(int H, int n_req, const int32_t* n_exact_tokens, const int32_t* n_int8_pages, int per_wave,
+                       std::vector<int>& cnt) {
+  int min_units = 0;
+  for (int b = 0; b < n_req; ++b) min_units += std::max(1, (n_exact_tokens[b] > 0) + (n_int8_pages[b] > 0));
+  if (min_units * H > kMaxUnits)
+    return fail(TPK_ERR_UNSUPPORTED, "%d (request, head, tier) segments exceed %d units", min_units * H, kMaxUnits);
+  // enough waves that segments average at least 4 units (balance across requests)
+  const int want = std::max((per_wave + H - 1) / H, 4 * min_units) * H;
+  const int waves = std::max(1, (want + per_wave - 1) / per_wave);
+  const int U = std::max(min_units, std::min(kMaxUnits, waves * per_wave) / H);
+  std::vector<double> wgt(2 * n_req);
+  std::vector<int> cap(2 * n_req);
+  cnt.assign(2 * n_req, 0);
+  double W = 0.0;
+  for (int b = 0; b < n_req; ++b) {
+    const int ne = n_exact_tokens[b], n8 = n_int8_pages[b];
+    wgt[2 * b] = 1024.0 * ne;
+    wgt[2 * b + 1] = (double)kRecordBytes * n8;
+    cap[2 * b] = ne > 0 ? (ne + kPageTokens - 1) / kPageTokens : (n8 > 0 ? 0 : 1);  // empty request: one empty unit
+    cap[2 * b + 1] = n8;
+    W += wgt[2 * b] + wgt[2 * b + 1];
+  }
+  int used = 0;
+  std::vector<std::pair<double, int>> rem;
+  std::vector<double> ideal(2 * n_req, 0.0);
+  for (int x = 0; x < 2 * n_req; ++x) {
+    if (cap[x] == 0) continue;
+    ideal[x] = W > 0 ? U * wgt[x] / W : 0.0;
+    cnt[x] = std::min(cap[x], std::max(1, (int)std::floor(ideal[x])));
+    used += cnt[x];
+    if (cnt[x] < cap[x]) rem.push_back({ideal[x] - std::floor(ideal[x]), x});
+  }
+  // the one-unit minimum of small segments can overshoot the budget: take units
+  // back from the most over-allocated segments (U >= min_units, so this ends)
+  while (used > U) {
+    int best = -1;
+    double over = -1e300;
+    for (int x = 0; x < 2 * n_req; ++x)
+      if (cnt[x] > 1 && cnt[x] - ideal[x] > over) {
+        over = cnt[x] - ideal[x];
+        best = x;
+      }
+    if (best < 0) break;
+    cnt[best] -= 1;
+    used -= 1;
+  }
+  std::sort(rem.begin(), rem.end(), [](const std::pair<double, int>& a, const std::pair<double, int>& c) {
+    return a.first > c.first || (a.first == c.first && a.second < c.second);
+  });
+  for (size_t k = 0; used < U && k < rem.size(); ++k) {
+    cnt[rem[k].second] += 1;
+    used += 1;
+  }
+  for (int b = 0; b < n_req; ++b)
+    if (cnt[2 * b] > 32767 || cnt[2 * b + 1] > 32767) return fail(TPK_ERR_UNSUPPORTED, "request %d: too many splits", b);
+  if (used * H > kMaxUnits) return fail(TPK_ERR_UNSUPPORTED, "could not plan within %d units", kMaxUnits);
+  return TPK_OK;
+}
+
 tpk_status launch_decode(const tpk_shape* s, const DecodeParams& p, const ReqPlan* req, cudaStream_t st) {
   cudaError_t e = use_simt(s) ? launch_decode_simt(p, req, st) : launch_decode_mma(p, req, st);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
@@ -354,73 +420,15 @@ tpk_status tpk_decode_hybrid_batched(const tpk_shape* shape, int n_req, const vo
   }
   if (any_e && (!k_pool || !v_pool || !page_table)) return fail(TPK_ERR_INVALID, "null BF16 pool or page table");
   if (any_8 && (!rec_pool || !page_table8)) return fail(TPK_ERR_INVALID, "null 8-bit pool or page table");
-  // ---- split plan.  Every request's heads share one split of each tier.  The
-  // U = waves * per_wave / H unit budget per head (waves: the fewest whole
-  // waves of resident blocks giving every segment about 4 units) is shared among the
-  // (request, tier) segments in proportion to their bytes (largest remainder,
-  // at least one unit per non-empty segment, at most one per page), so units
-  // carry about equal bytes and whole waves of resident blocks are filled.
-  const int per_wave = num_sms() * blocks_per_sm(shape);
-  int min_units = 0;
-  for (int b = 0; b < n_req; ++b) min_units += std::max(1, (n_exact_tokens[b] > 0) + (n_int8_pages[b] > 0));
-  if (min_units * H > kMaxUnits)
-    return fail(TPK_ERR_UNSUPPORTED, "%d (request, head, tier) segments exceed %d units", min_units * H, kMaxUnits);
-  // enough waves that segments average at least 4 units (balance across requests)
-  const int want = std::max((per_wave + H - 1) / H, 4 * min_units) * H;
-  const int waves = std::max(1, (want + per_wave - 1) / per_wave);
-  const int U = std::max(min_units, std::min(kMaxUnits, waves * per_wave) / H);
-  std::vector<double> wgt(2 * n_req);
-  std::vector<int> cap(2 * n_req), cnt(2 * n_req);
-  double W = 0.0;
-  for (int b = 0; b < n_req; ++b) {
-    const int ne = n_exact_tokens[b], n8 = n_int8_pages[b];
-    wgt[2 * b] = 1024.0 * ne;
-    wgt[2 * b + 1] = (double)kRecordBytes * n8;
-    cap[2 * b] = ne > 0 ? (ne + kPageTokens - 1) / kPageTokens : (n8 > 0 ? 0 : 1);  // empty request: one empty unit
-    cap[2 * b + 1] = n8;
-    W += wgt[2 * b] + wgt[2 * b + 1];
-  }
-  int used = 0;
-  std::vector<std::pair<double, int>> rem;
-  std::vector<double> ideal(2 * n_req, 0.0);
-  for (int x = 0; x < 2 * n_req; ++x) {
-    if (cap[x] == 0) {
-      cnt[x] = 0;
-      continue;
-    }
-    ideal[x] = W > 0 ? U * wgt[x] / W : 0.0;
-    cnt[x] = std::min(cap[x], std::max(1, (int)std::floor(ideal[x])));
-    used += cnt[x];
-    if (cnt[x] < cap[x]) rem.push_back({ideal[x] - std::floor(ideal[x]), x});
-  }
-  // the one-unit minimum of small segments can overshoot the budget: take units
-  // back from the most over-allocated segments (U >= min_units, so this ends)
-  while (used > U) {
-    int best = -1;
-    double over = -1e300;
-    for (int x = 0; x < 2 * n_req; ++x)
-      if (cnt[x] > 1 && cnt[x] - ideal[x] > over) {
-        over = cnt[x] - ideal[x];
-        best = x;
-      }
-    if (best < 0) break;
-    cnt[best] -= 1;
-    used -= 1;
-  }
-  std::sort(rem.begin(), rem.end(), [](const std::pair<double, int>& a, const std::pair<double, int>& c) {
-    return a.first > c.first || (a.first == c.first && a.second < c.second);
-  });
-  for (size_t k = 0; used < U && k < rem.size(); ++k) {
-    cnt[rem[k].second] += 1;
-    used += 1;
-  }
+  std::vector<int> cnt;
+  st = plan_splits(H, n_req, n_exact_tokens, n_int8_pages, num_sms() * blocks_per_sm(shape), cnt);
+  if (st != TPK_OK) return st;
   DecodeParams p;
   fill_common(p, shape, q);
   std::vector<ReqPlan> req(n_req);
   int units = 0;
   for (int b = 0; b < n_req; ++b) {
     const int se = cnt[2 * b], s8 = cnt[2 * b + 1];
-    if (se > 32767 || s8 > 32767) return fail(TPK_ERR_UNSUPPORTED, "request %d: too many splits", b);
     req[b] = ReqPlan{units, req_page_off[b], 0, n_exact_tokens[b], req_page_off8[b], 0, n_int8_pages[b],
                        (int16_t)se, (int16_t)s8};
     units += H * (se + s8);
@@ -454,6 +462,33 @@ tpk_status tpk_decode_hybrid_batched(const tpk_shape* shape, int n_req, const vo
     cudaError_t e = launch_fold(p, req.data(), reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "fold launch");
   }
+  return TPK_OK;
+}
+
+tpk_status tpk_hybrid_plan(const tpk_shape* shape, int n_req, const int32_t* n_exact_tokens,
+                           const int32_t* n_int8_pages, int resident_blocks, int32_t* splits_exact,
+                           int32_t* splits_int8, int32_t* n_units) {
+  tpk_status st = check_shape(shape);
+  if (st != TPK_OK) return st;
+  if (n_req < 1 || n_req > kMaxReqPerLaunch) return fail(TPK_ERR_INVALID, "n_req %d out of [1, %d]", n_req, kMaxReqPerLaunch);
+  if (!n_exact_tokens || !n_int8_pages || !splits_exact || !splits_int8 || !n_units)
+    return fail(TPK_ERR_INVALID, "null pointer argument");
+  if (resident_blocks < 0) return fail(TPK_ERR_INVALID, "resident_blocks %d < 0", resident_blocks);
+  for (int b = 0; b < n_req; ++b) {
+    if (n_exact_tokens[b] < 0 || n_int8_pages[b] < 0) return fail(TPK_ERR_INVALID, "request %d: negative length", b);
+    if (n_int8_pages[b] > 0x7fffffff / kPageTokens) return fail(TPK_ERR_INVALID, "request %d: too many pages", b);
+  }
+  const int per_wave = resident_blocks > 0 ? resident_blocks : num_sms() * blocks_per_sm(shape);
+  std::vector<int> cnt;
+  st = plan_splits(shape->kv_heads, n_req, n_exact_tokens, n_int8_pages, per_wave, cnt);
+  if (st != TPK_OK) return st;
+  int units = 0;
+  for (int b = 0; b < n_req; ++b) {
+    splits_exact[b] = cnt[2 * b];
+    splits_int8[b] = cnt[2 * b + 1];
+    units += shape->kv_heads * (cnt[2 * b] + cnt[2 * b + 1]);
+  }
+  *n_units = units;
   return TPK_OK;
 }
 
