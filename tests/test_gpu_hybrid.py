@@ -162,3 +162,15 @@ def test_maximum_kv_heads():
     w = synth.make_workload([64 + 40], 40, H=1024, seed=63)
     assert w.n8[0] == 1
     check_hybrid(w, tpk.IMPL_TENSOR, gpu_records=True, what="1024 heads")
+
+
+def test_plan_on_this_device():
+    """The plan the call makes on this GPU for the 128K hybrid: one wave of the
+    tensor-core kernel (one block per SM), split 2 + 36 per head."""
+    t = __import__("torch")
+    sms = t.cuda.get_device_properties(0).multi_processor_count
+    se, s8, units = tpk.hybrid_plan(tpk.Shape(4, impl=tpk.IMPL_TENSOR), [4096], [1984], 0)
+    assert units == sms * (sms // 4 * 4 == sms) or units <= 2048
+    assert units % 4 == 0 and (se[0] + s8[0]) * 4 == units
+    if sms == 152:
+        assert (se[0], s8[0], units) == (2, 36, 152)
