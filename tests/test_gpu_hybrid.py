@@ -170,7 +170,7 @@ def test_plan_on_this_device():
     t = __import__("torch")
     sms = t.cuda.get_device_properties(0).multi_processor_count
     se, s8, units = tpk.hybrid_plan(tpk.Shape(4, impl=tpk.IMPL_TENSOR), [4096], [1984], 0)
-    assert units == sms * (sms // 4 * 4 == sms) or units <= 2048
-    assert units % 4 == 0 and (se[0] + s8[0]) * 4 == units
+    assert units <= 2048 and (se[0] + s8[0]) * 4 == units
+    assert units >= sms // 4 * 4   # at least one full wave of the resident blocks
     if sms == 152:
         assert (se[0], s8[0], units) == (2, 36, 152)
