@@ -174,3 +174,17 @@ def test_plan_on_this_device():
     assert units >= sms // 4 * 4   # at least one full wave of the resident blocks
     if sms == 152:
         assert (se[0], s8[0], units) == (2, 36, 152)
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+@pytest.mark.parametrize("log2_scale", [-24, -8, 3, 6])
+def test_extreme_query_scales(impl, log2_scale):
+    """q times 2^k (exact in bfloat16): near-uniform weights for small k, a few
+    dominant tokens for large k (lse near 1,000 nats at 2^6, in both tiers).  Larger
+    scales leave float32 itself: at 2^12 the lse is 65,000 nats, where one float32
+    ulp exceeds the 1e-3 bar."""
+    w = synth.make_workload([64 * 20 + 30, 900], 200, H=2, seed=64, key_sigma="outliers")
+    q = synth.bf16_to_f32(w.q).astype(np.float64) * 2.0 ** log2_scale
+    w.q = synth.f32_to_bf16(q.astype(np.float32))
+    assert np.array_equal(synth.bf16_to_f32(w.q).astype(np.float64), q)
+    check_hybrid(w, impl, what=f"q x 2^{log2_scale}")
