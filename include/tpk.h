@@ -384,6 +384,17 @@ tpk_status tpk_tiers_sync(tpk_tiers* tiers);
 tpk_status tpk_tiers_destroy(tpk_tiers* tiers);
 
 /*
+ * Measurement hook: while set, every decode-kernel launch of the library (the
+ * partial calls and the decode launch of the multi-request call, not its fold) is
+ * preceded by a record of `before` and followed by a record of `after` on the
+ * launch stream (cudaEvent_t created with timing enabled), as external records, so
+ * a CUDA graph captured meanwhile records them on each replay and
+ * cudaEventElapsedTime(before, after) is the decode kernel's own duration.  Both
+ * null clears it.  Process-wide; set it only while no other thread launches.
+ */
+tpk_status tpk_set_decode_timing_events(void* before, void* after);
+
+/*
  * Device status word: bit 0 = a page-table entry outside the pool was skipped,
  * bit 1 = a bounded device-side wait gave up, bit 2 = a malformed 13-bit record was
  * skipped.  Synchronises `stream`, stores the word in *flags and, if reset != 0,

@@ -88,6 +88,11 @@ def test_pack13_arguments_are_validated_before_any_device_call(L):
     assert L.tpk_kv_unpack13_pages(ctypes.byref(tpk.Shape(4, group=4)), 16, 0, 16, 16, 1, 16, 16, None) == 2
 
 
+def test_timing_events_come_in_pairs(L):
+    assert L.tpk_set_decode_timing_events(ctypes.c_void_p(16), None) == 1
+    assert L.tpk_set_decode_timing_events(None, None) == 0
+
+
 def test_hybrid_host_metadata_is_validated(L):
     s = tpk.Shape(2)
     need = L.tpk_hybrid_workspace_bytes(ctypes.byref(s), 2)

@@ -199,3 +199,42 @@ def test_extreme_query_scales(impl, log2_scale):
     assert np.array_equal(np.isfinite(lse), np.isfinite(ol))
     fin = np.isfinite(ol)
     assert (np.abs(lse[fin] - ol[fin]) <= 1e-3 + 1e-5 * np.abs(ol[fin])).all()
+
+
+def test_decode_timing_events_bracket_the_decode_kernel():
+    """The measurement hook: events recorded around the decode launch inside a
+    captured graph time the decode kernel alone (shorter than the whole step)."""
+    t = __import__("torch")
+    w = synth.hybrid_128k(seed=2, n_tokens=32768, recent=1024)
+    d = DevWorkload(w, tpk.IMPL_TENSOR)
+    d.quantize_gpu()
+    nbytes = tpk.hybrid_workspace_bytes(d.shape, w.B)
+    ws = t.zeros(nbytes, dtype=t.uint8, device="cuda")
+    o = t.empty(w.B, w.H * w.G, 256, dtype=t.float32, device="cuda")
+    lse = t.empty(w.B, w.H * w.G, dtype=t.float32, device="cuda")
+    s = t.cuda.Stream()
+    step = lambda: tpk.decode_hybrid_batched(d.shape, w.B, d.q, d.k, d.v, d.rec, d.pt, d.off, w.n_ex, d.pt8,
+                                             d.off8, w.n8, o, lse, ws, nbytes, s)
+    before, after = t.cuda.Event(enable_timing=True), t.cuda.Event(enable_timing=True)
+    a, b = t.cuda.Event(enable_timing=True), t.cuda.Event(enable_timing=True)
+    with t.cuda.stream(s):
+        step()
+        before.record(s)
+        after.record(s)
+        s.synchronize()
+        tpk.set_decode_timing_events(before, after)
+        try:
+            g = t.cuda.CUDAGraph()
+            with t.cuda.graph(g, stream=s, capture_error_mode="thread_local"):
+                step()
+        finally:
+            tpk.set_decode_timing_events()
+        for _ in range(3):
+            a.record(s)
+            g.replay()
+            b.record(s)
+            s.synchronize()
+            k_ms, step_ms = before.elapsed_time(after), a.elapsed_time(b)
+            assert 0 < k_ms < step_ms
+    st, flags = tpk.get_device_status(reset=True)
+    assert st == 0, flags

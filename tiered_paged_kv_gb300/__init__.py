@@ -20,6 +20,7 @@ __all__ = [
     "Shape", "TpkError", "lib", "RECORD_BYTES", "IMPL_DEFAULT", "IMPL_SIMT", "IMPL_TENSOR",
     "kv_quantize_pages", "kv_quantize_pages_given_scales", "decode_attn_exact", "decode_attn_int8",
     "merge_lse", "hybrid_workspace_bytes", "workspace_init", "decode_hybrid_batched", "hybrid_plan",
+    "set_decode_timing_events",
     "get_device_status",
     "static_scratch_bytes", "decode_hybrid_batched_static", "Stager", "Tiers", "TiersPlan",
     "PACK13_RECORD_BYTES", "PACK13_PLANE_ENC", "PACK13_PLANE_RAW", "kv_pack13_pages", "kv_unpack13_pages",
@@ -85,6 +86,8 @@ def lib():
         L.tpk_workspace_init.argtypes = [vp, sz, vp]
         L.tpk_decode_hybrid_batched.argtypes = [sp, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         L.tpk_get_device_status.argtypes = [ctypes.POINTER(ctypes.c_int), i32, vp]
+        L.tpk_set_decode_timing_events.argtypes = [vp, vp]
+        L.tpk_set_decode_timing_events.restype = i32
         ip = ctypes.POINTER(ctypes.c_int32)
         L.tpk_hybrid_plan.argtypes = [sp, i32, ip, ip, i32, ip, ip, ip]
         L.tpk_hybrid_plan.restype = i32
@@ -240,6 +243,13 @@ def hybrid_plan(shape, n_exact_tokens, n_int8_pages, resident_blocks=0):
                                  int(resident_blocks), se.ctypes.data_as(ip), s8.ctypes.data_as(ip),
                                  ctypes.byref(units)))
     return se, s8, units.value
+
+
+def set_decode_timing_events(before=None, after=None):
+    """Record two torch.cuda.Event (timing enabled) around every decode-kernel
+    launch until called with no events (see tpk_set_decode_timing_events)."""
+    _check(lib().tpk_set_decode_timing_events(before.cuda_event if before is not None else None,
+                                              after.cuda_event if after is not None else None))
 
 
 def get_device_status(reset=True, stream=None):

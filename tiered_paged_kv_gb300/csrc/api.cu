@@ -230,9 +230,22 @@ tpk_status plan_splits(int H, int n_req, const int32_t* n_exact_tokens, const in
   return TPK_OK;
 }
 
+// Timing events recorded around every decode-kernel launch while set (see
+// tpk_set_decode_timing_events); external records, so that a captured graph
+// records them on each replay.
+cudaEvent_t g_decode_ev[2] = {nullptr, nullptr};
+
 tpk_status launch_decode(const tpk_shape* s, const DecodeParams& p, const ReqPlan* req, cudaStream_t st) {
+  if (g_decode_ev[0]) {
+    cudaError_t e = cudaEventRecordWithFlags(g_decode_ev[0], st, cudaEventRecordExternal);
+    if (e != cudaSuccess) return cuda_fail(e, "timing event");
+  }
   cudaError_t e = use_simt(s) ? launch_decode_simt(p, req, st) : launch_decode_mma(p, req, st);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  if (g_decode_ev[1]) {
+    e = cudaEventRecordWithFlags(g_decode_ev[1], st, cudaEventRecordExternal);
+    if (e != cudaSuccess) return cuda_fail(e, "timing event");
+  }
   return TPK_OK;
 }
 
@@ -462,6 +475,13 @@ tpk_status tpk_decode_hybrid_batched(const tpk_shape* shape, int n_req, const vo
     cudaError_t e = launch_fold(p, req.data(), reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "fold launch");
   }
+  return TPK_OK;
+}
+
+tpk_status tpk_set_decode_timing_events(void* before, void* after) {
+  if ((before == nullptr) != (after == nullptr)) return fail(TPK_ERR_INVALID, "set both timing events or neither");
+  g_decode_ev[0] = static_cast<cudaEvent_t>(before);
+  g_decode_ev[1] = static_cast<cudaEvent_t>(after);
   return TPK_OK;
 }
 
