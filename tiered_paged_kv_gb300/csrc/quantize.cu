@@ -26,6 +26,8 @@
 //      rounded quotients (by reciprocal multiplication, with IEEE divisions
 //      wherever that could differ).
 // Fields are written at their swizzled positions (kc_byte, vc_byte, ks_index).
+#include <cmath>
+
 #include "common.cuh"
 
 namespace tpk {
@@ -33,7 +35,7 @@ namespace tpk {
 struct QSmem {
   alignas(128) uint16_t k[kPageTokens][kHeadDim];
   uint64_t bar;
-  double red_m[8];
+  float2 red_m[8];
   int red_e[8];
   double invG;
   alignas(16) float s[kHeadDim];
@@ -126,6 +128,33 @@ __device__ __forceinline__ bool fast_scale(float scale) { return scale >= 0x1p-1
 
 constexpr int kQuantThreads = 256;  // one thread per channel in the per-channel phases
 
+// ---- float-float arithmetic on the FP32 pipe (GB300's FP64 rate is a small
+// fraction of its FP32 rate): a value is hi + lo with |lo| about ulp(hi) / 2 or
+// less.  Knuth's TwoSum and the FMA product error; the _rn intrinsics keep the
+// compiler from contracting the error terms away.
+struct DF {
+  float hi, lo;
+};
+__device__ __forceinline__ DF df_fast_renorm(float s, float e) {  // |s| >= |e|
+  const float h = __fadd_rn(s, e);
+  return {h, __fsub_rn(e, __fsub_rn(h, s))};
+}
+__device__ __forceinline__ DF df_mul(DF a, DF b) {
+  const float p = __fmul_rn(a.hi, b.hi);
+  float e = fmaf(a.hi, b.hi, -p);
+  e = __fadd_rn(e, __fadd_rn(__fmul_rn(a.hi, b.lo), __fmul_rn(a.lo, b.hi)));
+  return df_fast_renorm(p, e);
+}
+__device__ __forceinline__ DF df_add(DF a, DF b) {
+  const float s = __fadd_rn(a.hi, b.hi), bb = __fsub_rn(s, a.hi);
+  const float e = __fadd_rn(__fadd_rn(__fsub_rn(a.hi, __fsub_rn(s, bb)), __fsub_rn(b.hi, bb)), __fadd_rn(a.lo, b.lo));
+  const float h = __fadd_rn(s, e);  // s may be smaller than e after cancellation: full TwoSum
+  const float hb = __fsub_rn(h, s);
+  return {h, __fadd_rn(__fsub_rn(s, __fsub_rn(h, hb)), __fsub_rn(e, hb))};
+}
+// 2^(-i / 256), i = 0..255, as float pairs (filled from the host once per device)
+__constant__ float2 c_pow2_neg[256];
+
 
 __global__ void __launch_bounds__(kQuantThreads, 2) quantize_kernel(const __grid_constant__ QuantParams p) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -145,6 +174,9 @@ __global__ void __launch_bounds__(kQuantThreads, 2) quantize_kernel(const __grid
       int64_t off = (src * p.H + h) * (int64_t)(kPageTokens * kHeadDim);
       mbar_arrive_expect_tx(&S.bar, kBf16PageHeadBytes);
       bulk_g2s(&S.k[0][0], p.k_pool + off, kBf16PageHeadBytes, &S.bar);
+      // the values are read from global memory: start bringing them into L2 now
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p.v_pool + off), "r"(kBf16PageHeadBytes)
+                   : "memory");
     }
   }
   __syncthreads();
@@ -209,8 +241,8 @@ __global__ void __launch_bounds__(kQuantThreads, 2) quantize_kernel(const __grid
     //    is scaled by a power of two 2^-e (e the exponent of its largest |k|), so
     //    every square of a bfloat16 is exact in float32 and below 4; the squares
     //    are added with TwoSum into a float pair (relative error below 2^-42),
-    //    then the mean is formed in double with the scale put back.  A zero
-    //    channel takes a = 2^-63 before the logarithm.
+    //    then the mean is formed in double with the scale put back (for step 4).
+    //    A zero channel takes a = 2^-63, i.e. a mean square of 2^-252.
     float vmax = 0.f;
     #pragma unroll 16
     for (int t = 0; t < kPageTokens; ++t) vmax = fmaxf(vmax, fabsf(bf16_lo(__ldg(&gv[t][c]))));
@@ -218,48 +250,80 @@ __global__ void __launch_bounds__(kQuantThreads, 2) quantize_kernel(const __grid
     double ms;
     float kmax = 0.f;
     for (int t = 0; t < kPageTokens; ++t) kmax = fmaxf(kmax, fabsf(bf16_lo(S.k[t][c])));
-    if (kmax > 0.f) {
-      int e = 0;
-      frexpf(kmax, &e);
-      const float sc = ldexpf(1.f, -e);  // kmax * sc in [0.5, 1)
-      float hi = 0.f, lo = 0.f;
+    const bool kmax_pos = kmax > 0.f;
+    float hsum = 0.f, lsum = 0.f;  // sum of the scaled squares, as a float pair
+    int kexp = 0;
+    if (kmax_pos) {
+      frexpf(kmax, &kexp);
+      const float sc = ldexpf(1.f, -kexp);  // kmax * sc in [0.5, 1)
       for (int t = 0; t < kPageTokens; ++t) {
         const float y = bf16_lo(S.k[t][c]) * sc;
         const float sq = y * y;
-        const float sum = hi + sq, bb = sum - hi;
-        lo += (hi - (sum - bb)) + (sq - bb);
-        hi = sum;
+        const float sum = hsum + sq, bb = sum - hsum;
+        lsum += (hsum - (sum - bb)) + (sq - bb);
+        hsum = sum;
       }
-      ms = ldexp((double)hi + (double)lo, 2 * e - 6);  // mean over 64 tokens
+      ms = ldexp((double)hsum + (double)lsum, 2 * kexp - 6);  // mean over 64 tokens
     } else {
       ms = 0x1p-252;
     }
-    // 3. geometric mean of ms over channels: product of mantissas, sum of exponents
-    int expo = 0;
-    double mant = frexp(ms, &expo);
+    // 3. geometric mean G of ms over channels, as 1 / G: the product of the mean
+    //    squares as a normalised float pair m (in [1, 2]) and an exponent sum E,
+    //    multiplied in a shuffle tree; then 1 / G = (m 2^E)^(-1/256) = m^(-1/256)
+    //    2^(-E/256), with m^(-1/256) by two Newton steps on z^256 m = 1 (seeded in
+    //    float, each step squaring the error) and 2^(-E/256) = 2^-q 2^(-r/256), E =
+    //    256 q + r, from a table.  Relative error about 2^-45, all on the FP32 pipe.
+    DF m;
+    int E;
+    if (kmax_pos) {
+      m = df_fast_renorm(hsum, lsum);
+      const int k = ilogbf(m.hi);
+      m = {ldexpf(m.hi, -k), ldexpf(m.lo, -k)};
+      E = 2 * kexp - 6 + k;
+    } else {
+      m = {1.f, 0.f};  // 2^-252: a = 2^-63
+      E = -252;
+    }
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) {
-      const double mo = __shfl_xor_sync(0xffffffffu, mant, off);
-      const int eo = __shfl_xor_sync(0xffffffffu, expo, off);
-      int t;
-      mant = frexp(mant * mo, &t);
-      expo += eo + t;
+      const DF mo = {__shfl_xor_sync(0xffffffffu, m.hi, off), __shfl_xor_sync(0xffffffffu, m.lo, off)};
+      E += __shfl_xor_sync(0xffffffffu, E, off);
+      m = df_mul(m, mo);
+      if (m.hi >= 2.f) {
+        m = {m.hi * 0.5f, m.lo * 0.5f};
+        E += 1;
+      }
     }
     if ((tid & 31) == 0) {
-      S.red_m[tid >> 5] = mant;
-      S.red_e[tid >> 5] = expo;
+      S.red_m[tid >> 5] = make_float2(m.hi, m.lo);
+      S.red_e[tid >> 5] = E;
     }
     __syncthreads();
     if (tid == 0) {
-      double m = S.red_m[0];
-      int e = S.red_e[0];
+      DF mm = {S.red_m[0].x, S.red_m[0].y};
+      int ee = S.red_e[0];
       for (int w = 1; w < kQuantThreads / 32; ++w) {
-        int t;
-        m = frexp(m * S.red_m[w], &t);
-        e += S.red_e[w] + t;
+        mm = df_mul(mm, DF{S.red_m[w].x, S.red_m[w].y});
+        ee += S.red_e[w];
+        if (mm.hi >= 2.f) {
+          mm = {mm.hi * 0.5f, mm.lo * 0.5f};
+          ee += 1;
+        }
       }
-      const double lnG = (log(m) + (double)e * 0.69314718055994530942) / kHeadDim;
-      S.invG = exp(-lnG);
+      DF z = {exp2f(-log2f(mm.hi) * (1.f / kHeadDim)), 0.f};
+      for (int it = 0; it < 2; ++it) {
+        DF z256 = z;
+#pragma unroll
+        for (int sq = 0; sq < 8; ++sq) z256 = df_mul(z256, z256);
+        const DF t = df_mul(z256, mm);                           // about 1
+        DF d = df_add(DF{1.f, 0.f}, DF{-t.hi, -t.lo});           // 1 - m z^256
+        d = {d.hi * (1.f / kHeadDim), d.lo * (1.f / kHeadDim)};  // (1 - m z^256) / 256
+        z = df_add(z, df_mul(z, d));
+      }
+      const int q = (ee >= 0) ? ee / kHeadDim : -((-ee + kHeadDim - 1) / kHeadDim);
+      const float2 w = c_pow2_neg[ee - kHeadDim * q];
+      const DF inv = df_mul(z, DF{w.x, w.y});
+      S.invG = ldexp((double)inv.hi + (double)inv.lo, -q);
     }
     __syncthreads();
     // 4. float32 neighbours of shat_c = (ms_c / G)^(1/4), clamped to 2^+-14.  A
@@ -435,11 +499,27 @@ __global__ void __launch_bounds__(kQuantThreads, 2) quantize_kernel(const __grid
 
 cudaError_t launch_quantize(const QuantParams& p, int n_pages, cudaStream_t stream) {
   static bool configured = false;
+  static bool table_ready[64] = {false};
   const int smem = (int)sizeof(QSmem);
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(quantize_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     configured = true;
+  }
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!table_ready[dev]) {  // 2^(-i/256) split into float pairs, once per device
+    float2 t[256];
+    for (int i = 0; i < 256; ++i) {
+      const double v = std::exp2(-i / 256.0);
+      const float hi = (float)v;
+      t[i] = make_float2(hi, (float)(v - (double)hi));
+    }
+    e = cudaMemcpyToSymbol(c_pow2_neg, t, sizeof t);
+    if (e != cudaSuccess) return e;
+    table_ready[dev] = true;
   }
   if (n_pages == 0) return cudaSuccess;
   quantize_kernel<<<n_pages * p.H, kQuantThreads, smem, stream>>>(p);
