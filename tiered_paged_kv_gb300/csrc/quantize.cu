@@ -10,8 +10,8 @@
 //   1. the keys are bulk-copied into shared memory (the values, read twice, come
 //      from global memory, so four blocks fit on an SM);
 //   2. thread c owns channel c: u_c = max|v| / 127, and the key mean square with
-//      compensated float32 additions of exact squares (relative error below
-//      2^-42);
+//      compensated float32 additions of exact squares in two chains of 32 (relative
+//      error below gamma_31^2 < 2^-38, the bound of Ogita, Rump and Oishi's Sum2);
 //   3. the geometric mean of the mean squares as a product of mantissas (double)
 //      and a sum of exponents, so the normalised fourth power x_c = ms_c / G
 //      needs one multiplication; shat_c = x_c^(1/4);
@@ -106,23 +106,43 @@ __device__ __forceinline__ uint32_t code_byte(float x, float scale) {
 constexpr float kCodeSlack = 0x1p-12f;
 __device__ __forceinline__ bool near_half(float z) { return 0.5f - fabsf(z - rintf(z)) <= kCodeSlack; }
 
+// ---- packed float pairs: one instruction does the FP32 work of two elements, which
+// halves the issue slots of the arithmetic below (the kernel is bound by instruction
+// issue).  b - a as fma(a, -1, b): the exact difference, rounded once, as a subtraction.
+__device__ __forceinline__ float2 sub2(float2 b, float2 a) { return __ffma2_rn(a, make_float2(-1.f, -1.f), b); }
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 // Four codes from estimates known to lie within 127 (1 + 2^-20) in magnitude (codes
-// of pages converted here: the scales come from the maxima, so no clamp is
-// needed): adding 1.5 * 2^23 puts z in [2^23, 2^24), where float32 spacing is 1, so
-// the addition rounds half to even exactly like rint, and the low byte of the sum's
-// encoding is rint(z) mod 256; XOR 0x80 makes it the stored byte rint(z) + 128.
-// Sets bit e of `near` when estimate e is within kCodeSlack of a half-integer.
-constexpr float kRoundMagic = 12582912.f;  // 1.5 * 2^23
-__device__ __forceinline__ uint32_t code_word4(const float (&z)[4], uint32_t& near, int shift) {
-  uint32_t t[4];
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const float te = __fadd_rn(z[e], kRoundMagic);
-    const float r = __fsub_rn(te, kRoundMagic);
-    near |= (uint32_t)(0.5f - fabsf(z[e] - r) <= kCodeSlack) << (shift + e);
-    t[e] = __float_as_uint(te);
-  }
-  return __byte_perm(__byte_perm(t[0], t[1], 0x0040), __byte_perm(t[2], t[3], 0x0040), 0x5410) ^ 0x80808080u;
+// of pages converted here: the scales come from the maxima, so no clamp is needed),
+// as one word of stored bytes.  Adding M = 1.5 * 2^23 + 128 puts z + M in [2^23,
+// 2^24), where float32 spacing is 1, so the sum rounds half to even exactly like
+// rint (M is even), and the low byte of its encoding is (rint(z) + 128) mod 256, the
+// stored byte.  With d = z - rint(z) (exact), z lies within kCodeSlack of a
+// half-integer iff |d| >= 1/2 - kCodeSlack, i.e. iff d^2 - (1/2 - kCodeSlack)^2 >= 0;
+// the square of 2047/4096 is a float, so one fused multiply-add gives that sign
+// exactly: e >= 0 (sign bit clear) marks an estimate to redo by division.
+constexpr float kRoundMagic = 12583040.f;       // 1.5 * 2^23 + 128
+constexpr float kNearSq = 4190209.f * 0x1p-24f;  // (1/2 - 2^-12)^2
+__device__ __forceinline__ uint32_t code_word4(float2 z01, float2 z23, float2& e01, float2& e23) {
+  const float2 m = make_float2(kRoundMagic, kRoundMagic), nc = make_float2(-kNearSq, -kNearSq);
+  const float2 t01 = __fadd2_rn(z01, m), t23 = __fadd2_rn(z23, m);
+  const float2 d01 = sub2(z01, sub2(t01, m)), d23 = sub2(z23, sub2(t23, m));
+  e01 = __ffma2_rn(d01, d01, nc);
+  e23 = __ffma2_rn(d23, d23, nc);
+  return __byte_perm(__byte_perm(__float_as_uint(t01.x), __float_as_uint(t01.y), 0x0040),
+                     __byte_perm(__float_as_uint(t23.x), __float_as_uint(t23.y), 0x0040), 0x5410);
+}
+// AND of the encodings: sign bit clear iff some e >= 0 (some estimate to redo)
+__device__ __forceinline__ uint32_t and_bits(float2 a, float2 b) {
+  return __float_as_uint(a.x) & __float_as_uint(a.y) & __float_as_uint(b.x) & __float_as_uint(b.y);
+}
+// bits shift, shift + 1 set where e.x, e.y >= 0
+__device__ __forceinline__ uint32_t near_bits(float2 e, int shift) {
+  return ((((__float_as_uint(e.x) >> 31) | ((__float_as_uint(e.y) >> 31) << 1))) ^ 3u) << shift;
 }
 __device__ __forceinline__ bool fast_scale(float scale) { return scale >= 0x1p-100f && scale <= 0x1p100f; }
 
@@ -211,12 +231,22 @@ __global__ void __launch_bounds__(kQuantThreads, 2) quantize_kernel(const __grid
         wv[e >> 2] |= quotient_byte(z) << (8 * (e & 3));
       }
     } else {
+      const float2 inv2 = make_float2(inv, inv);
+      float2 ev[8];
 #pragma unroll
       for (int g = 0; g < 4; ++g) {
-        float z[4];
+        const int t = t0 + 4 * g;
+        const float2 z01 =
+            __fmul2_rn(make_float2(bf16_lo(__ldg(&gv[t][ch])), bf16_lo(__ldg(&gv[t + 1][ch]))), inv2);
+        const float2 z23 =
+            __fmul2_rn(make_float2(bf16_lo(__ldg(&gv[t + 2][ch])), bf16_lo(__ldg(&gv[t + 3][ch]))), inv2);
+        wv[g] = code_word4(z01, z23, ev[2 * g], ev[2 * g + 1]);
+      }
+      const uint32_t all = and_bits(ev[0], ev[1]) & and_bits(ev[2], ev[3]) & and_bits(ev[4], ev[5]) &
+                           and_bits(ev[6], ev[7]);
+      if (!(all >> 31)) {  // rare: some estimate near a half-integer
 #pragma unroll
-        for (int e = 0; e < 4; ++e) z[e] = bf16_lo(__ldg(&gv[t0 + 4 * g + e][ch])) * inv;
-        wv[g] = code_word4(z, redo, 4 * g);
+        for (int j = 0; j < 8; ++j) redo |= near_bits(ev[j], 2 * j);
       }
     }
     uint8_t* dst = rec + kOffVc + vc_byte(ch, t0);
@@ -237,23 +267,42 @@ __global__ void __launch_bounds__(kQuantThreads, 2) quantize_kernel(const __grid
     __syncthreads();
     for (int it = tid; it < kValueItems; it += kQuantThreads) value_codes(it & 255, (it >> 8) * 16);
   } else {
-    // 2. thread c: u_c = max|v| / 127, and the key mean square.  The key channel
-    //    is scaled by a power of two 2^-e (e the exponent of its largest |k|), so
-    //    every square of a bfloat16 is exact in float32 and below 4; the squares
-    //    are added with TwoSum into a float pair (relative error below 2^-42),
-    //    then the mean is formed in double with the scale put back (for step 4).
+    // 2. thread c: u_c = max|v| / 127, and the key mean square: exact squares
+    //    added with TwoSum into float pairs, then the mean in double (for step 4).
     //    A zero channel takes a = 2^-63, i.e. a mean square of 2^-252.
     float vmax = 0.f;
-    #pragma unroll 16
-    for (int t = 0; t < kPageTokens; ++t) vmax = fmaxf(vmax, fabsf(bf16_lo(__ldg(&gv[t][c]))));
+#pragma unroll 16
+    for (int t = 0; t < kPageTokens; t += 2)
+      vmax = fmax3(vmax, fabsf(bf16_lo(__ldg(&gv[t][c]))), fabsf(bf16_lo(__ldg(&gv[t + 1][c]))));
     S.u[c] = __fdiv_rn(vmax, 127.f);
-    double ms;
+    // One pass over the key channel: max |k|, and the sum of squares in two TwoSum
+    // chains (even and odd tokens) as packed pairs.  A square of a bfloat16 is exact
+    // in float32 unless it underflows or overflows; for 2^-40 <= max|k| < 2^40 the sum
+    // stays far below overflow and the underflowing squares (|k| < 2^-63) are below
+    // 2^-60 of it, so the pair is used as is.  Outside that range the channel is
+    // summed again scaled by 2^-e (e the exponent of max|k|), which makes every
+    // square exact and below 1.
     float kmax = 0.f;
-    for (int t = 0; t < kPageTokens; ++t) kmax = fmaxf(kmax, fabsf(bf16_lo(S.k[t][c])));
+    float2 h2 = make_float2(0.f, 0.f), l2 = make_float2(0.f, 0.f);
+#pragma unroll 8
+    for (int t = 0; t < kPageTokens; t += 2) {
+      const float2 kk = make_float2(bf16_lo(S.k[t][c]), bf16_lo(S.k[t + 1][c]));
+      kmax = fmax3(kmax, fabsf(kk.x), fabsf(kk.y));
+      const float2 sq = __fmul2_rn(kk, kk);
+      const float2 sum = __fadd2_rn(h2, sq), bb = sub2(sum, h2);
+      l2 = __fadd2_rn(l2, __fadd2_rn(sub2(h2, sub2(sum, bb)), sub2(sq, bb)));
+      h2 = sum;
+    }
     const bool kmax_pos = kmax > 0.f;
-    float hsum = 0.f, lsum = 0.f;  // sum of the scaled squares, as a float pair
+    float hsum = 0.f, lsum = 0.f;  // the sum of squares (scaled by 2^-2kexp), as a float pair
     int kexp = 0;
-    if (kmax_pos) {
+    double ms;
+    if (kmax >= 0x1p-40f && kmax < 0x1p40f) {
+      const DF sum = df_add(DF{h2.x, l2.x}, DF{h2.y, l2.y});
+      hsum = sum.hi;
+      lsum = sum.lo;
+      ms = ldexp((double)hsum + (double)lsum, -6);  // mean over 64 tokens
+    } else if (kmax_pos) {
       frexpf(kmax, &kexp);
       const float sc = ldexpf(1.f, -kexp);  // kmax * sc in [0.5, 1)
       for (int t = 0; t < kPageTokens; ++t) {
@@ -263,7 +312,7 @@ __global__ void __launch_bounds__(kQuantThreads, 2) quantize_kernel(const __grid
         lsum += (hsum - (sum - bb)) + (sq - bb);
         hsum = sum;
       }
-      ms = ldexp((double)hsum + (double)lsum, 2 * kexp - 6);  // mean over 64 tokens
+      ms = ldexp((double)hsum + (double)lsum, 2 * kexp - 6);
     } else {
       ms = 0x1p-252;
     }
@@ -337,18 +386,31 @@ __global__ void __launch_bounds__(kQuantThreads, 2) quantize_kernel(const __grid
       } else if (x <= 0x1p-56) {
         lo = hi = 0x1p-14f;
       } else {
+        // the square root of the square root of x rounded to float lies within 2 ulp
+        // of shat: step from it, one neighbour at a time, to the bracket lo^4 <= x <
+        // hi^4 (hi the successor of lo); two evaluations as a rule
         float cc = sqrtf(sqrtf((float)x));
-        for (int it = 0; it < 4; ++it) {
-          if (pow4_diff(cc, x).sign > 0) cc = nextafterf(cc, 0.f);
-          else if (pow4_diff(nextafterf(cc, 0x1p127f), x).sign <= 0) cc = nextafterf(cc, 0x1p127f);
-          else break;
+        Pow4Diff dc = pow4_diff(cc, x);
+        float nb = cc;
+        Pow4Diff dn = dc;
+        if (dc.sign != 0) {
+          const float dir = dc.sign > 0 ? 0.f : 0x1p127f;  // towards shat
+          for (int it = 0; it < 4; ++it) {
+            nb = nextafterf(cc, dir);
+            dn = pow4_diff(nb, x);
+            if (dn.sign != dc.sign) break;  // shat lies between cc and nb (or at nb)
+            cc = nb;
+            dc = dn;
+          }
         }
-        const Pow4Diff d = pow4_diff(cc, x);
-        lo = hi = cc;
-        if (d.sign != 0) {
-          hi = nextafterf(cc, 0x1p127f);
+        if (dc.sign == 0 || dn.sign == 0) {
+          lo = hi = dc.sign == 0 ? cc : nb;  // shat is a float
+        } else {
+          const bool up = dc.sign < 0;  // cc below shat, nb above
+          lo = up ? cc : nb;
+          hi = up ? nb : cc;
           // ln(c / shat) = ln(1 + a) / 4 for the relative error a of the fourth power
-          const float a = d.rel, b = pow4_diff(hi, x).rel;
+          const float a = up ? dc.rel : dn.rel, b = up ? dn.rel : dc.rel;
           dl = fmaf(-0.125f * a, a, 0.25f * a);
           dh = fmaf(-0.125f * b, b, 0.25f * b);
         }
@@ -409,50 +471,54 @@ __global__ void __launch_bounds__(kQuantThreads, 2) quantize_kernel(const __grid
   //         2^-20 of the estimated maximum (the argmax is among them).
   {
     const int t = tid >> 2, q = tid & 3, lane = tid & 31;
-    // the estimates y = k * (1/s_c) of chunk k (8 channels); recomputed in each
-    // pass, which costs less than holding 64 of them in registers
-    auto estimates = [&](int k, float (&yv)[8]) {
+    // the estimates y = k * (1/s_c) of chunk k (8 channels, as 4 pairs); recomputed
+    // in each pass, which costs less than holding 64 of them in registers
+    auto estimates = [&](int k, float2(&y)[4]) {
       const int ch0 = q * 64 + ((k + lane) & 7) * 8;
       const uint4 w = *reinterpret_cast<const uint4*>(&S.k[t][ch0]);
       const float4 i0 = *reinterpret_cast<const float4*>(&S.inv_s[ch0]);
       const float4 i1 = *reinterpret_cast<const float4*>(&S.inv_s[ch0 + 4]);
-      yv[0] = bf16_lo(w.x) * i0.x;
-      yv[1] = bf16_hi(w.x) * i0.y;
-      yv[2] = bf16_lo(w.y) * i0.z;
-      yv[3] = bf16_hi(w.y) * i0.w;
-      yv[4] = bf16_lo(w.z) * i1.x;
-      yv[5] = bf16_hi(w.z) * i1.y;
-      yv[6] = bf16_lo(w.w) * i1.z;
-      yv[7] = bf16_hi(w.w) * i1.w;
+      y[0] = __fmul2_rn(make_float2(bf16_lo(w.x), bf16_hi(w.x)), make_float2(i0.x, i0.y));
+      y[1] = __fmul2_rn(make_float2(bf16_lo(w.y), bf16_hi(w.y)), make_float2(i0.z, i0.w));
+      y[2] = __fmul2_rn(make_float2(bf16_lo(w.z), bf16_hi(w.z)), make_float2(i1.x, i1.y));
+      y[3] = __fmul2_rn(make_float2(bf16_lo(w.w), bf16_hi(w.w)), make_float2(i1.z, i1.w));
     };
     float amax = 0.f;
 #pragma unroll 2
     for (int k = 0; k < 8; ++k) {
-      float yv[8];
-      estimates(k, yv);
+      float2 y[4];
+      estimates(k, y);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(yv[e]));
+      for (int j = 0; j < 4; ++j) amax = fmax3(amax, fabsf(y[j].x), fabsf(y[j].y));
     }
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-    // candidates for the exact maximum: a bit mask, then divisions for its bits only
+    // candidates for the exact maximum are the elements with |y| >= thr: a chunk
+    // holding one is marked by the sign of y^2 - T (T = thr^2 rounded down, so none
+    // is missed), and only the marked chunks' elements are tested and divided
     const float thr = amax * (1.f - 0x1p-20f);
-    uint64_t cand = 0;
+    const float nT = -__fmul_rd(thr, thr);
+    uint32_t chunks = s_fast ? 0u : 0xffu;
+    if (s_fast) {
 #pragma unroll 2
-    for (int k = 0; k < 8; ++k) {
-      float yv[8];
-      estimates(k, yv);
-      uint32_t m = 0;
+      for (int k = 0; k < 8; ++k) {
+        float2 y[4], e[4];
+        estimates(k, y);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) m |= (uint32_t)(!s_fast || fabsf(yv[e]) >= thr) << e;
-      cand |= (uint64_t)m << (8 * k);
+        for (int j = 0; j < 4; ++j) e[j] = __ffma2_rn(y[j], y[j], make_float2(nT, nT));
+        chunks |= (((and_bits(e[0], e[1]) & and_bits(e[2], e[3])) >> 31) ^ 1u) << k;
+      }
     }
     float ymax = 0.f;
-    while (cand) {
-      const int i = __ffsll((long long)cand) - 1;
-      cand &= cand - 1;
-      const int ch = q * 64 + (((i >> 3) + lane) & 7) * 8 + (i & 7);
-      ymax = fmaxf(ymax, fabsf(__fdiv_rn(bf16_lo(S.k[t][ch]), S.s[ch])));
+    while (chunks) {
+      const int k = __ffs(chunks) - 1;
+      chunks &= chunks - 1;
+      const int ch0 = q * 64 + ((k + lane) & 7) * 8;
+      for (int e = 0; e < 8; ++e) {
+        const float kv = bf16_lo(S.k[t][ch0 + e]);
+        if (!s_fast || fabsf(kv * S.inv_s[ch0 + e]) >= thr)
+          ymax = fmaxf(ymax, fabsf(__fdiv_rn(kv, S.s[ch0 + e])));
+      }
     }
     ymax = fmaxf(ymax, __shfl_xor_sync(0xffffffffu, ymax, 1));
     ymax = fmaxf(ymax, __shfl_xor_sync(0xffffffffu, ymax, 2));
@@ -462,24 +528,27 @@ __global__ void __launch_bounds__(kQuantThreads, 2) quantize_kernel(const __grid
     uint8_t* kc = rec + kOffKc;
 #pragma unroll 2
     for (int k = 0; k < 8; ++k) {
-      float yv[8];
-      estimates(k, yv);
+      float2 y[4];
+      estimates(k, y);
       const int ch0 = q * 64 + ((k + lane) & 7) * 8;
       uint32_t wk[2] = {0u, 0u};
       uint32_t redo = fast ? 0u : 0xffu;
       if (given) {  // r from the caller: any magnitude, so clamp
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          const float z = yv[e] * inv_r;
+          const float z = ((e & 1) ? y[e >> 1].y : y[e >> 1].x) * inv_r;
           redo |= (uint32_t)near_half(z) << e;
           wk[e >> 2] |= quotient_byte(z) << (8 * (e & 3));
         }
       } else {
+        float2 z[4], ev[4];
 #pragma unroll
-        for (int g = 0; g < 2; ++g) {
-          const float z[4] = {yv[4 * g] * inv_r, yv[4 * g + 1] * inv_r, yv[4 * g + 2] * inv_r,
-                              yv[4 * g + 3] * inv_r};
-          wk[g] = code_word4(z, redo, 4 * g);
+        for (int j = 0; j < 4; ++j) z[j] = __fmul2_rn(y[j], make_float2(inv_r, inv_r));
+        wk[0] = code_word4(z[0], z[1], ev[0], ev[1]);
+        wk[1] = code_word4(z[2], z[3], ev[2], ev[3]);
+        if (!((and_bits(ev[0], ev[1]) & and_bits(ev[2], ev[3])) >> 31)) {  // rare
+#pragma unroll
+          for (int j = 0; j < 4; ++j) redo |= near_bits(ev[j], 2 * j);
         }
       }
       // (ch0 is a multiple of 8: kc_byte(t, ch0 + e) = kc_byte(t, ch0) + e)
