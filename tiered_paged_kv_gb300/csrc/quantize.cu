@@ -10,11 +10,13 @@
 //   1. the keys are bulk-copied into shared memory (the values, read twice, come
 //      from global memory, so four blocks fit on an SM);
 //   2. thread c owns channel c: u_c = max|v| / 127, and the key mean square with
-//      compensated float32 additions of exact squares in two chains of 32 (relative
-//      error below gamma_31^2 < 2^-38, the bound of Ogita, Rump and Oishi's Sum2);
-//   3. the geometric mean of the mean squares as a product of mantissas (double)
-//      and a sum of exponents, so the normalised fourth power x_c = ms_c / G
-//      needs one multiplication; shat_c = x_c^(1/4);
+//      compensated float32 additions of exact squares, as a rule in two chains of
+//      32 (relative error below gamma_31^2 < 2^-38, or gamma_63^2 < 2^-36 for one
+//      chain of 64: the bound of Ogita, Rump and Oishi's Sum2);
+//   3. the geometric mean of the mean squares as a product of mantissas (float
+//      pairs) and a sum of exponents, so the normalised fourth power x_c = ms_c / G
+//      needs one multiplication; shat_c = x_c^(1/4); no double-precision arithmetic
+//      anywhere (its rate on this GPU is a small fraction of FP32's);
 //   4. the float32 neighbours of shat_c, found exactly (c^4 against x_c in
 //      integer arithmetic); then warp 0 walks the channels (lane j holds 8
 //      channels, the running log-error passes from lane to lane) choosing the
@@ -35,9 +37,11 @@ namespace tpk {
 struct QSmem {
   alignas(128) uint16_t k[kPageTokens][kHeadDim];
   uint64_t bar;
+  alignas(16) uint16_t vred[8][kHeadDim];  // per-warp maxima of |v| (bfloat16)
   float2 red_m[8];
   int red_e[8];
-  double invG;
+  float2 ig;  // 1 / G = (ig.x + ig.y) 2^ig_e
+  int ig_e;
   alignas(16) float s[kHeadDim];
   alignas(16) float inv_s[kHeadDim];
   alignas(16) float u[kHeadDim];
@@ -48,25 +52,23 @@ struct QSmem {
   int bad;
 };
 
-// c^4 - x for a normal float c and a normal double x: the sign exactly, and the
-// relative difference (c^4 - x) / x as a float estimate.  With c = mc 2^ec (mc
-// 24 bits) and x = mx 2^ex (mx 53 bits), c^4 - x = 2^(4ec) (mc^4 - mx 2^s) for
-// s = ex - 4ec; mc^4 < 2^96 is formed exactly in two 64-bit words, so the
-// comparison needs no double-precision arithmetic (scarce on this GPU).
+// c^4 - x for a normal float c and x = mx 2^ex, mx an integer in (2^53.99, 2^55): the
+// sign exactly, and the relative difference (c^4 - x) / x as a float estimate
+// (rcp_xm: about 2^54 / mx).  With c = mc 2^ec (mc 24 bits), c^4 - x = 2^(4ec) (mc^4 -
+// mx 2^s) for s = ex - 4ec; mc^4 < 2^96 is formed exactly in two 64-bit words, so the
+// comparison is integer arithmetic only.  For c within a few ulp of x^(1/4), the
+// only points evaluated, |c^4 - x| < 2^-19 x < 2^96 (bounds the magnitude's words).
 struct Pow4Diff {
   int sign;
   float rel;
 };
-__device__ __forceinline__ Pow4Diff pow4_diff(float c, double x) {
+__device__ __forceinline__ Pow4Diff pow4_diff(float c, uint64_t mx, int ex, float rcp_xm) {
   const uint32_t cb = __float_as_uint(c);
   const uint64_t mc = (cb & 0x7fffffu) | 0x800000u;
   const int ec = (int)((cb >> 23) & 0xff) - 150;
-  const uint64_t xb = (uint64_t)__double_as_longlong(x);
-  const uint64_t mx = (xb & 0xfffffffffffffull) | 0x10000000000000ull;
-  const int ex = (int)((xb >> 52) & 0x7ff) - 1075;
   const int s = ex - 4 * ec;
-  if (s <= 39) return {1, 1.f};    // mx 2^s < 2^92 <= mc^4
-  if (s >= 44) return {-1, -1.f};  // mx 2^s >= 2^96 > mc^4
+  if (s <= 37) return {1, 1.f};    // mx 2^s < 2^92 <= mc^4
+  if (s >= 43) return {-1, -1.f};  // mx 2^s > 2^96 > mc^4
   const uint64_t m2 = mc * mc;     // < 2^48
   const uint64_t p_lo = m2 * m2, p_hi = __umul64hi(m2, m2);
   const uint64_t q_lo = mx << s, q_hi = mx >> (64 - s);
@@ -79,10 +81,15 @@ __device__ __forceinline__ Pow4Diff pow4_diff(float c, double x) {
     m_lo = ~d_lo + 1u;
     m_hi = ~(uint64_t)d_hi + (m_lo == 0 ? 1u : 0u);
   }
-  const float mag = (float)m_hi * 0x1p64f + (float)m_lo;
-  const float rel = mag * (1.f / (float)mx) * __int_as_float((127 - s) << 23);
+  const float mag = (float)(uint32_t)m_hi * 0x1p64f + (float)(uint32_t)(m_lo >> 32) * 0x1p32f + (float)(uint32_t)m_lo;
+  const float rel = mag * rcp_xm * __int_as_float((127 - 54 - s) << 23);
   return {d_hi < 0 ? -1 : 1, d_hi < 0 ? -rel : rel};
 }
+
+// 2^k as a float, for -126 <= k <= 127
+__device__ __forceinline__ float pow2f(int k) { return __uint_as_float((uint32_t)(k + 127) << 23); }
+// the exponent of a positive normal float
+__device__ __forceinline__ int expo(float x) { return (int)((__float_as_uint(x) >> 23) & 0xff) - 127; }
 
 // The stored byte of a code: clamp(rint(q), -127, 127) + 128 (offset binary) for
 // the quotient q = x / scale, correctly rounded.
@@ -205,9 +212,9 @@ __global__ void __launch_bounds__(kQuantThreads, 2) quantize_kernel(const __grid
   if (__syncthreads_or(!landed)) return;
 
   uint8_t* rec = p.rec_pool + ((int64_t)p.dst[i] * p.H + h) * kRecordBytes;
-  // values are read from global memory (twice: the maximum, then the codes; a
-  // warp reads 32 neighbouring channels of one token, and the second pass hits
-  // L2), so only the keys occupy shared memory
+  // values are read from global memory, twice (the maxima with 16-byte row loads,
+  // then the codes, where a warp reads 32 neighbouring channels of one token and
+  // hits L2), so only the keys occupy shared memory
   const uint16_t(*gv)[kHeadDim] = reinterpret_cast<const uint16_t(*)[kHeadDim]>(
       p.v_pool + ((int64_t)p.src[i] * p.H + h) * (int64_t)(kPageTokens * kHeadDim));
   const int64_t gidx = (int64_t)i * p.H + h;  // index into given-scale arrays
@@ -268,13 +275,25 @@ __global__ void __launch_bounds__(kQuantThreads, 2) quantize_kernel(const __grid
     for (int it = tid; it < kValueItems; it += kQuantThreads) value_codes(it & 255, (it >> 8) * 16);
   } else {
     // 2. thread c: u_c = max|v| / 127, and the key mean square: exact squares
-    //    added with TwoSum into float pairs, then the mean in double (for step 4).
+    //    added with TwoSum into float pairs; the mean is kept as a normalised pair
+    //    and an exponent (for step 4).
     //    A zero channel takes a = 2^-63, i.e. a mean square of 2^-252.
-    float vmax = 0.f;
-#pragma unroll 16
-    for (int t = 0; t < kPageTokens; t += 2)
-      vmax = fmax3(vmax, fabsf(bf16_lo(__ldg(&gv[t][c]))), fabsf(bf16_lo(__ldg(&gv[t + 1][c]))));
-    S.u[c] = __fdiv_rn(vmax, 127.f);
+    {
+      // value maxima: warp w reads rows w, w + 8, .., w + 56 with 16-byte loads (lane
+      // l: channels 8l .. 8l + 7) and keeps the maxima of |v| as bfloat16 pairs (a
+      // maximum is exact in any format; NaN is passed over, as by fmaxf); the
+      // eight warps' maxima meet in shared memory after the next barrier
+      const int l = tid & 31, w = tid >> 5;
+      uint32_t m[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const uint4 x = __ldg(reinterpret_cast<const uint4*>(&gv[w + 8 * j][8 * l]));
+        const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) asm("max.bf16x2 %0, %0, %1;" : "+r"(m[i]) : "r"(xs[i] & 0x7fff7fffu));
+      }
+      *reinterpret_cast<uint4*>(&S.vred[w][8 * l]) = make_uint4(m[0], m[1], m[2], m[3]);
+    }
     // One pass over the key channel: max |k|, and the sum of squares in two TwoSum
     // chains (even and odd tokens) as packed pairs.  A square of a bfloat16 is exact
     // in float32 unless it underflows or overflows; for 2^-40 <= max|k| < 2^40 the sum
@@ -296,15 +315,13 @@ __global__ void __launch_bounds__(kQuantThreads, 2) quantize_kernel(const __grid
     const bool kmax_pos = kmax > 0.f;
     float hsum = 0.f, lsum = 0.f;  // the sum of squares (scaled by 2^-2kexp), as a float pair
     int kexp = 0;
-    double ms;
     if (kmax >= 0x1p-40f && kmax < 0x1p40f) {
       const DF sum = df_add(DF{h2.x, l2.x}, DF{h2.y, l2.y});
       hsum = sum.hi;
       lsum = sum.lo;
-      ms = ldexp((double)hsum + (double)lsum, -6);  // mean over 64 tokens
     } else if (kmax_pos) {
       frexpf(kmax, &kexp);
-      const float sc = ldexpf(1.f, -kexp);  // kmax * sc in [0.5, 1)
+      const float sc = ldexpf(1.f, -kexp);  // kmax * sc in [0.5, 1) (2^-128 for the largest)
       for (int t = 0; t < kPageTokens; ++t) {
         const float y = bf16_lo(S.k[t][c]) * sc;
         const float sq = y * y;
@@ -312,9 +329,6 @@ __global__ void __launch_bounds__(kQuantThreads, 2) quantize_kernel(const __grid
         lsum += (hsum - (sum - bb)) + (sq - bb);
         hsum = sum;
       }
-      ms = ldexp((double)hsum + (double)lsum, 2 * kexp - 6);
-    } else {
-      ms = 0x1p-252;
     }
     // 3. geometric mean G of ms over channels, as 1 / G: the product of the mean
     //    squares as a normalised float pair m (in [1, 2]) and an exponent sum E,
@@ -322,17 +336,21 @@ __global__ void __launch_bounds__(kQuantThreads, 2) quantize_kernel(const __grid
     //    2^(-E/256), with m^(-1/256) by two Newton steps on z^256 m = 1 (seeded in
     //    float, each step squaring the error) and 2^(-E/256) = 2^-q 2^(-r/256), E =
     //    256 q + r, from a table.  Relative error about 2^-45, all on the FP32 pipe.
-    DF m;
-    int E;
+    //    ms_c = mc 2^Ec (mc a float pair in [1, 2)) is kept for step 4.
+    DF mc;
+    int Ec;
     if (kmax_pos) {
-      m = df_fast_renorm(hsum, lsum);
-      const int k = ilogbf(m.hi);
-      m = {ldexpf(m.hi, -k), ldexpf(m.lo, -k)};
-      E = 2 * kexp - 6 + k;
+      mc = df_fast_renorm(hsum, lsum);
+      const int k = expo(mc.hi);
+      const float sc = pow2f(-k);
+      mc = {mc.hi * sc, mc.lo * sc};
+      Ec = 2 * kexp - 6 + k;  // the mean over 64 tokens: 2^-6
     } else {
-      m = {1.f, 0.f};  // 2^-252: a = 2^-63
-      E = -252;
+      mc = {1.f, 0.f};  // 2^-252: a = 2^-63
+      Ec = -252;
     }
+    DF m = mc;
+    int E = Ec;
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) {
       const DF mo = {__shfl_xor_sync(0xffffffffu, m.hi, off), __shfl_xor_sync(0xffffffffu, m.lo, off)};
@@ -348,6 +366,12 @@ __global__ void __launch_bounds__(kQuantThreads, 2) quantize_kernel(const __grid
       S.red_e[tid >> 5] = E;
     }
     __syncthreads();
+    {
+      float vmax = 0.f;
+#pragma unroll
+      for (int w = 0; w < 8; w += 2) vmax = fmax3(vmax, bf16_lo(S.vred[w][c]), bf16_lo(S.vred[w + 1][c]));
+      S.u[c] = __fdiv_rn(vmax, 127.f);
+    }
     if (tid == 0) {
       DF mm = {S.red_m[0].x, S.red_m[0].y};
       int ee = S.red_e[0];
@@ -372,32 +396,49 @@ __global__ void __launch_bounds__(kQuantThreads, 2) quantize_kernel(const __grid
       const int q = (ee >= 0) ? ee / kHeadDim : -((-ee + kHeadDim - 1) / kHeadDim);
       const float2 w = c_pow2_neg[ee - kHeadDim * q];
       const DF inv = df_mul(z, DF{w.x, w.y});
-      S.invG = ldexp((double)inv.hi + (double)inv.lo, -q);
+      S.ig = make_float2(inv.hi, inv.lo);
+      S.ig_e = -q;
     }
     __syncthreads();
     // 4. float32 neighbours of shat_c = (ms_c / G)^(1/4), clamped to 2^+-14.  A
     //    channel whose scale is fixed (clamped, or shat_c a float) gets lo = hi and
     //    zero log errors, so the walk keeps its running error unchanged there.
     {
-      const double x = ms * S.invG;
+      // x = ms_c / G = mc (1 / G) 2^(Ec + ig_e), as a float pair xm in [1, 2) and the
+      // exponent X
+      DF xm = df_mul(mc, DF{S.ig.x, S.ig.y});  // in (1/4, 2)
+      int X = Ec + S.ig_e;
+      {
+        const int kx = expo(xm.hi);
+        const float sc = pow2f(-kx);
+        xm = {xm.hi * sc, xm.lo * sc};
+        X += kx;
+      }
+      const bool at_pow2 = xm.hi == 1.f;  // x = 2^X (1 + xm.lo)
       float lo, hi, dl = 0.f, dh = 0.f;
-      if (x >= 0x1p56) {
+      if (X > 56 || (X == 56 && !(at_pow2 && xm.lo < 0.f))) {  // x >= 2^56
         lo = hi = 0x1p14f;
-      } else if (x <= 0x1p-56) {
+      } else if (X < -56 || (X == -56 && at_pow2 && xm.lo <= 0.f)) {  // x <= 2^-56
         lo = hi = 0x1p-14f;
       } else {
+        // x as an integer mantissa: mx = mh 2^31 + rint(xm.lo 2^54) with xm.hi = mh
+        // 2^-23 (|xm.lo| <= 2^-24), x = mx 2^(X - 54) to within 2^-54 of x
+        const uint32_t mh = (__float_as_uint(xm.hi) & 0x7fffffu) | 0x800000u;
+        const uint64_t mx = (uint64_t)((int64_t)((uint64_t)mh << 31) + (int64_t)__float2int_rn(xm.lo * 0x1p54f));
+        const int ex = X - 54;
+        const float rcp_xm = __frcp_rn(xm.hi);
         // the square root of the square root of x rounded to float lies within 2 ulp
         // of shat: step from it, one neighbour at a time, to the bracket lo^4 <= x <
         // hi^4 (hi the successor of lo); two evaluations as a rule
-        float cc = sqrtf(sqrtf((float)x));
-        Pow4Diff dc = pow4_diff(cc, x);
+        float cc = sqrtf(sqrtf(xm.hi * pow2f(X)));
+        Pow4Diff dc = pow4_diff(cc, mx, ex, rcp_xm);
         float nb = cc;
         Pow4Diff dn = dc;
         if (dc.sign != 0) {
           const float dir = dc.sign > 0 ? 0.f : 0x1p127f;  // towards shat
           for (int it = 0; it < 4; ++it) {
             nb = nextafterf(cc, dir);
-            dn = pow4_diff(nb, x);
+            dn = pow4_diff(nb, mx, ex, rcp_xm);
             if (dn.sign != dc.sign) break;  // shat lies between cc and nb (or at nb)
             cc = nb;
             dc = dn;
