@@ -151,3 +151,49 @@ def test_codes_at_half_integer_quotients(seed):
         _, _, s_, r_, u_ = oracle.record_fields(got[slot])
         again = oracle.codes_given(w.k_pool[slot, 0], w.v_pool[slot, 0], s_, r_, u_)
         assert np.array_equal(again, got[slot])
+
+
+@pytest.mark.parametrize("j", [-45, -30, -20, -15, 0, 15, 20, 30])
+def test_key_magnitudes_across_the_sum_paths(j):
+    """Keys scaled by 4^j: the channel sums run as two packed chains when max|k|
+    lies in [2^-40, 2^40) and as one scaled chain outside it; either way the
+    scales stay within 1 ulp of the oracle's (which are invariant under 4^j) and
+    the codes follow from them exactly."""
+    w = synth.make_workload([64 * 6], 0, H=2, seed=11, key_sigma="loguniform")
+    scale = np.float32(4.0 ** j)
+    for slot in w.int8_slots():
+        w.k_pool[slot] = synth.f32_to_bf16(synth.bf16_to_f32(w.k_pool[slot]) * scale)
+    ref = oracle_records(w).reshape(w.n_slots, w.H, oracle.REC_BYTES)
+    got = DevWorkload(w).quantize_gpu().reshape(w.n_slots, w.H, oracle.REC_BYTES)
+    for slot in w.int8_slots():
+        for h in range(w.H):
+            kc, vc, s, r, u = oracle.record_fields(got[slot, h])
+            _, _, s_o, r_o, u_o = oracle.record_fields(ref[slot, h])
+            assert ulp_distance(s, s_o).max() <= 1
+            assert np.all(np.abs(kc).max(axis=1)[r > 0] == 127)
+            again = oracle.codes_given(w.k_pool[slot, h], w.v_pool[slot, h], s, r, u)
+            assert np.array_equal(again, got[slot, h])
+
+
+def test_subnormal_and_near_maximum_channels():
+    """Channels of subnormal bfloat16 keys, of keys near the bfloat16 maximum, and
+    a channel at the single-pass bound 2^-40 / 2^40: scales within 1 ulp of the
+    oracle's (clamped where the oracle clamps), codes from the scales exactly."""
+    w = synth.make_workload([64 * 2], 0, H=1, seed=12)
+    rng = np.random.default_rng(12)
+    for slot in w.int8_slots():
+        k = synth.bf16_to_f32(w.k_pool[slot, 0])
+        k[:, 3] = rng.integers(-100, 100, 64) * np.float32(2.0 ** -133)     # subnormal
+        k[:, 4] = rng.uniform(-1.0, 1.0, 64).astype(np.float32) * np.float32(3.0e38)
+        k[:, 5] = np.float32(2.0 ** -40) * np.sign(rng.standard_normal(64)).astype(np.float32)
+        k[:, 6] = np.float32(2.0 ** 40) * rng.uniform(0.5, 0.99, 64).astype(np.float32)
+        w.k_pool[slot, 0] = synth.f32_to_bf16(k)
+    ref = oracle_records(w).reshape(w.n_slots, 1, oracle.REC_BYTES)
+    got = DevWorkload(w).quantize_gpu().reshape(w.n_slots, 1, oracle.REC_BYTES)
+    for slot in w.int8_slots():
+        kc, vc, s, r, u = oracle.record_fields(got[slot, 0])
+        _, _, s_o, r_o, u_o = oracle.record_fields(ref[slot, 0])
+        assert ulp_distance(s, s_o).max() <= 1
+        assert s[3] == np.float32(2.0 ** -14) and s[4] == np.float32(2.0 ** 14)
+        again = oracle.codes_given(w.k_pool[slot, 0], w.v_pool[slot, 0], s, r, u)
+        assert np.array_equal(again, got[slot, 0])
