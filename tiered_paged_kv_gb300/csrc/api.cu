@@ -72,29 +72,26 @@ tpk_status check_shape(const tpk_shape* s) {
 }
 
 int* status_ptr() {
+  static std::atomic<int*> ptrs[kMaxDevices] = {};
   int dev = 0;
-  cudaGetDevice(&dev);
-  static int* ptrs[64] = {nullptr};
-  if (dev < 0 || dev >= 64) return nullptr;
-  if (!ptrs[dev]) {
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  int* q = ptrs[dev].load(std::memory_order_relaxed);
+  if (!q) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_tpk_status) != cudaSuccess) return nullptr;
-    ptrs[dev] = static_cast<int*>(p);
+    q = static_cast<int*>(p);
+    ptrs[dev].store(q, std::memory_order_relaxed);
   }
-  return ptrs[dev];
+  return q;
 }
 
 int num_sms() {
-  static int cached[64] = {0};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64) dev = 0;
-  if (!cached[dev]) {
-    int n = 0;
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    cached[dev] = n > 0 ? n : 1;
-  }
-  return cached[dev];
+  static std::atomic<int> cached[kMaxDevices] = {};
+  return per_device_int(cached, [] {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    return n > 0 ? n : 1;
+  });
 }
 
 void fill_common(DecodeParams& p, const tpk_shape* s, const void* q) {
@@ -116,16 +113,19 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
 EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  if (!fn) {
+  static std::atomic<EncodeTiledFn> fn{nullptr};
+  EncodeTiledFn f = fn.load(std::memory_order_relaxed);
+  if (!f) {
     void* ptr = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
             cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+        q == cudaDriverEntryPointSuccess) {
+      f = reinterpret_cast<EncodeTiledFn>(ptr);
+      fn.store(f, std::memory_order_relaxed);
+    }
   }
-  return fn;
+  return f;
 }
 
 // The tensor-core kernel reads BF16 half-pages with TMA: each pool is a 2-D
@@ -155,13 +155,9 @@ tpk_status make_pool_maps(DecodeParams& p, const tpk_shape* s, const void* k_poo
 }
 
 int blocks_per_sm(const tpk_shape* s) {
-  static int simt = 0, mma = 0;
-  if (use_simt(s)) {
-    if (!simt) simt = decode_simt_blocks_per_sm();
-    return simt;
-  }
-  if (!mma) mma = decode_mma_blocks_per_sm();
-  return mma;
+  static std::atomic<int> simt[kMaxDevices] = {}, mma[kMaxDevices] = {};
+  if (use_simt(s)) return per_device_int(simt, decode_simt_blocks_per_sm);
+  return per_device_int(mma, decode_mma_blocks_per_sm);
 }
 
 // Split plan of the multi-request call: cnt[2b] / cnt[2b + 1] = units per KV head

@@ -5,7 +5,9 @@
 #include <cuda.h>  // CUtensorMap (type only; the encode entry point is fetched at run time)
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
+#include <mutex>
 
 namespace tpk {
 
@@ -181,6 +183,49 @@ struct QuantParams {
   int* status;
   int H;
 };
+
+// --------------------------------------------------- per-device host state
+// Kernel attributes (the dynamic shared-memory limit) and constant tables belong
+// to a device's context, so one-time setup runs once per device, not once per
+// process; several host threads may launch at once.
+constexpr int kMaxDevices = 64;
+
+class DeviceOnce {
+ public:
+  // Runs setup() for the current device unless it has succeeded there before; a
+  // failed setup is retried by the next call.
+  template <class F>
+  cudaError_t run(F&& setup) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    if (done_[dev].load(std::memory_order_acquire)) return cudaSuccess;
+    std::lock_guard<std::mutex> lock(mu_);
+    if (done_[dev].load(std::memory_order_relaxed)) return cudaSuccess;
+    e = setup();
+    if (e == cudaSuccess) done_[dev].store(true, std::memory_order_release);
+    return e;
+  }
+
+ private:
+  std::mutex mu_;
+  std::atomic<bool> done_[kMaxDevices] = {};
+};
+
+// A positive int per device, computed on first use (0: not known yet).  Racing
+// first calls compute the same value.
+template <class F>
+int per_device_int(std::atomic<int> (&cache)[kMaxDevices], F&& compute) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return compute();
+  int v = cache[dev].load(std::memory_order_relaxed);
+  if (v <= 0) {
+    v = compute();
+    cache[dev].store(v, std::memory_order_relaxed);
+  }
+  return v;
+}
 
 // ------------------------------------------------------------- PTX wrappers
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

@@ -735,14 +735,12 @@ __global__ void __launch_bounds__(kMmaThreads, 1) decode_mma_kernel(const __grid
 
 template <int R, bool IntQuery>
 static cudaError_t launch_mma(const DecodeParams& p, const ReqPlan* req, cudaStream_t stream) {
-  static bool configured = false;
+  static DeviceOnce once;
   const int smem = (int)sizeof(MmaSmem);
-  if (!configured) {
-    cudaError_t e =
-        cudaFuncSetAttribute(decode_mma_kernel<R, IntQuery>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  cudaError_t e = once.run([&] {
+    return cudaFuncSetAttribute(decode_mma_kernel<R, IntQuery>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  });
+  if (e != cudaSuccess) return e;
   Plan<R> plan = {};
   for (int b = 0; b < p.n_req; ++b) plan.req[b] = req[b];
   decode_mma_kernel<R, IntQuery><<<p.n_units, kMmaThreads, smem, stream>>>(p, plan);

@@ -317,13 +317,11 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_simt_kernel(const __gri
 
 template <int R>
 static cudaError_t launch_simt(const DecodeParams& p, const ReqPlan* req, cudaStream_t stream) {
-  static bool configured = false;
+  static DeviceOnce once;
   const int smem = (int)sizeof(DecSmem);
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(decode_simt_kernel<R>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  cudaError_t e = once.run(
+      [&] { return cudaFuncSetAttribute(decode_simt_kernel<R>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem); });
+  if (e != cudaSuccess) return e;
   Plan<R> plan = {};
   for (int b = 0; b < p.n_req; ++b) plan.req[b] = req[b];
   decode_simt_kernel<R><<<p.n_units, kDecThreads, smem, stream>>>(p, plan);

@@ -608,29 +608,20 @@ __global__ void __launch_bounds__(kQuantThreads, 2) quantize_kernel(const __grid
 }
 
 cudaError_t launch_quantize(const QuantParams& p, int n_pages, cudaStream_t stream) {
-  static bool configured = false;
-  static bool table_ready[64] = {false};
+  static DeviceOnce once;
   const int smem = (int)sizeof(QSmem);
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(quantize_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!table_ready[dev]) {  // 2^(-i/256) split into float pairs, once per device
-    float2 t[256];
+  const cudaError_t e = once.run([&] {
+    cudaError_t r = cudaFuncSetAttribute(quantize_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (r != cudaSuccess) return r;
+    float2 t[256];  // 2^(-i/256) split into float pairs
     for (int i = 0; i < 256; ++i) {
       const double v = std::exp2(-i / 256.0);
       const float hi = (float)v;
       t[i] = make_float2(hi, (float)(v - (double)hi));
     }
-    e = cudaMemcpyToSymbol(c_pow2_neg, t, sizeof t);
-    if (e != cudaSuccess) return e;
-    table_ready[dev] = true;
-  }
+    return cudaMemcpyToSymbol(c_pow2_neg, t, sizeof t);
+  });
+  if (e != cudaSuccess) return e;
   if (n_pages == 0) return cudaSuccess;
   quantize_kernel<<<n_pages * p.H, kQuantThreads, smem, stream>>>(p);
   return cudaGetLastError();
