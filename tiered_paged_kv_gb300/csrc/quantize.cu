@@ -524,32 +524,31 @@ __global__ void __launch_bounds__(kQuantThreads, 2) quantize_kernel(const __grid
       y[2] = __fmul2_rn(make_float2(bf16_lo(w.z), bf16_hi(w.z)), make_float2(i1.x, i1.y));
       y[3] = __fmul2_rn(make_float2(bf16_lo(w.w), bf16_hi(w.w)), make_float2(i1.z, i1.w));
     };
+    // pass 1: the row maximum of the estimates, and a mask of the chunks whose
+    // maximum lies within 2^-20 of the running maximum A when seen (all are dropped
+    // when a chunk's maximum m has fl(m (1 - 2^-20)) > A).  Every chunk holding an
+    // element >= thr = fl(amax (1 - 2^-20)) for the final row maximum amax is in
+    // the mask: a chunk left out or dropped has its maximum below fl(a (1 - 2^-20))
+    // for some running maximum a <= amax.  Only the marked chunks' elements are
+    // then tested against thr and divided (the argmax is among them).
     float amax = 0.f;
+    uint32_t chunks = 0u;
 #pragma unroll 2
     for (int k = 0; k < 8; ++k) {
       float2 y[4];
       estimates(k, y);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) amax = fmax3(amax, fabsf(y[j].x), fabsf(y[j].y));
+      float cm = fmax3(fabsf(y[0].x), fabsf(y[0].y), fabsf(y[1].x));
+      cm = fmax3(cm, fabsf(y[1].y), fabsf(y[2].x));
+      cm = fmax3(cm, fabsf(y[2].y), fabsf(y[3].x));
+      cm = fmaxf(cm, fabsf(y[3].y));
+      if (cm * (1.f - 0x1p-20f) > amax) chunks = 0u;
+      if (cm >= amax * (1.f - 0x1p-20f)) chunks |= 1u << k;
+      amax = fmaxf(amax, cm);
     }
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-    // candidates for the exact maximum are the elements with |y| >= thr: a chunk
-    // holding one is marked by the sign of y^2 - T (T = thr^2 rounded down, so none
-    // is missed), and only the marked chunks' elements are tested and divided
     const float thr = amax * (1.f - 0x1p-20f);
-    const float nT = -__fmul_rd(thr, thr);
-    uint32_t chunks = s_fast ? 0u : 0xffu;
-    if (s_fast) {
-#pragma unroll 2
-      for (int k = 0; k < 8; ++k) {
-        float2 y[4], e[4];
-        estimates(k, y);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) e[j] = __ffma2_rn(y[j], y[j], make_float2(nT, nT));
-        chunks |= (((and_bits(e[0], e[1]) & and_bits(e[2], e[3])) >> 31) ^ 1u) << k;
-      }
-    }
+    if (!s_fast) chunks = 0xffu;
     float ymax = 0.f;
     while (chunks) {
       const int k = __ffs(chunks) - 1;
