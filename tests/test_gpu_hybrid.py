@@ -67,6 +67,20 @@ def test_deterministic(impl):
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
 
 
+@pytest.mark.parametrize("seed", range(5))
+def test_configs_at_reduced_sizes_seeds_0_to_4(seed):
+    """Every workload recipe at a reduced size, seeds 0-4, both kernels (8-bit
+    records from the GPU conversion): the tiny hybrid, the all-exact history, the
+    outlier-key hybrid and a 4-request ragged batch."""
+    for impl in IMPLS:
+        check_hybrid(synth.tiny_hybrid(seed=seed), impl, gpu_records=True, what=f"tiny seed {seed}")
+        check_hybrid(synth.exact_32k(seed=seed, n_tokens=4096 + 37 * seed), impl, what=f"exact seed {seed}")
+        check_hybrid(synth.hybrid_128k(seed=seed, n_tokens=8192 + 64 * seed + 5, recent=512), impl,
+                     gpu_records=True, what=f"hybrid seed {seed}")
+        check_hybrid(synth.batched_hybrid(seed=seed, n_req=4, lo=1024, hi=6000, recent=256), impl,
+                     gpu_records=True, what=f"batch seed {seed}")
+
+
 @pytest.mark.parametrize("impl", IMPLS)
 def test_full_exact_32k(impl):
     w = synth.exact_32k(seed=1)
