@@ -9,7 +9,7 @@ import pytest
 import oracle
 import tiered_paged_kv_gb300 as tpk
 from tiered_paged_kv_gb300 import synth
-from tpk_testutil import DevWorkload, assert_close, oracle_records, torch
+from tpk_testutil import DevWorkload, assert_close, dev_u16, oracle_records, torch
 
 pytestmark = pytest.mark.gpu
 
@@ -81,6 +81,64 @@ def test_layers_through_two_slots(impl):
         assert np.array_equal(o, ro) and np.array_equal(lse, rl), f"layer {l}: staged != resident"
         oo, ol = oracle.hybrid_workload(w, rec, n_threads=8)
         assert_close(o, lse, oo, ol, f"layer {l}")
+
+
+@pytest.mark.parametrize("impl", [tpk.IMPL_SIMT, tpk.IMPL_TENSOR])
+def test_full_size_128k_layers_through_two_slots(impl):
+    """The host-resident workload at its full layer size: four layers of the 128K
+    hybrid history image (1,984 8-bit pages x 4 KV heads + 4,096 BF16 tokens, 295 MB
+    each), each layer with a query of its own, staged from pinned host memory
+    through two slots, each layer staged while the previous one decodes (the order
+    the bench times).  Every layer equals the resident decode of its history and
+    query bit for bit, and the oracle within the parity bar."""
+    import dataclasses
+
+    t = torch()
+    w = synth.hybrid_128k(seed=2)
+    rec = oracle_records(w)
+    img0, off = w.packed_image(rec)
+    L = 4
+    qs, imgs = [], []
+    for l in range(L):
+        q = synth.normal_bf16(300 + l, 0, w.q.size).reshape(w.q.shape)
+        img = img0.copy()
+        img[off["q"]:off["q"] + q.nbytes] = q.view(np.uint8).reshape(-1)
+        qs.append(q)
+        imgs.append(pinned(img))
+    del img0, img
+    nb = off["nbytes"]
+    slots = [t.empty(nb, dtype=t.uint8, device="cuda") for _ in range(2)]
+    stream = t.cuda.Stream()
+    nbytes = tpk.hybrid_workspace_bytes(tpk.Shape(w.H, impl=impl), w.B)
+    ws = t.empty(nbytes, dtype=t.uint8, device="cuda")
+    outs = []
+    with tpk.Stager(slots, nb) as st:
+        pending = st.stage([(imgs[0], 0, nb)])
+        for l in range(L):
+            nxt = st.stage([(imgs[l + 1], 0, nb)]) if l + 1 < L else None
+            slot, _ = pending
+            st.acquire(slot, stream)
+            o = t.full((w.B, w.H * w.G, 256), float("nan"), dtype=t.float32, device="cuda")
+            lse = t.full((w.B, w.H * w.G), float("nan"), dtype=t.float32, device="cuda")
+            with t.cuda.stream(stream):
+                decode_from_slot(slots[slot], off, w, impl, o, lse, ws, nbytes, stream)
+            st.release(slot, stream)
+            outs.append((o, lse))
+            pending = nxt
+        stream.synchronize()
+    del slots, imgs
+    d = DevWorkload(w, impl)
+    d.load_records(rec)
+    for l in range(L):
+        o = outs[l][0].cpu().numpy().astype(np.float64)
+        lse = outs[l][1].cpu().numpy().astype(np.float64)
+        d.q = dev_u16(qs[l])
+        ro, rl = d.hybrid()
+        assert np.array_equal(o, ro) and np.array_equal(lse, rl), f"layer {l}: staged != resident"
+        oo, ol = oracle.hybrid_workload(dataclasses.replace(w, q=qs[l]), rec, n_threads=8)
+        assert_close(o, lse, oo, ol, f"layer {l}")
+    st_, flags = tpk.get_device_status(reset=True)
+    assert st_ == 0, flags
 
 
 def test_lifecycle_is_enforced():
