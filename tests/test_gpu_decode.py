@@ -92,6 +92,38 @@ def test_split_at_random_point_then_merge_equals_unsplit(impl):
                      full_l[0], f"split at {x}")
 
 
+def merge_on_gpu(parts_o, parts_l):
+    """Fold partials [k][rows][256], [k][rows] into an empty accumulator on the GPU."""
+    t = torch()
+    k, rows = parts_l.shape
+    acc_o = dev_f32(np.zeros((rows, 256)))
+    acc_l = dev_f32(np.full(rows, -np.inf))
+    tpk.merge_lse(k, rows, 256, dev_f32(parts_o), dev_f32(parts_l), acc_o, acc_l)
+    t.cuda.synchronize()
+    return acc_o.cpu().numpy().astype(np.float64), acc_l.cpu().numpy().astype(np.float64)
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+def test_full_exact_32k_split_at_random_point(impl):
+    """The exact-tier workload at full size (32,768 tokens in 512 pages at a seeded
+    permutation of slots, 4 KV heads x 8 query rows): the history cut at seeded
+    uniform points in [1, N - 1], each side decoded by its own call and every
+    partial merged on the GPU, against one call over the whole history (merged
+    the same way) and against the oracle's unsplit attention."""
+    w = synth.exact_32k(seed=1)
+    N = int(w.n_tokens[0])
+    d = DevWorkload(w, impl)
+    u_o, u_l = merge_on_gpu(*run_exact(d, 0, N, 32))
+    oo, ol = oracle.partial_exact(w.H, w.G, w.q[0], w.k_pool, w.v_pool, w.pages[0], 0, N)
+    assert_close(u_o, u_l, oo, ol, "unsplit")
+    for x in synth.randint(1, synth.TID_SPLIT, 3, 1, N - 1):
+        a_o, a_l = run_exact(d, 0, int(x), 16)
+        b_o, b_l = run_exact(d, int(x), N, 16)
+        m_o, m_l = merge_on_gpu(np.concatenate([a_o, b_o]), np.concatenate([a_l, b_l]))
+        assert_close(m_o, m_l, u_o, u_l, f"split at {x} vs unsplit")
+        assert_close(m_o, m_l, oo, ol, f"split at {x} vs oracle")
+
+
 def test_merge_matches_oracle_and_empty_is_identity():
     t = torch()
     rows = 24
