@@ -19,7 +19,8 @@ e2e    = the same metric through the library's host-resident path: the step's
          lse back.
 tiers_128k = each tier alone over a 131,072-token history (all BF16: 536.9 MB; all
          8-bit: 287.3 MB), same call and timing, for the exact and the 8-bit
-         kernel paths separately.
+         kernel paths separately; kernel_* = the decode kernel alone, timed as
+         the roofline's.
 batched_16 = the 16-request batched hybrid decode (8K-64K tokens each, 1.35 GB),
          one multi-request call per step, same timing.
 host_resident = 16 layers of such history images in pinned host memory through
@@ -354,11 +355,14 @@ def run_batched(impl, args, stream, dev, flush, flush_r, peak, int_query=0):
     st, flags = tpk.get_device_status(reset=True, stream=stream)
     if st != 0:
         raise RuntimeError(f"device status {st} flags {flags} (batched)")
+    kms = decode_kernel_times(step, args.tier_steps, stream, flush, flush_r)
     ms = statistics.median(times)
     gbs = w.history_bytes() / (ms * 1e-3) / 1e9
+    kgbs = w.history_bytes() / (kms * 1e-3) / 1e9
     return {"history_bytes": w.history_bytes(), "requests": B, "tokens": int(w.n_tokens.sum()),
             "us_per_step_median": round(ms * 1e3, 2), "GBps": round(gbs, 1), "hbm_frac": round(gbs / peak, 4),
-            "steps": len(times),
+            "steps": len(times), "kernel_us_mean": round(kms * 1e3, 2), "kernel_GBps": round(kgbs, 1),
+            "kernel_hbm_frac": round(kgbs / peak, 4),
             "workload": "16 requests, lengths uniform in [8192, 65536] (seed 3), 2048 BF16 recent each, "
                         "4 KV heads x 8 q rows, head_dim 256, outlier keys"}
 
@@ -403,10 +407,14 @@ def run_tier(which, impl, args, stream, dev, flush, flush_r, peak, int_query=0):
     st, flags = tpk.get_device_status(reset=True, stream=stream)
     if st != 0:
         raise RuntimeError(f"device status {st} flags {flags} ({which} tier)")
+    kms = decode_kernel_times(step, args.tier_steps, stream, flush, flush_r)
     ms = statistics.median(times)
     gbs = w.history_bytes() / (ms * 1e-3) / 1e9
+    kgbs = w.history_bytes() / (kms * 1e-3) / 1e9
     return {"history_bytes": w.history_bytes(), "us_per_step_median": round(ms * 1e3, 2),
             "GBps": round(gbs, 1), "hbm_frac": round(gbs / peak, 4), "steps": len(times),
+            "kernel_us_mean": round(kms * 1e3, 2), "kernel_GBps": round(kgbs, 1),
+            "kernel_hbm_frac": round(kgbs / peak, 4),
             "workload": f"131072 tokens {'all BF16' if which == 'exact' else 'all 8-bit (2048 pages)'}, "
                         "4 KV heads x 8 q rows, head_dim 256, outlier keys, seed 12"}
 
