@@ -226,7 +226,7 @@ def oracle_quant_time(w, n_threads):
     """Time the oracle's page conversion (as it stands) on host cores: every 8-bit
     page of the workload on one thread, then the same pages split over n_threads
     threads (the C oracle releases the GIL).  Returns GB/s of BF16 read + records
-    written, as the GPU conversion figure counts them."""
+    written, as the GPU conversion figure counts them, and the oracle's records."""
     import oracle
     from concurrent.futures import ThreadPoolExecutor
     s8 = w.int8_slots()
@@ -246,7 +246,7 @@ def oracle_quant_time(w, n_threads):
     nb = len(s8) * w.H * per_ph
     return {"value": round(nb / dt / 1e9, 4), "unit": "GB/s", "cores": n, "value_1_thread": round(nb / dt1 / 1e9, 4),
             "sample": f"all {len(s8)} 8-bit pages x {w.H} heads of the workload ({dt1:.1f} s on one thread, "
-                      f"{dt:.2f} s on {n})", "kind": "oracle"}
+                      f"{dt:.2f} s on {n})", "kind": "oracle"}, rec
 
 
 def head_slice(w, heads, rec_host):
@@ -533,8 +533,9 @@ def run_gpu(args, dist, rank, world):
     # ---- CPU oracle baseline (rank 0, N = 1)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
-        rec_host = rec.cpu().numpy()
         n_thr = os.cpu_count() or 1
+        # the oracle's own page conversion (timed), whose records its decode then reads
+        quant_cpu, rec_host = oracle_quant_time(w, n_thr)
         # repeat whole oracle steps until about 10 s of CPU work has been timed
         reps, dt = 0, 0.0
         while reps == 0 or dt * cores < 10.0:
@@ -550,7 +551,7 @@ def run_gpu(args, dist, rank, world):
                "value_1_thread": round(reps1 * nb1 / dt1 / 1e9, 4),
                "sample_1_thread": f"one KV head of the same step on one thread, {reps1} times, {dt1:.1f} s",
                "host_cores_available": os.cpu_count(),
-               "page_conversion": oracle_quant_time(w, n_thr)}
+               "page_conversion": quant_cpu}
     achieved = hist_bytes / (kernel_ms * 1e-3) / 1e9  # the decode kernel alone
     # secondary ceiling: the step's multiply-adds (QK and PV: 2 G d per token and KV
     # head) on the CUDA cores alone (128 FP32 lanes per SM at the maximum SM clock)

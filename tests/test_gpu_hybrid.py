@@ -16,9 +16,14 @@ NT = 16  # oracle threads
 
 
 def check_hybrid(w, impl, gpu_records=False, what=""):
+    """GPU hybrid decode against the oracle.  The oracle always converts the pages
+    itself from the BF16 inputs; with gpu_records the GPU converts them on its side
+    and decodes its own records (end to end), otherwise it decodes the oracle's."""
     d = DevWorkload(w, impl)
-    rec = d.quantize_gpu() if gpu_records else oracle_records(w)
-    if not gpu_records:
+    rec = oracle_records(w)
+    if gpu_records:
+        d.quantize_gpu()
+    else:
         d.load_records(rec)
     o, lse = d.hybrid()
     oo, ol = oracle.hybrid_workload(w, rec, n_threads=NT)

@@ -58,9 +58,13 @@ def test_int8_partials_on_same_codes(kind, pb, pe, S):
 
 
 def check_hybrid(w, gpu_records=False, what=""):
+    """As in the float-query tests: the oracle converts the pages itself; with
+    gpu_records the GPU decodes records it converted on its side."""
     d = iq_workload(w)
-    rec = d.quantize_gpu() if gpu_records else oracle_records(w)
-    if not gpu_records:
+    rec = oracle_records(w)
+    if gpu_records:
+        d.quantize_gpu()
+    else:
         d.load_records(rec)
     o, lse = d.hybrid()
     status_clean()
@@ -132,3 +136,18 @@ def test_full_hybrid_128k():
     print(f"hybrid 128K: worst merged error vs unquantised: integer query gpu {e_gpu:.4g}, oracle {e_orc:.4g}; "
           f"float query oracle {e_flt:.4g} (max|o| {np.abs(of).max():.4g}); parity {err}")
     assert abs(e_gpu - e_orc) <= 1e-3 * np.abs(oo).max()
+
+
+def test_full_batched_16():
+    """The 16-request batch at full size (lengths uniform in [8K, 64K], 2,048 recent
+    BF16 tokens each, 1.35 GB of history) through the integer-query variant, with
+    the GPU's own records."""
+    check_hybrid(synth.batched_hybrid(seed=3), gpu_records=True, what="batched 16, integer query")
+
+
+def test_full_int8_tier_128k():
+    """All 131,072 tokens 8-bit (2,048 pages x 4 KV heads), the single-tier line the
+    bench times, through the integer-query variant."""
+    w = synth.make_workload([131072], 0, H=4, seed=12, key_sigma="outliers")
+    assert (w.n_ex == 0).all()
+    check_hybrid(w, gpu_records=True, what="all 8-bit 128K, integer query")

@@ -12,7 +12,7 @@ import pytest
 import oracle
 import tiered_paged_kv_gb300 as tpk
 from tiered_paged_kv_gb300 import synth
-from tpk_testutil import REC_POISON, assert_close, dev_u16, torch
+from tpk_testutil import REC_POISON, assert_close, dev_u16, oracle_records, torch
 
 pytestmark = pytest.mark.gpu
 
@@ -44,6 +44,9 @@ def test_histories_grow_and_pages_are_published(impl):
     conv, dec = t.cuda.Stream(), t.cuda.Stream()
     n = [min(f, 700 + 300 * b) for b, f in enumerate(final)]   # starting lengths
     published_total = 0
+    # the oracle's records of every page the loop can publish: the whole pages older
+    # than the recent window at the final lengths
+    rec_orc = oracle_records(split_view(w, final, [max(0, (f - recent) // 64) for f in final]))
     with tpk.Tiers(shape, B, max_pages, recent, k, v, rec, scratch, nbytes) as tiers:
         for step in range(16):
             for b in range(B):
@@ -62,8 +65,9 @@ def test_histories_grow_and_pages_are_published(impl):
                                           plan["page_table8"], plan["req_page_off8"], n8, o, lse, ws, ws_bytes, dec)
             dec.synchronize()
             view = split_view(w, n, n8)
-            rec_host = rec.cpu().numpy()          # the records the decode read (published pages are final)
-            oo, ol = oracle.hybrid_workload(view, rec_host, n_threads=8)
+            # the same pages through the oracle's own records (the GPU converted them on
+            # its side)
+            oo, ol = oracle.hybrid_workload(view, rec_orc, n_threads=8)
             assert_close(o.cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64), oo, ol,
                          f"step {step}")
             n = [min(f, x + 97 + 31 * b) for b, (f, x) in enumerate(zip(final, n))]
