@@ -569,6 +569,11 @@ def run_gpu(args, dist, rank, world):
         "us_per_step_p10_p90": [round(np.percentile(times, 10) * 1e3, 2), round(np.percentile(times, 90) * 1e3, 2)],
         "hbm_frac": round(hist_bytes / (ms_mean * 1e-3) / 1e9 / peak, 4),  # the whole step, as `value`
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "dtype_detail": ("BF16 and 8-bit history in; tensor-core products with f32 accumulation: 8-bit tier on "
+                         "f16 inputs (codes exact, the folded query as high + low planes, probabilities as one "
+                         "plane), exact tier on bf16 inputs (query and history exact, probabilities as high + low "
+                         "planes); softmax, rescales and the merge in f32"
+                         if args.kernel != "simt" else "BF16 and 8-bit history in; f32 arithmetic throughout"),
         "data": "synthetic",
         "config": {"workload": WORKLOAD, "history_bytes_per_step": hist_bytes, "kernel": args.kernel,
                    "query": "8-bit integer query on the 8-bit tier" if args.int_query else "float",
