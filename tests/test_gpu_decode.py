@@ -124,6 +124,28 @@ def test_full_exact_32k_split_at_random_point(impl):
         assert_close(m_o, m_l, oo, ol, f"split at {x} vs oracle")
 
 
+@pytest.mark.parametrize("impl", IMPLS)
+def test_full_int8_tier_128k_split_at_random_page(impl):
+    """The 8-bit tier of the 128K hybrid workload at full size (1,984 pages x 4 KV
+    heads, the oracle's records) through the primitive 8-bit call: the page range cut
+    at seeded pages, each side decoded by its own call and every partial merged on
+    the GPU, against one call over the whole range and against the oracle."""
+    w = synth.hybrid_128k(seed=2)
+    P = int(w.n8[0])
+    rec = oracle_records(w)
+    d = DevWorkload(w, impl)
+    d.load_records(rec)
+    u_o, u_l = merge_on_gpu(*run_int8(d, 0, P, 38))
+    oo, ol = oracle.partial_int8(w.H, w.G, w.q[0], rec, w.pages[0], 0, P)
+    assert_close(u_o, u_l, oo, ol, "unsplit")
+    for x in synth.randint(2, synth.TID_SPLIT, 2, 1, P - 1):
+        a_o, a_l = run_int8(d, 0, int(x), 19)
+        b_o, b_l = run_int8(d, int(x), P, 19)
+        m_o, m_l = merge_on_gpu(np.concatenate([a_o, b_o]), np.concatenate([a_l, b_l]))
+        assert_close(m_o, m_l, u_o, u_l, f"split at page {x} vs unsplit")
+        assert_close(m_o, m_l, oo, ol, f"split at page {x} vs oracle")
+
+
 def test_merge_matches_oracle_and_empty_is_identity():
     t = torch()
     rows = 24
