@@ -25,6 +25,24 @@ def ulp_distance(a, b):
     return np.abs(ai - bi)
 
 
+def check_own_record(got, ref, what=""):
+    """A record the GPU converted against the oracle's record of the same page-head
+    (converted by the oracle from the same BF16 page): key channel scales within 1
+    ulp, and wherever every scale agrees (all but a few page-heads of the 128K
+    workload, whose conversion has 75 of 2,031,616 scales 1 ulp apart) the whole record
+    identical, codes included -- given the same s_c, both sides form r_t, u_c and
+    the codes by the same correctly rounded float32 steps.  A page-head whose scales
+    differ has its codes covered by the given-scales tests, which fix the scales on
+    both sides.  Returns the number of channel scales that differ."""
+    _, _, s, r, u = oracle.record_fields(got)
+    _, _, s_o, r_o, u_o = oracle.record_fields(ref)
+    assert ulp_distance(s, s_o).max() <= 1, what
+    n = int((s != s_o).sum())
+    if n == 0:
+        assert np.array_equal(got, ref), what
+    return n
+
+
 @pytest.mark.parametrize("name", sorted(WORKLOADS))
 def test_codes_bit_exact_given_oracle_scales(name):
     w = WORKLOADS[name]()
@@ -55,8 +73,7 @@ def test_own_scales_within_one_ulp_and_invariants(name):
         for h in range(w.H):
             kc, vc, s, r, u = oracle.record_fields(got[slot, h])
             _, _, s_o, r_o, u_o = oracle.record_fields(ref[slot, h])
-            assert ulp_distance(s, s_o).max() <= 1
-            n_diff += int((s != s_o).sum())
+            n_diff += check_own_record(got[slot, h], ref[slot, h], f"slot {slot} head {h}")
             assert np.array_equal(u, u_o)          # u depends on V alone: same float32 ops
             assert kc.min() >= -127 and vc.min() >= -127
             assert np.all(np.abs(kc).max(axis=1)[r > 0] == 127)
@@ -64,11 +81,6 @@ def test_own_scales_within_one_ulp_and_invariants(name):
             clamped = (s == np.float32(2.0 ** -14)) | (s == np.float32(2.0 ** 14))
             if not clamped.any():
                 assert abs(np.exp(np.log(s.astype(np.float64)).sum()) - 1.0) <= 1e-6
-            # the GPU's codes follow from its own scales exactly
-            k = w.k_pool[slot, h]
-            v = w.v_pool[slot, h]
-            again = oracle.codes_given(k, v, s, r, u)
-            assert np.array_equal(again, got[slot, h])
     print(f"{name}: {n_diff} channel scales differ from the oracle by 1 ulp")
 
 
@@ -89,7 +101,36 @@ def test_zero_rows_channels_and_clamp():
         assert s[5] == np.float32(2.0 ** -14) and s[200] == np.float32(2.0 ** 14)
         assert np.all(kc[:, 5] == 0) and r[9] == 0 and np.all(kc[9] == 0)
         assert u[7] == 0 and np.all(vc[:, 7] == 0)
-        assert ulp_distance(s, s_o).max() <= 1
+        check_own_record(got[slot, 0], ref[slot, 0], f"slot {slot}")
+
+
+def test_full_hybrid_128k_conversion():
+    """Every 8-bit page of the 128K hybrid workload (1,984 pages x 4 KV heads, keys
+    with outlier channels) converted in one call: each record against the oracle's
+    conversion of the same page-head."""
+    w = synth.hybrid_128k(seed=2)
+    ref = oracle_records(w).reshape(w.n_slots, w.H, oracle.REC_BYTES)
+    got = DevWorkload(w).quantize_gpu().reshape(w.n_slots, w.H, oracle.REC_BYTES)
+    st, flags = tpk.get_device_status(reset=True)
+    assert st == 0, flags
+    s8 = w.int8_slots()
+    if not np.array_equal(got[s8], ref[s8]):
+        n = sum(check_own_record(got[slot, h], ref[slot, h], f"slot {slot} head {h}")
+                for slot in s8 for h in range(w.H))
+        print(f"hybrid 128K: {n} channel scales differ from the oracle by 1 ulp")
+        # the pages holding those page-heads, converted again with the oracle's scales
+        # given: their records must then equal the oracle's byte for byte
+        diff = np.array([slot for slot in s8 if not np.array_equal(got[slot], ref[slot])], np.int32)
+        fields = [[oracle.record_fields(ref[slot, h]) for h in range(w.H)] for slot in diff]
+        ks = np.array([[f[2] for f in row] for row in fields], np.float32)
+        kt = np.array([[f[3] for f in row] for row in fields], np.float32)
+        vs = np.array([[f[4] for f in row] for row in fields], np.float32)
+        d = DevWorkload(w)
+        sl = dev_i32(diff)
+        tpk.kv_quantize_pages_given_scales(d.shape, d.k, d.v, sl, sl, len(diff), dev_f32(ks), dev_f32(kt),
+                                           dev_f32(vs), d.rec)
+        again = d.rec.cpu().numpy().reshape(w.n_slots, w.H, oracle.REC_BYTES)
+        assert np.array_equal(again[diff], ref[diff])
 
 
 def test_bad_slot_is_skipped_and_reported():
@@ -145,12 +186,11 @@ def test_codes_at_half_integer_quotients(seed):
     for i, slot in enumerate(slots):
         ref = oracle.codes_given(w.k_pool[slot, 0], w.v_pool[slot, 0], ks[i], kt[i], vs[i])
         assert np.array_equal(got[slot], ref), f"page {i}"
-    # own scales: the codes follow from the scales the GPU wrote, exactly
+    # own scales: the GPU's conversion against the oracle's conversion of the same pages
     got = d.quantize_gpu().reshape(w.n_slots, oracle.REC_BYTES)
+    own = oracle_records(w).reshape(w.n_slots, oracle.REC_BYTES)
     for slot in slots:
-        _, _, s_, r_, u_ = oracle.record_fields(got[slot])
-        again = oracle.codes_given(w.k_pool[slot, 0], w.v_pool[slot, 0], s_, r_, u_)
-        assert np.array_equal(again, got[slot])
+        check_own_record(got[slot], own[slot], f"own scales, slot {slot}")
 
 
 @pytest.mark.parametrize("j", [-45, -30, -20, -15, 0, 15, 20, 30])
@@ -168,11 +208,8 @@ def test_key_magnitudes_across_the_sum_paths(j):
     for slot in w.int8_slots():
         for h in range(w.H):
             kc, vc, s, r, u = oracle.record_fields(got[slot, h])
-            _, _, s_o, r_o, u_o = oracle.record_fields(ref[slot, h])
-            assert ulp_distance(s, s_o).max() <= 1
+            check_own_record(got[slot, h], ref[slot, h], f"4^{j}, slot {slot} head {h}")
             assert np.all(np.abs(kc).max(axis=1)[r > 0] == 127)
-            again = oracle.codes_given(w.k_pool[slot, h], w.v_pool[slot, h], s, r, u)
-            assert np.array_equal(again, got[slot, h])
 
 
 def test_subnormal_and_near_maximum_channels():
@@ -192,8 +229,5 @@ def test_subnormal_and_near_maximum_channels():
     got = DevWorkload(w).quantize_gpu().reshape(w.n_slots, 1, oracle.REC_BYTES)
     for slot in w.int8_slots():
         kc, vc, s, r, u = oracle.record_fields(got[slot, 0])
-        _, _, s_o, r_o, u_o = oracle.record_fields(ref[slot, 0])
-        assert ulp_distance(s, s_o).max() <= 1
+        check_own_record(got[slot, 0], ref[slot, 0], f"slot {slot}")
         assert s[3] == np.float32(2.0 ** -14) and s[4] == np.float32(2.0 ** 14)
-        again = oracle.codes_given(w.k_pool[slot, 0], w.v_pool[slot, 0], s, r, u)
-        assert np.array_equal(again, got[slot, 0])
