@@ -39,6 +39,8 @@ def lib():
     if _lib is None:
         L = ctypes.CDLL(build())
         i32, vp = ctypes.c_int, ctypes.c_void_p
+        L.orc_compensated_walk.argtypes = [i32, vp, vp, vp]
+        L.orc_compensated_walk.restype = None
         L.orc_channel_scales.argtypes = [vp, vp, vp]
         L.orc_channel_scales.restype = i32
         L.orc_codes_given.argtypes = [vp] * 6
@@ -91,6 +93,18 @@ def channel_scales(k_page):
     sh = np.empty(D_HEAD, np.float64)
     n = lib().orc_channel_scales(_p(k), _p(s), _p(sh))
     return s, sh, n
+
+
+def compensated_walk(dlo, dhi):
+    """The channel walk of the compensated rounding alone: given each channel's
+    log errors of its lower (dlo <= 0) and upper (dhi >= 0) float32 neighbour,
+    returns take_hi (int32, 1 where the upper neighbour is stored)."""
+    dlo = _c(dlo, np.float64)
+    dhi = _c(dhi, np.float64)
+    assert dlo.shape == dhi.shape and dlo.ndim == 1
+    out = np.empty(dlo.size, np.int32)
+    lib().orc_compensated_walk(dlo.size, _p(dlo), _p(dhi), _p(out))
+    return out
 
 
 def quantize_page_head(k_page, v_page):

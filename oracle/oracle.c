@@ -98,6 +98,28 @@ static float bf16_float(uint16_t b) {
 /* ================================================================ quantiser */
 
 /*
+ * Compensated rounding of the key channel scales (the reading that makes the
+ * stored float32 scales multiply to one [FMT]): channel c may be stored as its
+ * lower or its upper float32 neighbour, whose log errors ln(neighbour / shat_c)
+ * are dlo[c] <= 0 <= dhi[c].  Walk c = 0 .. n-1 keeping the running log error E
+ * of the product (E = 0 at the start); channel c takes the lower neighbour when
+ * |E + dlo[c]| <= |E + dhi[c]| (so the lower one on a tie), else the upper one,
+ * and E grows by the chosen error.  take_hi[c] = 1 marks the upper neighbour.
+ */
+void orc_compensated_walk(int n, const double* dlo, const double* dhi, int* take_hi) {
+  double E = 0.0;
+  for (int c = 0; c < n; ++c) {
+    if (fabs(E + dlo[c]) <= fabs(E + dhi[c])) {
+      take_hi[c] = 0;
+      E += dlo[c];
+    } else {
+      take_hi[c] = 1;
+      E += dhi[c];
+    }
+  }
+}
+
+/*
  * Key channel scales of one page-head [FMT].
  *   ms_c  = mean_t k_tc^2 (double);  a_c = sqrt(sqrt(ms_c))   (sqrt of the RMS)
  *   g     = exp(mean_c ln a_c)       (geometric mean, so prod_c a_c/g = 1)
@@ -130,25 +152,26 @@ int orc_channel_scales(const uint16_t* k, float* s_out, double* shat_out) {
     if (v > hi_b) { v = hi_b; ++clamped; }
     shat[c] = v;
   }
-  double E = 0.0;
+  /* the two float32 neighbours of each shat_c and their log errors; a channel
+     whose shat_c is a float has lo = hi and zero errors (it leaves E unchanged) */
+  float lo[D_HEAD], hi[D_HEAD];
+  double dlo[D_HEAD], dhi[D_HEAD];
   for (int c = 0; c < D_HEAD; ++c) {
     double sh = shat[c];
     float f = (float)sh;
     if ((double)f == sh) {
-      s_out[c] = f;
+      lo[c] = hi[c] = f;
+      dlo[c] = dhi[c] = 0.0;
       continue;
     }
-    float lo = ((double)f < sh) ? f : nextafterf(f, 0.0f);
-    float hi = nextafterf(lo, INFINITY);
-    double dlo = log((double)lo / sh), dhi = log((double)hi / sh);
-    if (fabs(E + dlo) <= fabs(E + dhi)) {
-      s_out[c] = lo;
-      E += dlo;
-    } else {
-      s_out[c] = hi;
-      E += dhi;
-    }
+    lo[c] = ((double)f < sh) ? f : nextafterf(f, 0.0f);
+    hi[c] = nextafterf(lo[c], INFINITY);
+    dlo[c] = log((double)lo[c] / sh);
+    dhi[c] = log((double)hi[c] / sh);
   }
+  int take_hi[D_HEAD];
+  orc_compensated_walk(D_HEAD, dlo, dhi, take_hi);
+  for (int c = 0; c < D_HEAD; ++c) s_out[c] = take_hi[c] ? hi[c] : lo[c];
   if (shat_out)
     for (int c = 0; c < D_HEAD; ++c) shat_out[c] = shat[c];
   return clamped;

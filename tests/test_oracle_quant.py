@@ -108,6 +108,58 @@ def test_channel_scales_multiply_to_one(seed, kind):
     assert np.all((lo.astype(np.float64) <= shat) & (shat <= hi.astype(np.float64)))
 
 
+def test_compensated_walk_hand_worked():
+    """The walk's decision rule on log errors worked by hand (u = 2^-26, every sum
+    exact in double): a channel takes its lower neighbour when |E + dlo| <= |E +
+    dhi| -- the lower one on a tie -- and E grows by the chosen error."""
+    u = 2.0 ** -26
+    dlo = np.array([-3, -3, -1, -2, 0, -1, -1], np.float64) * u
+    dhi = np.array([1, 1, 3, 2, 0, 1, 3], np.float64) * u
+    # c0  E = 0:   |-3u| > |u|   -> upper, E = u
+    # c1  E = u:   |-2u| = |2u|  -> tie: lower, E = -2u
+    # c2  E = -2u: |-3u| > |u|   -> upper, E = u
+    # c3  E = u:   |-u| < |3u|   -> lower, E = -u
+    # c4  E = -u:  |-u| = |-u|   -> (a scale that is a float: both errors 0) lower, E = -u
+    # c5  E = -u:  |-2u| > |0|   -> upper, E = 0
+    # c6  E = 0:   |-u| < |3u|   -> lower, E = -u
+    assert list(oracle.compensated_walk(dlo, dhi)) == [1, 0, 1, 0, 0, 1, 0]
+
+
+def key_page(seed, kind):
+    sig = None
+    if kind == "loguniform":
+        sig = 10.0 ** (2.0 * synth.uniform(seed, 100, D) - 1.0)
+    elif kind == "outliers":
+        sig = np.ones(D)
+        sig[synth.permutation(seed, 101, D)[:4]] = 20.0
+    return synth.normal_bf16(seed, 102, T * D, sigma=sig).reshape(T, D)
+
+
+def test_compensated_rounding_keeps_product_one_where_plain_rounding_fails():
+    """Over 900 seeded page-heads (unit, log-uniform and outlier keys) the stored
+    float32 channel scales multiply to 1 within 1e-6 (the invariant the page
+    format's normalisation fixes), while rounding the same exact scales shat_c to
+    nearest one by one misses 1e-6 on some of them -- so this test fails if the
+    compensated walk is dropped."""
+    worst, rn_fail, rn_worst = 0.0, 0, 0.0
+    for seed in range(300):
+        for kind in ("unit", "loguniform", "outliers"):
+            s, shat, clamped = oracle.channel_scales(key_page(1000 + seed, kind))
+            assert clamped == 0
+            # the stored scale is one of the two float32 neighbours of shat
+            lo = np.nextafter(s, np.float32(0)).astype(np.float64)
+            hi = np.nextafter(s, np.float32(np.inf)).astype(np.float64)
+            assert np.all((lo <= shat) & (shat <= hi))
+            err = abs(np.expm1(np.sum(np.log(s.astype(np.float64)))))
+            worst = max(worst, err)
+            rn = shat.astype(np.float32).astype(np.float64)  # round to nearest, channel by channel
+            e_rn = abs(np.expm1(np.sum(np.log(rn))))
+            rn_worst = max(rn_worst, e_rn)
+            rn_fail += e_rn > 1e-6
+    assert worst <= 1e-6, worst
+    assert rn_fail >= 1, f"plain rounding never missed 1e-6 (worst {rn_worst:.2e}): the set does not test the walk"
+
+
 def test_channel_scale_is_sqrt_rms_ratio():
     """Two channel groups with RMS ratio 16 -> scale ratio 4 (sqrt of RMS), product 1."""
     K = np.ones((T, D))
