@@ -199,6 +199,14 @@ def max_over_ranks(dist, x):
     return float(t.item())
 
 
+def host_cores():
+    """The cores this process may run on (its affinity set)."""
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except (AttributeError, OSError):
+        return os.cpu_count() or 1
+
+
 def barrier(dist):
     if dist is not None:
         dist.barrier()
@@ -219,7 +227,7 @@ def oracle_time(w, rec_host, n_threads, sample_heads=None):
     t0 = time.perf_counter()
     oracle.hybrid_workload(w, rec_host, n_threads=n_threads)
     dt = time.perf_counter() - t0
-    return dt, w.history_bytes(), min(n_threads, w.B * w.H)
+    return dt, w.history_bytes(), min(n_threads, w.B * w.H * w.G)
 
 
 def oracle_quant_time(w, n_threads):
@@ -533,7 +541,7 @@ def run_gpu(args, dist, rank, world):
     # ---- CPU oracle baseline (rank 0, N = 1)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
-        n_thr = os.cpu_count() or 1
+        n_thr = host_cores()
         # the oracle's own page conversion (timed), whose records its decode then reads
         quant_cpu, rec_host = oracle_quant_time(w, n_thr)
         # repeat whole oracle steps until about 10 s of CPU work has been timed
@@ -547,10 +555,10 @@ def run_gpu(args, dist, rank, world):
             reps1, dt1 = reps1 + 1, dt1 + d
         cpu = {"value": round(reps * nb / dt / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
                "sample": f"the full 128K hybrid step (all 4 KV heads) {reps} times, {dt:.1f} s on {cores} threads "
-                         f"(threads over (request, KV head))",
+                         f"(threads over (request, KV head, query row))",
                "value_1_thread": round(reps1 * nb1 / dt1 / 1e9, 4),
                "sample_1_thread": f"one KV head of the same step on one thread, {reps1} times, {dt1:.1f} s",
-               "host_cores_available": os.cpu_count(),
+               "host_cores_available": n_thr,
                "page_conversion": quant_cpu}
     achieved = hist_bytes / (kernel_ms * 1e-3) / 1e9  # the decode kernel alone
     # secondary ceiling: the step's multiply-adds (QK and PV: 2 G d per token and KV

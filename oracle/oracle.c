@@ -360,11 +360,19 @@ void orc_pack13_pages(int H, const uint16_t* k_pool, const uint16_t* v_pool, con
 /* ================================================================ attention */
 
 /*
+ * Where the rows of one attention come from: a function that fills row[0..d)
+ * with key (or value) i of the range, dequantised to double.
+ */
+typedef void (*row_fn)(const void* src, int i, double* row);
+
+/*
  * Softmax of one query row over n precomputed scores s_t, in double:
  *   m = max_t s_t;  l = sum_t exp(s_t - m);  o = sum_t exp(s_t - m) v_t / l;
  *   lse = m + ln l.   n = 0 gives o = 0 and lse = -inf (the empty partial).
+ * value_row(src, t, .) supplies v_t.
  */
-static void attend_scores(int n, int d, const double* s, const double* V, double* orow, double* lse) {
+static void attend_scores(int n, int d, const double* s, row_fn value_row, const void* src, double* orow,
+                          double* lse) {
   for (int c = 0; c < d; ++c) orow[c] = 0.0;
   if (n == 0) {
     *lse = -INFINITY;
@@ -374,92 +382,140 @@ static void attend_scores(int n, int d, const double* s, const double* V, double
   for (int t = 0; t < n; ++t)
     if (s[t] > m) m = s[t];
   double l = 0.0;
+  double* v = (double*)malloc(sizeof(double) * d);
   for (int t = 0; t < n; ++t) {
     double w = exp(s[t] - m);
     l += w;
-    for (int c = 0; c < d; ++c) orow[c] += w * V[(int64_t)t * d + c];
+    value_row(src, t, v);
+    for (int c = 0; c < d; ++c) orow[c] += w * v[c];
   }
+  free(v);
   for (int c = 0; c < d; ++c) orow[c] /= l;
   *lse = m + log(l);
 }
 
 /*
- * Softmax attention of `rows` query rows over n tokens, in double:
+ * Softmax attention of one query row over n tokens, in double:
  *   s_t = scale * q . k_t, then attend_scores.
  */
-void orc_attend(int n, int d, int rows, const double* q, const double* K, const double* V, double scale,
-                double* o, double* lse) {
+static void attend_row(int n, int d, const double* q, row_fn key_row, row_fn value_row, const void* src,
+                       double scale, double* orow, double* lse) {
   double* s = (double*)malloc(sizeof(double) * (n > 0 ? n : 1));
-  for (int r = 0; r < rows; ++r) {
-    for (int t = 0; t < n; ++t) {
-      double acc = 0.0;
-      for (int c = 0; c < d; ++c) acc += q[(int64_t)r * d + c] * K[(int64_t)t * d + c];
-      s[t] = scale * acc;
-    }
-    attend_scores(n, d, s, V, o + (int64_t)r * d, lse + r);
+  double* k = (double*)malloc(sizeof(double) * d);
+  for (int t = 0; t < n; ++t) {
+    key_row(src, t, k);
+    double acc = 0.0;
+    for (int c = 0; c < d; ++c) acc += q[c] * k[c];
+    s[t] = scale * acc;
   }
+  free(k);
+  attend_scores(n, d, s, value_row, src, orow, lse);
   free(s);
 }
 
-/* Exact-tier partial for KV head h [ATT, MERGE]: BF16 tokens [tok_begin, tok_end)
- * of a paged history (token t lives in slot page_table[t / 64], row t % 64). */
-static void partial_exact_head(int H, int G, int h, const uint16_t* q, const uint16_t* k_pool,
-                               const uint16_t* v_pool, const int32_t* page_table, int tok_begin, int tok_end,
-                               double* o, double* lse) {
-  const int d = D_HEAD;
-  int n = tok_end > tok_begin ? tok_end - tok_begin : 0;
-  double* K = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1) * d);
-  double* V = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1) * d);
-  double* qd = (double*)malloc(sizeof(double) * (size_t)G * d);
-  for (int i = 0; i < n; ++i) {
-    int t = tok_begin + i;
-    int64_t slot = page_table[t / T_PAGE];
-    int64_t base = ((slot * H + h) * T_PAGE + t % T_PAGE) * (int64_t)d;
-    for (int c = 0; c < d; ++c) {
-      K[(int64_t)i * d + c] = bf16_value(k_pool[base + c]);
-      V[(int64_t)i * d + c] = bf16_value(v_pool[base + c]);
-    }
-  }
-  for (int g = 0; g < G; ++g)
-    for (int c = 0; c < d; ++c) qd[g * d + c] = bf16_value(q[((int64_t)h * G + g) * d + c]);
-  orc_attend(n, d, G, qd, K, V, 1.0 / sqrt((double)d), o + (int64_t)h * G * d, lse + h * G);
-  free(K);
-  free(V);
-  free(qd);
+/* dense [n][d] arrays of keys and values */
+typedef struct {
+  int d;
+  const double *K, *V;
+} dense_src;
+static void dense_key(const void* p, int i, double* row) {
+  const dense_src* S = (const dense_src*)p;
+  memcpy(row, S->K + (int64_t)i * S->d, sizeof(double) * S->d);
+}
+static void dense_value(const void* p, int i, double* row) {
+  const dense_src* S = (const dense_src*)p;
+  memcpy(row, S->V + (int64_t)i * S->d, sizeof(double) * S->d);
 }
 
-/* 8-bit-tier partial for KV head h [FMT, ATT]: pages [page_begin, page_end) of the
- * record pool, page p in slot page_table8[p]; dequantise, then attend. */
-static void partial_int8_head(int H, int G, int h, const uint16_t* q, const uint8_t* rec_pool,
-                              const int32_t* page_table8, int page_begin, int page_end, double* o, double* lse) {
-  const int d = D_HEAD;
+/*
+ * Softmax attention of `rows` query rows over n tokens (dense K, V), in double.
+ */
+void orc_attend(int n, int d, int rows, const double* q, const double* K, const double* V, double scale,
+                double* o, double* lse) {
+  dense_src S = {d, K, V};
+  for (int r = 0; r < rows; ++r)
+    attend_row(n, d, q + (int64_t)r * d, dense_key, dense_value, &S, scale, o + (int64_t)r * d, lse + r);
+}
+
+/* BF16 tokens [tok_begin, ...) of KV head h in a paged history: token t lives in
+ * slot page_table[t / 64], row t % 64 [ATT, MERGE]. */
+typedef struct {
+  int H, h, tok_begin;
+  const uint16_t *k_pool, *v_pool;
+  const int32_t* page_table;
+} exact_src;
+static int64_t exact_base(const exact_src* S, int i) {
+  int t = S->tok_begin + i;
+  int64_t slot = S->page_table[t / T_PAGE];
+  return ((slot * S->H + S->h) * T_PAGE + t % T_PAGE) * (int64_t)D_HEAD;
+}
+static void exact_key(const void* p, int i, double* row) {
+  const exact_src* S = (const exact_src*)p;
+  int64_t base = exact_base(S, i);
+  for (int c = 0; c < D_HEAD; ++c) row[c] = bf16_value(S->k_pool[base + c]);
+}
+static void exact_value(const void* p, int i, double* row) {
+  const exact_src* S = (const exact_src*)p;
+  int64_t base = exact_base(S, i);
+  for (int c = 0; c < D_HEAD; ++c) row[c] = bf16_value(S->v_pool[base + c]);
+}
+
+/* 8-bit pages [page_begin, ...) of KV head h, page p in slot page_table8[p],
+ * dequantised [FMT]: k_tc = kc_tc s_c r_t, v_tc = vc_tc u_c. */
+typedef struct {
+  int H, h, page_begin;
+  const uint8_t* rec_pool;
+  const int32_t* page_table8;
+} int8_src;
+static const uint8_t* int8_record(const int8_src* S, int i) {
+  return S->rec_pool + ((int64_t)S->page_table8[S->page_begin + i / T_PAGE] * S->H + S->h) * REC_BYTES;
+}
+static void int8_key(const void* p, int i, double* row) {
+  const uint8_t* rec = int8_record((const int8_src*)p, i);
+  const int t = i % T_PAGE;
+  float s_stored[D_HEAD], r;
+  memcpy(s_stored, rec + OFF_KS_CHAN, sizeof s_stored);
+  memcpy(&r, rec + OFF_KS_TOK + 4 * t, 4);
+  for (int c = 0; c < D_HEAD; ++c)
+    row[c] = (double)((int)rec[OFF_KC + kc_pos(t, c)] - 128) * (double)s_stored[ks_pos(c)] * (double)r;
+}
+static void int8_value(const void* p, int i, double* row) {
+  const uint8_t* rec = int8_record((const int8_src*)p, i);
+  const int t = i % T_PAGE;
+  float u[D_HEAD];
+  memcpy(u, rec + OFF_VS_CHAN, sizeof u);
+  for (int c = 0; c < D_HEAD; ++c) row[c] = (double)((int)rec[OFF_VC + vc_pos(c, t)] - 128) * (double)u[c];
+}
+
+static void query_row(const uint16_t* q, int r, double* qd) {
+  for (int c = 0; c < D_HEAD; ++c) qd[c] = bf16_value(q[(int64_t)r * D_HEAD + c]);
+}
+
+/* Exact-tier partial of query row g of KV head h [ATT, MERGE] over BF16 tokens
+ * [tok_begin, tok_end); q is [H*G][256], the result goes to row h*G + g. */
+static void partial_exact_row(int H, int G, int h, int g, const uint16_t* q, const uint16_t* k_pool,
+                              const uint16_t* v_pool, const int32_t* page_table, int tok_begin, int tok_end,
+                              double* o, double* lse) {
+  int n = tok_end > tok_begin ? tok_end - tok_begin : 0;
+  exact_src S = {H, h, tok_begin, k_pool, v_pool, page_table};
+  double qd[D_HEAD];
+  int r = h * G + g;
+  query_row(q, r, qd);
+  attend_row(n, D_HEAD, qd, exact_key, exact_value, &S, 1.0 / sqrt((double)D_HEAD), o + (int64_t)r * D_HEAD,
+             lse + r);
+}
+
+/* 8-bit-tier partial of query row g of KV head h [FMT, ATT] over pages
+ * [page_begin, page_end): dequantise, then attend. */
+static void partial_int8_row(int H, int G, int h, int g, const uint16_t* q, const uint8_t* rec_pool,
+                             const int32_t* page_table8, int page_begin, int page_end, double* o, double* lse) {
   int np = page_end > page_begin ? page_end - page_begin : 0;
-  int n = np * T_PAGE;
-  double* K = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1) * d);
-  double* V = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1) * d);
-  double* qd = (double*)malloc(sizeof(double) * (size_t)G * d);
-  for (int p = 0; p < np; ++p) {
-    const uint8_t* rec = rec_pool + ((int64_t)page_table8[page_begin + p] * H + h) * REC_BYTES;
-    const uint8_t* kc = rec + OFF_KC;
-    const uint8_t* vc = rec + OFF_VC;
-    float s[D_HEAD], r[T_PAGE], u[D_HEAD], s_stored[D_HEAD];
-    memcpy(s_stored, rec + OFF_KS_CHAN, sizeof s_stored);
-    for (int c = 0; c < D_HEAD; ++c) s[c] = s_stored[ks_pos(c)];
-    memcpy(r, rec + OFF_KS_TOK, sizeof r);
-    memcpy(u, rec + OFF_VS_CHAN, sizeof u);
-    for (int t = 0; t < T_PAGE; ++t)
-      for (int c = 0; c < d; ++c) {
-        int64_t i = ((int64_t)p * T_PAGE + t) * d + c;
-        K[i] = (double)((int)kc[kc_pos(t, c)] - 128) * (double)s[c] * (double)r[t];
-        V[i] = (double)((int)vc[vc_pos(c, t)] - 128) * (double)u[c];
-      }
-  }
-  for (int g = 0; g < G; ++g)
-    for (int c = 0; c < d; ++c) qd[g * d + c] = bf16_value(q[((int64_t)h * G + g) * d + c]);
-  orc_attend(n, d, G, qd, K, V, 1.0 / sqrt((double)d), o + (int64_t)h * G * d, lse + h * G);
-  free(K);
-  free(V);
-  free(qd);
+  int8_src S = {H, h, page_begin, rec_pool, page_table8};
+  double qd[D_HEAD];
+  int r = h * G + g;
+  query_row(q, r, qd);
+  attend_row(np * T_PAGE, D_HEAD, qd, int8_key, int8_value, &S, 1.0 / sqrt((double)D_HEAD),
+             o + (int64_t)r * D_HEAD, lse + r);
 }
 
 /*
@@ -490,63 +546,57 @@ float orc_query_codes(const uint16_t* q_row, const float* s, int8_t* qi) {
   return m / 127.0f;
 }
 
-/* 8-bit-tier partial with the integer query [IQ, FMT, ATT]: per page and row the
- * query is coded by orc_query_codes with the page's s_c, and
+/* 8-bit-tier partial of query row g with the integer query [IQ, FMT, ATT]: per
+ * page the row's query is coded by orc_query_codes with the page's s_c, and
  *   score_t = scale * alpha * r_t * sum_c qi_c kc_tc   (the sum is exact);
  * values are dequantised (v = vc * u_c) and attended in double. */
-static void partial_int8_iq_head(int H, int G, int h, const uint16_t* q, const uint8_t* rec_pool,
-                                 const int32_t* page_table8, int page_begin, int page_end, double* o,
-                                 double* lse) {
+static void partial_int8_iq_row(int H, int G, int h, int g, const uint16_t* q, const uint8_t* rec_pool,
+                                const int32_t* page_table8, int page_begin, int page_end, double* o,
+                                double* lse) {
   const int d = D_HEAD;
   const double scale = 1.0 / sqrt((double)d);
   int np = page_end > page_begin ? page_end - page_begin : 0;
   int n = np * T_PAGE;
-  double* V = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1) * d);
-  double* sc = (double*)malloc(sizeof(double) * (size_t)G * (n > 0 ? n : 1));
+  int8_src S = {H, h, page_begin, rec_pool, page_table8};
+  double* sc = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+  const int r = h * G + g;
   for (int p = 0; p < np; ++p) {
     const uint8_t* rec = rec_pool + ((int64_t)page_table8[page_begin + p] * H + h) * REC_BYTES;
     const uint8_t* kc = rec + OFF_KC;
-    const uint8_t* vc = rec + OFF_VC;
-    float s[D_HEAD], r[T_PAGE], u[D_HEAD], s_stored[D_HEAD];
+    float s[D_HEAD], rt[T_PAGE], s_stored[D_HEAD];
     memcpy(s_stored, rec + OFF_KS_CHAN, sizeof s_stored);
     for (int c = 0; c < D_HEAD; ++c) s[c] = s_stored[ks_pos(c)];
-    memcpy(r, rec + OFF_KS_TOK, sizeof r);
-    memcpy(u, rec + OFF_VS_CHAN, sizeof u);
-    for (int t = 0; t < T_PAGE; ++t)
-      for (int c = 0; c < d; ++c)
-        V[((int64_t)p * T_PAGE + t) * d + c] = (double)((int)vc[vc_pos(c, t)] - 128) * (double)u[c];
-    for (int g = 0; g < G; ++g) {
-      int8_t qi[D_HEAD];
-      const float alpha = orc_query_codes(q + ((int64_t)h * G + g) * d, s, qi);
-      for (int t = 0; t < T_PAGE; ++t) {
-        int64_t dot = 0;
-        for (int c = 0; c < d; ++c) dot += (int64_t)qi[c] * ((int)kc[kc_pos(t, c)] - 128);
-        sc[(int64_t)g * n + p * T_PAGE + t] = scale * (double)alpha * (double)r[t] * (double)dot;
-      }
+    memcpy(rt, rec + OFF_KS_TOK, sizeof rt);
+    int8_t qi[D_HEAD];
+    const float alpha = orc_query_codes(q + (int64_t)r * d, s, qi);
+    for (int t = 0; t < T_PAGE; ++t) {
+      int64_t dot = 0;
+      for (int c = 0; c < d; ++c) dot += (int64_t)qi[c] * ((int)kc[kc_pos(t, c)] - 128);
+      sc[p * T_PAGE + t] = scale * (double)alpha * (double)rt[t] * (double)dot;
     }
   }
-  for (int g = 0; g < G; ++g)
-    attend_scores(n, d, sc + (int64_t)g * n, V, o + ((int64_t)h * G + g) * d, lse + h * G + g);
-  free(V);
+  attend_scores(n, d, sc, int8_value, &S, o + (int64_t)r * d, lse + r);
   free(sc);
 }
 
 void orc_partial_exact(int H, int G, const uint16_t* q, const uint16_t* k_pool, const uint16_t* v_pool,
                        const int32_t* page_table, int tok_begin, int tok_end, double* o, double* lse) {
   for (int h = 0; h < H; ++h)
-    partial_exact_head(H, G, h, q, k_pool, v_pool, page_table, tok_begin, tok_end, o, lse);
+    for (int g = 0; g < G; ++g)
+      partial_exact_row(H, G, h, g, q, k_pool, v_pool, page_table, tok_begin, tok_end, o, lse);
 }
 
 void orc_partial_int8(int H, int G, const uint16_t* q, const uint8_t* rec_pool, const int32_t* page_table8,
                       int page_begin, int page_end, double* o, double* lse) {
   for (int h = 0; h < H; ++h)
-    partial_int8_head(H, G, h, q, rec_pool, page_table8, page_begin, page_end, o, lse);
+    for (int g = 0; g < G; ++g) partial_int8_row(H, G, h, g, q, rec_pool, page_table8, page_begin, page_end, o, lse);
 }
 
 void orc_partial_int8_iq(int H, int G, const uint16_t* q, const uint8_t* rec_pool, const int32_t* page_table8,
                          int page_begin, int page_end, double* o, double* lse) {
   for (int h = 0; h < H; ++h)
-    partial_int8_iq_head(H, G, h, q, rec_pool, page_table8, page_begin, page_end, o, lse);
+    for (int g = 0; g < G; ++g)
+      partial_int8_iq_row(H, G, h, g, q, rec_pool, page_table8, page_begin, page_end, o, lse);
 }
 
 /*
@@ -597,48 +647,32 @@ typedef struct {
   const int32_t *page_table8, *req_page_off8, *n_int8_pages;
   double *o, *lse;
   int int_query; /* 1: the 8-bit partials use the integer query [IQ] */
-  int next;      /* next (request, head) item, under the lock */
+  int next;      /* next (request, head, query row) item, under the lock */
   pthread_mutex_t lock;
 } hybrid_job;
 
+/* Query row g of KV head h of request b: both tiers' partials of that row, folded
+ * by orc_merge [TIERS, MERGE]. */
 static void hybrid_item(hybrid_job* J, int item) {
   const int d = D_HEAD;
-  int b = item / J->H, h = item % J->H;
-  int rows = J->H * J->G;
+  const int G = J->G, rows = J->H * G;
+  const int b = item / rows, h = (item % rows) / G, g = item % G;
+  const int r = h * G + g;
   double* parts_o = (double*)malloc(sizeof(double) * 2 * (size_t)rows * d);
   double* parts_lse = (double*)malloc(sizeof(double) * 2 * (size_t)rows);
   const uint16_t* qb = J->q + (int64_t)b * rows * d;
-  partial_exact_head(J->H, J->G, h, qb, J->k_pool, J->v_pool, J->page_table + J->req_page_off[b], 0,
-                     J->n_exact_tokens[b], parts_o, parts_lse);
-  (J->int_query ? partial_int8_iq_head : partial_int8_head)(J->H, J->G, h, qb, J->rec_pool,
-                                                             J->page_table8 + J->req_page_off8[b], 0,
-                                                             J->n_int8_pages[b], parts_o + (int64_t)rows * d,
-                                                             parts_lse + rows);
-  /* gather this head's G rows of both partials and fold them [TIERS, MERGE] */
-  double po[2 * 8 * D_HEAD], pl[2 * 8], oo[8 * D_HEAD], ll[8];
-  double *po_h = po, *pl_h = pl, *oo_h = oo, *ll_h = ll;
-  int G = J->G;
-  double* heap = 0;
-  if (G > 8) {
-    heap = (double*)malloc(sizeof(double) * (size_t)(2 * G * d + 2 * G + G * d + G));
-    po_h = heap;
-    pl_h = po_h + 2 * G * d;
-    oo_h = pl_h + 2 * G;
-    ll_h = oo_h + G * d;
+  partial_exact_row(J->H, G, h, g, qb, J->k_pool, J->v_pool, J->page_table + J->req_page_off[b], 0,
+                    J->n_exact_tokens[b], parts_o, parts_lse);
+  (J->int_query ? partial_int8_iq_row : partial_int8_row)(J->H, G, h, g, qb, J->rec_pool,
+                                                           J->page_table8 + J->req_page_off8[b], 0,
+                                                           J->n_int8_pages[b], parts_o + (int64_t)rows * d,
+                                                           parts_lse + rows);
+  double po[2 * D_HEAD], pl[2];
+  for (int i = 0; i < 2; ++i) {
+    pl[i] = parts_lse[(int64_t)i * rows + r];
+    memcpy(po + (int64_t)i * d, parts_o + ((int64_t)i * rows + r) * d, sizeof(double) * d);
   }
-  for (int i = 0; i < 2; ++i)
-    for (int g = 0; g < G; ++g) {
-      int r = h * G + g;
-      pl_h[i * G + g] = parts_lse[(int64_t)i * rows + r];
-      memcpy(po_h + ((int64_t)i * G + g) * d, parts_o + ((int64_t)i * rows + r) * d, sizeof(double) * d);
-    }
-  orc_merge(2, G, d, po_h, pl_h, oo_h, ll_h);
-  for (int g = 0; g < G; ++g) {
-    int r = h * G + g;
-    J->lse[(int64_t)b * rows + r] = ll_h[g];
-    memcpy(J->o + ((int64_t)b * rows + r) * d, oo_h + (int64_t)g * d, sizeof(double) * d);
-  }
-  free(heap);
+  orc_merge(2, 1, d, po, pl, J->o + ((int64_t)b * rows + r) * d, J->lse + (int64_t)b * rows + r);
   free(parts_o);
   free(parts_lse);
 }
@@ -649,7 +683,7 @@ static void* hybrid_worker(void* arg) {
     pthread_mutex_lock(&J->lock);
     int item = J->next++;
     pthread_mutex_unlock(&J->lock);
-    if (item >= J->B * J->H) break;
+    if (item >= J->B * J->H * J->G) break;
     hybrid_item(J, item);
   }
   return 0;
@@ -662,7 +696,7 @@ static void* hybrid_worker(void* arg) {
  * [0, n_int8_pages[b]) (CSR page_table8 / req_page_off8), folded by orc_merge.
  * o is [B][H*G][256], lse is [B][H*G].  int_query = 1 takes the 8-bit partials
  * with the integer query.  Work is spread over n_threads threads by (request, KV
- * head); the result does not depend on the thread count.
+ * head, query row); the result does not depend on the thread count.
  */
 void orc_hybrid_batched(int B, int H, int G, const uint16_t* q, const uint16_t* k_pool, const uint16_t* v_pool,
                         const uint8_t* rec_pool, const int32_t* page_table, const int32_t* req_page_off,

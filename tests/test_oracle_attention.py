@@ -234,3 +234,17 @@ def test_hybrid_all_exact_requests_and_thread_count():
     of, lf = oracle.full_precision_workload(w)
     assert np.array_equal(o1, o3) and np.array_equal(l1, l3)
     assert np.array_equal(o1, of) and np.array_equal(l1, lf)
+
+
+def test_hybrid_result_independent_of_thread_count():
+    """The oracle spreads (request, KV head, query row) items over threads; the
+    result must not depend on how many threads take them."""
+    w = synth.make_workload([900, 64, 300], 128, H=2, seed=11, key_sigma="outliers")
+    rec = np.zeros(w.n_slots * w.H * oracle.REC_BYTES, np.uint8)
+    s = w.int8_slots()
+    oracle.quantize_pages(w.H, w.k_pool, w.v_pool, s, s, rec)
+    for iq in (False, True):
+        o1, l1 = oracle.hybrid_workload(w, rec, n_threads=1, int_query=iq)
+        for nt in (5, 16, 64):
+            o, l = oracle.hybrid_workload(w, rec, n_threads=nt, int_query=iq)
+            assert np.array_equal(o, o1) and np.array_equal(l, l1), (iq, nt)
