@@ -395,6 +395,23 @@ tpk_status tpk_tiers_destroy(tpk_tiers* tiers);
 tpk_status tpk_set_decode_timing_events(void* before, void* after);
 
 /*
+ * Test hook for the bounded device-side waits (no counterpart in the pages: it
+ * lets a test make a wait run out without faulting or hanging the GPU).  Every
+ * wait of a decode kernel on an mbarrier (for a copy to land, for a partner warp,
+ * for a slot to be released) gives up after wait_limit_ns of wall time -- 0
+ * restores the default of two seconds -- then sets bit 1 of the device status
+ * word, lets the copies it issued land (each such wait bounded the same way) and
+ * returns without writing its partial.  stall_unit >= 0 makes the tensor-core
+ * decode kernel's thread block of that index (a split unit; tpk_hybrid_plan gives
+ * the layout) leave its first history item unissued: no copy is made and nothing
+ * arrives on that item's barrier, so the waits on it run out; the results of that
+ * launch are then undefined.  -1 turns it off.  Process-wide, for the decode
+ * launches made while it is set; set it only while no other thread launches.
+ * Returns TPK_ERR_INVALID for stall_unit < -1 or a limit above 60 s.
+ */
+tpk_status tpk_set_test_wait(uint64_t wait_limit_ns, int stall_unit);
+
+/*
  * Device status word: bit 0 = a page-table entry outside the pool was skipped,
  * bit 1 = a bounded device-side wait gave up, bit 2 = a malformed 13-bit record was
  * skipped.  Synchronises `stream`, stores the word in *flags and, if reset != 0,

@@ -91,6 +91,11 @@ def test_pack13_arguments_are_validated_before_any_device_call(L):
 def test_timing_events_come_in_pairs(L):
     assert L.tpk_set_decode_timing_events(ctypes.c_void_p(16), None) == 1
     assert L.tpk_set_decode_timing_events(None, None) == 0
+    # the bounded-wait test hook: refusals, then back to the defaults
+    assert L.tpk_set_test_wait(0, -2) == 1
+    assert L.tpk_set_test_wait(61 * 10 ** 9, -1) == 1
+    assert L.tpk_set_test_wait(10 ** 6, 3) == 0
+    assert L.tpk_set_test_wait(0, -1) == 0
 
 
 def test_hybrid_host_metadata_is_validated(L):

@@ -8,10 +8,12 @@ from tiered_paged_kv_gb300 import synth
 
 # Parity tolerances.  Outputs: max |o_gpu - o_oracle| <= O_TOL * max |o_oracle|
 # (the bar the method is held to against the oracle on the same codes).  lse:
-# absolute, natural-log units; a shift d of lse scales a partial's merge weight
-# by exp(d), so 1e-3 matches the relative bar on o.
+# absolute, natural-log units, held near the precision the kernels reach (about
+# 7e-5 observed: float32 scores, and the 8-bit tier's products on code + 1152 with
+# the offset removed after the sum); queries scaled far beyond unit variance have
+# a bar of their own that grows with |lse| (see test_extreme_query_scales).
 O_TOL = 1e-3
-LSE_TOL = 1e-3
+LSE_TOL = 2e-4
 
 # Record slots no page uses are filled with this byte: every scale reads as a NaN
 # (0xffffffff), so a stray read of an unused record shows up in the output.

@@ -88,6 +88,8 @@ def lib():
         L.tpk_get_device_status.argtypes = [ctypes.POINTER(ctypes.c_int), i32, vp]
         L.tpk_set_decode_timing_events.argtypes = [vp, vp]
         L.tpk_set_decode_timing_events.restype = i32
+        L.tpk_set_test_wait.argtypes = [ctypes.c_uint64, i32]
+        L.tpk_set_test_wait.restype = i32
         ip = ctypes.POINTER(ctypes.c_int32)
         L.tpk_hybrid_plan.argtypes = [sp, i32, ip, ip, i32, ip, ip, ip]
         L.tpk_hybrid_plan.restype = i32
@@ -250,6 +252,13 @@ def set_decode_timing_events(before=None, after=None):
     launch until called with no events (see tpk_set_decode_timing_events)."""
     _check(lib().tpk_set_decode_timing_events(before.cuda_event if before is not None else None,
                                               after.cuda_event if after is not None else None))
+
+
+def set_test_wait(wait_limit_ns=0, stall_unit=-1):
+    """Test hook of the bounded device waits (see tpk_set_test_wait): every decode
+    wait gives up after wait_limit_ns (0: the default two seconds); stall_unit >= 0
+    leaves that decode block's first item unissued so its waits run out."""
+    _check(lib().tpk_set_test_wait(int(wait_limit_ns), int(stall_unit)))
 
 
 def get_device_status(reset=True, stream=None):

@@ -94,8 +94,15 @@ int num_sms() {
   });
 }
 
+// Test hook of the bounded waits (tpk_set_test_wait).
+std::atomic<uint64_t> g_test_wait_ns{0};
+std::atomic<int> g_test_stall_unit{-1};
+
 void fill_common(DecodeParams& p, const tpk_shape* s, const void* q) {
   std::memset(&p, 0, sizeof(p));
+  const uint64_t w = g_test_wait_ns.load(std::memory_order_relaxed);
+  p.wait_ns = w > 0 ? w : kWaitLimitNs;
+  p.stall_unit = g_test_stall_unit.load(std::memory_order_relaxed);
   p.q = static_cast<const uint16_t*>(q);
   p.kv_slots = s->kv_slots;
   p.rec_slots = s->rec_slots;
@@ -478,6 +485,14 @@ tpk_status tpk_set_decode_timing_events(void* before, void* after) {
   if ((before == nullptr) != (after == nullptr)) return fail(TPK_ERR_INVALID, "set both timing events or neither");
   g_decode_ev[0] = static_cast<cudaEvent_t>(before);
   g_decode_ev[1] = static_cast<cudaEvent_t>(after);
+  return TPK_OK;
+}
+
+tpk_status tpk_set_test_wait(uint64_t wait_limit_ns, int stall_unit) {
+  if (stall_unit < -1) return fail(TPK_ERR_INVALID, "stall_unit %d < -1", stall_unit);
+  if (wait_limit_ns > 60000000000ull) return fail(TPK_ERR_INVALID, "wait limit above 60 s");
+  g_test_wait_ns.store(wait_limit_ns, std::memory_order_relaxed);
+  g_test_stall_unit.store(stall_unit, std::memory_order_relaxed);
   return TPK_OK;
 }
 

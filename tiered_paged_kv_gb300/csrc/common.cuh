@@ -88,6 +88,8 @@ struct DecodeParams {
   int mode;
   int n_req;
   int n_units;
+  uint64_t wait_ns;         // limit of every bounded wait (kWaitLimitNs unless a test sets it)
+  int stall_unit;           // test hook: this block's first item is never issued (-1: none)
 };
 
 struct UnitInfo {
@@ -268,17 +270,19 @@ __device__ __forceinline__ uint64_t global_ns() {
   return t;
 }
 
-// Bounded wait on an mbarrier phase: gives up after about two seconds of wall
-// time, sets kStatusTimeout in the device status word and returns false.
+// Bounded wait on an mbarrier phase: gives up after limit_ns of wall time (two
+// seconds unless a launch passes its own limit), sets kStatusTimeout in the
+// device status word and returns false.
 constexpr int kStatusTimeout = 2;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status) {
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status,
+                                          uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   for (;;) {
     for (int i = 0; i < 64; ++i)
       if (mbar_try_wait(bar, parity)) return true;
-    if (global_ns() - t0 > kWaitLimitNs) {
+    if (global_ns() - t0 > limit_ns) {
       atomicOr(status, kStatusTimeout);
       return false;
     }

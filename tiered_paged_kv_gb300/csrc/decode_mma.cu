@@ -169,6 +169,9 @@ __device__ __forceinline__ void mma_issue(const DecodeParams& p, const UnitInfo&
   int64_t lim = ui.tier == 0 ? p.kv_slots : p.rec_slots;
   const bool ok = slot >= 0 && (lim == 0 || slot < lim);
   S.valid[s] = ok;
+  // test hook (tpk_set_test_wait): the chosen block's first item is neither copied
+  // nor arrived on, so every wait on it runs out
+  if (j == 0 && (int)blockIdx.x == p.stall_unit) return;
   if (!ok) {
     atomicOr(p.status, kStatusBadSlot);
     mbar_arrive(&S.full[s]);
@@ -230,6 +233,7 @@ struct PairSync {
   uint64_t* bar;    // the pair's mbarrier (count 2: one arrival per warp)
   uint32_t parity;  // phase of this item
   int* status;
+  uint64_t limit;   // wait limit (ns)
 };
 template <int N, int RowStride>
 __device__ __forceinline__ bool pair_exchange(float (&v)[N], uint8_t* mine, const uint8_t* theirs, const PairSync& ps) {
@@ -241,7 +245,7 @@ __device__ __forceinline__ bool pair_exchange(float (&v)[N], uint8_t* mine, cons
         make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
   __syncwarp();
   if (lane == 0) mbar_arrive(ps.bar);
-  if (!mbar_wait(ps.bar, ps.parity, ps.status)) return false;
+  if (!mbar_wait(ps.bar, ps.parity, ps.status, ps.limit)) return false;
 #pragma unroll
   for (int k = 0; k < N / 4; ++k) {
     const float4 o = *reinterpret_cast<const float4*>(theirs + ((32 * k + lane) >> 3) * RowStride + (lane & 7) * 16);
@@ -420,7 +424,7 @@ __device__ __forceinline__ bool qk_int_query(uint8_t* rec, int h, const PairSync
     }
   __syncwarp();
   if (lane == 0) mbar_arrive(psync.bar);
-  if (!mbar_wait(psync.bar, psync.parity, psync.status)) return false;
+  if (!mbar_wait(psync.bar, psync.parity, psync.status, psync.limit)) return false;
 #pragma unroll
   for (int k = 0; k < 16; ++k) {
     const int off = ((16 * t + k) >> 2) * kHeadDim + 4 * (g + 8 * ((k + t) & 3));
@@ -657,16 +661,16 @@ __global__ void __launch_bounds__(kMmaThreads, 1) decode_mma_kernel(const __grid
       // wait on full[s] would then match that item's phase, so first wait for its
       // release (empty[s] is at most one phase behind here: item j - 12 belonged
       // to this pair), after which full[s]'s pending phase is item j's.
-      if (j >= kMmaSlots && !mbar_wait(&S.empty[s], ((j / kMmaSlots) - 1) & 1, p.status)) {
+      if (j >= kMmaSlots && !mbar_wait(&S.empty[s], ((j / kMmaSlots) - 1) & 1, p.status, p.wait_ns)) {
         S.abort = 1;
         break;
       }
-      if (!mbar_wait(&S.full[s], (j / kMmaSlots) & 1, p.status)) {
+      if (!mbar_wait(&S.full[s], (j / kMmaSlots) & 1, p.status, p.wait_ns)) {
         S.abort = 1;
         break;
       }
       if (S.valid[s]) {
-        const PairSync psync{&S.pairbar[pair], pair_phase & 1, p.status};
+        const PairSync psync{&S.pairbar[pair], pair_phase & 1, p.status, p.wait_ns};
         ++pair_phase;
         const bool ok = ui.tier == 1
                             ? process_int8_record<IntQuery>(S.slot[s], half, psync, S, qk_scale, m_run, l_run, O)
@@ -701,7 +705,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) decode_mma_kernel(const __grid
     // reports the timeout.
     if (tid == 0)
       for (int s = 0; s < kMmaSlots; ++s)
-        if (S.fills[s] > 0) mbar_wait(&S.full[s], (S.fills[s] - 1) & 1, p.status);
+        if (S.fills[s] > 0) mbar_wait(&S.full[s], (S.fills[s] - 1) & 1, p.status, p.wait_ns);
     __syncthreads();
     return;
   }

@@ -163,7 +163,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_simt_kernel(const __gri
 
   for (int j = 0; j < it.n; ++j) {
     const int s = j % kStages;
-    const bool landed = mbar_wait(&S.full[s], (j / kStages) & 1, p.status);
+    const bool landed = mbar_wait(&S.full[s], (j / kStages) & 1, p.status, p.wait_ns);
     if (!__syncthreads_and(landed)) {  // the block agrees on whether a wait gave up
       stop = j;
       break;
@@ -291,7 +291,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_simt_kernel(const __gri
     // and leave without writing a result; the status word reports the timeout.
     if (tid == 0)
       for (int jj = stop; jj < min(stop + kStages, it.n); ++jj)
-        mbar_wait(&S.full[jj % kStages], (jj / kStages) & 1, p.status);
+        mbar_wait(&S.full[jj % kStages], (jj / kStages) & 1, p.status, p.wait_ns);
     __syncthreads();
     return;
   }
