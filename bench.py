@@ -327,10 +327,11 @@ def decode_kernel_times(step, steps, stream, flush, flush_r):
     return sum(out) / len(out)
 
 
-def run_batched(impl, args, stream, dev, flush, flush_r, peak, int_query=0):
+def run_batched(impl, args, stream, dev, flush, flush_r, peak, int_query=0, keep=None):
     """The 16-request batched hybrid decode (lengths uniform in [8K, 64K], 2048
     recent BF16 tokens each, 4 KV heads x 8 q rows, outlier keys, seed 3): one
-    multi-request call per step, each request with its own page tables."""
+    multi-request call per step, each request with its own page tables.  With
+    keep (a dict), the workload and the step's output are stored in it."""
     import torch
 
     import tiered_paged_kv_gb300 as tpk
@@ -364,6 +365,9 @@ def run_batched(impl, args, stream, dev, flush, flush_r, peak, int_query=0):
     if st != 0:
         raise RuntimeError(f"device status {st} flags {flags} (batched)")
     kms = decode_kernel_times(step, args.tier_steps, stream, flush, flush_r)
+    if keep is not None:
+        stream.synchronize()
+        keep["w"], keep["o"] = w, o.cpu().numpy()
     ms = statistics.median(times)
     gbs = w.history_bytes() / (ms * 1e-3) / 1e9
     kgbs = w.history_bytes() / (kms * 1e-3) / 1e9
@@ -425,6 +429,96 @@ def run_tier(which, impl, args, stream, dev, flush, flush_r, peak, int_query=0):
             "kernel_hbm_frac": round(kgbs / peak, 4),
             "workload": f"131072 tokens {'all BF16' if which == 'exact' else 'all 8-bit (2048 pages)'}, "
                         "4 KV heads x 8 q rows, head_dim 256, outlier keys, seed 12"}
+
+
+def run_exact_32k(impl, args, stream, dev, flush, flush_r, peak):
+    """The exact tier alone: a 32,768-token BF16 history of one request (4 KV heads x
+    8 q rows, head_dim 256, K, V, q ~ N(0, 1)) at a seeded permutation of page slots
+    (seed 1).  Timed: the multi-request call per step (graph replays, L2 flushed),
+    and the decode kernel alone.  Beside it, the same history cut at the seeded
+    token index into two primitive exact calls whose partials one merge folds:
+    its step time and its largest difference from the unsplit result."""
+    import torch
+
+    import tiered_paged_kv_gb300 as tpk
+    from tiered_paged_kv_gb300 import synth
+
+    w = synth.exact_32k(seed=1)
+    H, G, N = w.H, w.G, int(w.n_tokens[0])
+    cut = int(w.meta["split_at"])
+    shape = tpk.Shape(H, impl=impl, kv_slots=w.n_slots, rec_slots=1)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    s1 = max(1, min(sms // H - 1, round(sms // H * cut / N)))
+    s2 = max(1, sms // H - s1)
+    with torch.cuda.stream(stream):
+        kp = torch.from_numpy(w.k_pool.view(np.int16)).to(dev)
+        vp = torch.from_numpy(w.v_pool.view(np.int16)).to(dev)
+        q = torch.from_numpy(w.q.view(np.int16)).to(dev)
+        rec = torch.zeros(16, dtype=torch.uint8, device=dev)
+        pt, off = w.exact_page_table()
+        pt_d = torch.from_numpy(np.concatenate([pt, np.zeros(1, np.int32)])).to(dev)
+        pt8_d = torch.zeros(1, dtype=torch.int32, device=dev)
+        off8 = np.zeros(2, np.int32)
+        o = torch.empty(1, H * G, 256, dtype=torch.float32, device=dev)
+        lse = torch.empty(1, H * G, dtype=torch.float32, device=dev)
+        nbytes = tpk.hybrid_workspace_bytes(shape, 1)
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        o_part = torch.empty(s1 + s2, H * G, 256, dtype=torch.float32, device=dev)
+        lse_part = torch.empty(s1 + s2, H * G, dtype=torch.float32, device=dev)
+        o_acc = torch.empty(H * G, 256, dtype=torch.float32, device=dev)
+        lse_acc = torch.empty(H * G, dtype=torch.float32, device=dev)
+
+    def step():
+        tpk.decode_hybrid_batched(shape, 1, q, kp, vp, rec, pt_d, off, w.n_ex, pt8_d, off8, w.n8, o, lse, ws,
+                                  nbytes, stream)
+
+    def step_split():
+        o_acc.zero_()
+        lse_acc.fill_(float("-inf"))
+        tpk.decode_attn_exact(shape, q, kp, vp, pt_d, 0, cut, s1, o_part[:s1], lse_part[:s1], stream)
+        tpk.decode_attn_exact(shape, q, kp, vp, pt_d, cut, N, s2, o_part[s1:], lse_part[s1:], stream)
+        tpk.merge_lse(s1 + s2, H * G, 256, o_part, lse_part, o_acc, lse_acc, stream)
+
+    times = graph_times(step, args.tier_steps, 3, stream, flush, flush_r)
+    kms = decode_kernel_times(step, args.tier_steps, stream, flush, flush_r)
+    times_split = graph_times(step_split, args.tier_steps, 3, stream, flush, flush_r)
+    stream.synchronize()
+    st, flags = tpk.get_device_status(reset=True, stream=stream)
+    if st != 0:
+        raise RuntimeError(f"device status {st} flags {flags} (exact 32K)")
+    o_u, l_u = o[0].cpu().numpy(), lse[0].cpu().numpy()
+    o_s, l_s = o_acc.cpu().numpy(), lse_acc.cpu().numpy()
+    ms, ms_split = statistics.median(times), statistics.median(times_split)
+    hb = w.history_bytes()
+    gbs, kgbs = hb / (ms * 1e-3) / 1e9, hb / (kms * 1e-3) / 1e9
+    return {"history_bytes": hb, "us_per_step_median": round(ms * 1e3, 2), "GBps": round(gbs, 1),
+            "hbm_frac": round(gbs / peak, 4), "steps": len(times), "kernel_us_mean": round(kms * 1e3, 2),
+            "kernel_GBps": round(kgbs, 1), "kernel_hbm_frac": round(kgbs / peak, 4),
+            "split_merge": {"split_at": cut, "splits": [s1, s2],
+                            "us_per_step_median": round(ms_split * 1e3, 2),
+                            "max_abs_do_over_max_o": float(np.abs(o_s - o_u).max() / np.abs(o_u).max()),
+                            "max_abs_dlse": float(np.abs(l_s - l_u).max()),
+                            "how": "two tpk_decode_attn_exact calls ([0, cut), [cut, N)) + one tpk_merge_lse "
+                                   "into a fresh accumulator, against the unsplit call"},
+            "workload": "32768 tokens all BF16, 1 request, 4 KV heads x 8 q rows, head_dim 256, K, V, q ~ N(0, 1), "
+                        "page slots at a seeded permutation (seed 1)"}
+
+
+def hybrid_error(w, o_gpu, rec_host, n_thr):
+    """Worst merged error of the hybrid result against attention over the original
+    BF16 history (no quantisation), for the oracle's hybrid step on its own records
+    and for the GPU's result: max |o - o_fp| over rows and channels (the pages'
+    bound is 0.005), also over max |o_fp| and as an RMS ratio."""
+    import oracle
+    of, _ = oracle.full_precision_workload(w, n_threads=n_thr)
+    oo, _ = oracle.hybrid_workload(w, rec_host, n_threads=n_thr)
+    out = {"bound": 0.005, "max_abs_o_fp": float(np.abs(of).max())}
+    for name, o in (("oracle", oo), ("gpu", np.asarray(o_gpu, np.float64).reshape(of.shape))):
+        e = np.abs(o - of)
+        out[name] = {"max_abs": round(float(e.max()), 6), "max_abs_over_max_o": round(float(e.max() / np.abs(of).max()), 6),
+                     "rms_rel": round(float(np.sqrt((e ** 2).mean() / (of ** 2).mean())), 6),
+                     "bound_met": bool(e.max() <= 0.005)}
+    return out
 
 
 def run_gpu(args, dist, rank, world):
@@ -526,20 +620,30 @@ def run_gpu(args, dist, rank, world):
 
     # ---- each tier alone at 128K (the exact and the 8-bit kernel paths)
     peak, peak_kind = hbm_peak()
-    tiers = batched = int_query = None
+    stream.synchronize()
+    o_step = o.cpu().numpy()  # the timed step's result (for the hybrid error below)
+    tiers = batched = int_query = exact32 = None
+    batch_keep = {}
     if args.tier_steps > 0:
         tiers = {k: run_tier(k, impl, args, stream, dev, flush, flush_r, peak) for k in ("exact", "int8")}
-        batched = run_batched(impl, args, stream, dev, flush, flush_r, peak)
+        exact32 = run_exact_32k(impl, args, stream, dev, flush, flush_r, peak)
+        batched = run_batched(impl, args, stream, dev, flush, flush_r, peak, keep=batch_keep)
         if impl != tpk.IMPL_SIMT and not args.int_query:
             int_query = run_int_query(w, shape, step, args, stream, dev, flush, flush_r, peak, impl,
                                       (q, kp, vp, rec, pt_d, off, pt8_d, off8, o, lse, ws, nbytes))
+
+    # ---- the economic gate at 32K, 64K and 128K (link model from measured stager copies)
+    gate_obj = None
+    if args.gate:
+        gate_obj = run_gate(args, stream, dev, flush, flush_r, [32768, 65536, 131072],
+                            layers_measured=args.gate_layers)
 
     # ---- end to end from pinned host memory (packed history, identity page tables)
     e2e = run_e2e(args, w, rec, shape, stream, dev, dist)
     host_res = run_host_resident(args, w, rec, shape, stream, dev, dist) if args.layers > 0 else None
 
     # ---- CPU oracle baseline (rank 0, N = 1)
-    cpu = None
+    cpu = herr = None
     if rank == 0 and world == 1 and not args.no_cpu:
         n_thr = host_cores()
         # the oracle's own page conversion (timed), whose records its decode then reads
@@ -560,6 +664,18 @@ def run_gpu(args, dist, rank, world):
                "sample_1_thread": f"one KV head of the same step on one thread, {reps1} times, {dt1:.1f} s",
                "host_cores_available": n_thr,
                "page_conversion": quant_cpu}
+        # worst merged error against unquantised attention (the oracle's and the GPU's)
+        herr = {"hybrid_128k": hybrid_error(w, o_step, rec_host, n_thr)}
+        if batch_keep:
+            import oracle
+            wb = batch_keep["w"]
+            rec_b = np.zeros(wb.n_slots * wb.H * oracle.REC_BYTES, np.uint8)
+            sb = wb.int8_slots()
+            from concurrent.futures import ThreadPoolExecutor
+            with ThreadPoolExecutor(n_thr) as ex:
+                list(ex.map(lambda sl: oracle.quantize_pages(wb.H, wb.k_pool, wb.v_pool, sl, sl, rec_b),
+                            np.array_split(sb, n_thr)))
+            herr["batched_16"] = hybrid_error(wb, batch_keep["o"], rec_b, n_thr)
     achieved = hist_bytes / (kernel_ms * 1e-3) / 1e9  # the decode kernel alone
     # secondary ceiling: the step's multiply-adds (QK and PV: 2 G d per token and KV
     # head) on the CUDA cores alone (128 FP32 lanes per SM at the maximum SM clock)
@@ -614,7 +730,10 @@ def run_gpu(args, dist, rank, world):
         "e2e": e2e,
         "host_resident": host_res,
         "tiers_128k": tiers,
+        "exact_32k": exact32,
         "batched_16": batched,
+        "hybrid_error": herr,
+        "gate": gate_obj,
         "int_query_variant": int_query,
         "gpu_launches": args.steps * launches_per_step,
         "clocks": clk.summary(),
@@ -850,17 +969,172 @@ def run_host_resident(args, w, rec_dev, shape, stream, dev, dist, layers=None, s
             "workload": label or f"{layers} layers x the 128K hybrid history (one pinned host image per layer)"}
 
 
-def run_gate_sweep(args):
-    """Exact vs hybrid over history lengths (the pages' economic gate: bytes saved
-    per token against GPU time added): for each length, an all-BF16 history and a
-    hybrid one (4096 recent BF16 tokens, older pages 8-bit) of one request, 4 KV
-    heads x 8 q rows, outlier keys; device-resident decode time (graph replays, L2
-    flushed) and host-resident step time per layer (layers staged through two slots)."""
+def measure_link(stream, dev, sizes_mb=(1, 4, 16, 64, 256), reps=3):
+    """Copies through the stager (pinned host -> device slot), timed on the device
+    between the stager's own events around each staging: (bytes, us) samples and
+    the fitted transfer model latency + bytes / rate."""
     import torch
 
     import tiered_paged_kv_gb300 as tpk
-    from tiered_paged_kv_gb300 import build as tbuild
+    from tiered_paged_kv_gb300 import gate
+
+    top = max(sizes_mb) << 20
+    host = torch.empty(top, dtype=torch.uint8).pin_memory()
+    host.fill_(1)
+    slots = [torch.empty(top, dtype=torch.uint8, device=dev) for _ in range(2)]
+    samples = []
+    with tpk.Stager(slots, top) as st:
+        for mb in sizes_mb:
+            for r in range(reps + 1):
+                slot, _ = st.stage([(host, 0, mb << 20)])
+                ms = st.copy_ms(slot)
+                st.acquire(slot, stream)
+                st.release(slot, stream)
+                if r > 0:  # the first copy of each size warms up
+                    samples.append((mb << 20, ms * 1e3))
+        st.sync()
+    stream.synchronize()
+    del host, slots
+    return gate.fit_link(samples), samples
+
+
+def run_gate(args, stream, dev, flush, flush_r, sizes, layers_measured=4, layers_model=16):
+    """The economic gate at each history size: three candidate formats of one
+    request's history (4 KV heads x 8 q rows, outlier keys, seed 20) -- exact (all
+    BF16), the 8-bit hybrid (4096 recent BF16 tokens, older pages 8-bit) and the
+    lossless 13-bit tier (all pages 13-bit, unpacked on the device each step) --
+    each described by the bytes its history image moves over the host link per
+    layer and step and by its device time (kernels per step, graph replays with L2
+    flushed, plus its page conversion amortised over a page's 64 tokens).  Verdict:
+    accept when the transfer time saved per token (at layers_model layers, with
+    the link model fitted to measured stager copies) exceeds the GPU time added.
+    The model's host-resident step (layers_measured layers staged through two
+    slots) is printed beside the measured one."""
+    import dataclasses
+
+    import torch
+
+    import tiered_paged_kv_gb300 as tpk
+    from tiered_paged_kv_gb300 import gate
     from tiered_paged_kv_gb300 import synth
+
+    link, samples = measure_link(stream, dev)
+    R = tpk.PACK13_RECORD_BYTES
+    rows = []
+    for n in sizes:
+        w = synth.make_workload([n], 4096, H=4, seed=20, key_sigma="outliers")
+        we = dataclasses.replace(w, n8=np.zeros_like(w.n8), n_ex=w.n_tokens.copy())
+        H, G = w.H, w.G
+        shape = tpk.Shape(H, kv_slots=w.n_slots, rec_slots=w.n_slots)
+        ex_all, off_all = we.exact_page_table()
+        ne_all = len(ex_all)
+        with torch.cuda.stream(stream):
+            kp = torch.from_numpy(w.k_pool.view(np.int16)).to(dev)
+            vp = torch.from_numpy(w.v_pool.view(np.int16)).to(dev)
+            q = torch.from_numpy(w.q.view(np.int16)).to(dev)
+            rec = torch.zeros(w.n_slots * H * tpk.RECORD_BYTES, dtype=torch.uint8, device=dev)
+            s8 = torch.from_numpy(w.int8_slots()).to(dev)
+            n8 = len(w.int8_slots())
+            pool13 = torch.zeros(w.n_slots * H * R, dtype=torch.uint8, device=dev)
+            ex_d = torch.from_numpy(ex_all.astype(np.int32)).to(dev)
+            offs = (np.repeat(ex_all.astype(np.int64), H) * H + np.tile(np.arange(H), ne_all)) * R
+            offs_d = torch.from_numpy(offs).to(dev)
+            k2, v2 = torch.zeros_like(kp), torch.zeros_like(vp)
+            o = torch.empty(1, H * G, 256, dtype=torch.float32, device=dev)
+            lse = torch.empty(1, H * G, dtype=torch.float32, device=dev)
+            nbytes = tpk.hybrid_workspace_bytes(shape, 1)
+            ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+            pt_e = torch.from_numpy(np.concatenate([ex_all.astype(np.int32), np.zeros(1, np.int32)])).to(dev)
+            pth, offh = w.exact_page_table()
+            pt8h, off8h = w.int8_page_table()
+            pt_h = torch.from_numpy(np.concatenate([pth, np.zeros(1, np.int32)])).to(dev)
+            pt8_h = torch.from_numpy(np.concatenate([pt8h, np.zeros(1, np.int32)])).to(dev)
+            zeros8 = np.zeros(2, np.int32)
+            pt8_none = torch.zeros(1, dtype=torch.int32, device=dev)
+
+        def timed_once(fn, reps=5):
+            ev = []
+            with torch.cuda.stream(stream):
+                fn()
+                for i in range(reps):
+                    flush.fill_(float(i))
+                    flush_r.max()
+                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a.record(stream)
+                    fn()
+                    b.record(stream)
+                    ev.append((a, b))
+                stream.synchronize()
+            return statistics.median([a.elapsed_time(b) for a, b in ev]) * 1e3
+
+        conv_us = timed_once(lambda: tpk.kv_quantize_pages(shape, kp, vp, s8, s8, n8, rec, stream))
+        pack_us = timed_once(lambda: tpk.kv_pack13_pages(shape, kp, vp, ex_d, ex_d, ne_all, pool13, w.n_slots,
+                                                         stream))
+
+        def dec_exact(k=kp, v=vp):
+            tpk.decode_hybrid_batched(shape, 1, q, k, v, rec, pt_e, off_all, we.n_ex, pt8_none, zeros8, we.n8, o,
+                                      lse, ws, nbytes, stream)
+
+        def dec_hybrid():
+            tpk.decode_hybrid_batched(shape, 1, q, kp, vp, rec, pt_h, offh, w.n_ex, pt8_h, off8h, w.n8, o, lse, ws,
+                                      nbytes, stream)
+
+        def dec_13():
+            tpk.kv_unpack13_pages(shape, pool13, pool13.numel(), offs_d, ex_d, ne_all, k2, v2, stream)
+            dec_exact(k2, v2)
+
+        dev_us = {"exact": statistics.median(graph_times(dec_exact, 20, 3, stream, flush, flush_r)) * 1e3,
+                  "hybrid": statistics.median(graph_times(dec_hybrid, 20, 3, stream, flush, flush_r)) * 1e3,
+                  "lossless": statistics.median(graph_times(dec_13, 20, 3, stream, flush, flush_r)) * 1e3}
+        st, flags = tpk.get_device_status(reset=True, stream=stream)
+        if st != 0:
+            raise RuntimeError(f"device status {st} flags {flags} (gate {n})")
+        # page conversion, amortised: one page of each head converts once per 64 tokens
+        amort = {"exact": 0.0, "hybrid": conv_us / max(n8, 1) / 64.0,
+                 "lossless": pack_us / max(ne_all, 1) / 64.0}
+        hr = {"exact": run_host_resident(args, we, rec, shape, stream, dev, None, layers=layers_measured, steps=3,
+                                         label=f"{layers_measured} layers x {n} tokens exact"),
+              "hybrid": run_host_resident(args, w, rec, shape, stream, dev, None, layers=layers_measured, steps=3,
+                                          label=f"{layers_measured} layers x {n} tokens hybrid"),
+              "lossless": run_host_resident(args, we, rec, shape, stream, dev, None, layers=layers_measured,
+                                            steps=3, label=f"{layers_measured} layers x {n} tokens 13-bit",
+                                            pack13_dev=pool13)}
+        cands = {k: gate.Candidate(k, hr[k]["slot_bytes"], dev_us[k] + amort[k]) for k in dev_us}
+        row = {"tokens": n}
+        for k, c in cands.items():
+            step_only = gate.Candidate(k, c.link_bytes, dev_us[k])
+            pred = gate.predict_step_us(link, step_only, layers_measured) * 1e-3
+            meas = hr[k]["ms_per_step"]
+            row[k] = {"link_bytes_per_layer": int(c.link_bytes), "device_us": round(dev_us[k], 2),
+                      "conversion_us_per_token": round(amort[k], 4),
+                      f"host_ms_{layers_measured}_layers": {"predicted": round(pred, 4), "measured": round(meas, 4),
+                                                            "rel_err": round(pred / meas - 1.0, 4)}}
+            if k != "exact":
+                net = gate.net_saving_us(link, cands["exact"], c, layers=layers_model)
+                row[k][f"net_saving_us_per_token_{layers_model}_layers"] = round(net, 2)
+                row[k]["verdict"] = "accept" if gate.accept(link, cands["exact"], c, layers=layers_model) else "reject"
+                row[k]["device_time_ratio"] = round(c.device_us / cands["exact"].device_us, 4)
+        rows.append(row)
+        print(json.dumps(row), flush=True, file=sys.stderr)
+        del kp, vp, q, rec, pool13, k2, v2, ws
+        torch.cuda.empty_cache()
+    return {"link": {"latency_us": round(link.latency_us, 2), "rate_GBps": round(link.rate_GBps, 2),
+                     "samples": len(samples), "copy_MB": sorted({int(b) >> 20 for b, _ in samples}),
+                     "how": "least-squares line through stager copies timed on the device (tpk_stager_copy_ms)"},
+            "rule": f"accept when (bytes saved per layer x {layers_model} layers) / link rate exceeds the device "
+                    f"time added per token (decode and unpack per step, page conversion per 64 tokens)",
+            "workload": "1 request, 4 KV heads x 8 q rows, head_dim 256, outlier keys, seed 20; hybrid: 4096 "
+                        "recent BF16 tokens",
+            "rows": rows}
+
+
+def run_gate_sweep(args):
+    """The economic gate over history lengths (--gate-lengths), printed as one
+    JSON line: per size the candidates' bytes, device times, net saving per token
+    and verdict, and the model's host-resident step beside the measured one."""
+    import torch
+
+    from tiered_paged_kv_gb300 import build as tbuild
 
     torch.cuda.set_device(0)
     tbuild.build()
@@ -869,52 +1143,9 @@ def run_gate_sweep(args):
     with torch.cuda.stream(stream):
         flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
         flush_r = torch.zeros(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
-    peak, _ = hbm_peak()
-    rows = []
-    for n in [int(x) for x in args.gate_lengths.split(",")]:
-        row = {"tokens": n}
-        for tier in ("exact", "hybrid"):
-            w = synth.make_workload([n], None if tier == "exact" else 4096, H=4, seed=20, key_sigma="outliers")
-            H, G = w.H, w.G
-            shape = tpk.Shape(H, kv_slots=w.n_slots, rec_slots=w.n_slots)
-            with torch.cuda.stream(stream):
-                kp = torch.from_numpy(w.k_pool.view(np.int16)).to(dev)
-                vp = torch.from_numpy(w.v_pool.view(np.int16)).to(dev)
-                q = torch.from_numpy(w.q.view(np.int16)).to(dev)
-                rec = torch.zeros(max(16, w.n_slots * H * tpk.RECORD_BYTES * int(tier == "hybrid")),
-                                  dtype=torch.uint8, device=dev)
-                if tier == "hybrid":
-                    slots = torch.from_numpy(w.int8_slots()).to(dev)
-                    tpk.kv_quantize_pages(shape, kp, vp, slots, slots, len(slots), rec, stream)
-                pt, off = w.exact_page_table()
-                pt8, off8 = w.int8_page_table()
-                pt_d = torch.from_numpy(np.concatenate([pt, np.zeros(1, np.int32)])).to(dev)
-                pt8_d = torch.from_numpy(np.concatenate([pt8, np.zeros(1, np.int32)])).to(dev)
-                o = torch.empty(1, H * G, 256, dtype=torch.float32, device=dev)
-                lse = torch.empty(1, H * G, dtype=torch.float32, device=dev)
-                nbytes = tpk.hybrid_workspace_bytes(shape, 1)
-                ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
-
-            def step():
-                tpk.decode_hybrid_batched(shape, 1, q, kp, vp, rec, pt_d, off, w.n_ex, pt8_d, off8, w.n8, o, lse,
-                                          ws, nbytes, stream)
-
-            dev_ms = statistics.median(graph_times(step, 20, 3, stream, flush, flush_r))
-            hr = run_host_resident(args, w, rec, shape, stream, dev, None, layers=args.gate_layers, steps=3,
-                                   label=f"{args.gate_layers} layers x {n} tokens {tier}")
-            row[tier] = {"history_bytes": w.history_bytes(), "device_us": round(dev_ms * 1e3, 2),
-                         "device_GBps": round(w.history_bytes() / (dev_ms * 1e-3) / 1e9, 1),
-                         "host_ms_per_layer": round(hr["ms_per_step"] / hr["layers"], 4),
-                         "link_GBps": hr["link_GBps"], "link_peak_GBps": hr["link_peak_GBps"]}
-            del kp, vp, q, rec, ws
-        e, h = row["exact"], row["hybrid"]
-        row["bytes_saved_per_layer_step"] = e["history_bytes"] - h["history_bytes"]
-        row["device_us_added"] = round(h["device_us"] - e["device_us"], 2)
-        row["host_ms_added_per_layer"] = round(h["host_ms_per_layer"] - e["host_ms_per_layer"], 4)
-        row["host_speedup"] = round(e["host_ms_per_layer"] / h["host_ms_per_layer"], 3)
-        rows.append(row)
-        print(json.dumps(row), flush=True, file=sys.stderr)
-    print(json.dumps({"mode": "gate_sweep", "hbm_peak_GBps": peak, "rows": rows}), flush=True)
+    sizes = [int(x) for x in args.gate_lengths.split(",")]
+    out = run_gate(args, stream, dev, flush, flush_r, sizes, layers_measured=args.gate_layers)
+    print(json.dumps({"mode": "gate_sweep", **out}), flush=True)
 
 
 def run_lossless(args):
@@ -1174,6 +1405,8 @@ def main():
                     help="lossless 13-bit exact tier against BF16 over --gate-lengths (pack, unpack, device and "
                          "host-resident steps)")
     ap.add_argument("--gate-layers", type=int, default=4)
+    ap.add_argument("--no-gate", dest="gate", action="store_false",
+                    help="skip the economic gate at 32K, 64K and 128K in the bench line")
     ap.add_argument("--tiers-loop", action="store_true",
                     help="instead of the bench line: a decode loop with incremental conversion and publication")
     ap.add_argument("--tiers-steps", type=int, default=256)

@@ -333,6 +333,15 @@ tpk_status tpk_stager_stage(tpk_stager* stager, int n_regions, const void* const
 tpk_status tpk_stager_acquire(tpk_stager* stager, int slot, tpk_stream_t stream);
 tpk_status tpk_stager_release(tpk_stager* stager, int slot, tpk_stream_t stream);
 tpk_status tpk_stager_sync(tpk_stager* stager);
+/*
+ * Measured link behaviour ("Judge a representation by the bytes it stops
+ * moving": a transfer model derived from the bus's measured behaviour): *ms =
+ * the device time of the copies of the slot's latest staging, between events the
+ * stager records on its copy stream right before the first and right after the
+ * last of them (after the wait for the slot's release, so the copies alone).
+ * Waits for those copies to finish; the slot's state is unchanged.
+ */
+tpk_status tpk_stager_copy_ms(tpk_stager* stager, int slot, float* ms);
 
 /*
  * Incremental conversion and publication during decode ("ActiveKV": history

@@ -104,8 +104,9 @@ def lib():
         L.tpk_stager_acquire.argtypes = [vp, i32, vp]
         L.tpk_stager_release.argtypes = [vp, i32, vp]
         L.tpk_stager_sync.argtypes = [vp]
+        L.tpk_stager_copy_ms.argtypes = [vp, i32, ctypes.POINTER(ctypes.c_float)]
         for name in ("tpk_stager_create", "tpk_stager_destroy", "tpk_stager_stage", "tpk_stager_acquire",
-                     "tpk_stager_release", "tpk_stager_sync"):
+                     "tpk_stager_release", "tpk_stager_sync", "tpk_stager_copy_ms"):
             getattr(L, name).restype = i32
         L.tpk_tiers_device_bytes.argtypes = [i32, i32]
         L.tpk_tiers_device_bytes.restype = sz
@@ -300,6 +301,12 @@ class Stager:
 
     def sync(self):
         _check(lib().tpk_stager_sync(self._h))
+
+    def copy_ms(self, slot):
+        """Device time (ms) of the copies of the slot's latest staging (waits for them)."""
+        ms = ctypes.c_float(0.0)
+        _check(lib().tpk_stager_copy_ms(self._h, int(slot), ctypes.byref(ms)))
+        return ms.value
 
     def close(self):
         if getattr(self, "_h", None) is not None and self._h.value:

@@ -30,8 +30,10 @@ struct tpk_stager {
   size_t slot_bytes = 0;
   std::vector<char*> slots;
   std::vector<int> state;
-  std::vector<cudaEvent_t> ready;   // recorded on the copy stream after a slot's copies
+  std::vector<cudaEvent_t> begun;   // recorded on the copy stream before a slot's copies (timing)
+  std::vector<cudaEvent_t> ready;   // recorded on the copy stream after a slot's copies (timing)
   std::vector<cudaEvent_t> freed;   // recorded on the consumer stream at release
+  std::vector<bool> timed;          // begun/ready bracket the slot's latest staging
   std::vector<bool> freed_recorded;
   cudaStream_t copy = nullptr;
   int next = 0;
@@ -55,6 +57,8 @@ tpk_status scuda(cudaError_t e, const char* what) {
 
 void release_resources(tpk_stager* st) {
   if (st->copy) cudaStreamSynchronize(st->copy);
+  for (cudaEvent_t e : st->begun)
+    if (e) cudaEventDestroy(e);
   for (cudaEvent_t e : st->ready)
     if (e) cudaEventDestroy(e);
   for (cudaEvent_t e : st->freed)
@@ -104,12 +108,15 @@ tpk_status tpk_stager_create(int n_slots, void* const* slots, size_t slot_bytes,
   st->slot_bytes = slot_bytes;
   for (int i = 0; i < n_slots; ++i) st->slots.push_back(static_cast<char*>(slots[i]));
   st->state.assign(n_slots, kFree);
+  st->begun.assign(n_slots, nullptr);
   st->ready.assign(n_slots, nullptr);
   st->freed.assign(n_slots, nullptr);
   st->freed_recorded.assign(n_slots, false);
+  st->timed.assign(n_slots, false);
   e = cudaStreamCreateWithFlags(&st->copy, cudaStreamNonBlocking);
   for (int i = 0; e == cudaSuccess && i < n_slots; ++i) {
-    e = cudaEventCreateWithFlags(&st->ready[i], cudaEventDisableTiming);
+    e = cudaEventCreate(&st->begun[i]);
+    if (e == cudaSuccess) e = cudaEventCreate(&st->ready[i]);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&st->freed[i], cudaEventDisableTiming);
   }
   if (e != cudaSuccess) {
@@ -161,14 +168,16 @@ tpk_status tpk_stager_stage(tpk_stager* st, int n_regions, const void* const* ho
     cudaError_t e = cudaStreamWaitEvent(st->copy, st->freed[slot], 0);
     if (e != cudaSuccess) return scuda(e, "copy stream wait for the slot's release");
   }
+  cudaError_t e = cudaEventRecord(st->begun[slot], st->copy);
+  if (e != cudaSuccess) return scuda(e, "copy start event");
   for (int i = 0; i < n_regions; ++i) {
     if (bytes[i] == 0) continue;
-    cudaError_t e = cudaMemcpyAsync(st->slots[slot] + slot_offset[i], host_src[i], bytes[i], cudaMemcpyHostToDevice,
-                                    st->copy);
+    e = cudaMemcpyAsync(st->slots[slot] + slot_offset[i], host_src[i], bytes[i], cudaMemcpyHostToDevice, st->copy);
     if (e != cudaSuccess) return scuda(e, "staging copy");
   }
-  cudaError_t e = cudaEventRecord(st->ready[slot], st->copy);
+  e = cudaEventRecord(st->ready[slot], st->copy);
   if (e != cudaSuccess) return scuda(e, "ready event");
+  st->timed[slot] = true;
   st->state[slot] = kStaged;
   st->next = (slot + 1) % (int)st->slots.size();
   if (slot_out) *slot_out = slot;
@@ -196,6 +205,18 @@ tpk_status tpk_stager_release(tpk_stager* st, int slot, tpk_stream_t stream) {
   if (e != cudaSuccess) return scuda(e, "release event");
   st->freed_recorded[slot] = true;
   st->state[slot] = kFree;
+  return TPK_OK;
+}
+
+tpk_status tpk_stager_copy_ms(tpk_stager* st, int slot, float* ms) {
+  tpk_status s = check_slot(st, slot);
+  if (s != TPK_OK) return s;
+  if (!ms) return sfail(TPK_ERR_INVALID, "null output pointer");
+  if (!st->timed[slot]) return sfail(TPK_ERR_INVALID, "slot %d has not been staged yet", slot);
+  cudaError_t e = cudaEventSynchronize(st->ready[slot]);
+  if (e != cudaSuccess) return scuda(e, "wait for the staging copies");
+  e = cudaEventElapsedTime(ms, st->begun[slot], st->ready[slot]);
+  if (e != cudaSuccess) return scuda(e, "copy time");
   return TPK_OK;
 }
 
