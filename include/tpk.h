@@ -348,9 +348,10 @@ tpk_status tpk_stager_copy_ms(tpk_stager* stager, int slot, float* ms);
  * converted in the background and published to the decoder; "model
  * quantization": only whole pages older than the recent tokens become 8-bit).
  *
- * A tier manager follows the paged histories of n_req requests of one layer
- * (page p of request b in BF16 slot slots[p]; its record goes to the same slot of
- * rec_pool).  Each tpk_tiers_step:
+ * A tier manager follows the paged histories of n_req requests (page p of
+ * request b in BF16 slot slots[p]; its record goes to the same slot of rec_pool),
+ * in one layer or, with tpk_tiers_create_layers below, in several.  Each
+ * tpk_tiers_step:
  *   1. publishes the pages whose conversion has finished (its event completed):
  *      they leave the exact tier and join the 8-bit tier;
  *   2. starts, on conv_stream, the conversion of every whole page that is now
@@ -387,6 +388,33 @@ tpk_status tpk_tiers_create(const tpk_shape* shape, int n_req, int max_pages, in
                             const void* v_pool, void* rec_pool, void* dev_scratch, size_t dev_scratch_bytes,
                             tpk_tiers** out);
 tpk_status tpk_tiers_update(tpk_tiers* tiers, int b, int n_tokens, const int32_t* page_slots);
+/*
+ * The same manager over n_layers attention layers ("model quantization", "An
+ * 8-bit page format shaped for its kernel": conversion only for pages fully
+ * written in every layer, served exact until published).  The layers share the
+ * requests' page tables: page p of request b lives in slot page_slots[p] of every
+ * layer's pools (k_pools[l], v_pools[l]: dev BF16 pools; rec_pools[l]: dev record
+ * pools; host arrays of n_layers pointers), so one plan serves every layer's
+ * decode call.  A page becomes eligible once it is older than the recent window
+ * and every layer has written it; its conversion runs in every layer on
+ * conv_stream, and it is published -- in all layers at once -- at the first step
+ * after one event recorded behind all of them.  host_rec_pools (NULL, or
+ * n_layers pinned host record pools laid out like the device ones) receive a copy
+ * of every converted record before that event ("ActiveKV", "The idea": host
+ * memory holds the authoritative copy), so a published page's records are in the
+ * host image too; the caller must not stage a page's records before it is
+ * published.  tpk_tiers_create is this with one layer and no host pools.
+ * tpk_tiers_update_layers records request b's history like tpk_tiers_update and
+ * the tokens each layer has written so far (layer_written: host int32[n_layers],
+ * each in [64 * (pages converted or being converted), n_tokens]); NULL, and
+ * tpk_tiers_update, mean every layer has written all n_tokens.
+ */
+tpk_status tpk_tiers_create_layers(const tpk_shape* shape, int n_layers, int n_req, int max_pages, int recent_tokens,
+                                   const void* const* k_pools, const void* const* v_pools, void* const* rec_pools,
+                                   void* const* host_rec_pools, void* dev_scratch, size_t dev_scratch_bytes,
+                                   tpk_tiers** out);
+tpk_status tpk_tiers_update_layers(tpk_tiers* tiers, int b, int n_tokens, const int32_t* page_slots,
+                                   const int32_t* layer_written);
 tpk_status tpk_tiers_step(tpk_tiers* tiers, tpk_stream_t conv_stream, tpk_stream_t decode_stream,
                           tpk_tiers_plan* plan);
 tpk_status tpk_tiers_sync(tpk_tiers* tiers);

@@ -112,11 +112,13 @@ def lib():
         L.tpk_tiers_device_bytes.restype = sz
         L.tpk_tiers_create.argtypes = [sp, i32, i32, i32, vp, vp, vp, vp, sz, pp]
         L.tpk_tiers_update.argtypes = [vp, i32, i32, vp]
+        L.tpk_tiers_create_layers.argtypes = [sp, i32, i32, i32, i32, pp, pp, pp, pp, vp, sz, pp]
+        L.tpk_tiers_update_layers.argtypes = [vp, i32, i32, vp, vp]
         L.tpk_tiers_step.argtypes = [vp, vp, vp, ctypes.POINTER(TiersPlan)]
         L.tpk_tiers_sync.argtypes = [vp]
         L.tpk_tiers_destroy.argtypes = [vp]
         for name in ("tpk_tiers_create", "tpk_tiers_update", "tpk_tiers_step", "tpk_tiers_sync",
-                     "tpk_tiers_destroy"):
+                     "tpk_tiers_destroy", "tpk_tiers_create_layers", "tpk_tiers_update_layers"):
             getattr(L, name).restype = i32
         for name in ("tpk_kv_quantize_pages", "tpk_kv_quantize_pages_given_scales", "tpk_kv_pack13_pages",
                      "tpk_kv_unpack13_pages", "tpk_decode_attn_exact",
@@ -329,18 +331,37 @@ class Tiers:
     def device_bytes(n_req, max_pages):
         return int(lib().tpk_tiers_device_bytes(int(n_req), int(max_pages)))
 
-    def __init__(self, shape, n_req, max_pages, recent_tokens, k_pool, v_pool, rec_pool, scratch, scratch_bytes):
-        self._keep = (shape, k_pool, v_pool, rec_pool, scratch)
+    def __init__(self, shape, n_req, max_pages, recent_tokens, k_pool, v_pool, rec_pool, scratch, scratch_bytes,
+                 host_rec_pools=None):
+        """One layer: k_pool, v_pool, rec_pool are device buffers.  Several layers
+        (tpk_tiers_create_layers): lists of one buffer per layer, and optionally
+        host_rec_pools, pinned host record pools that receive every converted record."""
+        self._keep = (shape, k_pool, v_pool, rec_pool, scratch, host_rec_pools)
         self.n_req = int(n_req)
         h = ctypes.c_void_p()
-        _check(lib().tpk_tiers_create(ctypes.byref(shape), self.n_req, int(max_pages), int(recent_tokens),
-                                      _ptr(k_pool), _ptr(v_pool), _ptr(rec_pool), _ptr(scratch), int(scratch_bytes),
-                                      ctypes.byref(h)))
+        if isinstance(k_pool, (list, tuple)):
+            n = len(k_pool)
+            self.n_layers = n
+            arr = lambda xs: (ctypes.c_void_p * n)(*[_ptr(x) for x in xs])
+            host = arr(host_rec_pools) if host_rec_pools is not None else None
+            _check(lib().tpk_tiers_create_layers(ctypes.byref(shape), n, self.n_req, int(max_pages),
+                                                 int(recent_tokens), arr(k_pool), arr(v_pool), arr(rec_pool), host,
+                                                 _ptr(scratch), int(scratch_bytes), ctypes.byref(h)))
+        else:
+            self.n_layers = 1
+            _check(lib().tpk_tiers_create(ctypes.byref(shape), self.n_req, int(max_pages), int(recent_tokens),
+                                          _ptr(k_pool), _ptr(v_pool), _ptr(rec_pool), _ptr(scratch),
+                                          int(scratch_bytes), ctypes.byref(h)))
         self._h = h
 
-    def update(self, b, n_tokens, page_slots):
+    def update(self, b, n_tokens, page_slots, layer_written=None):
+        """layer_written: tokens each layer has written (None: all n_tokens)."""
         arr, p = _host_i32(page_slots)
-        _check(lib().tpk_tiers_update(self._h, int(b), int(n_tokens), p))
+        if layer_written is None:
+            _check(lib().tpk_tiers_update(self._h, int(b), int(n_tokens), p))
+        else:
+            lw, plw = _host_i32(layer_written)
+            _check(lib().tpk_tiers_update_layers(self._h, int(b), int(n_tokens), p, plw))
 
     def step(self, conv_stream=None, decode_stream=None):
         """Returns a dict: device page tables (raw pointers) and host numpy copies of

@@ -1,16 +1,26 @@
 // Incremental page conversion and publication during decode.
 //
-// A tier manager follows the histories of n_req requests of one layer.  Every
-// step it (1) publishes the pages whose conversion has finished -- they move from
-// the exact tier to the 8-bit tier -- (2) starts the conversion of pages that have
-// become older than the recent window on the caller's conversion stream, and (3)
-// uploads the step's two page tables (in the decode stream's order) for the
-// multi-request decode call.  A page is served exact until its conversion's
-// event has completed, so the decode never reads a half-written record; the
-// swap from one tier to the other happens between steps, through the page tables
-// ("ActiveKV": compressed history converted in the background and published to
-// the decoder; "model quantization": only whole pages older than the recent
-// tokens become 8-bit).
+// A tier manager follows the histories of n_req requests across n_layers
+// attention layers that share one page table per request (page p of a request
+// sits in the same slot of every layer's pools).  Every step it (1) publishes
+// the pages whose conversion has finished in every layer -- they move from the
+// exact tier to the 8-bit tier, in all layers at once, because the layers share
+// the tables -- (2) starts, on the caller's conversion stream, the conversion in
+// every layer of each whole page that is older than the recent window and has
+// been written by every layer, and (3) uploads the step's two page tables (in the
+// decode stream's order) for the multi-request decode call.  A page is served
+// exact until the event recorded after all its layers' conversions has
+// completed, so no decode reads a half-written record; the swap from one tier to
+// the other happens between steps, through the page tables ("ActiveKV":
+// compressed history converted in the background and published to the decoder;
+// "model quantization", "An 8-bit page format shaped for its kernel": conversion
+// only for pages fully written in every layer, served exact until published).
+//
+// Host-authoritative history ("ActiveKV", "The idea": host memory holds the
+// authoritative copy, the GPU the slices a step needs): when pinned host record
+// pools are given, each converted record is also copied into its layer's host
+// pool before the conversion's event, so a published page's records are in the
+// host image too, ready to be staged.
 //
 // Record slot of a page = its BF16 slot (the record pool is indexed like the KV
 // pools).  All device and pinned host buffers are allocated once, at creation.
@@ -47,7 +57,8 @@ constexpr int kPage = 64;
 
 struct Request {
   int n_tokens = 0;
-  std::vector<int32_t> slots;  // BF16 slot of each logical page
+  std::vector<int32_t> slots;  // BF16 slot of each logical page (the same in every layer)
+  std::vector<int> written;    // tokens each layer has written
   int published = 0;           // pages [0, published) are served from records
   int converting = 0;          // pages [published, published + converting) are being converted
 };
@@ -62,10 +73,10 @@ struct Conversion {
 struct tpk_tiers {
   tpk_shape shape;
   int device = 0;
-  int n_req = 0, max_pages = 0, recent = 0;
-  const void* k_pool = nullptr;
-  const void* v_pool = nullptr;
-  void* rec_pool = nullptr;
+  int n_req = 0, max_pages = 0, recent = 0, n_layers = 1;
+  std::vector<const void*> k_pool, v_pool;  // per layer (device)
+  std::vector<void*> rec_pool;              // per layer (device)
+  std::vector<void*> host_rec;              // per layer (pinned host), or empty
   std::vector<Request> req;
   std::deque<Conversion> inflight;
   std::vector<cudaEvent_t> spare_events;
@@ -99,17 +110,30 @@ size_t tpk_tiers_device_bytes(int n_req, int max_pages) {
   return 4 * ((pt + 255) & ~size_t(255)) + ((conv + 255) & ~size_t(255));
 }
 
-tpk_status tpk_tiers_create(const tpk_shape* shape, int n_req, int max_pages, int recent_tokens, const void* k_pool,
-                            const void* v_pool, void* rec_pool, void* dev_scratch, size_t dev_scratch_bytes,
-                            tpk_tiers** out) {
+tpk_status tpk_tiers_create_layers(const tpk_shape* shape, int n_layers, int n_req, int max_pages, int recent_tokens,
+                                   const void* const* k_pools, const void* const* v_pools, void* const* rec_pools,
+                                   void* const* host_rec_pools, void* dev_scratch, size_t dev_scratch_bytes,
+                                   tpk_tiers** out) {
   if (!out) return tfail(TPK_ERR_INVALID, "null output pointer");
   *out = nullptr;
   if (!shape || shape->kv_heads < 1) return tfail(TPK_ERR_INVALID, "bad shape");
   if (shape->group != 8 || shape->head_dim != 256 || shape->page_tokens != kPage)
     return tfail(TPK_ERR_UNSUPPORTED, "only group 8, head_dim 256, 64-token pages");
+  if (n_layers < 1 || n_layers > 1024) return tfail(TPK_ERR_INVALID, "n_layers %d out of [1, 1024]", n_layers);
   if (n_req < 1 || max_pages < 1) return tfail(TPK_ERR_INVALID, "n_req %d, max_pages %d", n_req, max_pages);
   if (recent_tokens < 0) return tfail(TPK_ERR_INVALID, "recent_tokens %d < 0", recent_tokens);
-  if (!k_pool || !v_pool || !rec_pool) return tfail(TPK_ERR_INVALID, "null pool");
+  if (!k_pools || !v_pools || !rec_pools) return tfail(TPK_ERR_INVALID, "null pool array");
+  for (int l = 0; l < n_layers; ++l) {
+    if (!k_pools[l] || !v_pools[l] || !rec_pools[l]) return tfail(TPK_ERR_INVALID, "layer %d: null pool", l);
+    if (host_rec_pools) {
+      if (!host_rec_pools[l]) return tfail(TPK_ERR_INVALID, "layer %d: null host record pool", l);
+      cudaPointerAttributes a;
+      cudaError_t e = cudaPointerGetAttributes(&a, host_rec_pools[l]);
+      if (e != cudaSuccess) return tcuda(e, "cudaPointerGetAttributes (host record pool)");
+      if (a.type != cudaMemoryTypeHost)
+        return tfail(TPK_ERR_INVALID, "layer %d: the host record pool is not pinned host memory", l);
+    }
+  }
   const size_t need = tpk_tiers_device_bytes(n_req, max_pages);
   if (!dev_scratch || dev_scratch_bytes < need)
     return tfail(TPK_ERR_NOMEM, "device scratch %zu bytes < %zu required", dev_scratch_bytes, need);
@@ -119,10 +143,13 @@ tpk_status tpk_tiers_create(const tpk_shape* shape, int n_req, int max_pages, in
   t->n_req = n_req;
   t->max_pages = max_pages;
   t->recent = recent_tokens;
-  t->k_pool = k_pool;
-  t->v_pool = v_pool;
-  t->rec_pool = rec_pool;
+  t->n_layers = n_layers;
+  t->k_pool.assign(k_pools, k_pools + n_layers);
+  t->v_pool.assign(v_pools, v_pools + n_layers);
+  t->rec_pool.assign(rec_pools, rec_pools + n_layers);
+  if (host_rec_pools) t->host_rec.assign(host_rec_pools, host_rec_pools + n_layers);
   t->req.resize(n_req);
+  for (auto& r : t->req) r.written.assign(n_layers, 0);
   cudaGetDevice(&t->device);
   const size_t pt = (((size_t)n_req * max_pages * sizeof(int32_t)) + 255) & ~size_t(255);
   char* base = static_cast<char*>(dev_scratch);
@@ -160,7 +187,15 @@ tpk_status tpk_tiers_create(const tpk_shape* shape, int n_req, int max_pages, in
   return TPK_OK;
 }
 
-tpk_status tpk_tiers_update(tpk_tiers* t, int b, int n_tokens, const int32_t* page_slots) {
+tpk_status tpk_tiers_create(const tpk_shape* shape, int n_req, int max_pages, int recent_tokens, const void* k_pool,
+                            const void* v_pool, void* rec_pool, void* dev_scratch, size_t dev_scratch_bytes,
+                            tpk_tiers** out) {
+  return tpk_tiers_create_layers(shape, 1, n_req, max_pages, recent_tokens, &k_pool, &v_pool, &rec_pool, nullptr,
+                                 dev_scratch, dev_scratch_bytes, out);
+}
+
+tpk_status tpk_tiers_update_layers(tpk_tiers* t, int b, int n_tokens, const int32_t* page_slots,
+                                   const int32_t* layer_written) {
   if (!t) return tfail(TPK_ERR_INVALID, "null tier manager");
   if (b < 0 || b >= t->n_req) return tfail(TPK_ERR_INVALID, "request %d out of [0, %d)", b, t->n_req);
   Request& r = t->req[b];
@@ -168,17 +203,28 @@ tpk_status tpk_tiers_update(tpk_tiers* t, int b, int n_tokens, const int32_t* pa
   const int pages = (n_tokens + kPage - 1) / kPage;
   if (pages > t->max_pages) return tfail(TPK_ERR_INVALID, "request %d: %d pages > max_pages %d", b, pages, t->max_pages);
   if (pages > 0 && !page_slots) return tfail(TPK_ERR_INVALID, "null page slots");
-  // pages already converted or being converted must keep their slots
+  // pages already converted or being converted must keep their slots, and stay
+  // written in every layer
   const int fixed = r.published + r.converting;
   for (int p = 0; p < fixed && p < pages; ++p)
     if (page_slots[p] != r.slots[p])
       return tfail(TPK_ERR_INVALID, "request %d: page %d moved while converted or being converted", b, p);
+  if (layer_written)
+    for (int l = 0; l < t->n_layers; ++l)
+      if (layer_written[l] < kPage * fixed || layer_written[l] > n_tokens)
+        return tfail(TPK_ERR_INVALID, "request %d, layer %d: %d tokens written, outside [%d, %d]", b, l,
+                     layer_written[l], kPage * fixed, n_tokens);
   for (int p = 0; p < pages; ++p)
     if (page_slots[p] < 0 || (t->shape.kv_slots > 0 && page_slots[p] >= t->shape.kv_slots))
       return tfail(TPK_ERR_BOUNDS, "request %d: page %d slot %d outside the pool", b, p, page_slots[p]);
   r.slots.assign(page_slots, page_slots + pages);
   r.n_tokens = n_tokens;
+  for (int l = 0; l < t->n_layers; ++l) r.written[l] = layer_written ? layer_written[l] : n_tokens;
   return TPK_OK;
+}
+
+tpk_status tpk_tiers_update(tpk_tiers* t, int b, int n_tokens, const int32_t* page_slots) {
+  return tpk_tiers_update_layers(t, b, n_tokens, page_slots, nullptr);
 }
 
 // Publish finished conversions (in launch order), start new ones, upload the page
@@ -220,13 +266,15 @@ tpk_status tpk_tiers_step(tpk_tiers* t, tpk_stream_t conv_stream, tpk_stream_t d
   int32_t* h_pt = hs;
   int32_t* h_pt8 = hs + table_words;
   int32_t* h_conv = hs + 2 * table_words;
-  // 3. new conversions: whole pages older than the recent window
+  // 3. new conversions: whole pages older than the recent window and written by
+  //    every layer
   int n_conv = 0;
   int started = 0;
   std::vector<std::pair<int, int>> batch;  // (request, count), in the order of h_conv
   for (int b = 0; b < t->n_req; ++b) {
     Request& r = t->req[b];
-    const int eligible = r.n_tokens > t->recent ? (r.n_tokens - t->recent) / kPage : 0;
+    int eligible = r.n_tokens > t->recent ? (r.n_tokens - t->recent) / kPage : 0;
+    for (int l = 0; l < t->n_layers; ++l) eligible = std::min(eligible, r.written[l] / kPage);
     const int first = r.published + r.converting;
     const int count = eligible - first;
     if (count <= 0) continue;
@@ -248,8 +296,26 @@ tpk_status tpk_tiers_step(tpk_tiers* t, tpk_stream_t conv_stream, tpk_stream_t d
     if (e == cudaSuccess) e = cudaEventRecord(t->stage_conv_done[g], cs);
     if (e != cudaSuccess) return tcuda(e, "conversion slot upload");
     t->stage_conv_used[g] = true;
-    tpk_status st = tpk_kv_quantize_pages(&t->shape, t->k_pool, t->v_pool, d, d, n_conv, t->rec_pool, conv_stream);
-    if (st != TPK_OK) return st;
+    for (int l = 0; l < t->n_layers; ++l) {
+      tpk_status st =
+          tpk_kv_quantize_pages(&t->shape, t->k_pool[l], t->v_pool[l], d, d, n_conv, t->rec_pool[l], conv_stream);
+      if (st != TPK_OK) return st;
+    }
+    // the host image gets every converted record before any of the events below
+    // (runs of consecutive slots as one copy)
+    if (!t->host_rec.empty()) {
+      const size_t per_slot = (size_t)t->shape.kv_heads * TPK_RECORD_BYTES;
+      for (int l = 0; l < t->n_layers; ++l)
+        for (int i = 0; i < n_conv;) {
+          int j = i + 1;
+          while (j < n_conv && h_conv[j] == h_conv[j - 1] + 1) ++j;
+          const size_t off = (size_t)h_conv[i] * per_slot;
+          e = cudaMemcpyAsync(static_cast<char*>(t->host_rec[l]) + off, static_cast<const char*>(t->rec_pool[l]) + off,
+                              (size_t)(j - i) * per_slot, cudaMemcpyDeviceToHost, cs);
+          if (e != cudaSuccess) return tcuda(e, "record copy to the host image");
+          i = j;
+        }
+    }
     for (const auto& bc : batch) {
       cudaEvent_t ev;
       if (!t->spare_events.empty()) {
