@@ -10,13 +10,31 @@ import tiered_paged_kv_gb300 as tpk
 from tiered_paged_kv_gb300 import synth
 
 # Parity tolerances.  Outputs: max |o_gpu - o_oracle| <= O_TOL * max |o_oracle|
-# (the bar the method is held to against the oracle on the same codes).  lse:
-# absolute, natural-log units, held near the precision the kernels reach (about
-# 7e-5 observed: float32 scores, and the 8-bit tier's products on code + 1152 with
-# the offset removed after the sum); queries scaled far beyond unit variance have
-# a bar of their own that grows with |lse| (see test_extreme_query_scales).
+# (the bar the method is held to against the oracle on the same codes).  lse
+# (natural-log units), held near the precision each tier's kernel reaches:
+#  - exact tier only: LSE_TOL_EXACT absolute (bf16 inputs, float32 scores;
+#    observed at most 1.1e-6 over the suite);
+#  - with 8-bit pages: LSE_TOL_8BIT + LSE_REL_8BIT * max|lse|, capped at 1e-3.  The
+#    8-bit tier's products run on code + 1152 with the offset removed after the
+#    float32 sum, which keeps about 15 bits of a score relative to its size
+#    (observed at most 1e-4 + 2.7e-5 max|lse|, and 5.3e-4 in all, over the suite).
+# Queries scaled far beyond unit variance have a bar of their own that grows with
+# |lse| (test_extreme_query_scales).
 O_TOL = 1e-3
-LSE_TOL = float(os.environ.get("TPK_LSE_TOL", "2e-4"))
+LSE_TOL_EXACT = 1e-5
+LSE_TOL_8BIT = 1e-4
+LSE_REL_8BIT = 4e-5
+LSE_CAP = 1e-3
+
+
+def lse_bar(ol, exact_only=False):
+    """The lse bar of one comparison (ol: the oracle's lse)."""
+    if exact_only:
+        return LSE_TOL_EXACT
+    fin = np.isfinite(ol)
+    m = np.abs(ol[fin]).max() if fin.any() else 0.0
+    return min(LSE_CAP, LSE_TOL_8BIT + LSE_REL_8BIT * m)
+
 
 # Record slots no page uses are filled with this byte: every scale reads as a NaN
 # (0xffffffff), so a stray read of an unused record shows up in the output.
@@ -107,7 +125,8 @@ def _record(what, err, lerr, lse_max):
                                 "lse_err": float(lerr), "lse_absmax": float(lse_max)}) + "\n")
 
 
-def assert_close(o, lse, oo, ol, what=""):
+def assert_close(o, lse, oo, ol, what="", exact_only=False):
+    """o, lse against the oracle's oo, ol; exact_only: no 8-bit page took part."""
     scale = max(np.abs(oo).max(), 1e-30)
     err = np.abs(o - oo).max() / scale
     fin = np.isfinite(ol)
@@ -115,8 +134,9 @@ def assert_close(o, lse, oo, ol, what=""):
     assert np.all(lse[~fin] == ol[~fin]), f"{what}: empty rows differ"
     lerr = np.abs(lse[fin] - ol[fin]).max() if fin.any() else 0.0
     _record(what, err, lerr, np.abs(ol[fin]).max() if fin.any() else 0.0)
+    bar = lse_bar(ol, exact_only)
     assert err <= O_TOL, f"{what}: max|do|/max|o| = {err:.3e} > {O_TOL}"
-    assert lerr <= LSE_TOL, f"{what}: max|dlse| = {lerr:.3e} > {LSE_TOL}"
+    assert lerr <= bar, f"{what}: max|dlse| = {lerr:.3e} > {bar:.3e}"
     return err, lerr
 
 
