@@ -123,35 +123,43 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return d;
 }
 
-// Four codes from estimates known to lie within 127 (1 + 2^-20) in magnitude (codes
-// of pages converted here: the scales come from the maxima, so no clamp is needed),
-// as one word of stored bytes.  Adding M = 1.5 * 2^23 + 128 puts z + M in [2^23,
+// The magic number of the rounding below: for |z| <= 128, z + M lies in [2^23,
 // 2^24), where float32 spacing is 1, so the sum rounds half to even exactly like
-// rint (M is even), and the low byte of its encoding is (rint(z) + 128) mod 256, the
-// stored byte.  With d = z - rint(z) (exact), z lies within kCodeSlack of a
-// half-integer iff |d| >= 1/2 - kCodeSlack, i.e. iff d^2 - (1/2 - kCodeSlack)^2 >= 0;
-// the square of 2047/4096 is a float, so one fused multiply-add gives that sign
-// exactly: e >= 0 (sign bit clear) marks an estimate to redo by division.
-constexpr float kRoundMagic = 12583040.f;       // 1.5 * 2^23 + 128
-constexpr float kNearSq = 4190209.f * 0x1p-24f;  // (1/2 - 2^-12)^2
-__device__ __forceinline__ uint32_t code_word4(float2 z01, float2 z23, float2& e01, float2& e23) {
-  const float2 m = make_float2(kRoundMagic, kRoundMagic), nc = make_float2(-kNearSq, -kNearSq);
-  const float2 t01 = __fadd2_rn(z01, m), t23 = __fadd2_rn(z23, m);
-  const float2 d01 = sub2(z01, sub2(t01, m)), d23 = sub2(z23, sub2(t23, m));
-  e01 = __ffma2_rn(d01, d01, nc);
-  e23 = __ffma2_rn(d23, d23, nc);
-  return __byte_perm(__byte_perm(__float_as_uint(t01.x), __float_as_uint(t01.y), 0x0040),
-                     __byte_perm(__float_as_uint(t23.x), __float_as_uint(t23.y), 0x0040), 0x5410);
-}
-// AND of the encodings: sign bit clear iff some e >= 0 (some estimate to redo)
-__device__ __forceinline__ uint32_t and_bits(float2 a, float2 b) {
-  return __float_as_uint(a.x) & __float_as_uint(a.y) & __float_as_uint(b.x) & __float_as_uint(b.y);
-}
-// bits shift, shift + 1 set where e.x, e.y >= 0
-__device__ __forceinline__ uint32_t near_bits(float2 e, int shift) {
-  return ((((__float_as_uint(e.x) >> 31) | ((__float_as_uint(e.y) >> 31) << 1))) ^ 3u) << shift;
-}
+// rint (M is even), and the low byte of its encoding is (rint(z) + 128) mod 256,
+// the stored byte.
+constexpr float kRoundMagic = 12583040.f;  // 1.5 * 2^23 + 128
 __device__ __forceinline__ bool fast_scale(float scale) { return scale >= 0x1p-100f && scale <= 0x1p100f; }
+
+// Four codes of pages converted here (estimates within 127 (1 + 2^-20) in
+// magnitude: the scales come from the maxima, so no clamp is needed) from an
+// interval around each quotient estimate: the estimate x * w (w = 1/scale, or
+// y * (1/r_t) for keys) lies within a relative 6 * 2^-24 of the correctly rounded
+// quotient, so x * w widened by 2^-20 each way brackets it.  tA = x * w (1 + 2^-20)
+// + M and tB = x * w (1 - 2^-20) + M, each one fused multiply-add rounded to an
+// integer, agree iff rint is constant over the interval -- then it is the code;
+// else (diff nonzero) the byte is redone by division.  The low byte of tA's
+// encoding is the stored byte; four of them make one word.
+constexpr float kIvHi = 1.f + 0x1p-20f, kIvLo = 1.f - 0x1p-20f;
+__device__ __forceinline__ uint32_t code_word4_iv(float2 x01, float2 x23, float2 wa, float2 wb, uint32_t& diff,
+                                                  float2 (&ta)[2], float2 (&tb)[2]) {
+  const float2 m = make_float2(kRoundMagic, kRoundMagic);
+  ta[0] = __ffma2_rn(x01, wa, m);
+  ta[1] = __ffma2_rn(x23, wa, m);
+  tb[0] = __ffma2_rn(x01, wb, m);
+  tb[1] = __ffma2_rn(x23, wb, m);
+  diff |= (__float_as_uint(ta[0].x) ^ __float_as_uint(tb[0].x));
+  diff |= (__float_as_uint(ta[0].y) ^ __float_as_uint(tb[0].y));
+  diff |= (__float_as_uint(ta[1].x) ^ __float_as_uint(tb[1].x));
+  diff |= (__float_as_uint(ta[1].y) ^ __float_as_uint(tb[1].y));
+  return __byte_perm(__byte_perm(__float_as_uint(ta[0].x), __float_as_uint(ta[0].y), 0x0040),
+                     __byte_perm(__float_as_uint(ta[1].x), __float_as_uint(ta[1].y), 0x0040), 0x5410);
+}
+__device__ __forceinline__ uint32_t diff_bits4(const float2 (&ta)[2], const float2 (&tb)[2], int shift) {
+  return ((uint32_t)(__float_as_uint(ta[0].x) != __float_as_uint(tb[0].x)) |
+          ((uint32_t)(__float_as_uint(ta[0].y) != __float_as_uint(tb[0].y)) << 1) |
+          ((uint32_t)(__float_as_uint(ta[1].x) != __float_as_uint(tb[1].x)) << 2) |
+          ((uint32_t)(__float_as_uint(ta[1].y) != __float_as_uint(tb[1].y)) << 3)) << shift;
+}
 
 constexpr int kQuantThreads = 256;  // one thread per channel in the per-channel phases
 
@@ -238,22 +246,19 @@ __global__ void __launch_bounds__(kQuantThreads, 2) quantize_kernel(const __grid
         wv[e >> 2] |= quotient_byte(z) << (8 * (e & 3));
       }
     } else {
-      const float2 inv2 = make_float2(inv, inv);
-      float2 ev[8];
+      const float2 wa = make_float2(inv * kIvHi, inv * kIvHi), wb = make_float2(inv * kIvLo, inv * kIvLo);
+      float2 ta[4][2], tb[4][2];
+      uint32_t diff = 0u;
 #pragma unroll
       for (int g = 0; g < 4; ++g) {
         const int t = t0 + 4 * g;
-        const float2 z01 =
-            __fmul2_rn(make_float2(bf16_lo(__ldg(&gv[t][ch])), bf16_lo(__ldg(&gv[t + 1][ch]))), inv2);
-        const float2 z23 =
-            __fmul2_rn(make_float2(bf16_lo(__ldg(&gv[t + 2][ch])), bf16_lo(__ldg(&gv[t + 3][ch]))), inv2);
-        wv[g] = code_word4(z01, z23, ev[2 * g], ev[2 * g + 1]);
+        const float2 x01 = make_float2(bf16_lo(__ldg(&gv[t][ch])), bf16_lo(__ldg(&gv[t + 1][ch])));
+        const float2 x23 = make_float2(bf16_lo(__ldg(&gv[t + 2][ch])), bf16_lo(__ldg(&gv[t + 3][ch])));
+        wv[g] = code_word4_iv(x01, x23, wa, wb, diff, ta[g], tb[g]);
       }
-      const uint32_t all = and_bits(ev[0], ev[1]) & and_bits(ev[2], ev[3]) & and_bits(ev[4], ev[5]) &
-                           and_bits(ev[6], ev[7]);
-      if (!(all >> 31)) {  // rare: some estimate near a half-integer
+      if (diff) {  // rare: the interval holds a half-integer
 #pragma unroll
-        for (int j = 0; j < 8; ++j) redo |= near_bits(ev[j], 2 * j);
+        for (int g = 0; g < 4; ++g) redo |= diff_bits4(ta[g], tb[g], 4 * g);
       }
     }
     uint8_t* dst = rec + kOffVc + vc_byte(ch, t0);
@@ -565,6 +570,7 @@ __global__ void __launch_bounds__(kQuantThreads, 2) quantize_kernel(const __grid
     const float r = given ? p.g_ktok[gidx * kPageTokens + t] : __fdiv_rn(ymax, 127.f);
     const bool fast = s_fast && fast_scale(r);
     const float inv_r = fast ? __frcp_rn(r) : 0.f;
+    const float2 ra = make_float2(inv_r * kIvHi, inv_r * kIvHi), rb = make_float2(inv_r * kIvLo, inv_r * kIvLo);
     uint8_t* kc = rec + kOffKc;
 #pragma unroll 2
     for (int k = 0; k < 8; ++k) {
@@ -581,14 +587,12 @@ __global__ void __launch_bounds__(kQuantThreads, 2) quantize_kernel(const __grid
           wk[e >> 2] |= quotient_byte(z) << (8 * (e & 3));
         }
       } else {
-        float2 z[4], ev[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) z[j] = __fmul2_rn(y[j], make_float2(inv_r, inv_r));
-        wk[0] = code_word4(z[0], z[1], ev[0], ev[1]);
-        wk[1] = code_word4(z[2], z[3], ev[2], ev[3]);
-        if (!((and_bits(ev[0], ev[1]) & and_bits(ev[2], ev[3])) >> 31)) {  // rare
-#pragma unroll
-          for (int j = 0; j < 4; ++j) redo |= near_bits(ev[j], 2 * j);
+        float2 ta[2][2], tb[2][2];
+        uint32_t diff = 0u;
+        wk[0] = code_word4_iv(y[0], y[1], ra, rb, diff, ta[0], tb[0]);
+        wk[1] = code_word4_iv(y[2], y[3], ra, rb, diff, ta[1], tb[1]);
+        if (diff) {  // rare
+          redo |= diff_bits4(ta[0], tb[0], 0) | diff_bits4(ta[1], tb[1], 4);
         }
       }
       // (ch0 is a multiple of 8: kc_byte(t, ch0 + e) = kc_byte(t, ch0) + e)
