@@ -34,6 +34,11 @@
  *            lse:         float32 [rows], natural log of sum exp(sm_scale q.k).
  * Empty      An empty token or page range yields lse = -inf and o = 0, the valid
  *            empty partial; a merge never reads the o of a -inf partial.
+ * Contexts   Per device the library resolves once, on first use, the device
+ *            addresses of its status word and static scratch, its kernels'
+ *            shared-memory limits and its constant tables; they belong to the
+ *            device's primary context.  Do not call cudaDeviceReset (or otherwise
+ *            end that context) between calls of the library in one process.
  */
 #ifndef TPK_H
 #define TPK_H
