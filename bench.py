@@ -1114,6 +1114,8 @@ def run_gate(args, stream, dev, flush, flush_r, sizes, layers_measured=4, layers
                 row[k][f"net_saving_us_per_token_{layers_model}_layers"] = round(net, 2)
                 row[k]["verdict"] = "accept" if gate.accept(link, cands["exact"], c, layers=layers_model) else "reject"
                 row[k]["device_time_ratio"] = round(c.device_us / cands["exact"].device_us, 4)
+                # history resident in HBM instead: no link to save on, the device time decides
+                row[k]["device_resident_verdict"] = "accept" if c.device_us < cands["exact"].device_us else "reject"
         rows.append(row)
         print(json.dumps(row), flush=True, file=sys.stderr)
         del kp, vp, q, rec, pool13, k2, v2, ws
