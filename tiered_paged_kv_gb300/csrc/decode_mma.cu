@@ -157,15 +157,23 @@ __device__ __forceinline__ uint32_t swz(int r, int chunk) {  // byte offset of (
   return (chunk >> 3) * 4096 + r * 128 + (((chunk & 7) ^ (r & 7)) << 4);
 }
 
-// (pt_staged: the page table is in shared memory; the first items are issued
-// before it is, straight from the global table)
+// The page-table entry of item j: from the shared-memory copy, or from the global
+// table for entries past the copy.
+__device__ __forceinline__ int64_t item_slot(const DecodeParams& p, const UnitInfo& ui, const Items& it,
+                                             const MmaSmem& S, int j) {
+  const int page = item_page(ui, it, j);
+  const int idx = page - it.pg_first;
+  return idx < kPtCache ? S.pt[idx] : __ldg((ui.tier == 0 ? p.page_table : p.page_table8) + ui.pt_off + page);
+}
+// The page-table entry of item j straight from the global table (the first items
+// are issued before the shared-memory copy exists).
+__device__ __forceinline__ int64_t item_slot_global(const DecodeParams& p, const UnitInfo& ui, const Items& it, int j) {
+  return __ldg((ui.tier == 0 ? p.page_table : p.page_table8) + ui.pt_off + item_page(ui, it, j));
+}
+
+// Issue the copy of item j, whose page-table entry is `slot`, into slot s.
 __device__ __forceinline__ void mma_issue(const DecodeParams& p, const UnitInfo& ui, const Items& it, MmaSmem& S,
-                                          int j, int s, bool pt_staged = true) {
-  int page = item_page(ui, it, j);
-  int idx = page - it.pg_first;
-  int64_t slot = pt_staged && idx < kPtCache
-                     ? S.pt[idx]
-                     : __ldg((ui.tier == 0 ? p.page_table : p.page_table8) + ui.pt_off + page);
+                                          int j, int s, int64_t slot) {
   int64_t lim = ui.tier == 0 ? p.kv_slots : p.rec_slots;
   const bool ok = slot >= 0 && (lim == 0 || slot < lim);
   S.valid[s] = ok;
@@ -592,7 +600,11 @@ __global__ void __launch_bounds__(kMmaThreads, 1) decode_mma_kernel(const __grid
 
   const UnitInfo ui = decode_unit(p, plan.req, blockIdx.x);
   const Items it = unit_items(ui);
-  if (tid == 0) {
+  // One thread (the block's last) sets up the barriers and issues the copies; the
+  // others meanwhile bring the unit's page-table entries and query rows into
+  // shared memory, so the two memory round trips of the start overlap.
+  constexpr int kIssuer = kMmaThreads - 1;
+  if (tid == kIssuer) {
     for (int s = 0; s < kMmaSlots; ++s) {
       mbar_init(&S.full[s], 1);
       mbar_init(&S.empty[s], 2);
@@ -601,30 +613,45 @@ __global__ void __launch_bounds__(kMmaThreads, 1) decode_mma_kernel(const __grid
     for (int s = 0; s < kMmaSlots; ++s) S.rel[s] = S.fills[s] = 0;
     S.abort = 0;
     fence_mbar_init();
-    // the first three items go out at once, straight from the global page table;
-    // the next three after the prologue, and every later item is issued by the warp
-    // that releases its slot's previous item last.  (All six at once made every
-    // block's first record land later: measured 0.9 µs slower per 128K step.)
-    for (int j = 0; j < min(it.n, kFirstIssue); ++j) {
-      mma_issue(p, ui, it, S, j, j, false);
-      S.fills[j] = 1;
-    }
-  }
-  load_page_table(p, ui, it, S);
-  {
-    const uint32_t* q32 = reinterpret_cast<const uint32_t*>(p.q + (int64_t)(ui.b * p.H + ui.h) * kGroup * kHeadDim);
-    for (int i = tid; i < kGroup * kHeadDim / 2; i += blockDim.x) (&S.q[0][0])[i] = __ldg(q32 + i);
+    // The first three items go out at once, straight from the global page table
+    // (their entries loaded together first: one memory round trip); the next
+    // three as soon as the page table is in shared memory, and every later item
+    // is issued by the warp that releases its slot's previous item last.  (All six
+    // at once made every block's first record land later: measured 0.9 µs slower
+    // per 128K step.)
+    int64_t first[kFirstIssue];
+#pragma unroll
+    for (int j = 0; j < kFirstIssue; ++j) first[j] = j < it.n ? item_slot_global(p, ui, it, j) : 0;
+#pragma unroll
+    for (int j = 0; j < kFirstIssue; ++j)
+      if (j < it.n) {
+        mma_issue(p, ui, it, S, j, j, first[j]);
+        S.fills[j] = 1;
+      }
+  } else {
+    const int32_t* pt = (ui.tier == 0 ? p.page_table : p.page_table8) + ui.pt_off + it.pg_first;
+    const int n = min(it.n_pages, kPtCache);
+    for (int i = tid; i < n; i += kMmaThreads - 1) S.pt[i] = __ldg(pt + i);
+    const uint4* q128 = reinterpret_cast<const uint4*>(p.q + (int64_t)(ui.b * p.H + ui.h) * kGroup * kHeadDim);
+    for (int i = tid; i < kGroup * kHeadDim / 8; i += kMmaThreads - 1)
+      reinterpret_cast<uint4*>(&S.q[0][0])[i] = __ldg(q128 + i);
   }
   __syncthreads();
-  // Float copy of q times 2^-(e+1), e the exponent of the row's max |q|: with
-  // s_c <= 2^14 every q'_c = q_c s_c of this row then stays below 2^13, inside
-  // f16 range, whatever the page.
+  // 8-bit tier: a float copy of q times 2^-(e+1), e the exponent of the row's max
+  // |q|: with s_c <= 2^14 every q'_c = q_c s_c of this row then stays below 2^13,
+  // inside f16 range, whatever the page.  Thread (g, t) of every warp reads a
+  // quarter of row g with 16-byte loads for the row maximum; warp w writes
+  // channels 32w .. 32w + 31 of the float copy.  (The exact tier reads the bf16
+  // rows as they are and starts at once.)
   float qk_scale = p.qscale;
-  if (warp < kCons) {
+  if (ui.tier == 1) {
     float qmax = 0.f;
-    for (int c = t; c < kHeadDim / 2; c += 4) {
-      const uint32_t w = S.q[g][c];
-      qmax = fmaxf(qmax, fmaxf(fabsf(bf16_lo(w)), fabsf(bf16_hi(w))));
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const uint4 w = *reinterpret_cast<const uint4*>(&S.q[g][4 * (t + 4 * k)]);
+      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) qmax = fmaxf(qmax, fmaxf(fabsf(bf16_lo(ws[e])), fabsf(bf16_hi(ws[e]))));
     }
     qmax = fmaxf(qmax, __shfl_xor_sync(kAll, qmax, 1));
     qmax = fmaxf(qmax, __shfl_xor_sync(kAll, qmax, 2));
@@ -632,17 +659,24 @@ __global__ void __launch_bounds__(kMmaThreads, 1) decode_mma_kernel(const __grid
     frexpf(qmax, &e);
     const float sc = qmax > 0.f ? ldexpf(1.f, -(e + 1)) : 1.f;
     qk_scale = p.qscale / sc;
-    if (warp == 0)
-      for (int c = t; c < kHeadDim / 2; c += 4) {
-        const uint32_t w = S.q[g][c];
-        S.qs[g][ks_index(2 * c)] = bf16_lo(w) * sc;  // same channel permutation as the record's s_c
-        S.qs[g][ks_index(2 * c + 1)] = bf16_hi(w) * sc;
-      }
+    // lane (g, t): row g, channels 32 warp + 8 t .. + 7 (every lane of row g holds
+    // the row's scale)
+    const uint4 w = *reinterpret_cast<const uint4*>(&S.q[g][16 * warp + 4 * t]);
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int e2 = 0; e2 < 4; ++e2) {
+      const int c = 32 * warp + 8 * t + 2 * e2;
+      S.qs[g][ks_index(c)] = bf16_lo(ws[e2]) * sc;  // same channel permutation as the record's s_c
+      S.qs[g][ks_index(c + 1)] = bf16_hi(ws[e2]) * sc;
+    }
+    __syncthreads();
   }
-  __syncthreads();
-  if (tid == 0) {
+  // The next three items.  (Issuing a copy can stall its thread while earlier
+  // copies are still under way, so this comes after the block-wide steps: only
+  // the issuer's own warp waits, and its pair's first item is among these.)
+  if (tid == kIssuer) {
     for (int j = kFirstIssue; j < min(it.n, kMmaSlots); ++j) {
-      mma_issue(p, ui, it, S, j, j);
+      mma_issue(p, ui, it, S, j, j, item_slot(p, ui, it, S, j));
       S.fills[j] = 1;
     }
   }
@@ -691,7 +725,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) decode_mma_kernel(const __grid
           if (atomicAdd(&S.rel[s], 1) == 1) {
             S.rel[s] = 0;
             __threadfence_block();
-            mma_issue(p, ui, it, S, j + kMmaSlots, s);
+            mma_issue(p, ui, it, S, j + kMmaSlots, s, item_slot(p, ui, it, S, j + kMmaSlots));
             S.fills[s] += 1;
           }
         }
