@@ -116,13 +116,17 @@ __device__ __forceinline__ UnitInfo decode_unit(const DecodeParams& p, const Req
     ui.tier = 0;
     ui.split = k;
     ui.n_splits = r.splits_e;
-    int pg0 = r.e_begin / kPageTokens;
-    int pg1 = (r.e_end + kPageTokens - 1) / kPageTokens;
+    // the exact tier is cut on page boundaries for the primitive call (its
+    // documented pieces) and on half-page boundaries (the kernels' item) in the
+    // multi-request launch, where finer cuts even out the units' lengths
+    const int gran = p.mode == kModePrimitive ? kPageTokens : kPageTokens / 2;
+    int pg0 = r.e_begin / gran;
+    int pg1 = (r.e_end + gran - 1) / gran;
     int P = pg1 - pg0;
     int pa = pg0 + (int)((int64_t)P * k / r.splits_e);
     int pb = pg0 + (int)((int64_t)P * (k + 1) / r.splits_e);
-    ui.tok_begin = max(r.e_begin, pa * kPageTokens);
-    ui.tok_end = min(r.e_end, pb * kPageTokens);
+    ui.tok_begin = max(r.e_begin, pa * gran);
+    ui.tok_end = min(r.e_end, pb * gran);
     if (ui.tok_end < ui.tok_begin) ui.tok_end = ui.tok_begin;
     ui.pt_off = r.pt_off;
   } else {
