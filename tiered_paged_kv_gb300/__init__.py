@@ -148,8 +148,12 @@ def _stream(s):
 
 
 def _host_i32(a):
+    """(array kept alive by the caller, its address) of a host int32 array; an
+    int32 C-contiguous ndarray is passed as it is, anything else is copied."""
+    if isinstance(a, np.ndarray) and a.dtype == np.int32 and a.flags.c_contiguous:
+        return a, a.ctypes.data
     arr = np.ascontiguousarray(np.asarray(a), dtype=np.int32)
-    return arr, arr.ctypes.data_as(ctypes.c_void_p)
+    return arr, arr.ctypes.data
 
 
 def _check(status):
