@@ -231,3 +231,57 @@ def test_subnormal_and_near_maximum_channels():
         kc, vc, s, r, u = oracle.record_fields(got[slot, 0])
         check_own_record(got[slot, 0], ref[slot, 0], f"slot {slot}")
         assert s[3] == np.float32(2.0 ** -14) and s[4] == np.float32(2.0 ** 14)
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_random_adversarial_pages(seed):
+    """Seeded page-heads built to stress the conversion: per-channel key magnitudes
+    2^U(-40, 40) and value magnitudes 2^U(-60, 60) (so some key channels clamp at
+    2^+-14 and the sums take both paths), heavy-tailed entries (Gaussian over uniform), whole zero channels
+    and rows, and channels rounded to eighths of their maximum (many equal
+    magnitudes and exact half-integer quotients).  The GPU's own records against the oracle's: scales within 1 ulp,
+    identical records where the scales agree; and with the oracle's scales given,
+    identical records everywhere."""
+    rng = np.random.default_rng(400 + seed)
+    w = synth.make_workload([64 * 32], 0, H=2, seed=20 + seed)
+    for slot in w.int8_slots():
+        for h in range(w.H):
+            k = rng.standard_normal((64, 256)) / np.maximum(rng.uniform(size=(64, 256)), 0.02)
+            v = rng.standard_normal((64, 256))
+            k *= 2.0 ** rng.uniform(-40, 40, 256)[None, :]
+            v *= 2.0 ** rng.uniform(-60, 60, 256)[None, :]
+            if rng.uniform() < 0.5:
+                k[:, rng.integers(0, 256, 3)] = 0.0
+                v[:, rng.integers(0, 256, 3)] = 0.0
+            if rng.uniform() < 0.5:
+                k[rng.integers(0, 64, 2), :] = 0.0
+            if rng.uniform() < 0.5:  # coarse grid: many equal magnitudes and exact half quotients
+                c = rng.integers(0, 256, 16)
+                m = np.maximum(np.abs(k[:, c]).max(axis=0), 1e-30)
+                k[:, c] = np.round(k[:, c] / m * 8) / 8 * m
+                mv = np.maximum(np.abs(v[:, c]).max(axis=0), 1e-30)
+                v[:, c] = np.round(v[:, c] / mv * 8) / 8 * mv
+            w.k_pool[slot, h] = synth.f32_to_bf16(np.clip(k, -3e38, 3e38).astype(np.float32))
+            w.v_pool[slot, h] = synth.f32_to_bf16(np.clip(v, -3e38, 3e38).astype(np.float32))
+    ref = oracle_records(w).reshape(w.n_slots, w.H, oracle.REC_BYTES)
+    d = DevWorkload(w)
+    got = d.quantize_gpu().reshape(w.n_slots, w.H, oracle.REC_BYTES)
+    for slot in w.int8_slots():
+        for h in range(w.H):
+            kc, vc, s, r, u = oracle.record_fields(got[slot, h])
+            check_own_record(got[slot, h], ref[slot, h], f"seed {seed}, slot {slot} head {h}")
+            assert kc.min() >= -127 and vc.min() >= -127
+            assert np.all(np.abs(kc).max(axis=1)[r > 0] == 127)
+            assert np.all(np.abs(vc).max(axis=0)[u > 0] == 127)
+    # the oracle's scales given: every byte identical
+    slots = w.int8_slots()
+    recs = ref[slots]
+    fields = [[oracle.record_fields(recs[i, h]) for h in range(w.H)] for i in range(len(slots))]
+    ks = np.array([[f[2] for f in row] for row in fields], np.float32)
+    kt = np.array([[f[3] for f in row] for row in fields], np.float32)
+    vs = np.array([[f[4] for f in row] for row in fields], np.float32)
+    s_d = dev_i32(slots)
+    d2 = DevWorkload(w)
+    tpk.kv_quantize_pages_given_scales(d2.shape, d2.k, d2.v, s_d, s_d, len(slots), dev_f32(ks), dev_f32(kt),
+                                       dev_f32(vs), d2.rec)
+    assert np.array_equal(d2.rec.cpu().numpy().reshape(w.n_slots, w.H, oracle.REC_BYTES)[slots], recs)
