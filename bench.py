@@ -364,9 +364,20 @@ def decode_kernel_loop_times(step_fns, n_steps, stream):
     return sum(a.elapsed_time(b) for a, b in evs) / n_steps
 
 
-def loop_fields(hist_bytes, ms, peak):
-    gbs = hist_bytes / (ms * 1e-3) / 1e9
-    return {"loop_us_per_step": round(ms * 1e3, 2), "loop_GBps": round(gbs, 1), "loop_hbm_frac": round(gbs / peak, 4)}
+def step_fields(hist_bytes, ms_loop, ms_iso, n_iso, peak):
+    """A workload's step figures: timed as the headline is (steps back to back in
+    one graph over two resident copies), and each step alone beside it (one graph
+    replay between events, L2 flushed before it)."""
+    out = {"us_per_step": round(ms_loop * 1e3, 2)}
+    if hist_bytes is not None:
+        gbs = hist_bytes / (ms_loop * 1e-3) / 1e9
+        out.update({"GBps": round(gbs, 1), "hbm_frac": round(gbs / peak, 4)})
+    iso = {"us_per_step_median": round(ms_iso * 1e3, 2), "steps": n_iso}
+    if hist_bytes is not None:
+        g = hist_bytes / (ms_iso * 1e-3) / 1e9
+        iso.update({"GBps": round(g, 1), "hbm_frac": round(g / peak, 4)})
+    out["isolated"] = iso
+    return out
 
 
 def decode_kernel_times(step, steps, stream, flush, flush_r):
@@ -446,17 +457,16 @@ def run_batched(impl, args, stream, dev, flush, flush_r, peak, int_query=0, keep
     st, flags = tpk.get_device_status(reset=True, stream=stream)
     if st != 0:
         raise RuntimeError(f"device status {st} flags {flags} (batched)")
-    kms = decode_kernel_times(step, args.tier_steps, stream, flush, flush_r)
+    kms = decode_kernel_loop_times([step, step2], max(10, args.tier_steps), stream)
     if keep is not None:
         stream.synchronize()
         keep["w"], keep["o"] = w, o.cpu().numpy()
     ms = statistics.median(times)
-    gbs = w.history_bytes() / (ms * 1e-3) / 1e9
     kgbs = w.history_bytes() / (kms * 1e-3) / 1e9
     return {"history_bytes": w.history_bytes(), "requests": B, "tokens": int(w.n_tokens.sum()),
-            "us_per_step_median": round(ms * 1e3, 2), "GBps": round(gbs, 1), "hbm_frac": round(gbs / peak, 4),
-            "steps": len(times), "kernel_us_mean": round(kms * 1e3, 2), "kernel_GBps": round(kgbs, 1),
-            "kernel_hbm_frac": round(kgbs / peak, 4), **loop_fields(w.history_bytes(), lms, peak),
+            **step_fields(w.history_bytes(), lms, ms, len(times), peak),
+            "kernel_us_mean": round(kms * 1e3, 2), "kernel_GBps": round(kgbs, 1),
+            "kernel_hbm_frac": round(kgbs / peak, 4),
             "workload": "16 requests, lengths uniform in [8192, 65536] (seed 3), 2048 BF16 recent each, "
                         "4 KV heads x 8 q rows, head_dim 256, outlier keys"}
 
@@ -509,14 +519,12 @@ def run_tier(which, impl, args, stream, dev, flush, flush_r, peak, int_query=0):
     st, flags = tpk.get_device_status(reset=True, stream=stream)
     if st != 0:
         raise RuntimeError(f"device status {st} flags {flags} ({which} tier)")
-    kms = decode_kernel_times(step, args.tier_steps, stream, flush, flush_r)
+    kms = decode_kernel_loop_times([step, step2], max(10, args.tier_steps), stream)
     ms = statistics.median(times)
-    gbs = w.history_bytes() / (ms * 1e-3) / 1e9
     kgbs = w.history_bytes() / (kms * 1e-3) / 1e9
-    return {"history_bytes": w.history_bytes(), "us_per_step_median": round(ms * 1e3, 2),
-            "GBps": round(gbs, 1), "hbm_frac": round(gbs / peak, 4), "steps": len(times),
+    return {"history_bytes": w.history_bytes(), **step_fields(w.history_bytes(), lms, ms, len(times), peak),
             "kernel_us_mean": round(kms * 1e3, 2), "kernel_GBps": round(kgbs, 1),
-            "kernel_hbm_frac": round(kgbs / peak, 4), **loop_fields(w.history_bytes(), lms, peak),
+            "kernel_hbm_frac": round(kgbs / peak, 4),
             "workload": f"131072 tokens {'all BF16' if which == 'exact' else 'all 8-bit (2048 pages)'}, "
                         "4 KV heads x 8 q rows, head_dim 256, outlier keys, seed 12"}
 
@@ -577,7 +585,7 @@ def run_exact_32k(impl, args, stream, dev, flush, flush_r, peak):
         tpk.merge_lse(s1 + s2, H * G, 256, o_part, lse_part, o_acc, lse_acc, stream)
 
     times = graph_times(step, args.tier_steps, 3, stream, flush, flush_r)
-    kms = decode_kernel_times(step, args.tier_steps, stream, flush, flush_r)
+    kms = decode_kernel_loop_times([step, step2], max(10, args.tier_steps), stream)
     times_split = graph_times(step_split, args.tier_steps, 3, stream, flush, flush_r)
     lms = loop_times([step, step2], max(10, args.tier_steps), stream)
     stream.synchronize()
@@ -588,10 +596,9 @@ def run_exact_32k(impl, args, stream, dev, flush, flush_r, peak):
     o_s, l_s = o_acc.cpu().numpy(), lse_acc.cpu().numpy()
     ms, ms_split = statistics.median(times), statistics.median(times_split)
     hb = w.history_bytes()
-    gbs, kgbs = hb / (ms * 1e-3) / 1e9, hb / (kms * 1e-3) / 1e9
-    return {"history_bytes": hb, "us_per_step_median": round(ms * 1e3, 2), "GBps": round(gbs, 1),
-            "hbm_frac": round(gbs / peak, 4), "steps": len(times), "kernel_us_mean": round(kms * 1e3, 2),
-            "kernel_GBps": round(kgbs, 1), "kernel_hbm_frac": round(kgbs / peak, 4), **loop_fields(hb, lms, peak),
+    kgbs = hb / (kms * 1e-3) / 1e9
+    return {"history_bytes": hb, **step_fields(hb, lms, ms, len(times), peak), "kernel_us_mean": round(kms * 1e3, 2),
+            "kernel_GBps": round(kgbs, 1), "kernel_hbm_frac": round(kgbs / peak, 4),
             "split_merge": {"split_at": cut, "splits": [s1, s2],
                             "us_per_step_median": round(ms_split * 1e3, 2),
                             "max_abs_do_over_max_o": float(np.abs(o_s - o_u).max() / np.abs(o_u).max()),
@@ -643,9 +650,7 @@ def run_tiny(impl, args, stream, dev, flush, flush_r, peak, keep=None):
     if keep is not None:
         keep["w"], keep["o"] = w, o.cpu().numpy()
     ms = statistics.median(times)
-    return {"history_bytes": w.history_bytes(), "us_per_step_median": round(ms * 1e3, 2),
-            "GBps": round(w.history_bytes() / (ms * 1e-3) / 1e9, 1), "steps": len(times),
-            "loop_us_per_step": round(lms * 1e3, 2),
+    return {"history_bytes": w.history_bytes(), **step_fields(None, lms, ms, len(times), peak),
             "workload": "1 request, 1 KV head x 8 q rows, head_dim 256, 1024 tokens = 12 8-bit pages + 256 BF16, "
                         "K, V with per-channel std log-uniform in [0.1, 10], seed 0 (launch-bound: a parity "
                         "config)"}
